@@ -1,0 +1,374 @@
+"""CPU oracle for the Mixture-of-Transformers (MoT) token-routed dense projection.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports, calls or executes this
+module: only the tests, the smoke check of ``__graft_entry__`` and the CPU-baseline leg
+of ``bench.py`` (including its ``--impl reference`` arm) may use it. It shares no code
+with the CUDA library and never reads a value produced by it, except where a function
+below says it takes the GPU's own bf16 GEMM output as input ("teacher-forced" stage
+checks of the epilogue, which no CPU can reproduce bit for bit after a tensor-core
+accumulation).
+
+Sources (web pages; cited by title and section):
+  [RFC-435]  "[RFC][BAGEL-7B-MoT][CUDA/ROCm] WS1/WS2 kernel roadmap and integration plan #435"
+  [PR-1402]  "[omni, model, ops, ckpt, config, docs] feat: support Bagel in SeedOmni - #1402"
+  [PR-503]   "[WS1][CUDA][Qwen3-Next] MoE route/combine contract with a batch-invariant
+              grouped expert GEMM (RFC #428 stack 5/8) - #503"
+
+What the path computes ([RFC-435] §1 Motivation, item 1): every GEMM and norm of a packed
+batch picks, per token, one of two weight sets -- und (text and ViT tokens, modality 0)
+or gen (VAE-latent tokens, modality 1) -- by a fixed index, with no learned router.
+
+Two programs:
+  G  -- the fp64 golden. Every quantity is computed in float64; the declared bf16 cast
+        points ([RFC-435] §3 Numerical contract: "casts only at declared boundaries") are
+        emulated by a direct round-to-nearest-even to bf16. Reductions use any order.
+  E  -- the fp32 contract emulator. It restates, in float32 with every operation rounded
+        separately (no fused multiply-add), the fixed non-GEMM arithmetic of the kernels:
+        the fixed 32-wide chunked reduction trees, the IEEE division and square root, and
+        the cast points. It is what the CUDA kernels must match bit for bit.
+
+Inputs are numpy arrays. Floating-point tensors are float64 (G) or float32 (E) arrays
+that hold bf16 values exactly; ``mod`` is a uint8 array of 0/1; ``pos`` an int array.
+``eps`` is the float32 parameter the kernels receive; both programs use its exact value.
+
+Parity status: every function here is pinned by tests/test_oracle_pins.py (closed forms,
+brute force on integer-valued inputs, invariants, hand-derived values in tests/golden/).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+F32 = np.float32
+
+# Largest finite bf16 value: (2 - 2^-7) * 2^127.
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+
+# ---------------------------------------------------------------------------
+# rounding to bf16
+# ---------------------------------------------------------------------------
+
+def bf16(x) -> np.ndarray:
+    """Round each value to the nearest bf16 number, ties to even, in one step.
+
+    bf16 keeps 8 significant bits and the float32 exponent range, so the spacing of
+    bf16 numbers near |x| in [2^(e-1), 2^e) is 2^(e-8); below the smallest normal
+    2^-126 the spacing stays 2^-133. Dividing by that power of two is exact, and numpy's
+    ``round`` takes halves to even. Values past the largest finite bf16 after rounding
+    become infinities ([PR-503] RMSNorm commit: one round-to-nearest cast at the store).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)                                  # x = m * 2^e, 0.5 <= |m| < 1
+    quantum = np.ldexp(1.0, np.maximum(e, -125) - 8)
+    r = np.round(x / quantum) * quantum
+    return np.where(np.abs(r) > BF16_MAX, np.copysign(np.inf, x), r)
+
+
+def bf16_f32(x) -> np.ndarray:
+    """bf16 rounding of float32 values, returned as float32 (E's cast)."""
+    return bf16(np.asarray(x, dtype=np.float32).astype(np.float64)).astype(F32)
+
+
+def _eps32(eps: float) -> float:
+    return float(F32(eps))
+
+
+def _check_mod(mod) -> np.ndarray:
+    mod = np.asarray(mod)
+    if mod.size and (mod.min() < 0 or mod.max() > 1):
+        raise ValueError("modality index must be 0 (und) or 1 (gen)")
+    return mod.astype(np.int64)
+
+
+# ---------------------------------------------------------------------------
+# G: fp64 golden
+# ---------------------------------------------------------------------------
+
+def g_fused_add_rmsnorm(x, res, w, mod, eps):
+    """Residual add, then RMSNorm with the row's own weight set.
+
+    [RFC-435] §5 claim order names mot_fused_add_rmsnorm; §1 item 1: the norm picks its
+    weight set per token. The RMSNorm convention is the one of [PR-503]'s zero-centred
+    RMSNorm commit with offset 0: statistics in fp32 (here fp64), y = x * rstd * w with
+    the weight multiply after the upcast and one trailing cast.
+      s      = bf16(x + res)                 (the new residual stream, res_out)
+      rstd   = 1 / sqrt(sum_j s_j^2 / H + eps)
+      y_pre  = s * rstd * w[mod[r]]
+      y      = bf16(y_pre)
+    Returns a dict with y, y_pre (before the final cast), res_out and rstd.
+    """
+    mod = _check_mod(mod)
+    x = np.asarray(x, np.float64)
+    res = np.asarray(res, np.float64)
+    w = np.asarray(w, np.float64)
+    H = x.shape[1]
+    s = bf16(x + res)
+    ms = np.sum(s * s, axis=1) / H
+    rstd = 1.0 / np.sqrt(ms + _eps32(eps))
+    y_pre = s * rstd[:, None] * w[mod]
+    return {"y": bf16(y_pre), "y_pre": y_pre, "res_out": s, "rstd": rstd}
+
+
+def g_routed_matmul(a, w, mod):
+    """acc[r, n] = sum_k a[r, k] * w[mod[r], n, k], in float64.
+
+    The routed dense projection: each row is multiplied by the weight set its modality
+    selects ([RFC-435] §1 item 1); w is [2][N][K] in the nn.Linear (out, in) layout.
+    Each expert's rows go through one plain matmul, so a row's result is by definition
+    the dense layer of its own expert ([PR-503] grouped expert GEMM commit: the grouped
+    result equals the per-expert GEMM loop).
+    """
+    mod = _check_mod(mod)
+    a = np.asarray(a, np.float64)
+    w = np.asarray(w, np.float64)
+    acc = np.zeros((a.shape[0], w.shape[1]), np.float64)
+    for e in (0, 1):
+        rows = np.nonzero(mod == e)[0]
+        if rows.size:
+            acc[rows] = a[rows] @ w[e].T
+    return acc
+
+
+def g_routed_gemm_cast(a, w, mod):
+    """Plain routed projection (O and down projections): out = bf16(acc).
+
+    [PR-1402] "What does this PR do?": MoT routes the O projection per branch (und/gen);
+    [RFC-435] §5 names mot_routed_gemm.
+    """
+    acc = g_routed_matmul(a, w, mod)
+    return {"out": bf16(acc), "out_pre": acc}
+
+
+def rope_inv_freq(theta: float, D: int) -> np.ndarray:
+    """inv_i = theta^(-2i/D) for i < D/2, built in fp64 and stored in fp32.
+
+    [RFC-435] §3 BAGEL-specific rules: tables built in FP64, stored in FP32.
+    """
+    i = np.arange(D // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / D).astype(F32)
+
+
+def rope_cos_sin(theta: float, D: int, pos) -> tuple[np.ndarray, np.ndarray]:
+    """bf16 cos/sin of the angle pos * inv_i, for each position and i < D/2.
+
+    The angle is the fp32 product of the position and inv_i; cos and sin are evaluated
+    in fp64 of that fp32 angle, stored in fp32, and cast to bf16 at the RoPE boundary
+    ([RFC-435] §2 Reference hazards: "QK norm runs in FP32, then RoPE and Q/K in BF16").
+    Returns float64 arrays [len(pos)][D/2] holding bf16 values.
+    """
+    inv = rope_inv_freq(theta, D)
+    ang = np.asarray(pos).astype(F32)[:, None] * inv[None, :]
+    ang64 = ang.astype(np.float64)
+    c = bf16(np.cos(ang64).astype(F32))
+    s = bf16(np.sin(ang64).astype(F32))
+    return c, s
+
+
+def g_rope_bf16(u, c, s):
+    """RoPE in BF16 on a head u[..., D] with the half-split (rotate-half) pairing.
+
+    Element i < D/2 pairs with i + D/2: the rotation partner of element i is -u_{i+D/2}
+    for i < D/2 and u_{i-D/2} for i >= D/2; each product and the sum are rounded to bf16
+    in turn ([RFC-435] §2 Reference hazards: RoPE and Q/K in BF16).
+      out_i = bf16( bf16(u_i * c_i') + bf16(partner_i * s_i') ),  i' = i mod D/2
+    Returns (out, pre) with pre the value before the final cast.
+    """
+    h = u.shape[-1] // 2
+    u1, u2 = u[..., :h], u[..., h:]
+    pre1 = bf16(u1 * c) + bf16(-u2 * s)
+    pre2 = bf16(u2 * c) + bf16(u1 * s)
+    pre = np.concatenate([pre1, pre2], axis=-1)
+    return bf16(pre), pre
+
+
+def g_rope_exact(u, pos, theta: float, D: int):
+    """Cast-free RoPE in fp64 (same pairing and direction as g_rope_bf16).
+
+    Used only by the pins on the rotation itself (norm preservation, relative
+    position, complex-multiplication form).
+    """
+    i = np.arange(D // 2, dtype=np.float64)
+    ang = np.asarray(pos, np.float64)[:, None] * np.power(float(theta), -2.0 * i / D)[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    h = D // 2
+    u1, u2 = u[..., :h], u[..., h:]
+    return np.concatenate([u1 * c - u2 * s, u2 * c + u1 * s], axis=-1)
+
+
+def g_qkv_norm_rope(y, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta):
+    """Routed QKV projection, per-head QK RMSNorm in fp32, RoPE and Q/K in BF16.
+
+    [PR-1402] "What does this PR do?": MoT dual-branch routed Q/K/V projections with
+    fused qkv_proj_{und,gen} weights, per-head QK RMSNorm and packed RoPE;
+    [RFC-435] §2 Reference hazards: QK norm in FP32, then RoPE and Q/K in BF16.
+      acc  = routed(y, w_qkv) (+ b_qkv[mod] if given)       columns ordered q, k, v heads
+      q    = bf16(acc)                                      (GEMM output boundary)
+      Q, K heads:  u = bf16(q * rstd_head * g[mod]),  rstd_head = 1/sqrt(sum q^2 / D + eps)
+                   out = RoPE_bf16(u, cos, sin of pos)
+      V heads:     out = q
+    The per-head norm weight g is q_norm or k_norm, [2][D], one vector per expert shared
+    by all heads of that kind. Returns out, out_pre (value before the final cast), q, acc.
+    """
+    mod = _check_mod(mod)
+    eps = _eps32(eps)
+    acc = g_routed_matmul(y, w_qkv, mod)
+    if b_qkv is not None:
+        acc = acc + np.asarray(b_qkv, np.float64)[mod]
+    q = bf16(acc)
+    out = q.copy()
+    out_pre = acc.copy()
+    c, s = rope_cos_sin(theta, D, pos)
+    q_norm = np.asarray(q_norm, np.float64)
+    k_norm = np.asarray(k_norm, np.float64)
+    for h in range(Hq + Hkv):
+        g = q_norm if h < Hq else k_norm
+        cols = slice(h * D, (h + 1) * D)
+        qh = q[:, cols]
+        ms = np.sum(qh * qh, axis=1) / D
+        rstd = 1.0 / np.sqrt(ms + eps)
+        u = bf16(qh * rstd[:, None] * g[mod])
+        o, pre = g_rope_bf16(u, c, s)
+        out[:, cols] = o
+        out_pre[:, cols] = pre
+    return {"out": out, "out_pre": out_pre, "q": q, "acc": acc}
+
+
+def g_swiglu(acc_gate, acc_up):
+    """SiLU(gate) * up with the gate and up GEMM outputs cast to bf16 first.
+
+    [PR-503] grouped expert GEMM commit: gate_up GEMM, then SwiGLU in FP32, one BF16
+    cast; the gated-norm commit: SiLU uses the accurate exponential.
+      g = bf16(acc_gate), u = bf16(acc_up), h = bf16( g / (1 + exp(-g)) * u )
+    """
+    g = bf16(acc_gate)
+    u = bf16(acc_up)
+    pre = g / (1.0 + np.exp(-g)) * u
+    return {"h": bf16(pre), "h_pre": pre, "g": g, "u": u}
+
+
+def g_routed_swiglu(a, w_gate, w_up, mod):
+    """Routed gate/up projections followed by the SwiGLU epilogue ([RFC-435] §5 mot_swiglu_mlp)."""
+    return g_swiglu(g_routed_matmul(a, w_gate, mod), g_routed_matmul(a, w_up, mod))
+
+
+def g_layer(x, res, w_norm, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta):
+    """The whole projection step: fused add-RMSNorm, then the routed QKV with norm and RoPE."""
+    n = g_fused_add_rmsnorm(x, res, w_norm, mod, eps)
+    r = g_qkv_norm_rope(n["y"], w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta)
+    r.update({"y": n["y"], "y_pre": n["y_pre"], "res_out": n["res_out"]})
+    return r
+
+
+# ---------------------------------------------------------------------------
+# E: fp32 contract emulator
+# ---------------------------------------------------------------------------
+
+def e_fused_add_rmsnorm(x, res, w, mod, eps, return_stats: bool = False):
+    """fp32 restatement of the fused add-RMSNorm with its fixed reduction tree.
+
+    The reduction is a fixed 32-wide chunked sum ([PR-503] zero-centred RMSNorm commit,
+    "On exactness against vLLM": the fixed 32-wide chunked sum is what buys batch
+    invariance), defined here as:
+      lane l in [0, 32) owns columns 256*j + 8*l + t, j = 0 .. H/256-1, t = 0 .. 7;
+      p_l = sequential fp32 sum of s^2 from 0.0, j outer, t inner;
+      the 32 partials combine by an xor butterfly with offsets 16, 8, 4, 2, 1,
+      each step p_l <- p_l + p_(l xor off)  (every lane ends with the same value).
+    Then ms = p / H (IEEE division), rstd = 1 / sqrt(ms + eps) (IEEE sqrt and division),
+    y = bf16((s * rstd) * w[mod]) left to right, each operation rounded on its own.
+    """
+    mod = _check_mod(mod)
+    x32 = np.asarray(x, np.float64).astype(F32)
+    r32 = np.asarray(res, np.float64).astype(F32)
+    w32 = np.asarray(w, np.float64).astype(F32)
+    T, H = x32.shape
+    if H % 256:
+        raise ValueError("the reduction tree is defined for H a multiple of 256")
+    s = bf16_f32(x32 + r32)
+    lanes = np.arange(32)
+    p = np.zeros((T, 32), F32)
+    for j in range(H // 256):
+        for t in range(8):
+            v = s[:, 256 * j + 8 * lanes + t]
+            p = p + v * v
+    for off in (16, 8, 4, 2, 1):
+        p = p + p[:, lanes ^ off]
+    ss = p[:, 0]
+    ms = ss / F32(H)
+    rstd = F32(1.0) / np.sqrt(ms + F32(eps))
+    y = bf16_f32((s * rstd[:, None]) * w32[mod])
+    out = {"y": y, "res_out": s}
+    if return_stats:
+        out.update({"ss": ss, "rstd": rstd, "lane_partials": p})
+    return out
+
+
+def e_head_rstd(qh, eps):
+    """rstd of one head in fp32 with the head's fixed chunk tree.
+
+    The D values split into 32-wide chunks; each chunk is a sequential fp32 sum of q^2
+    from 0.0; the chunk partials are folded left to right ((c0 + c1) + c2) + c3.
+    ms = ss / D, rstd = 1 / sqrt(ms + eps).
+    """
+    T, D = qh.shape
+    chunks = []
+    for c in range(D // 32):
+        acc = np.zeros(T, F32)
+        for t in range(32):
+            v = qh[:, 32 * c + t]
+            acc = acc + v * v
+        chunks.append(acc)
+    ss = chunks[0]
+    for c in chunks[1:]:
+        ss = ss + c
+    ms = ss / F32(D)
+    return F32(1.0) / np.sqrt(ms + F32(eps)), ss
+
+
+def e_rope_bf16(u, c, s):
+    """fp32 restatement of g_rope_bf16 (each product and the sum rounded to bf16)."""
+    h = u.shape[-1] // 2
+    u1, u2 = u[..., :h], u[..., h:]
+    o1 = bf16_f32(bf16_f32(u1 * c) + bf16_f32(-u2 * s))
+    o2 = bf16_f32(bf16_f32(u2 * c) + bf16_f32(u1 * s))
+    return np.concatenate([o1, o2], axis=-1)
+
+
+def e_qk_norm_rope(q, q_norm, k_norm, cos, sin, mod, Hq, Hkv, D, eps, return_stats: bool = False):
+    """Teacher-forced epilogue check: per-head QK RMSNorm and BF16 RoPE on a given q.
+
+    q is the bf16 GEMM output (float values), [T][(Hq+2Hkv)*D]; cos and sin are the bf16
+    table rows of each token's position, [T][D/2]. Q and K heads become
+    RoPE_bf16(bf16((q * rstd) * g[mod])); V heads pass through unchanged.
+    """
+    mod = _check_mod(mod)
+    q32 = np.asarray(q, np.float64).astype(F32)
+    c32 = np.asarray(cos, np.float64).astype(F32)
+    s32 = np.asarray(sin, np.float64).astype(F32)
+    gq = np.asarray(q_norm, np.float64).astype(F32)
+    gk = np.asarray(k_norm, np.float64).astype(F32)
+    out = q32.copy()
+    stats = []
+    for h in range(Hq + Hkv):
+        g = gq if h < Hq else gk
+        cols = slice(h * D, (h + 1) * D)
+        qh = q32[:, cols]
+        rstd, ss = e_head_rstd(qh, eps)
+        u = bf16_f32((qh * rstd[:, None]) * g[mod])
+        out[:, cols] = e_rope_bf16(u, c32, s32)
+        stats.append(ss)
+    if return_stats:
+        return out, np.stack(stats, axis=1)
+    return out
+
+
+def e_swiglu(g, u):
+    """fp32 SwiGLU on bf16 gate/up values: h = bf16((g / (1 + exp(-g))) * u).
+
+    exp is the host's float32 exponential, so this matches a GPU's expf only to within
+    an ulp or two; comparisons against it use a tolerance.
+    """
+    g32 = np.asarray(g, np.float64).astype(F32)
+    u32 = np.asarray(u, np.float64).astype(F32)
+    silu = g32 / (F32(1.0) + np.exp(-g32))
+    return bf16_f32(silu * u32)

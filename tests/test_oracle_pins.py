@@ -1,0 +1,411 @@
+"""Pins of the CPU oracle against facts outside itself (no GPU).
+
+Each test checks the oracle against something it does not compute itself: a library
+routine for bf16 rounding, hand-derived values (tests/golden/hand_values.json), closed
+forms, brute force on integer-valued inputs where every sum is exact, and invariants
+of the mathematics (scale invariance of RMSNorm, RoPE as a complex rotation). The
+inputs are chosen so that a plausible slip in the oracle -- a dropped term, a wrong
+sign or index, a transposed operand, a wrong expert, a different reduction order --
+fails at least one of them.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mot_oracle as O
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_values.json")))
+F32 = np.float32
+
+
+def _hex(s):
+    return float("inf") if s == "inf" else float.fromhex(s)
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding
+# ---------------------------------------------------------------------------
+
+def test_bf16_hand_cases():
+    for c in GOLDEN["bf16_round"]["cases"]:
+        got = O.bf16(np.array([_hex(c["x"])]))[0]
+        exp = _hex(c["expected"])
+        assert got == exp, (c, got)
+        assert math.copysign(1.0, got) == math.copysign(1.0, exp)
+
+
+def test_bf16_matches_torch_on_float32_values():
+    # torch's float32 -> bf16 conversion is an independent round-to-nearest-even.
+    rng = np.random.default_rng(7)
+    a = rng.standard_normal(200_000).astype(F32) * F32(3.0)
+    b = np.ldexp(rng.standard_normal(20_000).astype(F32), rng.integers(-140, 120, 20_000)).astype(F32)
+    bits = rng.integers(0, 2**16, 20_000).astype(np.uint32)
+    ties = ((bits << 16) | 0x8000).view(F32)              # exact half-way cases
+    ties = ties[np.isfinite(ties)]
+    v = np.concatenate([a, b, ties, np.array([0.0, -0.0, 1e-45, -1e-45], F32)])
+    ref = torch.from_numpy(v).to(torch.bfloat16).float().numpy().astype(np.float64)
+    got = O.bf16(v.astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+    assert np.array_equal(np.signbit(got), np.signbit(ref))
+
+
+# ---------------------------------------------------------------------------
+# fused add-RMSNorm
+# ---------------------------------------------------------------------------
+
+def test_add_rmsnorm_constant_row_closed_form():
+    gd = GOLDEN["add_rmsnorm_constant_row"]
+    H = gd["H"]
+    eps = _hex(gd["eps"])
+    assert eps == float(F32(1e-6))
+    w = np.stack([np.full(H, 0.75), np.full(H, 1.25)])
+    for case in gd["cases"]:
+        c = _hex(case["c"])
+        ratio = _hex(case["c_over_rms"])
+        x = np.full((2, H), c)
+        res = np.zeros((2, H))
+        mod = np.array([0, 1])
+        g = O.g_fused_add_rmsnorm(x, res, w, mod, 1e-6)
+        np.testing.assert_allclose(g["y_pre"][0], 0.75 * ratio, rtol=1e-15)
+        np.testing.assert_allclose(g["y_pre"][1], 1.25 * ratio, rtol=1e-15)
+        np.testing.assert_array_equal(g["res_out"], x)
+        e = O.e_fused_add_rmsnorm(x, res, w, mod, 1e-6)
+        # fp32 statistics: within one bf16 step of the closed form
+        for r, wr in ((0, 0.75), (1, 1.25)):
+            step = 2.0 ** (math.frexp(wr * ratio)[1] - 8)
+            assert np.all(np.abs(e["y"][r] - wr * ratio) <= step), (c, e["y"][r][:4])
+
+
+def test_add_rmsnorm_residual_is_rounded_sum():
+    # res_out = bf16(x + res): 1 + 2^-9 is a tie that rounds to 1, 1 + 3*2^-9 rounds up.
+    H = 256
+    x = np.zeros((1, H))
+    res = np.zeros((1, H))
+    x[0, 0], res[0, 0] = 1.0, 2.0 ** -9
+    x[0, 1], res[0, 1] = 1.0, 3 * 2.0 ** -9
+    x[0, 2], res[0, 2] = 0.5, 0.25
+    w = np.ones((2, H))
+    for out in (O.g_fused_add_rmsnorm(x, res, w, [0], 1e-6), O.e_fused_add_rmsnorm(x, res, w, [0], 1e-6)):
+        assert out["res_out"][0, 0] == 1.0
+        assert out["res_out"][0, 1] == 1.0 + 2.0 ** -7
+        assert out["res_out"][0, 2] == 0.75
+
+
+def test_add_rmsnorm_scale_invariance_bitwise():
+    # With eps = 0, scaling a row by a power of two leaves RMSNorm unchanged, exactly.
+    rng = np.random.default_rng(3)
+    T, H = 8, 512
+    s = O.bf16(rng.standard_normal((T, H)))
+    w = O.bf16(1.0 + 0.1 * rng.standard_normal((2, H)))
+    mod = np.array([0, 1] * 4)
+    zero = np.zeros((T, H))
+    for k in (-6, 3, 9):
+        for fn in (O.g_fused_add_rmsnorm, O.e_fused_add_rmsnorm):
+            a = fn(s, zero, w, mod, 0.0)["y"]
+            b = fn(s * 2.0 ** k, zero, w, mod, 0.0)["y"]
+            np.testing.assert_array_equal(a, b)
+
+
+def test_add_rmsnorm_routes_weight_set_per_row():
+    # Expert weights 1 and 2: gen rows are exactly twice the und rows (x2 is exact in bf16).
+    rng = np.random.default_rng(4)
+    H = 256
+    s = O.bf16(rng.standard_normal((1, H)))
+    x = np.repeat(s, 4, axis=0)
+    w = np.stack([np.ones(H), 2 * np.ones(H)])
+    mod = np.array([1, 0, 0, 1])
+    for fn in (O.g_fused_add_rmsnorm, O.e_fused_add_rmsnorm):
+        y = fn(x, np.zeros_like(x), w, mod, 1e-6)["y"]
+        np.testing.assert_array_equal(y[0], 2 * y[1])
+        np.testing.assert_array_equal(y[3], 2 * y[2])
+        np.testing.assert_array_equal(y[1], y[2])
+
+
+def test_add_rmsnorm_e_tree_order_hand_values():
+    gd = GOLDEN["add_rmsnorm_tree_sum"]
+    H = 512
+    x = np.zeros((2, H))
+    x[0, 0] = 4096.0
+    x[0, 1:8] = 1.0
+    for lane in range(1, 32):
+        x[0, 8 * lane] = 1.0
+    x[1, 0:8] = 1.0
+    x[1, 256] = 4096.0
+    e = O.e_fused_add_rmsnorm(x, np.zeros_like(x), np.ones((2, H)), [0, 0], 1e-6, return_stats=True)
+    assert e["ss"][0] == gd["row_A_sum_of_squares"]
+    assert e["ss"][1] == gd["row_B_sum_of_squares"]
+    # every lane of the butterfly holds the same total
+    assert np.all(e["lane_partials"][0] == e["lane_partials"][0, 0])
+
+
+def test_add_rmsnorm_e_within_half_step_of_g():
+    rng = np.random.default_rng(5)
+    T, H = 64, 768
+    x = O.bf16(rng.standard_normal((T, H)))
+    res = O.bf16(rng.standard_normal((T, H)))
+    w = O.bf16(1 + 0.1 * rng.standard_normal((2, H)))
+    mod = rng.integers(0, 2, T)
+    g = O.g_fused_add_rmsnorm(x, res, w, mod, 1e-6)
+    e = O.e_fused_add_rmsnorm(x, res, w, mod, 1e-6)
+    np.testing.assert_array_equal(e["res_out"], g["res_out"])
+    _, ex = np.frexp(g["y_pre"])
+    half = np.ldexp(1.0, ex - 9)
+    assert np.all(np.abs(e["y"] - g["y_pre"]) <= half * (1 + 1e-5) + 1e-30)
+
+
+# ---------------------------------------------------------------------------
+# routed GEMM
+# ---------------------------------------------------------------------------
+
+def _brute_routed(a, w, mod):
+    T, K = a.shape
+    N = w.shape[1]
+    out = [[0 for _ in range(N)] for _ in range(T)]
+    for r in range(T):
+        for n in range(N):
+            acc = 0
+            for k in range(K):
+                acc += int(a[r][k]) * int(w[mod[r]][n][k])
+            out[r][n] = acc
+    return np.array(out, dtype=np.float64)
+
+
+def test_routed_matmul_brute_force_integers():
+    # Integer values: every product and sum is exact, so the result is unique.
+    rng = np.random.default_rng(11)
+    T, K, N = 7, 5, 3                 # non-square: a transposed operand cannot pass
+    a = rng.integers(-4, 5, (T, K))
+    w = rng.integers(-3, 4, (2, N, K))
+    mod = np.array([0, 1, 1, 0, 1, 0, 0])
+    np.testing.assert_array_equal(O.g_routed_matmul(a, w, mod), _brute_routed(a, w, mod))
+    out = O.g_routed_gemm_cast(a, w, mod)
+    np.testing.assert_array_equal(out["out"], _brute_routed(a, w, mod))
+
+
+def test_routed_matmul_single_modality_is_dense():
+    rng = np.random.default_rng(12)
+    a = rng.integers(-4, 5, (6, 4))
+    w = rng.integers(-3, 4, (2, 5, 4))
+    for e in (0, 1):
+        mod = np.full(6, e)
+        dense = np.array([[sum(int(a[r, k]) * int(w[e, n, k]) for k in range(4)) for n in range(5)]
+                          for r in range(6)], dtype=np.float64)
+        np.testing.assert_array_equal(O.g_routed_matmul(a, w, mod), dense)
+
+
+def test_routed_rows_depend_only_on_themselves():
+    rng = np.random.default_rng(13)
+    a = rng.integers(-50, 51, (9, 8)).astype(np.float64)      # exact sums in any order
+    w = rng.integers(-50, 51, (2, 6, 8)).astype(np.float64)
+    mod = rng.integers(0, 2, 9)
+    full = O.g_routed_matmul(a, w, mod)
+    for r in range(9):
+        one = O.g_routed_matmul(a[r:r + 1], w, mod[r:r + 1])
+        np.testing.assert_array_equal(one[0], full[r])
+
+
+def test_modality_out_of_range_rejected():
+    with pytest.raises(ValueError):
+        O.g_routed_matmul(np.ones((2, 2)), np.ones((2, 2, 2)), [0, 2])
+
+
+# ---------------------------------------------------------------------------
+# QK norm and RoPE
+# ---------------------------------------------------------------------------
+
+def _onehot_qkv(c_q, c_k, Hq, Hkv, D):
+    """y = e_0 and W[:, n, 0] = c: the GEMM output of every Q (K) column is exactly c_q (c_k)."""
+    N = (Hq + 2 * Hkv) * D
+    w = np.zeros((2, N, 64))
+    w[:, : Hq * D, 0] = c_q
+    w[:, Hq * D: (Hq + Hkv) * D, 0] = c_k
+    w[:, (Hq + Hkv) * D:, 0] = 0.5
+    y = np.zeros((2, 64))
+    y[:, 0] = 1.0
+    return y, w
+
+
+@pytest.mark.parametrize("c_q,c_k", [(1.5, -3.0), (2.0 ** -10, -(2.0 ** -11))])
+def test_qk_norm_constant_head_closed_form_at_position_zero(c_q, c_k):
+    # A head of equal values c normalizes to g * c / sqrt(c^2 + eps); small c makes eps visible.
+    Hq, Hkv, D = 2, 1, 128
+    eps = float(F32(1e-6))
+    y, w = _onehot_qkv(c_q, c_k, Hq, Hkv, D)
+    qn = np.stack([np.full(D, 0.75), np.full(D, 1.25)])
+    kn = np.stack([np.full(D, 1.5), np.full(D, 0.5)])
+    mod = np.array([0, 1])
+    g = O.g_qkv_norm_rope(y, w, None, qn, kn, np.array([0, 0]), mod, Hq, Hkv, D, 1e-6, 1e6)
+    c, s = O.rope_cos_sin(1e6, D, np.array([0, 0]))
+    e_out = O.e_qk_norm_rope(g["q"], qn, kn, c, s, mod, Hq, Hkv, D, 1e-6)
+    for r, e in ((0, 0), (1, 1)):
+        qv = O.bf16(qn[e, 0] * c_q / math.sqrt(c_q * c_q + eps))
+        kv = O.bf16(kn[e, 0] * c_k / math.sqrt(c_k * c_k + eps))
+        for out in (g["out"], e_out):
+            assert np.all(out[r, : Hq * D] == qv)
+            assert np.all(out[r, Hq * D: (Hq + Hkv) * D] == kv)
+            assert np.all(out[r, (Hq + Hkv) * D:] == 0.5)       # V passes through
+
+
+def test_qk_norm_scale_invariance_and_bias():
+    rng = np.random.default_rng(21)
+    Hq, Hkv, D, T = 2, 1, 64, 6
+    N = (Hq + 2 * Hkv) * D
+    y = O.bf16(rng.standard_normal((T, 128)))
+    w = O.bf16(0.05 * rng.standard_normal((2, N, 128)))
+    qn = O.bf16(1 + 0.1 * rng.standard_normal((2, D)))
+    kn = O.bf16(1 + 0.1 * rng.standard_normal((2, D)))
+    mod = rng.integers(0, 2, T)
+    pos = rng.integers(0, 1000, T)
+    a = O.g_qkv_norm_rope(y, w, None, qn, kn, pos, mod, Hq, Hkv, D, 0.0, 1e6)
+    b = O.g_qkv_norm_rope(y * 8.0, w, None, qn, kn, pos, mod, Hq, Hkv, D, 0.0, 1e6)
+    np.testing.assert_array_equal(a["out"][:, : (Hq + Hkv) * D], b["out"][:, : (Hq + Hkv) * D])
+    np.testing.assert_array_equal(a["out"][:, (Hq + Hkv) * D:] * 8.0, b["out"][:, (Hq + Hkv) * D:])
+    # a bias of the row's own expert is added before the cast
+    bias = O.bf16(rng.standard_normal((2, N)))
+    c = O.g_qkv_norm_rope(y, w, bias, qn, kn, pos, mod, Hq, Hkv, D, 1e-6, 1e6)
+    np.testing.assert_array_equal(c["acc"], a["acc"] + bias[mod])
+
+
+def test_qk_head_tree_order_hand_value():
+    gd = GOLDEN["qk_head_tree_sum"]
+    D = 128
+    q = np.zeros((1, 3 * D))
+    q[0, 0] = 4096.0
+    q[0, 1:32] = 1.0
+    q[0, 32] = 1.0
+    q[0, 64] = 1.0
+    q[0, 96:98] = 1.0
+    cs = np.ones((1, D // 2)), np.zeros((1, D // 2))
+    _, ss = O.e_qk_norm_rope(q, np.ones((2, D)), np.ones((2, D)), cs[0], cs[1], [0], 1, 1, D, 1e-6,
+                             return_stats=True)
+    assert ss[0, 0] == gd["sum_of_squares"]
+
+
+def test_rope_table_hand_values():
+    gd = GOLDEN["rope"]
+    c, s = O.rope_cos_sin(1e6, 128, np.array([0, 1]))
+    assert np.all(c[0] == 1.0) and np.all(s[0] == 0.0)
+    assert c[1, 0] == gd["pos1_i0_cos"] and s[1, 0] == gd["pos1_i0_sin"]
+    inv = O.rope_inv_freq(1e6, 128)
+    assert inv[0] == 1.0
+    # successive frequencies shrink by theta^(2/D), to fp32 rounding
+    np.testing.assert_allclose(inv[:-1] / inv[1:], 1e6 ** (2 / 128), rtol=3e-7)
+
+
+def test_rope_position_zero_is_identity():
+    rng = np.random.default_rng(31)
+    D = 128
+    u = O.bf16(rng.standard_normal((5, D)))
+    u[u == 0] = 1.0
+    c, s = O.rope_cos_sin(1e6, D, np.zeros(5, np.int64))
+    out, _ = O.g_rope_bf16(u, c, s)
+    np.testing.assert_array_equal(out, u)
+    np.testing.assert_array_equal(O.e_rope_bf16(u.astype(F32), c.astype(F32), s.astype(F32)), u.astype(F32))
+
+
+def test_rope_is_complex_rotation():
+    # (out_i + j out_{i+D/2}) = (u_i + j u_{i+D/2}) * exp(j * pos * theta^(-2i/D))
+    rng = np.random.default_rng(32)
+    D, theta = 64, 1e6
+    u = rng.standard_normal((7, D))
+    pos = rng.integers(0, 5000, 7)
+    out = O.g_rope_exact(u, pos, theta, D)
+    i = np.arange(D // 2)
+    z = (u[:, : D // 2] + 1j * u[:, D // 2:]) * np.exp(1j * pos[:, None] * theta ** (-2.0 * i / D))
+    np.testing.assert_allclose(out[:, : D // 2], z.real, atol=1e-12)
+    np.testing.assert_allclose(out[:, D // 2:], z.imag, atol=1e-12)
+    # direction (hand value): e_0 at position 1 sends +sin(1) to element D/2
+    e0 = np.zeros((1, D))
+    e0[0, 0] = 1.0
+    r = O.g_rope_exact(e0, np.array([1]), theta, D)
+    assert abs(r[0, 0] - math.cos(1.0)) < 1e-15 and abs(r[0, D // 2] - math.sin(1.0)) < 1e-15
+
+
+def test_rope_norm_and_relative_position():
+    rng = np.random.default_rng(33)
+    D = 128
+    q = rng.standard_normal((1, D))
+    k = rng.standard_normal((1, D))
+    h = D // 2
+    r = O.g_rope_exact(q, np.array([37]), 1e6, D)
+    np.testing.assert_allclose(r[:, :h] ** 2 + r[:, h:] ** 2, q[:, :h] ** 2 + q[:, h:] ** 2, rtol=1e-12)
+    dots = []
+    for m, n in ((40, 15), (1040, 1015), (25, 0)):
+        dots.append(float(np.sum(O.g_rope_exact(q, np.array([m]), 1e6, D) * O.g_rope_exact(k, np.array([n]), 1e6, D))))
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-9)
+
+
+def test_rope_bf16_agrees_with_exact_rotation():
+    # BF16 RoPE stays within a few bf16 steps of the exact rotation of the same u.
+    rng = np.random.default_rng(34)
+    D = 128
+    u = O.bf16(rng.standard_normal((32, D)))
+    pos = rng.integers(0, 4096, 32)
+    c, s = O.rope_cos_sin(1e6, D, pos)
+    out, _ = O.g_rope_bf16(u, c, s)
+    assert np.max(np.abs(out - O.g_rope_exact(u, pos, 1e6, D))) < 0.08
+
+
+def test_e_qk_epilogue_matches_g_on_same_q():
+    rng = np.random.default_rng(35)
+    Hq, Hkv, D, T = 4, 2, 64, 40
+    N = (Hq + 2 * Hkv) * D
+    y = O.bf16(rng.standard_normal((T, 256)))
+    w = O.bf16(0.02 * rng.standard_normal((2, N, 256)))
+    qn = O.bf16(1 + 0.1 * rng.standard_normal((2, D)))
+    kn = O.bf16(1 + 0.1 * rng.standard_normal((2, D)))
+    mod = rng.integers(0, 2, T)
+    pos = np.arange(T)
+    g = O.g_qkv_norm_rope(y, w, None, qn, kn, pos, mod, Hq, Hkv, D, 1e-6, 1e6)
+    c, s = O.rope_cos_sin(1e6, D, pos)
+    e = O.e_qk_norm_rope(g["q"], qn, kn, c, s, mod, Hq, Hkv, D, 1e-6)
+    # same q in: E and G differ only by fp32 vs fp64 statistics -> rare one-step flips
+    _, ex = np.frexp(np.maximum(np.abs(g["out"]), 2.0 ** -100))
+    step = np.ldexp(1.0, ex - 8)
+    diff = np.abs(e - g["out"])
+    assert np.all(diff <= 2 * step)
+    assert np.mean(diff > 0) < 0.01
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU
+# ---------------------------------------------------------------------------
+
+def test_swiglu_hand_values():
+    for c in GOLDEN["swiglu"]["cases"]:
+        g = O.g_swiglu(np.array([c["g"]]), np.array([c["u"]]))
+        assert g["h"][0] == c["h"]
+        e = O.e_swiglu(np.array([c["g"]]), np.array([c["u"]]))
+        assert e[0] == c["h"]
+
+
+def test_swiglu_limits_and_e_agreement():
+    g = O.g_swiglu(np.array([30.0, -30.0]), np.array([1.0, 1.0]))
+    assert g["h"][0] == 30.0 and abs(g["h"][1]) < 1e-11
+    rng = np.random.default_rng(41)
+    ag = rng.standard_normal(5000) * 3
+    au = rng.standard_normal(5000) * 3
+    ref = O.g_swiglu(ag, au)
+    e = O.e_swiglu(ref["g"], ref["u"])
+    _, ex = np.frexp(np.maximum(np.abs(ref["h_pre"]), 2.0 ** -100))
+    assert np.all(np.abs(e - ref["h_pre"]) <= np.ldexp(1.0, ex - 8))
+
+
+def test_layer_composition():
+    # the layer is the norm followed by the projection on the norm's bf16 output
+    from mixture_transformers_token_gb300 import workloads as W
+    shape, inp = W.tiny_layer(seed=2)
+    f = {k: (v.float().numpy().astype(np.float64) if isinstance(v, torch.Tensor) and v.is_floating_point() else
+             (v.numpy() if isinstance(v, torch.Tensor) else v)) for k, v in inp.items()}
+    lay = O.g_layer(f["x"], f["res"], f["w_norm"], f["w_qkv"], None, f["q_norm"], f["k_norm"], f["pos"],
+                    f["mod"], shape.Hq, shape.Hkv, shape.D, shape.eps, shape.theta)
+    n = O.g_fused_add_rmsnorm(f["x"], f["res"], f["w_norm"], f["mod"], shape.eps)
+    q = O.g_qkv_norm_rope(n["y"], f["w_qkv"], None, f["q_norm"], f["k_norm"], f["pos"], f["mod"],
+                          shape.Hq, shape.Hkv, shape.D, shape.eps, shape.theta)
+    np.testing.assert_array_equal(lay["out"], q["out"])
+    assert np.isfinite(lay["out"]).all()
