@@ -1,0 +1,195 @@
+/*
+ * mot.h -- C ABI of the Mixture-of-Transformers (MoT) token-routed dense projection
+ * library for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [RFC-435]  "[RFC][BAGEL-7B-MoT][CUDA/ROCm] WS1/WS2 kernel roadmap and integration plan #435"
+ *   [PR-1402]  "[omni, model, ops, ckpt, config, docs] feat: support Bagel in SeedOmni - #1402"
+ *   [PR-503]   "[WS1][CUDA][Qwen3-Next] MoE route/combine contract with a batch-invariant
+ *               grouped expert GEMM (RFC #428 stack 5/8) - #503"
+ *
+ * The method ([RFC-435] §1 Motivation, item 1): a packed batch of T token rows; each row
+ * uses one of two weight sets -- und (modality 0: text and ViT tokens) or gen (modality 1:
+ * VAE-latent tokens) -- chosen by a fixed per-token index; every GEMM and norm picks its
+ * weight set per row, and a row's output bytes must not depend on the modality mix, the
+ * order or the size of the pack.
+ *
+ * Conventions for every entry point
+ *   - Tensors are plain device pointers to dense row-major arrays; bf16 values are passed
+ *     as raw 16-bit patterns (mot_bf16). Every bf16 tensor and the workspace must start on
+ *     a 16-byte boundary. The caller owns all memory; the library allocates nothing and
+ *     keeps no state between calls apart from per-device attribute caches.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream of the current
+ *     device). Every pointer must belong to the stream's device (the device guard of
+ *     [PR-503]'s RMSNorm launcher commit); the launch runs on that device.
+ *   - Calls are asynchronous on `stream`. A nonzero return is a host-detected error: no
+ *     kernel was launched and no output was written (fail closed: [RFC-435] §3 Numerical
+ *     contract). Errors found on the device (a modality other than 0/1, a position
+ *     outside the RoPE table, a plan that does not match the call, a pipeline wait that
+ *     timed out) set bits in the workspace's error word, read by mot_device_status.
+ *     Outputs are defined only when both are clean.
+ *   - Numerics ([RFC-435] §3): fixed fp32 accumulation and reduction order, no split-K,
+ *     stream-K or atomics in any reduction, no TF32 or fast math, round-to-nearest-even
+ *     casts only at the points each entry point declares.
+ */
+#ifndef MOT_H
+#define MOT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOT_ABI_VERSION 1
+
+/* host-detected status codes (return values) */
+#define MOT_OK            0
+#define MOT_ERR_NULL      1  /* a required pointer is NULL */
+#define MOT_ERR_ALIGN     2  /* a pointer is not 16-byte aligned */
+#define MOT_ERR_GEOMETRY  3  /* unsupported shape: see each entry point */
+#define MOT_ERR_DEVICE    4  /* a pointer is not device memory of the stream's device */
+#define MOT_ERR_WORKSPACE 5  /* workspace smaller than mot_workspace_bytes(T) */
+#define MOT_ERR_ARCH      6  /* the stream's device is not compute capability 10.3 */
+#define MOT_ERR_CUDA      7  /* a CUDA runtime call or a launch failed */
+#define MOT_ERR_ARG       8  /* any other invalid argument (epilogue id, eps, P ...) */
+
+/* device-detected error bits, OR-ed into the workspace error word */
+#define MOT_DEV_BAD_MODALITY  0x1u  /* a modality index other than 0 or 1 */
+#define MOT_DEV_TIMEOUT       0x2u  /* a pipeline wait gave up after about one second */
+#define MOT_DEV_PLAN_MISMATCH 0x4u  /* the workspace holds no plan for this T */
+#define MOT_DEV_BAD_POSITION  0x8u  /* a RoPE position outside [0, P) (clamped to 0) */
+
+/* epilogues of mot_routed_gemm */
+#define MOT_EPI_CAST   0  /* out = bf16(acc) */
+#define MOT_EPI_SWIGLU 1  /* out = bf16(silu(bf16(acc_gate)) * bf16(acc_up)) */
+
+/* largest packed batch the library accepts */
+#define MOT_MAX_TOKENS (1 << 24)
+
+typedef uint16_t mot_bf16; /* raw bfloat16 bit pattern */
+
+/* ABI version of the loaded library; a binding refuses to run against another one
+ * (the stale-binding check of [PR-503]'s evidence-runner commit). */
+int mot_abi_version(void);
+
+/* Static, NUL-terminated description of a status code. */
+const char* mot_status_string(int status);
+
+/* Bytes of workspace needed for a pack of T rows (0 if T is out of range). The workspace
+ * holds the routing plan and the device error word; the caller allocates it. */
+size_t mot_workspace_bytes(int64_t T);
+
+/*
+ * mot_route_plan -- routing pre-pass ([RFC-435] §1 item 1: a fixed index set per token;
+ * §6 Contribution notes: both weight sets always present).
+ *   mod   [T] uint8 device array: 0 = und, 1 = gen.
+ *   ws    device workspace of at least mot_workspace_bytes(T) bytes.
+ * Writes into ws the row list of each expert in ascending row order and the table of
+ * 128-row tiles that the routed GEMMs walk, and clears the error word. A modality other
+ * than 0/1 sets MOT_DEV_BAD_MODALITY and leaves a plan with no tiles, so later GEMMs on
+ * this workspace write nothing. The plan depends only on mod, so one plan serves every
+ * routed GEMM of a layer.
+ */
+int mot_route_plan(const uint8_t* mod, int64_t T, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * mot_fused_add_rmsnorm -- residual add, then RMSNorm with the row's weight set
+ * ([RFC-435] §5 claim order, item 2; RMSNorm convention of [PR-503]'s zero-centred
+ * RMSNorm commit with offset 0; fixed 32-wide chunked reduction of its "On exactness
+ * against vLLM" section).
+ *   x, res    [T][H] bf16          inputs.
+ *   w         [2][H] bf16          norm weight of und (row 0) and gen (row 1).
+ *   mod       [T] uint8            modality of each row.
+ *   eps       > 0 and finite       added to the mean square inside the square root.
+ *   y         [T][H] bf16          normalized output.
+ *   res_out   [T][H] bf16          new residual stream; may alias res (in place).
+ *   ws        optional workspace   if not NULL, receives MOT_DEV_BAD_MODALITY.
+ * Per row: s = bf16(x + res) -> res_out; lane l of a 32-lane group owns columns
+ * 256j + 8l + t; p_l = sequential fp32 sum of s^2 (j outer, t inner); partials combine
+ * by an xor butterfly 16, 8, 4, 2, 1; rstd = 1 / sqrt(p / H + eps) with IEEE division and
+ * square root; y = bf16((s * rstd) * w[mod]). A row with an invalid modality gets res_out
+ * but no y. Geometry: H a multiple of 256, 256 <= H <= 8192; 1 <= T <= MOT_MAX_TOKENS.
+ */
+int mot_fused_add_rmsnorm(const mot_bf16* x, const mot_bf16* res, const mot_bf16* w,
+                          const uint8_t* mod, int64_t T, int H, float eps,
+                          mot_bf16* y, mot_bf16* res_out, void* ws, void* stream);
+
+/*
+ * mot_routed_qkv_norm_rope -- routed QKV projection with per-head QK RMSNorm in fp32 and
+ * RoPE with Q/K in bf16 ([PR-1402] "What does this PR do?": MoT dual-branch routed Q/K/V
+ * with fused qkv_proj_{und,gen} weights, per-head QK RMSNorm and packed RoPE; [RFC-435]
+ * §2 Reference hazards: QK norm in FP32, then RoPE and Q/K in BF16).
+ *   x         [T][H] bf16             normalized hidden states (mot_fused_add_rmsnorm's y).
+ *   w_qkv     [2][N][H] bf16          fused weights, N = (Hq + 2 Hkv) D, rows ordered
+ *                                     q heads, k heads, v heads (nn.Linear layout).
+ *   b_qkv     [2][N] bf16 or NULL     optional bias, added in fp32 before the cast.
+ *   q_norm_w, k_norm_w [2][D] bf16    per-expert QK-norm weights shared by all heads.
+ *   pos       [T] int32               RoPE position of each row, 0 <= pos < P.
+ *   rope_cs   [P][D/2][2] bf16        (cos, sin) table, see mot_rope_table_fill_host.
+ *   ws        workspace holding the plan of mot_route_plan for this T (same stream).
+ *   qkv_out   [T][N] bf16             output in the original row order.
+ * Per row r with e = mod[r]: acc = sum_k x[r][k] W[e][n][k] in fp32 (tensor cores, fixed
+ * K order); q = bf16(acc + b); for each Q/K head: rstd = 1/sqrt(ss/D + eps) with ss the
+ * fixed chunk tree (32-wide sequential chunks, left fold); u = bf16((q * rstd) * g[e]);
+ * out_i = bf16(bf16(u_i c) + bf16(partner_i s)) with partner -u_{i+D/2} (i < D/2) or
+ * u_{i-D/2}; V heads: out = q. Geometry: D in {64, 128}; Hq, Hkv >= 1; N a multiple of
+ * 256; H a multiple of 64; P >= 1.
+ */
+int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv, const mot_bf16* b_qkv,
+                             const mot_bf16* q_norm_w, const mot_bf16* k_norm_w,
+                             const int32_t* pos, const mot_bf16* rope_cs, int P,
+                             int64_t T, int H, int Hq, int Hkv, int D, float eps,
+                             void* ws, size_t ws_bytes, mot_bf16* qkv_out, void* stream);
+
+/*
+ * mot_routed_gemm -- routed dense projection for the O, gate/up and down projections
+ * ([RFC-435] §5 mot_routed_gemm and mot_swiglu_mlp; [PR-503] grouped expert GEMM commit:
+ * one writer per row, grouped result equal to the per-expert GEMM).
+ *   a    [T][K] bf16           input rows in the original order.
+ *   w    [2][N][K] bf16        per-expert weights (nn.Linear layout).
+ *   ws   workspace holding the plan of mot_route_plan for this T (same stream).
+ *   epilogue MOT_EPI_CAST:    out [T][N]   = bf16(acc).
+ *   epilogue MOT_EPI_SWIGLU:  w is the gate/up weight in the layout written by
+ *                             mot_swiglu_interleave (N = 2 I); out [T][I] =
+ *                             bf16(g / (1 + expf(-g)) * u), g = bf16(acc_gate),
+ *                             u = bf16(acc_up), fp32 arithmetic.
+ * Geometry: N a multiple of 256, K a multiple of 64.
+ */
+int mot_routed_gemm(const mot_bf16* a, const mot_bf16* w, int64_t T, int N, int K, int epilogue,
+                    void* ws, size_t ws_bytes, mot_bf16* out, void* stream);
+
+/*
+ * mot_swiglu_interleave -- one-time layout step for the gate/up weights.
+ *   w_gate, w_up  [2][I][K] bf16 device arrays.
+ *   w_gu          [2][2I][K] bf16 device array: for each block b of 128 rows,
+ *                 rows 256b .. 256b+127 are gate rows 128b .. and rows 256b+128 ..
+ *                 256b+255 the matching up rows, so one 256-row GEMM tile holds
+ *                 matching gate and up columns.
+ * Geometry: I a multiple of 128, K a multiple of 8.
+ */
+int mot_swiglu_interleave(const mot_bf16* w_gate, const mot_bf16* w_up, int I, int K,
+                          mot_bf16* w_gu, void* stream);
+
+/*
+ * mot_rope_table_fill_host -- host-side (cos, sin) table for positions 0 .. P-1.
+ *   host_cs  host array of P * D/2 * 2 bf16: entry [p][i] = (cos, sin) of the angle
+ *            fp32(p) * inv_i (an fp32 product), inv_i = theta^(-2i/D) built in fp64 and
+ *            stored in fp32; cos and sin are evaluated in fp64, stored in fp32 and cast to
+ *            bf16 ([RFC-435] §3: tables built in FP64, stored in FP32; §2: RoPE in BF16).
+ * Geometry: D even, 2 <= D <= 1024; 1 <= P <= MOT_MAX_TOKENS; theta > 1.
+ */
+int mot_rope_table_fill_host(double theta, int D, int P, mot_bf16* host_cs);
+
+/*
+ * mot_device_status -- synchronizes `stream` and copies the workspace error word
+ * (MOT_DEV_* bits, 0 = clean) to *flags.
+ */
+int mot_device_status(const void* ws, uint32_t* flags, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOT_H */

@@ -1,0 +1,248 @@
+"""MoT token-routed dense projection for GB300 (sm_103a): Python binding of libmot.so.
+
+Argument marshalling only. Every step of the path -- routing pre-pass, fused add-RMSNorm,
+routed GEMMs and their epilogues -- runs in the CUDA kernels of libmot.so, whose C ABI is
+declared in include/mot.h. PyTorch provides device memory and streams. There is no CPU
+fallback: a missing or stale library raises, and every nonzero status raises MotError.
+
+Functions keep the C names. Tensors are contiguous CUDA tensors: bf16 for activations and
+weights, uint8 for the modality index (0 = und, 1 = gen), int32 for positions, uint8 for
+the workspace.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MotError", "load_library", "library_path", "ABI_VERSION", "EPI_CAST", "EPI_SWIGLU",
+    "DEV_BAD_MODALITY", "DEV_TIMEOUT", "DEV_PLAN_MISMATCH", "DEV_BAD_POSITION",
+    "mot_abi_version", "mot_status_string", "mot_workspace_bytes", "mot_route_plan",
+    "mot_fused_add_rmsnorm", "mot_routed_qkv_norm_rope", "mot_routed_gemm",
+    "mot_swiglu_interleave", "mot_rope_table_fill_host", "mot_device_status",
+]
+
+ABI_VERSION = 1
+EPI_CAST = 0
+EPI_SWIGLU = 1
+DEV_BAD_MODALITY = 0x1
+DEV_TIMEOUT = 0x2
+DEV_PLAN_MISMATCH = 0x4
+DEV_BAD_POSITION = 0x8
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+_c_p = ctypes.c_void_p
+_c_i64 = ctypes.c_int64
+_c_i = ctypes.c_int
+_c_f = ctypes.c_float
+_c_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "mot_abi_version": (_c_i, []),
+    "mot_status_string": (ctypes.c_char_p, [_c_i]),
+    "mot_workspace_bytes": (_c_sz, [_c_i64]),
+    "mot_route_plan": (_c_i, [_c_p, _c_i64, _c_p, _c_sz, _c_p]),
+    "mot_fused_add_rmsnorm": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i, _c_f, _c_p, _c_p, _c_p, _c_p]),
+    "mot_routed_qkv_norm_rope": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i64, _c_i, _c_i, _c_i,
+                                        _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_routed_gemm": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_swiglu_interleave": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_p]),
+    "mot_rope_table_fill_host": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
+    "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
+}
+
+
+class MotError(RuntimeError):
+    """A nonzero status returned by libmot.so."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed with status {status}: {_lib().mot_status_string(status).decode()}")
+
+
+def library_path() -> str:
+    return os.environ.get("MOT_LIBRARY", os.path.join(_PKG, "libmot.so"))
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Loads libmot.so and declares its C signatures; raises if it is missing or stale."""
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run `python -m mixture_transformers_token_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if lib.mot_abi_version() != ABI_VERSION:
+        raise ImportError(f"{path} has ABI {lib.mot_abi_version()}, the binding expects {ABI_VERSION}")
+    return lib
+
+
+def _lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        _LIB = load_library()
+    return _LIB
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise MotError(fn, status)
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int | None = None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+    return t.data_ptr()
+
+
+def _stream(t: torch.Tensor, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def mot_abi_version() -> int:
+    return _lib().mot_abi_version()
+
+
+def mot_status_string(status: int) -> str:
+    return _lib().mot_status_string(status).decode()
+
+
+def mot_workspace_bytes(T: int) -> int:
+    return int(_lib().mot_workspace_bytes(T))
+
+
+def mot_route_plan(mod: torch.Tensor, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Builds the routing plan of `mod` in `ws` (allocated if None) and returns ws."""
+    T = mod.numel()
+    _dev(mod, "mod", torch.uint8, 1)
+    if ws is None:
+        ws = torch.empty(max(mot_workspace_bytes(T), 16), dtype=torch.uint8, device=mod.device)
+    _dev(ws, "ws", torch.uint8, 1)
+    _check("mot_route_plan", _lib().mot_route_plan(mod.data_ptr(), T, ws.data_ptr(), ws.numel(), _stream(mod, stream)))
+    return ws
+
+
+def mot_fused_add_rmsnorm(x, res, w, mod, eps: float, y=None, res_out=None, ws=None, stream=None):
+    """Residual add and routed RMSNorm; returns (y, res_out). res_out may be res (in place)."""
+    T, H = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    if res_out is None:
+        res_out = torch.empty_like(res)
+    for t, n in ((x, "x"), (res, "res"), (y, "y"), (res_out, "res_out")):
+        _dev(t, n, torch.bfloat16, 2)
+        if tuple(t.shape) != (T, H):
+            raise ValueError(f"{n} must be [{T}, {H}]")
+    _dev(w, "w", torch.bfloat16, 2)
+    _dev(mod, "mod", torch.uint8, 1)
+    if tuple(w.shape) != (2, H) or mod.numel() != T:
+        raise ValueError("w must be [2, H] and mod [T]")
+    wsp = _dev(ws, "ws", torch.uint8, 1) if ws is not None else None
+    _check("mot_fused_add_rmsnorm", _lib().mot_fused_add_rmsnorm(
+        x.data_ptr(), res.data_ptr(), w.data_ptr(), mod.data_ptr(), T, H, eps, y.data_ptr(), res_out.data_ptr(),
+        wsp, _stream(x, stream)))
+    return y, res_out
+
+
+def mot_routed_qkv_norm_rope(x, w_qkv, q_norm_w, k_norm_w, pos, rope_cs, Hq: int, Hkv: int, D: int, eps: float,
+                             ws, b_qkv=None, out=None, stream=None):
+    """Routed QKV GEMM + per-head QK RMSNorm + BF16 RoPE; `ws` must hold the plan for T rows."""
+    T, H = x.shape
+    N = (Hq + 2 * Hkv) * D
+    _dev(x, "x", torch.bfloat16, 2)
+    _dev(w_qkv, "w_qkv", torch.bfloat16, 3)
+    _dev(q_norm_w, "q_norm_w", torch.bfloat16, 2)
+    _dev(k_norm_w, "k_norm_w", torch.bfloat16, 2)
+    _dev(pos, "pos", torch.int32, 1)
+    _dev(rope_cs, "rope_cs", torch.bfloat16, 3)
+    _dev(ws, "ws", torch.uint8, 1)
+    if tuple(w_qkv.shape) != (2, N, H):
+        raise ValueError(f"w_qkv must be [2, {N}, {H}]")
+    if tuple(q_norm_w.shape) != (2, D) or tuple(k_norm_w.shape) != (2, D) or pos.numel() != T:
+        raise ValueError("q_norm_w/k_norm_w must be [2, D] and pos [T]")
+    if rope_cs.shape[1:] != (D // 2, 2):
+        raise ValueError("rope_cs must be [P, D/2, 2]")
+    bp = None
+    if b_qkv is not None:
+        bp = _dev(b_qkv, "b_qkv", torch.bfloat16, 2)
+        if tuple(b_qkv.shape) != (2, N):
+            raise ValueError(f"b_qkv must be [2, {N}]")
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    _dev(out, "out", torch.bfloat16, 2)
+    _check("mot_routed_qkv_norm_rope", _lib().mot_routed_qkv_norm_rope(
+        x.data_ptr(), w_qkv.data_ptr(), bp, q_norm_w.data_ptr(), k_norm_w.data_ptr(), pos.data_ptr(),
+        rope_cs.data_ptr(), rope_cs.shape[0], T, H, Hq, Hkv, D, eps, ws.data_ptr(), ws.numel(), out.data_ptr(),
+        _stream(x, stream)))
+    return out
+
+
+def mot_routed_gemm(a, w, ws, epilogue: int = EPI_CAST, out=None, stream=None):
+    """Routed GEMM: out[T][N] = bf16(a W^T) (cast) or out[T][N/2] = SwiGLU (interleaved gate/up w)."""
+    T, K = a.shape
+    _dev(a, "a", torch.bfloat16, 2)
+    _dev(w, "w", torch.bfloat16, 3)
+    _dev(ws, "ws", torch.uint8, 1)
+    if w.shape[0] != 2 or w.shape[2] != K:
+        raise ValueError("w must be [2, N, K]")
+    N = w.shape[1]
+    ncols = N // 2 if epilogue == EPI_SWIGLU else N
+    if out is None:
+        out = torch.empty((T, ncols), dtype=torch.bfloat16, device=a.device)
+    _dev(out, "out", torch.bfloat16, 2)
+    if tuple(out.shape) != (T, ncols):
+        raise ValueError(f"out must be [{T}, {ncols}]")
+    _check("mot_routed_gemm", _lib().mot_routed_gemm(
+        a.data_ptr(), w.data_ptr(), T, N, K, epilogue, ws.data_ptr(), ws.numel(), out.data_ptr(), _stream(a, stream)))
+    return out
+
+
+def mot_swiglu_interleave(w_gate, w_up, out=None, stream=None):
+    """[2][I][K] gate and up weights -> [2][2I][K] interleaved in 128-row blocks."""
+    _dev(w_gate, "w_gate", torch.bfloat16, 3)
+    _dev(w_up, "w_up", torch.bfloat16, 3)
+    _, I, K = w_gate.shape
+    if tuple(w_up.shape) != (2, I, K):
+        raise ValueError("w_up must match w_gate")
+    if out is None:
+        out = torch.empty((2, 2 * I, K), dtype=torch.bfloat16, device=w_gate.device)
+    _dev(out, "out", torch.bfloat16, 3)
+    _check("mot_swiglu_interleave", _lib().mot_swiglu_interleave(
+        w_gate.data_ptr(), w_up.data_ptr(), I, K, out.data_ptr(), _stream(w_gate, stream)))
+    return out
+
+
+def mot_rope_table_fill_host(theta: float, D: int, P: int) -> torch.Tensor:
+    """Host (cos, sin) table [P][D/2][2] as a CPU bf16 tensor (copy it to the device once)."""
+    t = torch.empty((P, D // 2, 2), dtype=torch.bfloat16)
+    _check("mot_rope_table_fill_host", _lib().mot_rope_table_fill_host(theta, D, P, t.data_ptr()))
+    return t
+
+
+def mot_device_status(ws, stream=None) -> int:
+    """Synchronizes the stream and returns the workspace's device error bits (0 = clean)."""
+    _dev(ws, "ws", torch.uint8, 1)
+    flags = ctypes.c_uint32(0)
+    _check("mot_device_status", _lib().mot_device_status(ws.data_ptr(), ctypes.byref(flags), _stream(ws, stream)))
+    return int(flags.value)

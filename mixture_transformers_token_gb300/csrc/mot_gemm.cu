@@ -1,0 +1,467 @@
+// Routed dense GEMM on the 5th-generation tensor cores, with three fused epilogues:
+//   cast          out = bf16(acc)                                  (O and down projections)
+//   SwiGLU        out = bf16(silu(bf16(acc_gate)) * bf16(acc_up))  (gate/up projection)
+//   QK-norm+RoPE  per-head fp32 RMSNorm, then BF16 RoPE           (fused QKV projection)
+//
+// Sources: [RFC][BAGEL-7B-MoT][CUDA/ROCm] WS1/WS2 kernel roadmap and integration plan #435
+// (§1 item 1: per-token weight sets; §2 Reference hazards: QK norm in FP32, then RoPE and Q/K
+// in BF16; §3 Numerical contract: fixed accumulation order, no split-K / stream-K / atomics,
+// casts only at declared boundaries); feat: support Bagel in SeedOmni - #1402 ("What does this
+// PR do?": routed Q/K/V and O projections, fused qkv_proj_{und,gen}, per-head QK RMSNorm,
+// packed RoPE); [WS1][CUDA][Qwen3-Next] MoE route/combine contract ... #503 (grouped expert
+// GEMM commit: one writer per row, grouped result equal to the per-expert GEMM; SwiGLU in
+// FP32 with one BF16 cast; gated-norm commit: accurate expf).
+//
+// Design (one CTA per SM, persistent):
+//   warp 0      TMA producer: W tiles (256 x 64) and A tiles (128 x 64) into a 4-stage ring.
+//               A rows come from the routing plan: one tiled load when the tile's rows are
+//               consecutive, else 32 four-row gathers (tile::gather4), one per lane.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and issues
+//               tcgen05.mma (M 128, N 256, K 16) from one thread, K blocks in ascending order.
+//   warps 2-5   epilogue: each thread owns one accumulator row (its TMEM lane), reads it with
+//               tcgen05.ld and writes the row's outputs to its original position.
+// Every tile of every pack uses the same tile shape, K order and instruction sequence, so a
+// row's bits depend only on the row and its expert's weights.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "mot.h"
+#include "mot_device.cuh"
+#include "mot_host.hpp"
+
+namespace mot {
+namespace gemm {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t ACC_COLS = BN;
+constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+
+enum Epi { EPI_CAST = 0, EPI_SWIGLU = 1, EPI_QKV64 = 2, EPI_QKV128 = 3 };
+
+struct Args {
+  const uint8_t* ws;  // routing plan
+  uint32_t* err;      // plan error word
+  int T, N, K;        // N weight rows per expert, K reduction length
+  int n_tiles;        // N / BN
+  uint16_t* out;
+  int ldo;
+  const uint16_t* bias;  // [2][N] or null (QKV only)
+  const uint16_t* qn;    // [2][D]
+  const uint16_t* kn;    // [2][D]
+  const int32_t* pos;    // [T]
+  const uint16_t* cs;    // [P][D/2][2]
+  int P;
+  int Hq, Hkv;
+  float eps;
+};
+
+__device__ __forceinline__ void store_row_u4(uint16_t* dst, const uint32_t* pk, int n_u4) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < n_u4; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
+// out = bf16(acc), 256 columns
+__device__ __forceinline__ void epi_cast(const Args& a, uint32_t taddr, bool valid, int grow, int nt) {
+  uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * BN;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32(taddr + c * 32, v);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
+    if (valid) store_row_u4(orow + c * 32, pk, 4);
+  }
+}
+
+// gate columns 0..127 and up columns 128..255 of the tile -> 128 outputs
+__device__ __forceinline__ void epi_swiglu(const Args& a, uint32_t taddr, bool valid, int grow, int nt) {
+  uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * (BN / 2);
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float g[32], u[32];
+    tmem_ld32(taddr + c * 32, g);
+    tmem_ld32(taddr + 128 + c * 32, u);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float h[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const float gb = bf_round(g[i + t]);
+        const float ub = bf_round(u[i + t]);
+        const float sg = __fdiv_rn(gb, __fadd_rn(1.0f, expf(-gb)));
+        h[t] = __fmul_rn(sg, ub);
+      }
+      pk[i / 2] = pack_bf2(h[0], h[1]);
+    }
+    if (valid) store_row_u4(orow + c * 32, pk, 4);
+  }
+}
+
+// Per-head QK RMSNorm (fp32, fixed chunk tree) and BF16 RoPE; V heads pass through.
+template <int D>
+__device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool valid, int grow, int e, int nt) {
+  constexpr int HEADS = BN / D;
+  constexpr int NP = D / 2;  // packed pairs per head
+  uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * BN;
+  int p = valid ? a.pos[grow] : 0;
+  if (p < 0 || p >= a.P) {
+    atomicOr(a.err, MOT_DEV_BAD_POSITION);
+    p = 0;
+  }
+  const uint16_t* csrow = a.cs + int64_t(p) * D;  // D/2 (cos, sin) pairs
+#pragma unroll 1
+  for (int hh = 0; hh < HEADS; ++hh) {
+    const int h = nt * HEADS + hh;
+    const int kind = h < a.Hq ? 0 : (h < a.Hq + a.Hkv ? 1 : 2);  // q, k, v
+    uint32_t qp[NP];
+    float csum[D / 32];
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      float v[32];
+      tmem_ld32(taddr + hh * D + c * 32, v);
+      if (a.bias != nullptr) {
+        const uint4* bp =
+            reinterpret_cast<const uint4*>(a.bias + int64_t(e) * a.N + int64_t(nt) * BN + hh * D + c * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 bb = __ldg(bp + q4);
+          const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[8 * q4 + 2 * k] = __fadd_rn(v[8 * q4 + 2 * k], bf_lo(bw[k]));
+            v[8 * q4 + 2 * k + 1] = __fadd_rn(v[8 * q4 + 2 * k + 1], bf_hi(bw[k]));
+          }
+        }
+      }
+      float part = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const uint32_t pk = pack_bf2(v[i], v[i + 1]);
+        qp[c * 16 + i / 2] = pk;
+        const float q0 = bf_lo(pk), q1 = bf_hi(pk);
+        part = __fadd_rn(part, __fmul_rn(q0, q0));
+        part = __fadd_rn(part, __fmul_rn(q1, q1));
+      }
+      csum[c] = part;
+    }
+    if (kind != 2) {
+      float ss = csum[0];
+#pragma unroll
+      for (int c = 1; c < D / 32; ++c) ss = __fadd_rn(ss, csum[c]);
+      const float ms = __fdiv_rn(ss, float(D));
+      const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+      const uint16_t* g = (kind == 0 ? a.qn : a.kn) + e * D;
+      // blocks of 8 rotation pairs (i, i + D/2)
+#pragma unroll
+      for (int m = 0; m < D / 16; ++m) {
+        const uint4 glo = __ldg(reinterpret_cast<const uint4*>(g + 8 * m));
+        const uint4 ghi = __ldg(reinterpret_cast<const uint4*>(g + NP + 8 * m));
+        const uint4 cs0 = __ldg(reinterpret_cast<const uint4*>(csrow + 16 * m));
+        const uint4 cs1 = __ldg(reinterpret_cast<const uint4*>(csrow + 16 * m + 8));
+        const uint32_t gl[4] = {glo.x, glo.y, glo.z, glo.w};
+        const uint32_t gh[4] = {ghi.x, ghi.y, ghi.z, ghi.w};
+        const uint32_t cw[8] = {cs0.x, cs0.y, cs0.z, cs0.w, cs1.x, cs1.y, cs1.z, cs1.w};  // (cos, sin) per pair
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t qa = qp[4 * m + k], qb = qp[NP / 2 + 4 * m + k];
+          float o1[2], o2[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const float xa = t ? bf_hi(qa) : bf_lo(qa);
+            const float xb = t ? bf_hi(qb) : bf_lo(qb);
+            const float ga = t ? bf_hi(gl[k]) : bf_lo(gl[k]);
+            const float gb = t ? bf_hi(gh[k]) : bf_lo(gh[k]);
+            const float c = bf_lo(cw[2 * k + t]), s = bf_hi(cw[2 * k + t]);
+            const float ua = bf_round(__fmul_rn(__fmul_rn(xa, rstd), ga));
+            const float ub = bf_round(__fmul_rn(__fmul_rn(xb, rstd), gb));
+            o1[t] = __fadd_rn(bf_round(__fmul_rn(ua, c)), bf_round(__fmul_rn(-ub, s)));
+            o2[t] = __fadd_rn(bf_round(__fmul_rn(ub, c)), bf_round(__fmul_rn(ua, s)));
+          }
+          qp[4 * m + k] = pack_bf2(o1[0], o1[1]);
+          qp[NP / 2 + 4 * m + k] = pack_bf2(o2[0], o2[1]);
+        }
+      }
+    }
+    if (valid) store_row_u4(orow + hh * D, qp, NP / 4);
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    routed_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_rows,
+                       const __grid_constant__ CUtensorMap tm_w, const Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* drain = bars + 2 * STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(args.ws);
+  const int num_m = hdr->num_m_tiles;
+  if (hdr->magic != kPlanMagic || hdr->T != args.T || num_m < 0 || num_m > max_m_tiles(args.T)) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.err, MOT_DEV_PLAN_MISMATCH);
+    return;
+  }
+  const int total = num_m * args.n_tiles;
+  if (int(blockIdx.x) >= total) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_a_rows);
+    tma_prefetch_desc(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const Tile* tiles = reinterpret_cast<const Tile*>(args.ws + tiles_offset(args.T));
+  const int32_t* perm = reinterpret_cast<const int32_t*>(args.ws + perm_offset());
+  const int kblocks = args.K / BK;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_parity = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const int mt = t % num_m, nt = t / num_m;
+      const Tile tl = tiles[mt];
+      const int wrow = tl.expert * args.N + nt * BN;
+      const bool gather = tl.row0 < 0;
+      int r[4] = {0, 0, 0, 0};
+      if (gather) {
+        const int last = tl.n_rows - 1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) r[j] = perm[tl.list_begin + min(4 * lane + j, last)];
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err));
+        if (!ok) break;
+        const uint32_t fb = smem_u32(&full[stage]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          tma_load_2d(smem_u32(sb + stage * B_BYTES), &tm_w, kb * BK, wrow, fb);
+          if (!gather) tma_load_2d(smem_u32(sa + stage * A_BYTES), &tm_a, kb * BK, tl.row0, fb);
+        }
+        __syncwarp();
+        if (gather) tma_gather4(smem_u32(sa + stage * A_BYTES + lane * 512), &tm_a_rows, kb * BK, r[0], r[1], r[2],
+                                r[3], fb);
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (ok) {
+      // wait until the MMA warp has released every stage, so no arrival is still in flight
+      for (int i = 0; i < STAGES; ++i) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err))) break;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // every load issued has landed before the CTA may exit
+    for (int s = 0; s < STAGES; ++s)
+      if ((issued >> s) & 1u) mbar_drain(smem_u32(&full[s]), (issued_parity >> s) & 1u);
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = tmem_base + acc * ACC_COLS;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(d, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+          mma_commit(smem_u32(&empty[stage]));
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(smem_u32(&tfull[acc]));
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    // every MMA issued has completed before tensor memory is released
+    if (lane == 0) mma_commit(smem_u32(drain));
+    __syncwarp();
+    mbar_drain(smem_u32(drain), 0);
+  } else {
+    // ---------------- epilogue ----------------
+    const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const int mt = t % num_m, nt = t / num_m;
+      const Tile tl = tiles[mt];
+      const bool valid = row_in_tile < tl.n_rows;
+      const int grow = valid ? perm[tl.list_begin + row_in_tile] : 0;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err))) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16);
+      if constexpr (EPI == EPI_CAST) epi_cast(args, taddr, valid, grow, nt);
+      if constexpr (EPI == EPI_SWIGLU) epi_swiglu(args, taddr, valid, grow, nt);
+      if constexpr (EPI == EPI_QKV64) epi_qkv<64>(args, taddr, valid, grow, tl.expert, nt);
+      if constexpr (EPI == EPI_QKV128) epi_qkv<128>(args, taddr, valid, grow, tl.expert, nt);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI>
+static int launch(const void* a, const void* w, int T, int N, int K, const Args& args, int dev, cudaStream_t s) {
+  CUtensorMap tm_a, tm_rows, tm_w;
+  if (!make_tmap_bf16(&tm_a, a, uint64_t(K), uint64_t(T), BK, BM) ||
+      !make_tmap_bf16(&tm_rows, a, uint64_t(K), uint64_t(T), BK, 1) ||
+      !make_tmap_bf16(&tm_w, w, uint64_t(K), uint64_t(2) * N, BK, BN))
+    return MOT_ERR_CUDA;
+  if (cudaFuncSetAttribute(routed_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES)) !=
+      cudaSuccess)
+    return MOT_ERR_CUDA;
+  const int64_t tiles_max = max_m_tiles(T) * int64_t(N / BN);
+  const int grid = int(tiles_max < sm_count(dev) ? tiles_max : sm_count(dev));
+  routed_gemm_kernel<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(tm_a, tm_rows, tm_w, args);
+  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+}
+
+}  // namespace gemm
+}  // namespace mot
+
+using namespace mot;
+
+extern "C" int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv, const mot_bf16* b_qkv,
+                                        const mot_bf16* q_norm_w, const mot_bf16* k_norm_w, const int32_t* pos,
+                                        const mot_bf16* rope_cs, int P, int64_t T, int H, int Hq, int Hkv, int D,
+                                        float eps, void* ws, size_t ws_bytes, mot_bf16* qkv_out, void* stream) {
+  if (!x || !w_qkv || !q_norm_w || !k_norm_w || !pos || !rope_cs || !ws || !qkv_out) return MOT_ERR_NULL;
+  if (T < 1 || T > MOT_MAX_TOKENS) return MOT_ERR_GEOMETRY;
+  if (D != 64 && D != 128) return MOT_ERR_GEOMETRY;
+  if (Hq < 1 || Hkv < 1 || Hq > 1024 || Hkv > 1024) return MOT_ERR_GEOMETRY;
+  const int64_t N = int64_t(Hq + 2 * Hkv) * D;
+  if (N % gemm::BN != 0 || N > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (H < gemm::BK || H % gemm::BK != 0 || H > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (P < 1 || P > MOT_MAX_TOKENS) return MOT_ERR_ARG;
+  if (!(eps > 0.0f) || !(eps < 3.0e38f)) return MOT_ERR_ARG;
+  if (!aligned16(x) || !aligned16(w_qkv) || (b_qkv && !aligned16(b_qkv)) || !aligned16(q_norm_w) ||
+      !aligned16(k_norm_w) || !aligned16(pos) || !aligned16(rope_cs) || !aligned16(ws) || !aligned16(qkv_out))
+    return MOT_ERR_ALIGN;
+  if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {x, w_qkv, b_qkv, q_norm_w, k_norm_w, pos, rope_cs, ws, qkv_out};
+  int dev = -1;
+  int st = check_device(s, ptrs, 9, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  gemm::Args a{};
+  a.ws = static_cast<const uint8_t*>(ws);
+  a.err = &static_cast<PlanHeader*>(ws)->error;
+  a.T = int(T);
+  a.N = int(N);
+  a.K = H;
+  a.n_tiles = int(N / gemm::BN);
+  a.out = qkv_out;
+  a.ldo = int(N);
+  a.bias = b_qkv;
+  a.qn = q_norm_w;
+  a.kn = k_norm_w;
+  a.pos = pos;
+  a.cs = rope_cs;
+  a.P = P;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.eps = eps;
+  if (D == 64) return gemm::launch<gemm::EPI_QKV64>(x, w_qkv, int(T), int(N), H, a, dev, s);
+  return gemm::launch<gemm::EPI_QKV128>(x, w_qkv, int(T), int(N), H, a, dev, s);
+}
+
+extern "C" int mot_routed_gemm(const mot_bf16* a_in, const mot_bf16* w, int64_t T, int N, int K, int epilogue,
+                               void* ws, size_t ws_bytes, mot_bf16* out, void* stream) {
+  if (!a_in || !w || !ws || !out) return MOT_ERR_NULL;
+  if (epilogue != MOT_EPI_CAST && epilogue != MOT_EPI_SWIGLU) return MOT_ERR_ARG;
+  if (T < 1 || T > MOT_MAX_TOKENS) return MOT_ERR_GEOMETRY;
+  if (N < gemm::BN || N % gemm::BN != 0 || N > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (K < gemm::BK || K % gemm::BK != 0 || K > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (!aligned16(a_in) || !aligned16(w) || !aligned16(ws) || !aligned16(out)) return MOT_ERR_ALIGN;
+  if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {a_in, w, ws, out};
+  int dev = -1;
+  int st = check_device(s, ptrs, 4, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  gemm::Args a{};
+  a.ws = static_cast<const uint8_t*>(ws);
+  a.err = &static_cast<PlanHeader*>(ws)->error;
+  a.T = int(T);
+  a.N = N;
+  a.K = K;
+  a.n_tiles = N / gemm::BN;
+  a.out = out;
+  a.ldo = epilogue == MOT_EPI_SWIGLU ? N / 2 : N;
+  if (epilogue == MOT_EPI_SWIGLU) return gemm::launch<gemm::EPI_SWIGLU>(a_in, w, int(T), N, K, a, dev, s);
+  return gemm::launch<gemm::EPI_CAST>(a_in, w, int(T), N, K, a, dev, s);
+}

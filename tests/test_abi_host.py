@@ -1,0 +1,163 @@
+"""Host-side tests of the C-ABI library (no GPU needed).
+
+The library must load on a machine without a GPU, export every entry point that
+include/mot.h declares, and reject invalid arguments before touching CUDA. The host-side
+RoPE table builder is compared with the oracle's table bit for bit.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_transformers_token_gb300 as mot
+from mixture_transformers_token_gb300 import build as mot_build
+from oracle import mot_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mot.h")
+
+MOT_OK, MOT_ERR_NULL, MOT_ERR_ALIGN, MOT_ERR_GEOMETRY = 0, 1, 2, 3
+MOT_ERR_DEVICE, MOT_ERR_WORKSPACE, MOT_ERR_ARCH, MOT_ERR_CUDA, MOT_ERR_ARG = 4, 5, 6, 7, 8
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mot_build.build()
+    return mot.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mot_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("mot_fused_add_rmsnorm", "mot_routed_qkv_norm_rope", "mot_routed_gemm", "mot_route_plan",
+                     "mot_workspace_bytes", "mot_abi_version", "mot_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.mot_abi_version() == mot.ABI_VERSION
+    seen = set()
+    for code in range(0, 9):
+        s = lib.mot_status_string(code).decode()
+        assert s and s not in seen
+        seen.add(s)
+    assert lib.mot_status_string(1234).decode() == "unknown status"
+
+
+def test_workspace_bytes(lib):
+    assert lib.mot_workspace_bytes(0) == 0
+    assert lib.mot_workspace_bytes(-5) == 0
+    assert lib.mot_workspace_bytes((1 << 24) + 1) == 0
+    prev = 0
+    for T in (1, 2, 127, 128, 129, 4096, 36864):
+        b = lib.mot_workspace_bytes(T)
+        # header + one int32 per row + one 16-byte tile record per 128 rows (+1)
+        assert b >= 64 + 4 * T + 16 * ((T + 127) // 128 + 1)
+        assert b % 16 == 0 and b >= prev
+        prev = b
+
+
+# fake, 16-byte aligned, non-NULL addresses: every check below fails before any CUDA call
+A = 1 << 20
+B = 2 << 20
+C = 3 << 20
+MIS = (4 << 20) + 8
+
+
+def test_route_plan_rejects(lib):
+    assert lib.mot_route_plan(None, 10, A, 1 << 20, None) == MOT_ERR_NULL
+    assert lib.mot_route_plan(A, 0, B, 1 << 20, None) == MOT_ERR_GEOMETRY
+    assert lib.mot_route_plan(A, (1 << 24) + 1, B, 1 << 30, None) == MOT_ERR_GEOMETRY
+    assert lib.mot_route_plan(A, 10, MIS, 1 << 20, None) == MOT_ERR_ALIGN
+    assert lib.mot_route_plan(A, 1000, B, 100, None) == MOT_ERR_WORKSPACE
+
+
+def test_add_rmsnorm_rejects(lib):
+    f = lib.mot_fused_add_rmsnorm
+    assert f(None, A, A, A, 4, 256, 1e-6, B, C, None, None) == MOT_ERR_NULL
+    assert f(A, A, A, A, 4, 255, 1e-6, B, C, None, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, A, 4, 128, 1e-6, B, C, None, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, A, 4, 8448, 1e-6, B, C, None, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, A, 0, 256, 1e-6, B, C, None, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, A, 4, 256, 0.0, B, C, None, None) == MOT_ERR_ARG
+    assert f(A, A, A, A, 4, 256, float("nan"), B, C, None, None) == MOT_ERR_ARG
+    assert f(MIS, A, A, A, 4, 256, 1e-6, B, C, None, None) == MOT_ERR_ALIGN
+    assert f(A, A, A, A, 4, 256, 1e-6, B, MIS, None, None) == MOT_ERR_ALIGN
+
+
+def test_qkv_rejects(lib):
+    f = lib.mot_routed_qkv_norm_rope
+
+    def call(**kw):
+        a = dict(x=A, w=A, b=None, qn=A, kn=A, pos=A, cs=A, P=64, T=64, H=256, Hq=4, Hkv=2, D=64, eps=1e-6, ws=B,
+                 wsb=1 << 20, out=C)
+        a.update(kw)
+        return f(a["x"], a["w"], a["b"], a["qn"], a["kn"], a["pos"], a["cs"], a["P"], a["T"], a["H"], a["Hq"],
+                 a["Hkv"], a["D"], a["eps"], a["ws"], a["wsb"], a["out"], None)
+
+    assert call(x=None) == MOT_ERR_NULL
+    assert call(ws=None) == MOT_ERR_NULL
+    assert call(D=96) == MOT_ERR_GEOMETRY
+    assert call(Hq=3, Hkv=1, D=64) == MOT_ERR_GEOMETRY          # N = 320 is not a multiple of 256
+    assert call(H=200) == MOT_ERR_GEOMETRY
+    assert call(T=0) == MOT_ERR_GEOMETRY
+    assert call(P=0) == MOT_ERR_ARG
+    assert call(eps=-1.0) == MOT_ERR_ARG
+    assert call(b=MIS) == MOT_ERR_ALIGN
+    assert call(out=MIS) == MOT_ERR_ALIGN
+    assert call(wsb=100) == MOT_ERR_WORKSPACE
+
+
+def test_routed_gemm_rejects(lib):
+    f = lib.mot_routed_gemm
+    assert f(None, A, 8, 256, 64, 0, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert f(A, A, 8, 256, 64, 7, B, 1 << 20, C, None) == MOT_ERR_ARG
+    assert f(A, A, 8, 320, 64, 0, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, 8, 256, 96, 0, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, 0, 256, 64, 0, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, MIS, 8, 256, 64, 0, B, 1 << 20, C, None) == MOT_ERR_ALIGN
+    assert f(A, A, 8, 256, 64, 0, B, 10, C, None) == MOT_ERR_WORKSPACE
+
+
+def test_interleave_and_status_reject(lib):
+    assert lib.mot_swiglu_interleave(A, A, 100, 64, B, None) == MOT_ERR_GEOMETRY
+    assert lib.mot_swiglu_interleave(None, A, 128, 64, B, None) == MOT_ERR_NULL
+    flags = ctypes.c_uint32(0)
+    assert lib.mot_device_status(None, ctypes.byref(flags), None) == MOT_ERR_NULL
+    assert lib.mot_device_status(MIS, ctypes.byref(flags), None) == MOT_ERR_ALIGN
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_valid_arguments_without_gpu_fail_closed(lib):
+    st = lib.mot_route_plan(A, 10, B, 1 << 20, None)
+    assert st in (MOT_ERR_CUDA, MOT_ERR_DEVICE)
+
+
+@pytest.mark.parametrize("D,P,theta", [(64, 64, 1e6), (128, 4096, 1e6), (128, 300, 1e4)])
+def test_rope_table_matches_oracle(D, P, theta):
+    t = mot.mot_rope_table_fill_host(theta, D, P)
+    c, s = O.rope_cos_sin(theta, D, np.arange(P))
+    got = t.float().numpy().astype(np.float64)
+    np.testing.assert_array_equal(got[:, :, 0], c)
+    np.testing.assert_array_equal(got[:, :, 1], s)
+
+
+def test_rope_table_rejects(lib):
+    buf = (ctypes.c_uint16 * 16)()
+    assert lib.mot_rope_table_fill_host(1e6, 3, 2, buf) == MOT_ERR_GEOMETRY
+    assert lib.mot_rope_table_fill_host(0.5, 4, 2, buf) == MOT_ERR_ARG
+    assert lib.mot_rope_table_fill_host(1e6, 4, 2, None) == MOT_ERR_NULL
