@@ -6,7 +6,7 @@ the fused residual-add RMSNorm and the routed QKV GEMM with its per-head QK RMSN
 RoPE epilogue. The workload is the BAGEL-shaped layer: T = 4096 packed bf16 tokens, hidden
 3584, Q 28 x 128, KV 4 x 128 (QKV out 4608), und/gen weight sets W ~ N(0, 0.02), the first 3072
 tokens und then a contiguous 1024-token gen block, positions 0..4095, eps 1e-6, theta 1e6.
-Inputs are synthetic and seeded (one pack per rank); L2 is flushed (a write of twice its
+Inputs are synthetic and seeded (one pack per rank); L2 is flushed (a write and a read of twice its
 size) before every timed step, outside the timed events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -40,7 +40,7 @@ NORM_BYTES = 8 * T * H + 4 * H + T                # read x, res; write y, res_ou
 
 # DRAM traffic of one QKV kernel launch from an ncu capture of this workload, keyed by the
 # hash of the kernel source it was taken on (null once the kernel has changed).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {"6369649da1fa59d7": 115413248}   # profiles/routed_gemm_qkv128_bagel_layer_T4096.md
 
 
 def src_hash(name: str) -> str:
@@ -105,7 +105,7 @@ class ClockSampler:
         sm = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
         smax = [float(r[3]) for r in inside if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in inside for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": reasons, "samples": len(inside),
                 "power_w_max": max((float(r[4]) for r in inside if r[4].replace(".", "").isdigit()), default=None)}
@@ -149,14 +149,20 @@ def run_ours(args, rank, world, local_rank):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * max(l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
 
+    def flush_l2(i):
+        # write twice L2 (evicts everything, our outputs' dirty lines are written back here),
+        # then read it back so the timed step starts with only clean lines in L2
+        flush.fill_(i)
+        flush.sum()
+
     def step(x, res):
         mot.mot_route_plan(d["mod"], ws)
         mot.mot_fused_add_rmsnorm(x, res, d["w_norm"], d["mod"], shape.eps, y=y, res_out=ro, ws=ws)
         mot.mot_routed_qkv_norm_rope(y, d["w_qkv"], d["q_norm"], d["k_norm"], d["pos"], cs, HQ, HKV, D, shape.eps,
                                      ws, out=out)
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
+    for i in range(args.warmup):
+        flush_l2(i)
         step(d["x"], d["res"])
     torch.cuda.synchronize()
     if mot.mot_device_status(ws) != 0:
@@ -173,7 +179,7 @@ def run_ours(args, rank, world, local_rank):
         sampler.mark("start")
     t_wall = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i)
+        flush_l2(i)
         e = ev[i]
         e[0].record(stream)
         mot.mot_route_plan(d["mod"], ws)
@@ -230,7 +236,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; random-init weights of the BAGEL layer shape)",
         "config": {"workload": WORKLOAD, "T": T, "hidden": H, "q_heads": HQ, "kv_heads": HKV, "head_dim": D,
                    "und_rows": 3072, "gen_rows": 1024, "step": "route plan + fused add-RMSNorm + routed QKV/QK-norm/RoPE",
-                   "l2": "flushed before every timed step (write of 2x L2, outside the timed events)",
+                   "l2": "flushed before every timed step (write then read of 2x L2, outside the timed events)",
                    "parallelism": f"replicas x{world} (one pack per GPU, no collective)"},
         "roofline": {"kernel": "routed_gemm_kernel<QKV128>", "bound": "tensor", "achieved": round(qkv_tflops, 2),
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(qkv_tflops / pk["bf16_tflops"], 4),
@@ -384,7 +390,7 @@ def run_reference(args, rank, world) -> dict | None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-baseline", dest="cpu_baseline", action="store_true", default=True)

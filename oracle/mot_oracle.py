@@ -196,31 +196,26 @@ def g_rope_exact(u, pos, theta: float, D: int):
     return np.concatenate([u1 * c - u2 * s, u2 * c + u1 * s], axis=-1)
 
 
-def g_qkv_norm_rope(y, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta):
-    """Routed QKV projection, per-head QK RMSNorm in fp32, RoPE and Q/K in BF16.
+def g_qk_norm_rope(q, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta):
+    """Per-head QK RMSNorm and BF16 RoPE on the bf16 GEMM output q (fp64 statistics).
 
-    [PR-1402] "What does this PR do?": MoT dual-branch routed Q/K/V projections with
-    fused qkv_proj_{und,gen} weights, per-head QK RMSNorm and packed RoPE;
-    [RFC-435] §2 Reference hazards: QK norm in FP32, then RoPE and Q/K in BF16.
-      acc  = routed(y, w_qkv) (+ b_qkv[mod] if given)       columns ordered q, k, v heads
-      q    = bf16(acc)                                      (GEMM output boundary)
+    [RFC-435] §2 Reference hazards: QK norm in FP32 (here fp64), then RoPE and Q/K in BF16.
       Q, K heads:  u = bf16(q * rstd_head * g[mod]),  rstd_head = 1/sqrt(sum q^2 / D + eps)
                    out = RoPE_bf16(u, cos, sin of pos)
       V heads:     out = q
-    The per-head norm weight g is q_norm or k_norm, [2][D], one vector per expert shared
-    by all heads of that kind. Returns out, out_pre (value before the final cast), q, acc.
+    The per-head norm weight g is q_norm or k_norm, [2][D], one vector per expert shared by
+    all heads of that kind. Returns out, out_pre (value before the final cast) and u, the
+    normalized heads [T][Hq+Hkv][D].
     """
     mod = _check_mod(mod)
     eps = _eps32(eps)
-    acc = g_routed_matmul(y, w_qkv, mod)
-    if b_qkv is not None:
-        acc = acc + np.asarray(b_qkv, np.float64)[mod]
-    q = bf16(acc)
+    q = np.asarray(q, np.float64)
     out = q.copy()
-    out_pre = acc.copy()
+    out_pre = q.copy()
     c, s = rope_cos_sin(theta, D, pos)
     q_norm = np.asarray(q_norm, np.float64)
     k_norm = np.asarray(k_norm, np.float64)
+    us = np.zeros((q.shape[0], Hq + Hkv, D))
     for h in range(Hq + Hkv):
         g = q_norm if h < Hq else k_norm
         cols = slice(h * D, (h + 1) * D)
@@ -231,7 +226,31 @@ def g_qkv_norm_rope(y, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, 
         o, pre = g_rope_bf16(u, c, s)
         out[:, cols] = o
         out_pre[:, cols] = pre
-    return {"out": out, "out_pre": out_pre, "q": q, "acc": acc}
+        us[:, h] = u
+    return {"out": out, "out_pre": out_pre, "u": us}
+
+
+def g_qkv_norm_rope(y, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta):
+    """Routed QKV projection, per-head QK RMSNorm in fp32, RoPE and Q/K in BF16.
+
+    [PR-1402] "What does this PR do?": MoT dual-branch routed Q/K/V projections with
+    fused qkv_proj_{und,gen} weights, per-head QK RMSNorm and packed RoPE.
+      acc  = routed(y, w_qkv) (+ b_qkv[mod] if given)       columns ordered q, k, v heads
+      q    = bf16(acc)                                      (GEMM output boundary)
+      out  = g_qk_norm_rope(q)
+    For V columns the value before the final cast is acc itself. Returns out, out_pre, q,
+    acc and u (the normalized Q/K heads).
+    """
+    mod = _check_mod(mod)
+    acc = g_routed_matmul(y, w_qkv, mod)
+    if b_qkv is not None:
+        acc = acc + np.asarray(b_qkv, np.float64)[mod]
+    q = bf16(acc)
+    r = g_qk_norm_rope(q, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta)
+    out_pre = r["out_pre"]
+    v0 = (Hq + Hkv) * D
+    out_pre[:, v0:] = acc[:, v0:]
+    return {"out": r["out"], "out_pre": out_pre, "q": q, "acc": acc, "u": r["u"]}
 
 
 def g_swiglu(acc_gate, acc_up):
@@ -349,6 +368,7 @@ def e_qk_norm_rope(q, q_norm, k_norm, cos, sin, mod, Hq, Hkv, D, eps, return_sta
     gk = np.asarray(k_norm, np.float64).astype(F32)
     out = q32.copy()
     stats = []
+    us = np.zeros((q32.shape[0], Hq + Hkv, D), F32)
     for h in range(Hq + Hkv):
         g = gq if h < Hq else gk
         cols = slice(h * D, (h + 1) * D)
@@ -357,8 +377,9 @@ def e_qk_norm_rope(q, q_norm, k_norm, cos, sin, mod, Hq, Hkv, D, eps, return_sta
         u = bf16_f32((qh * rstd[:, None]) * g[mod])
         out[:, cols] = e_rope_bf16(u, c32, s32)
         stats.append(ss)
+        us[:, h] = u
     if return_stats:
-        return out, np.stack(stats, axis=1)
+        return out, np.stack(stats, axis=1), us
     return out
 
 

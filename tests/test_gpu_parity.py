@@ -179,7 +179,7 @@ def test_swiglu_interleave_layout():
     assert_bitwise(gu, want, "interleaved gate/up layout")
 
 
-@pytest.mark.parametrize("T,K,I,n_gen,seed", [(500, 512, 256, 125, 1), (1, 256, 128, 1, 2), (2048, 1024, 512, 512, 3)])
+@pytest.mark.parametrize("T,K,I,n_gen,seed", [(500, 512, 256, 125, 1), (1, 256, 256, 1, 2), (2048, 1024, 512, 512, 3)])
 def test_routed_swiglu(T, K, I, n_gen, seed):
     a = W.bf16_normal(W.rng_for(seed, 71), (T, K))
     wg = W.bf16_normal(W.rng_for(seed, 72), (2, I, K), std=0.02)
@@ -216,22 +216,82 @@ def _qkv_run(shape, inp, with_bias=False):
     return out, ws, dev
 
 
+def _bf16_step(v):
+    """Spacing of bf16 numbers at |v| (2^-133 below the normal range)."""
+    _, ex = np.frexp(np.maximum(np.abs(v), 2.0 ** -126))
+    return np.ldexp(1.0, ex - 8)
+
+
+def _check_end_to_end(out, g, q_gpu, u_e, acc_abs, shape, what):
+    """End to end against the fp64 golden chain.
+
+    The relative-L2 bound holds for the whole output. An element may exceed 2e-2 only when a
+    legitimate one-step difference at a declared bf16 cast explains it: the GEMM's fp32
+    accumulation rounding q to the other bf16 neighbour of the exact value (anywhere in the
+    element's head, which moves rstd), the fp32 statistics rounding u the other way at the
+    element or its rotation partner, or the final cast alone (|out| >= 8). Every q itself must
+    lie within half a bf16 step plus the fp32 accumulation error bound 2 K 2^-24 sum|a||w|
+    (acc_abs) of the exact accumulation.
+    """
+    D, nqk = shape.D, shape.Hq + shape.Hkv
+    ref = g["out_pre"]
+    d = np.abs(out - ref)
+    rel = float(np.linalg.norm(out - ref) / np.linalg.norm(ref))
+    assert rel <= 4e-3, f"{what}: rel-L2 {rel:.3e}"
+    K = shape.H
+    gemm_err = np.abs(q_gpu - g["acc"])
+    allowed = 0.5 * _bf16_step(q_gpu) + 2.0 * K * 2.0 ** -24 * acc_abs
+    assert np.all(gemm_err <= allowed), f"{what}: GEMM output outside half a step plus the accumulation bound"
+    flips = q_gpu != g["q"]
+    bad = np.argwhere(d > 2e-2)
+    unexplained = []
+    for r, c in bad:
+        h, i = divmod(int(c), D)
+        j = (i + D // 2) % D
+        final_cast = d[r, c] <= 0.5 * _bf16_step(out[r, c]) * (1 + 1e-9)
+        q_flip = bool(np.any(flips[r, h * D:(h + 1) * D]))
+        u_flip = h < nqk and (u_e[r, h, i] != g["u"][r, h, i] or u_e[r, h, j] != g["u"][r, h, j])
+        if not (final_cast or q_flip or u_flip):
+            unexplained.append((int(r), int(c), float(out[r, c]), float(ref[r, c])))
+    assert not unexplained, f"{what}: unexplained |diff| > 2e-2 at {unexplained[:10]}"
+    # scale-aware sanity bound on Q/K columns: a few bf16 steps of the rotated pair (u_i, u_j)
+    cols = np.arange(nqk * D)
+    hh, ii = cols // D, cols % D
+    jj = (ii + D // 2) % D
+    scale = np.maximum(np.abs(g["u"][:, hh, ii]), np.abs(g["u"][:, hh, jj]))
+    assert np.all(d[:, : nqk * D] <= 3 * _bf16_step(scale) + _bf16_step(ref[:, : nqk * D])), \
+        f"{what}: error beyond 3 bf16 steps of the rotated pair"
+    print(f"{what}: max|diff| {d.max():.3e}, rel-L2 {rel:.2e}, {len(bad)} of {d.size} elements beyond 2e-2, "
+          f"each explained by a one-step flip at a bf16 cast; q flips at the GEMM cast: {int(flips.sum())}")
+
+
 def _check_qkv(shape, inp, out, ws, dev, rows=None, with_bias=False):
     assert mot.mot_device_status(ws) == 0
     mod = inp["mod"].numpy()
     pos = inp["pos"].numpy()
-    if not with_bias:
-        # fused == unfused: the epilogue restated by E on the GPU's own cast GEMM output
-        q = mot.mot_routed_gemm(dev["x"], dev["w_qkv"], ws, mot.EPI_CAST)
-        c, s = O.rope_cos_sin(shape.theta, shape.D, pos)
-        e_out = O.e_qk_norm_rope(f64(q), f64(inp["q_norm"]), f64(inp["k_norm"]), c, s, mod, shape.Hq, shape.Hkv,
-                                 shape.D, shape.eps)
-        assert_bitwise(out, np_bits(e_out), "fused QKV vs E on the cast GEMM output")
     r = np.arange(shape.T) if rows is None else rows
     g = O.g_qkv_norm_rope(f64(inp["x"])[r], f64(inp["w_qkv"]), f64(inp["b_qkv"]) if with_bias else None,
                           f64(inp["q_norm"]), f64(inp["k_norm"]), pos[r], mod[r], shape.Hq, shape.Hkv, shape.D,
                           shape.eps, shape.theta)
-    assert_tolerance(f64(out)[r], g["out_pre"], "QKV vs G")
+    outv = f64(out)[r]
+    if with_bias:
+        # no unfused bias path to teacher-force from: bounded end-to-end check
+        maxd = np.abs(outv - g["out_pre"])
+        assert np.all(maxd <= 3 * _bf16_step(np.maximum(np.abs(outv), np.abs(g["out_pre"]))))
+        assert float(np.linalg.norm(outv - g["out_pre"]) / np.linalg.norm(g["out_pre"])) <= 4e-3
+        return
+    # stage 1: the routed GEMM's bf16 output against the exact accumulation
+    q = mot.mot_routed_gemm(dev["x"], dev["w_qkv"], ws, mot.EPI_CAST)
+    qv = f64(q)
+    assert_tolerance(qv[r], g["acc"], "routed QKV GEMM (bf16 cast) vs G")
+    # stage 2: the fused epilogue equals the fp32 contract emulator on the GPU's own q, bit for bit
+    c, s = O.rope_cos_sin(shape.theta, shape.D, pos)
+    e_out, _, u_e = O.e_qk_norm_rope(qv, f64(inp["q_norm"]), f64(inp["k_norm"]), c, s, mod, shape.Hq, shape.Hkv,
+                                     shape.D, shape.eps, return_stats=True)
+    assert_bitwise(out, np_bits(e_out), "fused QKV vs E on the cast GEMM output")
+    # end to end against the golden chain
+    acc_abs = O.g_routed_matmul(np.abs(f64(inp["x"])[r]), np.abs(f64(inp["w_qkv"])), mod[r])
+    _check_end_to_end(outv, g, qv[r], u_e[r].astype(np.float64), acc_abs, shape, "QKV vs G")
 
 
 def test_qkv_tiny_layer():

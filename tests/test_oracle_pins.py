@@ -281,8 +281,8 @@ def test_qk_head_tree_order_hand_value():
     q[0, 64] = 1.0
     q[0, 96:98] = 1.0
     cs = np.ones((1, D // 2)), np.zeros((1, D // 2))
-    _, ss = O.e_qk_norm_rope(q, np.ones((2, D)), np.ones((2, D)), cs[0], cs[1], [0], 1, 1, D, 1e-6,
-                             return_stats=True)
+    _, ss, _ = O.e_qk_norm_rope(q, np.ones((2, D)), np.ones((2, D)), cs[0], cs[1], [0], 1, 1, D, 1e-6,
+                                return_stats=True)
     assert ss[0, 0] == gd["sum_of_squares"]
 
 
