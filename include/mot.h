@@ -54,6 +54,7 @@ extern "C" {
 #define MOT_ERR_ARCH      6  /* the stream's device is not compute capability 10.3 */
 #define MOT_ERR_CUDA      7  /* a CUDA runtime call or a launch failed */
 #define MOT_ERR_ARG       8  /* any other invalid argument (epilogue id, eps, P ...) */
+#define MOT_ERR_NOALLOC_LIMIT 9  /* T above MOT_NOALLOC_MAX_TOKENS (mot_routed_gemm_noalloc) */
 
 /* device-detected error bits, OR-ed into the workspace error word */
 #define MOT_DEV_BAD_MODALITY  0x1u  /* a modality index other than 0 or 1 */
@@ -67,6 +68,9 @@ extern "C" {
 
 /* largest packed batch the library accepts */
 #define MOT_MAX_TOKENS (1 << 24)
+
+/* largest packed batch of mot_routed_gemm_noalloc (its plan lives in a fixed device array) */
+#define MOT_NOALLOC_MAX_TOKENS 65536
 
 typedef uint16_t mot_bf16; /* raw bfloat16 bit pattern */
 
@@ -159,6 +163,29 @@ int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv, const mot
  */
 int mot_routed_gemm(const mot_bf16* a, const mot_bf16* w, int64_t T, int N, int K, int epilogue,
                     void* ws, size_t ws_bytes, mot_bf16* out, void* stream);
+
+/*
+ * mot_routed_gemm_noalloc -- mot_routed_gemm for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a deployment variant of the entry point above.
+ * Engines that reserve all device memory once at start-up, and plug-ins whose host framework
+ * owns the device memory and offers them no allocator, cannot provide the workspace that
+ * mot_routed_gemm needs. This call takes the modality index itself and keeps the routing plan
+ * in a fixed array of the library's own device memory (about 264 KB, held by every GPU that
+ * loads the library until the process exits), then runs the same routed GEMM. It calls no
+ * allocator of any kind.
+ *   a, w, epilogue, out   as for mot_routed_gemm (the same results, bit for bit).
+ *   mod                   [T] uint8 device array: 0 = und, 1 = gen.
+ *   device_flags          optional device uint32: receives the call's MOT_DEV_* bits once the
+ *                         call's work has run on `stream` (NULL: not reported).
+ * Limits: 1 <= T <= MOT_NOALLOC_MAX_TOKENS, else MOT_ERR_NOALLOC_LIMIT (above) or
+ * MOT_ERR_GEOMETRY (below); other geometry as for mot_routed_gemm.
+ * The first call on a device looks up the array's device address (once per device, under a
+ * lock); make that first call before any stream capture. All calls on a device share the one
+ * array: calls whose work can overlap on the GPU (different streams or host threads) race
+ * and must be ordered by the caller.
+ */
+int mot_routed_gemm_noalloc(const mot_bf16* a, const mot_bf16* w, const uint8_t* mod, int64_t T, int N, int K,
+                            int epilogue, mot_bf16* out, uint32_t* device_flags, void* stream);
 
 /*
  * mot_swiglu_interleave -- one-time layout step for the gate/up weights.

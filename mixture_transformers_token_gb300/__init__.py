@@ -22,7 +22,8 @@ __all__ = [
     "DEV_BAD_MODALITY", "DEV_TIMEOUT", "DEV_PLAN_MISMATCH", "DEV_BAD_POSITION",
     "mot_abi_version", "mot_status_string", "mot_workspace_bytes", "mot_route_plan",
     "mot_fused_add_rmsnorm", "mot_routed_qkv_norm_rope", "mot_routed_gemm",
-    "mot_swiglu_interleave", "mot_rope_table_fill_host", "mot_device_status",
+    "mot_swiglu_interleave", "mot_rope_table_fill_host", "mot_device_status", "mot_routed_gemm_noalloc",
+    "NOALLOC_MAX_TOKENS",
 ]
 
 ABI_VERSION = 1
@@ -32,6 +33,7 @@ DEV_BAD_MODALITY = 0x1
 DEV_TIMEOUT = 0x2
 DEV_PLAN_MISMATCH = 0x4
 DEV_BAD_POSITION = 0x8
+NOALLOC_MAX_TOKENS = 65536
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -51,6 +53,7 @@ _SIGNATURES = {
     "mot_routed_qkv_norm_rope": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i64, _c_i, _c_i, _c_i,
                                         _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_routed_gemm_noalloc": (_c_i, [_c_p, _c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_p, _c_p]),
     "mot_swiglu_interleave": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_p]),
     "mot_rope_table_fill_host": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
@@ -215,6 +218,29 @@ def mot_routed_gemm(a, w, ws, epilogue: int = EPI_CAST, out=None, stream=None):
         raise ValueError(f"out must be [{T}, {ncols}]")
     _check("mot_routed_gemm", _lib().mot_routed_gemm(
         a.data_ptr(), w.data_ptr(), T, N, K, epilogue, ws.data_ptr(), ws.numel(), out.data_ptr(), _stream(a, stream)))
+    return out
+
+
+def mot_routed_gemm_noalloc(a, w, mod, epilogue: int = EPI_CAST, out=None, device_flags=None, stream=None):
+    """mot_routed_gemm for callers that cannot allocate device memory: the routing plan is kept
+    in the library's own fixed device array (T <= NOALLOC_MAX_TOKENS), so no workspace is
+    passed. Calls whose work may overlap on the GPU share that array and must be ordered by
+    the caller. `device_flags`, an optional int32 CUDA tensor of one element, receives the
+    call's device error bits."""
+    T, K = a.shape
+    _dev(a, "a", torch.bfloat16, 2)
+    _dev(w, "w", torch.bfloat16, 3)
+    _dev(mod, "mod", torch.uint8, 1)
+    if w.shape[0] != 2 or w.shape[2] != K or mod.numel() != T:
+        raise ValueError("w must be [2, N, K] and mod [T]")
+    N = w.shape[1]
+    ncols = N // 2 if epilogue == EPI_SWIGLU else N
+    if out is None:
+        out = torch.empty((T, ncols), dtype=torch.bfloat16, device=a.device)
+    _dev(out, "out", torch.bfloat16, 2)
+    fp = _dev(device_flags, "device_flags", torch.int32, 1) if device_flags is not None else None
+    _check("mot_routed_gemm_noalloc", _lib().mot_routed_gemm_noalloc(
+        a.data_ptr(), w.data_ptr(), mod.data_ptr(), T, N, K, epilogue, out.data_ptr(), fp, _stream(a, stream)))
     return out
 
 

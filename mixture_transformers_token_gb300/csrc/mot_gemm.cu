@@ -26,6 +26,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "mot.h"
 #include "mot_device.cuh"
 #include "mot_host.hpp"
@@ -464,4 +466,89 @@ extern "C" int mot_routed_gemm(const mot_bf16* a_in, const mot_bf16* w, int64_t 
   a.ldo = epilogue == MOT_EPI_SWIGLU ? N / 2 : N;
   if (epilogue == MOT_EPI_SWIGLU) return gemm::launch<gemm::EPI_SWIGLU>(a_in, w, int(T), N, K, a, dev, s);
   return gemm::launch<gemm::EPI_CAST>(a_in, w, int(T), N, K, a, dev, s);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of mot_routed_gemm.
+//
+// Some callers cannot hand this library a workspace: engines that reserve all device
+// memory once at start-up and forbid any later allocation, and plug-ins whose host
+// framework owns the device memory and gives them no allocator. For them the routing plan
+// lives in the file-scope array below, which every GPU that loads the library keeps until
+// the process exits. Host code may not use the array's name as a device address (on the
+// host it only stands in for the symbol); its device address is looked up once per device
+// with cudaGetSymbolAddress while that device is current, on the first call made on that
+// device. All calls on a device share the array and it keeps the last call's plan, so calls
+// whose work overlaps on the GPU (other streams, or other host threads) race and must be
+// serialized by the caller. Each call rebuilds the plan, which rewrites every field the
+// GEMM reads and clears the error word first.
+// ---------------------------------------------------------------------------
+namespace mot {
+namespace noalloc {
+
+constexpr int64_t kMaxTokens = MOT_NOALLOC_MAX_TOKENS;
+constexpr size_t kScratchBytes = 64 + 4 * kMaxTokens + 16 * (kMaxTokens / kTileRows + 1);
+
+static __device__ __align__(256) uint8_t g_plan_scratch[kScratchBytes];
+
+static std::mutex g_mu;
+static void* g_scratch_addr[kMaxDevices];
+
+// Device address of g_plan_scratch on `dev`, which must be the current device.
+static int scratch_for(int dev, uint8_t** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return MOT_ERR_CUDA;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = static_cast<uint8_t*>(g_scratch_addr[dev]);
+  return MOT_OK;
+}
+
+__global__ void copy_error_word(const uint8_t* scratch, uint32_t* flags) {
+  *flags = reinterpret_cast<const PlanHeader*>(scratch)->error;
+}
+
+}  // namespace noalloc
+}  // namespace mot
+
+extern "C" int mot_routed_gemm_noalloc(const mot_bf16* a_in, const mot_bf16* w, const uint8_t* mod, int64_t T, int N,
+                                       int K, int epilogue, mot_bf16* out, uint32_t* device_flags, void* stream) {
+  if (!a_in || !w || !mod || !out) return MOT_ERR_NULL;
+  if (epilogue != MOT_EPI_CAST && epilogue != MOT_EPI_SWIGLU) return MOT_ERR_ARG;
+  if (T > noalloc::kMaxTokens) return MOT_ERR_NOALLOC_LIMIT;
+  if (T < 1) return MOT_ERR_GEOMETRY;
+  if (N < gemm::BN || N % gemm::BN != 0 || N > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (K < gemm::BK || K % gemm::BK != 0 || K > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (!aligned16(a_in) || !aligned16(w) || !aligned16(out) || (reinterpret_cast<uintptr_t>(device_flags) & 3u))
+    return MOT_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {a_in, w, mod, out, device_flags};
+  int dev = -1;
+  int st = check_device(s, ptrs, 5, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  uint8_t* ws = nullptr;
+  st = noalloc::scratch_for(dev, &ws);
+  if (st != MOT_OK) return st;
+  st = enqueue_route_plan(mod, int(T), ws, s);
+  if (st != MOT_OK) return st;
+  gemm::Args a{};
+  a.ws = ws;
+  a.err = &reinterpret_cast<PlanHeader*>(ws)->error;
+  a.T = int(T);
+  a.N = N;
+  a.K = K;
+  a.n_tiles = N / gemm::BN;
+  a.out = out;
+  a.ldo = epilogue == MOT_EPI_SWIGLU ? N / 2 : N;
+  st = epilogue == MOT_EPI_SWIGLU ? gemm::launch<gemm::EPI_SWIGLU>(a_in, w, int(T), N, K, a, dev, s)
+                                  : gemm::launch<gemm::EPI_CAST>(a_in, w, int(T), N, K, a, dev, s);
+  if (st != MOT_OK || device_flags == nullptr) return st;
+  noalloc::copy_error_word<<<1, 1, 0, s>>>(ws, device_flags);
+  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }

@@ -126,4 +126,8 @@ inline bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Enqueues the routing pre-pass into `ws` (at least plan_bytes(T) bytes) without argument
+// checks; used by entry points that have already validated their arguments.
+int enqueue_route_plan(const uint8_t* mod, int T, uint8_t* ws, cudaStream_t s);
+
 }  // namespace mot

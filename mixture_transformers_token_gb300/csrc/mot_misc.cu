@@ -54,6 +54,7 @@ extern "C" const char* mot_status_string(int status) {
     case MOT_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
     case MOT_ERR_CUDA: return "CUDA runtime error";
     case MOT_ERR_ARG: return "invalid argument";
+    case MOT_ERR_NOALLOC_LIMIT: return "T exceeds MOT_NOALLOC_MAX_TOKENS, the row limit of the allocation-free entry point";
     default: return "unknown status";
   }
 }

@@ -178,6 +178,11 @@ static cudaError_t launch_norm(const mot_bf16* x, const mot_bf16* res, const mot
   return cudaGetLastError();
 }
 
+int enqueue_route_plan(const uint8_t* mod, int T, uint8_t* ws, cudaStream_t s) {
+  route_plan_kernel<<<1, kRouteThreads, 0, s>>>(mod, T, ws);
+  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+}
+
 }  // namespace mot
 
 using namespace mot;

@@ -51,7 +51,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_status_strings(lib):
     assert lib.mot_abi_version() == mot.ABI_VERSION
     seen = set()
-    for code in range(0, 9):
+    for code in range(0, 10):
         s = lib.mot_status_string(code).decode()
         assert s and s not in seen
         seen.add(s)
@@ -131,6 +131,17 @@ def test_routed_gemm_rejects(lib):
     assert f(A, A, 0, 256, 64, 0, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
     assert f(A, MIS, 8, 256, 64, 0, B, 1 << 20, C, None) == MOT_ERR_ALIGN
     assert f(A, A, 8, 256, 64, 0, B, 10, C, None) == MOT_ERR_WORKSPACE
+
+
+def test_noalloc_rejects_before_touching_cuda(lib):
+    f = lib.mot_routed_gemm_noalloc
+    assert f(None, A, A, 8, 256, 64, 0, C, None, None) == MOT_ERR_NULL
+    assert f(A, A, A, 65537, 256, 64, 0, C, None, None) == 9          # above the scratch limit
+    assert "MOT_NOALLOC_MAX_TOKENS" in lib.mot_status_string(9).decode()
+    assert f(A, A, A, 0, 256, 64, 0, C, None, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, 8, 320, 64, 0, C, None, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, 8, 256, 64, 5, C, None, None) == MOT_ERR_ARG
+    assert f(MIS, A, A, 8, 256, 64, 0, C, None, None) == MOT_ERR_ALIGN
 
 
 def test_interleave_and_status_reject(lib):
