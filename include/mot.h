@@ -18,7 +18,8 @@
  *   - Tensors are plain device pointers to dense row-major arrays; bf16 values are passed
  *     as raw 16-bit patterns (mot_bf16). Every bf16 tensor and the workspace must start on
  *     a 16-byte boundary. The caller owns all memory; the library allocates nothing and
- *     keeps no state between calls apart from per-device attribute caches.
+ *     keeps no state between calls apart from per-device attribute caches and the fixed
+ *     plan array of mot_routed_gemm_noalloc.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream of the current
  *     device). Every pointer must belong to the stream's device (the device guard of
  *     [PR-503]'s RMSNorm launcher commit); the launch runs on that device.
@@ -109,16 +110,20 @@ int mot_route_plan(const uint8_t* mod, int64_t T, void* ws, size_t ws_bytes, voi
  *   eps       > 0 and finite       added to the mean square inside the square root.
  *   y         [T][H] bf16          normalized output.
  *   res_out   [T][H] bf16          new residual stream; may alias res (in place).
- *   ws        optional workspace   if not NULL, receives MOT_DEV_BAD_MODALITY.
+ *   ws        optional workspace   if not NULL (ws_bytes >= mot_workspace_bytes(T)), one extra
+ *                                  CTA of the same launch writes the routing plan of mod into
+ *                                  it, exactly as mot_route_plan does, so the layer's routed
+ *                                  GEMMs need no separate pre-pass launch.
  * Per row: s = bf16(x + res) -> res_out; lane l of a 32-lane group owns columns
  * 256j + 8l + t; p_l = sequential fp32 sum of s^2 (j outer, t inner); partials combine
  * by an xor butterfly 16, 8, 4, 2, 1; rstd = 1 / sqrt(p / H + eps) with IEEE division and
  * square root; y = bf16((s * rstd) * w[mod]). A row with an invalid modality gets res_out
- * but no y. Geometry: H a multiple of 256, 256 <= H <= 8192; 1 <= T <= MOT_MAX_TOKENS.
+ * but no y (MOT_DEV_BAD_MODALITY in ws). Geometry: H a multiple of 256, 256 <= H <= 8192;
+ * 1 <= T <= MOT_MAX_TOKENS.
  */
 int mot_fused_add_rmsnorm(const mot_bf16* x, const mot_bf16* res, const mot_bf16* w,
                           const uint8_t* mod, int64_t T, int H, float eps,
-                          mot_bf16* y, mot_bf16* res_out, void* ws, void* stream);
+                          mot_bf16* y, mot_bf16* res_out, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * mot_routed_qkv_norm_rope -- routed QKV projection with per-head QK RMSNorm in fp32 and

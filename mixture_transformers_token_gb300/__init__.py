@@ -49,7 +49,7 @@ _SIGNATURES = {
     "mot_status_string": (ctypes.c_char_p, [_c_i]),
     "mot_workspace_bytes": (_c_sz, [_c_i64]),
     "mot_route_plan": (_c_i, [_c_p, _c_i64, _c_p, _c_sz, _c_p]),
-    "mot_fused_add_rmsnorm": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i, _c_f, _c_p, _c_p, _c_p, _c_p]),
+    "mot_fused_add_rmsnorm": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i, _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "mot_routed_qkv_norm_rope": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i64, _c_i, _c_i, _c_i,
                                         _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
@@ -147,7 +147,8 @@ def mot_route_plan(mod: torch.Tensor, ws: torch.Tensor | None = None, stream=Non
 
 
 def mot_fused_add_rmsnorm(x, res, w, mod, eps: float, y=None, res_out=None, ws=None, stream=None):
-    """Residual add and routed RMSNorm; returns (y, res_out). res_out may be res (in place)."""
+    """Residual add and routed RMSNorm; returns (y, res_out). res_out may be res (in place).
+    If `ws` is given, the same launch also writes the routing plan of `mod` into it."""
     T, H = x.shape
     if y is None:
         y = torch.empty_like(x)
@@ -162,9 +163,10 @@ def mot_fused_add_rmsnorm(x, res, w, mod, eps: float, y=None, res_out=None, ws=N
     if tuple(w.shape) != (2, H) or mod.numel() != T:
         raise ValueError("w must be [2, H] and mod [T]")
     wsp = _dev(ws, "ws", torch.uint8, 1) if ws is not None else None
+    wsb = ws.numel() if ws is not None else 0
     _check("mot_fused_add_rmsnorm", _lib().mot_fused_add_rmsnorm(
         x.data_ptr(), res.data_ptr(), w.data_ptr(), mod.data_ptr(), T, H, eps, y.data_ptr(), res_out.data_ptr(),
-        wsp, _stream(x, stream)))
+        wsp, wsb, _stream(x, stream)))
     return y, res_out
 
 

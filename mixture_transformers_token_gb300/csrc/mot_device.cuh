@@ -115,7 +115,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         t0 = now;
       } else if (now - t0 > kWaitLimitNs) {
         *abort_flag = 1u;
-        atomicOr(err, MOT_DEV_TIMEOUT);
+        if (err != nullptr) atomicOr(err, MOT_DEV_TIMEOUT);
         return false;
       }
     }
@@ -143,6 +143,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
           dst),
       "l"(tmap), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// Contiguous bytes from global to shared memory (1D bulk copy); both addresses 16-byte
+// aligned and `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 // Four rows y0..y3 of a 2D tensor, columns x .. x+box-1, stored one after another in

@@ -18,19 +18,17 @@ namespace mot {
 // ---------------------------------------------------------------------------
 // routing pre-pass: one CTA builds the per-expert row lists and the tile table
 // ---------------------------------------------------------------------------
-constexpr int kRouteThreads = 1024;
-
-__global__ void __launch_bounds__(kRouteThreads) route_plan_kernel(const uint8_t* __restrict__ mod, int T,
-                                                                    uint8_t* __restrict__ ws) {
+// Each thread owns a contiguous segment of rows, so a block-wide scan of the und counts gives
+// every row its slot in the stable ascending lists. Works for any block of 32..1024 threads.
+__device__ void route_plan_block(const uint8_t* __restrict__ mod, int T, uint8_t* __restrict__ ws) {
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
   int32_t* perm = reinterpret_cast<int32_t*>(ws + perm_offset());
   Tile* tiles = reinterpret_cast<Tile*>(ws + tiles_offset(T));
   __shared__ int warp_incl[32];
 
+  const int nthr = blockDim.x, nwarps = nthr >> 5;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // each thread owns a contiguous segment of rows, so a block-wide scan of the und counts
-  // gives every row its slot in the stable ascending lists
-  const int seg = (T + kRouteThreads - 1) / kRouteThreads;
+  const int seg = (T + nthr - 1) / nthr;
   const int begin = min(tid * seg, T), end = min(begin + seg, T);
   int n_und = 0, bad = 0;
   for (int r = begin; r < end; ++r) {
@@ -47,7 +45,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_plan_kernel(const uint8_t
   if (lane == 31) warp_incl[warp] = incl;
   bad = __syncthreads_or(bad);
   if (warp == 0) {
-    int v = warp_incl[lane];
+    int v = lane < nwarps ? warp_incl[lane] : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int u = __shfl_up_sync(0xffffffffu, v, off);
@@ -56,7 +54,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_plan_kernel(const uint8_t
     warp_incl[lane] = v;
   }
   __syncthreads();
-  const int total_und = warp_incl[31];
+  const int total_und = warp_incl[nwarps - 1];
   if (bad) {
     if (tid == 0) {
       hdr->T = T;
@@ -79,7 +77,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_plan_kernel(const uint8_t
   const int total_gen = T - total_und;
   const int nt0 = (total_und + kTileRows - 1) / kTileRows;
   const int nt1 = (total_gen + kTileRows - 1) / kTileRows;
-  for (int t = tid; t < nt0 + nt1; t += kRouteThreads) {
+  for (int t = tid; t < nt0 + nt1; t += nthr) {
     const int e = t < nt0 ? 0 : 1;
     const int i = e == 0 ? t : t - nt0;
     const int cnt = e == 0 ? total_und : total_gen;
@@ -101,80 +99,171 @@ __global__ void __launch_bounds__(kRouteThreads) route_plan_kernel(const uint8_t
   }
 }
 
+constexpr int kRouteThreads = 1024;
+
+__global__ void __launch_bounds__(kRouteThreads) route_plan_kernel(const uint8_t* __restrict__ mod, int T,
+                                                                    uint8_t* __restrict__ ws) {
+  route_plan_block(mod, T, ws);
+}
+
 // ---------------------------------------------------------------------------
-// fused residual add + routed RMSNorm: one warp per row
+// fused residual add + routed RMSNorm, fed by bulk copies through shared memory
 // ---------------------------------------------------------------------------
-constexpr int kNormThreads = 128;
+// One CTA per SM, persistent over rows (blockIdx.x - 1) + k G. Warp 0 streams whole rows of x
+// and res into C shared-memory slots with 1D bulk copies (cp.async.bulk); consumer warp c owns
+// slot c and processes every C-th row of the CTA, keeping the row's s = bf16(x + res) in
+// registers so the slot returns to the producer right after the first pass; the norm weights
+// of both experts are copied into shared memory once per CTA. The arithmetic of a row is the
+// fixed tree: lane l owns columns 256 j + 8 l + t, sequential fp32 sum of s^2 (j outer, t
+// inner), xor butterfly 16, 8, 4, 2, 1. When a workspace is given, CTA 0 of the same launch
+// builds the routing plan (it is scheduled first and has an SM of its own).
+constexpr int kNormMaxConsumers = 12;
+constexpr size_t kNormSlotBudget = 180 * 1024;
+
+struct NormArgs {
+  const uint16_t* x;
+  const uint16_t* res;
+  const uint16_t* w;
+  const uint8_t* mod;
+  int T, H;
+  float eps;
+  uint16_t* y;
+  uint16_t* res_out;
+  uint32_t* err;     // error word or null
+  uint8_t* plan_ws;  // if not null, CTA 0 writes the routing plan here
+  int norm_blocks;
+  int consumers;     // consumer warps = row slots
+};
 
 template <int NJ>
-__global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(
-    const uint4* __restrict__ x, const uint4* res, const uint16_t* __restrict__ w,
-    const uint8_t* __restrict__ mod, int T, int H, float eps, uint4* __restrict__ y, uint4* res_out,
-    uint32_t* __restrict__ err) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = int64_t(blockIdx.x) * (kNormThreads / 32) + (threadIdx.x >> 5);
-  if (row >= T) return;
-  const int nj = H >> 8;
-  const int64_t base = row * (H >> 3);  // row start in 16-byte units
-  // lane l owns columns 256 j + 8 l + t: one 16-byte vector per j
-  uint4 xs[NJ], rs[NJ];
-#pragma unroll
-  for (int j = 0; j < NJ; ++j)
-    if (j < nj) {
-      xs[j] = __ldcs(x + base + 32 * j + lane);
-      rs[j] = __ldcs(res + base + 32 * j + lane);
-    }
-  const int m = mod[row];
-  float p = 0.0f;
-#pragma unroll
-  for (int j = 0; j < NJ; ++j)
-    if (j < nj) {
-      const uint32_t xv[4] = {xs[j].x, xs[j].y, xs[j].z, xs[j].w};
-      const uint32_t rv[4] = {rs[j].x, rs[j].y, rs[j].z, rs[j].w};
-      uint32_t sv[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sv[k] = pack_bf2(__fadd_rn(bf_lo(xv[k]), bf_lo(rv[k])), __fadd_rn(bf_hi(xv[k]), bf_hi(rv[k])));
-        const float s0 = bf_lo(sv[k]), s1 = bf_hi(sv[k]);
-        p = __fadd_rn(p, __fmul_rn(s0, s0));  // t = 2k
-        p = __fadd_rn(p, __fmul_rn(s1, s1));  // t = 2k + 1
-      }
-      xs[j] = make_uint4(sv[0], sv[1], sv[2], sv[3]);
-      __stcs(res_out + base + 32 * j + lane, xs[j]);
-    }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off));
-  if (m > 1) {
-    if (lane == 0 && err != nullptr) atomicOr(err, MOT_DEV_BAD_MODALITY);
+__global__ void __launch_bounds__(32 * (1 + kNormMaxConsumers), 1) add_rmsnorm_kernel(const NormArgs a) {
+  const int plan_ctas = a.plan_ws != nullptr ? 1 : 0;
+  if (int(blockIdx.x) < plan_ctas) {
+    route_plan_block(a.mod, a.T, a.plan_ws);
     return;
   }
-  const float ms = __fdiv_rn(p, float(H));
-  const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-  const uint4* wv = reinterpret_cast<const uint4*>(w + int64_t(m) * H);
-#pragma unroll
-  for (int j = 0; j < NJ; ++j)
-    if (j < nj) {
-      const uint4 ww = __ldg(wv + 32 * j + lane);
-      const uint32_t sv[4] = {xs[j].x, xs[j].y, xs[j].z, xs[j].w};
-      const uint32_t wq[4] = {ww.x, ww.y, ww.z, ww.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        o[k] = pack_bf2(__fmul_rn(__fmul_rn(bf_lo(sv[k]), rstd), bf_lo(wq[k])),
-                        __fmul_rn(__fmul_rn(bf_hi(sv[k]), rstd), bf_hi(wq[k])));
-      y[base + 32 * j + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+  const int b = int(blockIdx.x) - plan_ctas;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int C = a.consumers;
+  const uint32_t row_bytes = uint32_t(a.H) * 2;
+  uint8_t* wbuf = smem;                   // [2][H] norm weights
+  uint8_t* slots = smem + 2 * row_bytes;  // C x (x row, res row)
+  uint64_t* full = reinterpret_cast<uint64_t*>(slots + size_t(C) * 2 * row_bytes);
+  uint64_t* empty = full + kNormMaxConsumers;
+  uint64_t* wbar = empty + kNormMaxConsumers;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(wbar + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.norm_blocks;
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < C; ++c) {
+      mbar_init(smem_u32(&full[c]), 1);
+      mbar_init(smem_u32(&empty[c]), 1);
     }
+    mbar_init(smem_u32(wbar), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      mbar_arrive_expect_tx(smem_u32(wbar), 2 * row_bytes);
+      bulk_load(smem_u32(wbuf), a.w, 2 * row_bytes, smem_u32(wbar));
+      int issued = 0;
+      for (int k = 0;; ++k) {
+        const int64_t row = int64_t(b) + int64_t(k) * G;
+        if (row >= a.T) break;
+        const int c = k % C;
+        const uint32_t round = uint32_t(k / C);
+        if (!mbar_wait(smem_u32(&empty[c]), (round & 1u) ^ 1u, abort_flag, a.err)) break;
+        uint8_t* slot = slots + size_t(c) * 2 * row_bytes;
+        const uint32_t fb = smem_u32(&full[c]);
+        mbar_arrive_expect_tx(fb, 2 * row_bytes);
+        bulk_load(smem_u32(slot), a.x + row * a.H, row_bytes, fb);
+        bulk_load(smem_u32(slot + row_bytes), a.res + row * a.H, row_bytes, fb);
+        issued = k + 1;
+      }
+      // no copy may still be landing when the CTA exits: wait for the last fill of every slot
+      mbar_drain(smem_u32(wbar), 0);
+      for (int k = issued - C > 0 ? issued - C : 0; k < issued; ++k)
+        mbar_drain(smem_u32(&full[k % C]), uint32_t(k / C) & 1u);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int c = warp - 1;
+  if (c >= C) return;
+  const int nj = a.H >> 8;
+  const uint4* sx = reinterpret_cast<const uint4*>(slots + size_t(c) * 2 * row_bytes);
+  const uint4* sr = reinterpret_cast<const uint4*>(slots + size_t(c) * 2 * row_bytes + row_bytes);
+  if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(wbar), 0, abort_flag, a.err))) return;
+  for (int k = c;; k += C) {
+    const int64_t row = int64_t(b) + int64_t(k) * G;
+    if (row >= a.T) break;
+    const int m = a.mod[row];
+    const uint32_t round = uint32_t(k / C);
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[c]), round & 1u, abort_flag, a.err))) break;
+    const int64_t base = row * (a.H >> 3);  // row start in 16-byte units
+    uint4* ro = reinterpret_cast<uint4*>(a.res_out) + base;
+    uint4 sv[NJ];
+    float p = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (j < nj) {
+        const uint4 xv4 = sx[32 * j + lane], rv4 = sr[32 * j + lane];
+        const uint32_t xv[4] = {xv4.x, xv4.y, xv4.z, xv4.w};
+        const uint32_t rv[4] = {rv4.x, rv4.y, rv4.z, rv4.w};
+        uint32_t s4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          s4[q] = pack_bf2(__fadd_rn(bf_lo(xv[q]), bf_lo(rv[q])), __fadd_rn(bf_hi(xv[q]), bf_hi(rv[q])));
+          const float s0 = bf_lo(s4[q]), s1 = bf_hi(s4[q]);
+          p = __fadd_rn(p, __fmul_rn(s0, s0));  // t = 2q
+          p = __fadd_rn(p, __fmul_rn(s1, s1));  // t = 2q + 1
+        }
+        sv[j] = make_uint4(s4[0], s4[1], s4[2], s4[3]);
+        __stcs(ro + 32 * j + lane, sv[j]);
+      }
+    }
+    // the row now lives in registers: hand the slot back to the producer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[c]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off));
+    if (m <= 1) {
+      const float ms = __fdiv_rn(p, float(a.H));
+      const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+      const uint4* wv = reinterpret_cast<const uint4*>(wbuf + size_t(m) * row_bytes);
+      uint4* yo = reinterpret_cast<uint4*>(a.y) + base;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        if (j < nj) {
+          const uint4 ww = wv[32 * j + lane];
+          const uint32_t s4[4] = {sv[j].x, sv[j].y, sv[j].z, sv[j].w};
+          const uint32_t wq[4] = {ww.x, ww.y, ww.z, ww.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            o[q] = pack_bf2(__fmul_rn(__fmul_rn(bf_lo(s4[q]), rstd), bf_lo(wq[q])),
+                            __fmul_rn(__fmul_rn(bf_hi(s4[q]), rstd), bf_hi(wq[q])));
+          yo[32 * j + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    } else if (lane == 0 && a.err != nullptr && a.plan_ws == nullptr) {
+      atomicOr(a.err, MOT_DEV_BAD_MODALITY);  // with a plan CTA in the launch, the plan reports it
+    }
+  }
 }
 
 template <int NJ>
-static cudaError_t launch_norm(const mot_bf16* x, const mot_bf16* res, const mot_bf16* w, const uint8_t* mod,
-                               int T, int H, float eps, mot_bf16* y, mot_bf16* res_out, uint32_t* err,
-                               cudaStream_t s) {
-  const int rows_per_block = kNormThreads / 32;
-  const unsigned grid = unsigned((T + rows_per_block - 1) / rows_per_block);
-  add_rmsnorm_kernel<NJ><<<grid, kNormThreads, 0, s>>>(
-      reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(res), w, mod, T, H, eps,
-      reinterpret_cast<uint4*>(y), reinterpret_cast<uint4*>(res_out), err);
+static cudaError_t launch_norm(const NormArgs& a, int grid, size_t smem, cudaStream_t s) {
+  if (cudaFuncSetAttribute(add_rmsnorm_kernel<NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+      cudaSuccess)
+    return cudaErrorInvalidValue;
+  add_rmsnorm_kernel<NJ><<<grid, 32 * (1 + a.consumers), smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -198,35 +287,55 @@ extern "C" int mot_route_plan(const uint8_t* mod, int64_t T, void* ws, size_t ws
   int st = check_device(s, ptrs, 2, &dev);
   if (st != MOT_OK) return st;
   DeviceGuard guard(dev);
-  route_plan_kernel<<<1, kRouteThreads, 0, s>>>(mod, int(T), static_cast<uint8_t*>(ws));
-  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+  return enqueue_route_plan(mod, int(T), static_cast<uint8_t*>(ws), s);
 }
 
 extern "C" int mot_fused_add_rmsnorm(const mot_bf16* x, const mot_bf16* res, const mot_bf16* w,
                                      const uint8_t* mod, int64_t T, int H, float eps, mot_bf16* y,
-                                     mot_bf16* res_out, void* ws, void* stream) {
+                                     mot_bf16* res_out, void* ws, size_t ws_bytes, void* stream) {
   if (!x || !res || !w || !mod || !y || !res_out) return MOT_ERR_NULL;
   if (T < 1 || T > MOT_MAX_TOKENS || H < 256 || H > 8192 || H % 256 != 0) return MOT_ERR_GEOMETRY;
   if (!(eps > 0.0f) || !(eps < 3.0e38f)) return MOT_ERR_ARG;
   if (!aligned16(x) || !aligned16(res) || !aligned16(w) || !aligned16(y) || !aligned16(res_out) ||
       (ws && !aligned16(ws)))
     return MOT_ERR_ALIGN;
+  if (ws && ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const void* ptrs[] = {x, res, w, mod, y, res_out, ws};
   int dev = -1;
   int st = check_device(s, ptrs, 7, &dev);
   if (st != MOT_OK) return st;
   DeviceGuard guard(dev);
-  uint32_t* err = ws ? &static_cast<PlanHeader*>(ws)->error : nullptr;
+  const size_t row_bytes = size_t(H) * 2;
+  int C = int(kNormSlotBudget / (2 * row_bytes));
+  C = C > kNormMaxConsumers ? kNormMaxConsumers : C;
+  NormArgs a{};
+  a.x = x;
+  a.res = res;
+  a.w = w;
+  a.mod = mod;
+  a.T = int(T);
+  a.H = H;
+  a.eps = eps;
+  a.y = y;
+  a.res_out = res_out;
+  a.err = ws ? &static_cast<PlanHeader*>(ws)->error : nullptr;
+  a.plan_ws = static_cast<uint8_t*>(ws);
+  const int sms = sm_count(dev);
+  const int avail = ws ? (sms > 1 ? sms - 1 : 1) : sms;  // the plan CTA gets an SM of its own
+  a.norm_blocks = int(T < avail ? T : avail);
+  a.consumers = C;
+  const size_t smem = 2 * row_bytes + size_t(C) * 2 * row_bytes + (2 * kNormMaxConsumers + 2) * sizeof(uint64_t);
+  const int grid = a.norm_blocks + (ws ? 1 : 0);
   const int nj = H / 256;
   cudaError_t e;
   if (nj <= 4)
-    e = launch_norm<4>(x, res, w, mod, int(T), H, eps, y, res_out, err, s);
+    e = launch_norm<4>(a, grid, smem, s);
   else if (nj <= 8)
-    e = launch_norm<8>(x, res, w, mod, int(T), H, eps, y, res_out, err, s);
+    e = launch_norm<8>(a, grid, smem, s);
   else if (nj <= 16)
-    e = launch_norm<16>(x, res, w, mod, int(T), H, eps, y, res_out, err, s);
+    e = launch_norm<16>(a, grid, smem, s);
   else
-    e = launch_norm<32>(x, res, w, mod, int(T), H, eps, y, res_out, err, s);
+    e = launch_norm<32>(a, grid, smem, s);
   return e == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }

@@ -88,15 +88,17 @@ def test_route_plan_rejects(lib):
 
 def test_add_rmsnorm_rejects(lib):
     f = lib.mot_fused_add_rmsnorm
-    assert f(None, A, A, A, 4, 256, 1e-6, B, C, None, None) == MOT_ERR_NULL
-    assert f(A, A, A, A, 4, 255, 1e-6, B, C, None, None) == MOT_ERR_GEOMETRY
-    assert f(A, A, A, A, 4, 128, 1e-6, B, C, None, None) == MOT_ERR_GEOMETRY
-    assert f(A, A, A, A, 4, 8448, 1e-6, B, C, None, None) == MOT_ERR_GEOMETRY
-    assert f(A, A, A, A, 0, 256, 1e-6, B, C, None, None) == MOT_ERR_GEOMETRY
-    assert f(A, A, A, A, 4, 256, 0.0, B, C, None, None) == MOT_ERR_ARG
-    assert f(A, A, A, A, 4, 256, float("nan"), B, C, None, None) == MOT_ERR_ARG
-    assert f(MIS, A, A, A, 4, 256, 1e-6, B, C, None, None) == MOT_ERR_ALIGN
-    assert f(A, A, A, A, 4, 256, 1e-6, B, MIS, None, None) == MOT_ERR_ALIGN
+    assert f(None, A, A, A, 4, 256, 1e-6, B, C, None, 0, None) == MOT_ERR_NULL
+    assert f(A, A, A, A, 4, 255, 1e-6, B, C, None, 0, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, A, 4, 128, 1e-6, B, C, None, 0, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, A, 4, 8448, 1e-6, B, C, None, 0, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, A, 0, 256, 1e-6, B, C, None, 0, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, A, 4, 256, 0.0, B, C, None, 0, None) == MOT_ERR_ARG
+    assert f(A, A, A, A, 4, 256, float("nan"), B, C, None, 0, None) == MOT_ERR_ARG
+    assert f(MIS, A, A, A, 4, 256, 1e-6, B, C, None, 0, None) == MOT_ERR_ALIGN
+    assert f(A, A, A, A, 4, 256, 1e-6, B, MIS, None, 0, None) == MOT_ERR_ALIGN
+    assert f(A, A, A, A, 4, 256, 1e-6, B, C, MIS, 1 << 20, None) == MOT_ERR_ALIGN
+    assert f(A, A, A, A, 1000, 256, 1e-6, B, C, C, 100, None) == MOT_ERR_WORKSPACE
 
 
 def test_qkv_rejects(lib):

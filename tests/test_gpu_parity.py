@@ -71,6 +71,22 @@ def test_route_plan_bitwise(name):
     np.testing.assert_array_equal(p["tiles"], np.array(want, dtype=np.int32).reshape(-1, 4))
 
 
+@pytest.mark.parametrize("name", ["bern1", "bern1000", "blocks4096", "scatter8192"])
+def test_fused_norm_writes_the_same_plan(name):
+    # the extra CTA of mot_fused_add_rmsnorm builds exactly the plan of mot_route_plan
+    mod = _mods()[name].cuda()
+    T = mod.numel()
+    ref = mot.mot_route_plan(mod)
+    x, res, w, _ = _norm_inputs(T, 256, 11)
+    ws = torch.full_like(ref, 0xAB)
+    mot.mot_fused_add_rmsnorm(x.cuda(), res.cuda(), w.cuda(), mod, EPS, ws=ws)
+    assert mot.mot_device_status(ws) == 0
+    a, b = decode_plan(ws, T), decode_plan(ref, T)
+    assert (a["T"], a["count"], a["num_m_tiles"], a["magic"]) == (b["T"], b["count"], b["num_m_tiles"], b["magic"])
+    np.testing.assert_array_equal(a["perm"], b["perm"])
+    np.testing.assert_array_equal(a["tiles"], b["tiles"])
+
+
 def test_route_plan_rejects_bad_modality():
     mod = torch.zeros(500, dtype=torch.uint8)
     mod[321] = 2
