@@ -12,20 +12,26 @@
 // GEMM commit: one writer per row, grouped result equal to the per-expert GEMM; SwiGLU in
 // FP32 with one BF16 cast; gated-norm commit: accurate expf).
 //
-// Design (one CTA per SM, persistent):
-//   warp 0      TMA producer: W tiles (256 x 64) and A tiles (128 x 64) into a 4-stage ring.
-//               A rows come from the routing plan: one tiled load when the tile's rows are
-//               consecutive, else 32 four-row gathers (tile::gather4), one per lane.
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and issues
-//               tcgen05.mma (M 128, N 256, K 16) from one thread, K blocks in ascending order.
-//   warps 2-5   epilogue: each thread owns one accumulator row (its TMEM lane), reads it with
-//               tcgen05.ld and writes the row's outputs to its original position.
+// Design (persistent, one CTA per SM, CTA pairs in clusters of two):
+//   A pair of CTAs computes a 256 x 256 output tile with the 2-SM MMA: each CTA holds its own
+//   128-row tile of A (one 128-row tile of the routing plan; both tiles of the same expert) and
+//   half of the 256 weight rows, so a pipeline stage is 32 KB per CTA and six stages fit.
+//   warp 0      TMA producer of each CTA: its A tile (one tiled load when the tile's rows are
+//               consecutive, else 32 four-row gathers, one per lane) and its B half, signalled
+//               on the leader CTA's stage barrier.
+//   warp 1      allocates 512 TMEM columns in both CTAs (two 128 x 256 fp32 accumulators per
+//               CTA); in the leader CTA one thread issues tcgen05.mma.cta_group::2 (M 256,
+//               N 256, K 16), K blocks in ascending order, and multicasts its commits to both
+//               CTAs.
+//   warps 2-5   epilogue of each CTA: one thread per accumulator row (its TMEM lane), read with
+//               tcgen05.ld, written to the row's original position.
 // Every tile of every pack uses the same tile shape, K order and instruction sequence, so a
 // row's bits depend only on the row and its expert's weights.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "mot.h"
@@ -35,9 +41,12 @@
 namespace mot {
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128;       // A rows per CTA (the pair covers 256)
+constexpr int BN = 256;       // output columns per pair tile
+constexpr int BN_HALF = 128;  // weight rows held by each CTA of the pair
+constexpr int BK = 64, STAGES = 6;
 constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t B_BYTES = BN_HALF * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t ACC_COLS = BN;
@@ -198,8 +207,34 @@ __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool vali
   }
 }
 
+// Which 128-row tile of the plan this CTA of the pair works on for pair tile u.
+struct PairTile {
+  int expert, mt, nt;  // mt: this CTA's m-tile (its partner's if this half is empty)
+  bool has_rows;       // false for the empty half of an expert's last pair
+};
+
+__device__ __forceinline__ PairTile decode_pair(int u, int P0, int P, int nt0, int nt1, uint32_t rank) {
+  PairTile t;
+  const int p = u % P;
+  t.nt = u / P;
+  int first, count;
+  if (p < P0) {
+    t.expert = 0;
+    first = 2 * p;
+    count = nt0;
+  } else {
+    t.expert = 1;
+    first = 2 * (p - P0);
+    count = nt1;
+  }
+  const int base = t.expert == 0 ? 0 : nt0;
+  t.has_rows = first + int(rank) < count;
+  t.mt = base + (t.has_rows ? first + int(rank) : first);
+  return t;
+}
+
 template <int EPI>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     routed_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_rows,
                        const __grid_constant__ CUtensorMap tm_w, const Args args) {
   extern __shared__ uint8_t smem_raw[];
@@ -207,23 +242,29 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sa = smem;
   uint8_t* sb = smem + STAGES * A_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* full = bars;               // used in the leader: its arrival plus both CTAs' stage bytes
+  uint64_t* empty = bars + STAGES;     // per CTA: released by the leader's multicast commit
+  uint64_t* tfull = bars + 2 * STAGES; // per CTA: accumulator ready
+  uint64_t* tempty = bars + 2 * STAGES + 2;  // used in the leader: both CTAs' epilogues done
   uint64_t* drain = bars + 2 * STAGES + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(args.ws);
   const int num_m = hdr->num_m_tiles;
-  if (hdr->magic != kPlanMagic || hdr->T != args.T || num_m < 0 || num_m > max_m_tiles(args.T)) {
+  const int nt0 = (hdr->count[0] + kTileRows - 1) / kTileRows;
+  const int nt1 = (hdr->count[1] + kTileRows - 1) / kTileRows;
+  if (hdr->magic != kPlanMagic || hdr->T != args.T || num_m < 0 || num_m > max_m_tiles(args.T) ||
+      num_m != nt0 + nt1) {
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.err, MOT_DEV_PLAN_MISMATCH);
-    return;
+    return;  // uniform across the grid
   }
-  const int total = num_m * args.n_tiles;
-  if (int(blockIdx.x) >= total) return;
+  const int P0 = (nt0 + 1) / 2, P = P0 + (nt1 + 1) / 2;
+  const int total = P * args.n_tiles;
+  const int cluster = int(blockIdx.x >> 1), nclusters = int(gridDim.x >> 1);
+  if (cluster >= total) return;  // uniform across the pair
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -232,7 +273,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), 4);
+      mbar_init(smem_u32(&tempty[b]), 8);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0u;
@@ -242,11 +283,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tm_w);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialized before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -255,14 +296,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int kblocks = args.K / BK;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (both CTAs) ----------------
     int stage = 0;
-    uint32_t phase = 0, issued = 0, issued_parity = 0;
+    uint32_t phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const int mt = t % num_m, nt = t / num_m;
-      const Tile tl = tiles[mt];
-      const int wrow = tl.expert * args.N + nt * BN;
+    for (int u = cluster; u < total && ok; u += nclusters) {
+      const PairTile pt = decode_pair(u, P0, P, nt0, nt1, rank);
+      const Tile tl = tiles[pt.mt];
+      const int wrow = pt.expert * args.N + pt.nt * BN + int(rank) * BN_HALF;
       const bool gather = tl.row0 < 0;
       int r[4] = {0, 0, 0, 0};
       if (gather) {
@@ -273,17 +314,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int kb = 0; kb < kblocks; ++kb) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err));
         if (!ok) break;
-        const uint32_t fb = smem_u32(&full[stage]);
+        const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          tma_load_2d(smem_u32(sb + stage * B_BYTES), &tm_w, kb * BK, wrow, fb);
-          if (!gather) tma_load_2d(smem_u32(sa + stage * A_BYTES), &tm_a, kb * BK, tl.row0, fb);
+          // the leader arrives once for both CTAs' bytes; the peer's copies only complete bytes
+          // on the leader's barrier (a phase cannot complete before the leader's arrival)
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * STAGE_BYTES);
+          tma_load_2d_pair(smem_u32(sb + stage * B_BYTES), &tm_w, kb * BK, wrow, fb);
+          if (!gather) tma_load_2d_pair(smem_u32(sa + stage * A_BYTES), &tm_a, kb * BK, tl.row0, fb);
         }
         __syncwarp();
-        if (gather) tma_gather4(smem_u32(sa + stage * A_BYTES + lane * 512), &tm_a_rows, kb * BK, r[0], r[1], r[2],
-                                r[3], fb);
-        issued |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (gather)
+          tma_gather4_pair(smem_u32(sa + stage * A_BYTES + lane * 512), &tm_a_rows, kb * BK, r[0], r[1], r[2], r[3],
+                           fb);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -291,7 +333,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     if (ok) {
-      // wait until the MMA warp has released every stage, so no arrival is still in flight
+      // every stage released by the leader's MMAs: they no longer read this CTA's shared memory
       for (int i = 0; i < STAGES; ++i) {
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err))) break;
         if (++stage == STAGES) {
@@ -300,78 +342,103 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-    // every load issued has landed before the CTA may exit
-    for (int s = 0; s < STAGES; ++s)
-      if ((issued >> s) & 1u) mbar_drain(smem_u32(&full[s]), (issued_parity >> s) & 1u);
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-    int stage = 0, acc = 0;
-    uint32_t phase = 0, acc_phase = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d = tmem_base + acc * ACC_COLS;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err));
+    // ---------------- MMA issuer (leader CTA only) ----------------
+    if (rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = cluster; u < total && ok; u += nclusters) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err));
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
+        const uint32_t d = tmem_base + acc * ACC_COLS;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(d, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc, (kb | k) != 0);
-          mma_commit(smem_u32(&empty[stage]));
+            for (int k = 0; k < BK / 16; ++k)
+              mma_bf16_pair(d, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+            mma_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
+        if (!ok) break;
+        if (lane == 0) mma_commit_pair_multicast(smem_u32(&tfull[acc]), 0x3);
         __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(smem_u32(&tfull[acc]));
+      // every MMA issued has completed before tensor memory is released
+      if (lane == 0) mma_commit_pair(smem_u32(drain));
       __syncwarp();
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      mbar_drain(smem_u32(drain), 0);
     }
-    // every MMA issued has completed before tensor memory is released
-    if (lane == 0) mma_commit(smem_u32(drain));
-    __syncwarp();
-    mbar_drain(smem_u32(drain), 0);
   } else {
-    // ---------------- epilogue ----------------
+    // ---------------- epilogue (both CTAs) ----------------
     const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
     const int row_in_tile = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const int mt = t % num_m, nt = t / num_m;
-      const Tile tl = tiles[mt];
-      const bool valid = row_in_tile < tl.n_rows;
+    for (int u = cluster; u < total; u += nclusters) {
+      const PairTile pt = decode_pair(u, P0, P, nt0, nt1, rank);
+      const Tile tl = tiles[pt.mt];
+      const bool valid = pt.has_rows && row_in_tile < tl.n_rows;
       const int grow = valid ? perm[tl.list_begin + row_in_tile] : 0;
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16);
-      if constexpr (EPI == EPI_CAST) epi_cast(args, taddr, valid, grow, nt);
-      if constexpr (EPI == EPI_SWIGLU) epi_swiglu(args, taddr, valid, grow, nt);
-      if constexpr (EPI == EPI_QKV64) epi_qkv<64>(args, taddr, valid, grow, tl.expert, nt);
-      if constexpr (EPI == EPI_QKV128) epi_qkv<128>(args, taddr, valid, grow, tl.expert, nt);
+      if constexpr (EPI == EPI_CAST) epi_cast(args, taddr, valid, grow, pt.nt);
+      if constexpr (EPI == EPI_SWIGLU) epi_swiglu(args, taddr, valid, grow, pt.nt);
+      if constexpr (EPI == EPI_QKV64) epi_qkv<64>(args, taddr, valid, grow, pt.expert, pt.nt);
+      if constexpr (EPI == EPI_QKV128) epi_qkv<128>(args, taddr, valid, grow, pt.expert, pt.nt);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&tempty[acc]), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair may still touch its memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
+}
+
+// Clusters of the pair kernel that fit on the device at once (computed once per device).
+template <int EPI>
+static int max_active_pairs(int dev) {
+  static std::atomic<int> cache[kMaxDevices];
+  int v = cache[dev].load();
+  if (v > 0) return v;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 256, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, routed_gemm_kernel<EPI>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = sm_count(dev) / 2;
+  }
+  cache[dev].store(n);
+  return n;
 }
 
 template <int EPI>
@@ -379,14 +446,16 @@ static int launch(const void* a, const void* w, int T, int N, int K, const Args&
   CUtensorMap tm_a, tm_rows, tm_w;
   if (!make_tmap_bf16(&tm_a, a, uint64_t(K), uint64_t(T), BK, BM) ||
       !make_tmap_bf16(&tm_rows, a, uint64_t(K), uint64_t(T), BK, 1) ||
-      !make_tmap_bf16(&tm_w, w, uint64_t(K), uint64_t(2) * N, BK, BN))
+      !make_tmap_bf16(&tm_w, w, uint64_t(K), uint64_t(2) * N, BK, BN_HALF))
     return MOT_ERR_CUDA;
   if (cudaFuncSetAttribute(routed_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES)) !=
       cudaSuccess)
     return MOT_ERR_CUDA;
-  const int64_t tiles_max = max_m_tiles(T) * int64_t(N / BN);
-  const int grid = int(tiles_max < sm_count(dev) ? tiles_max : sm_count(dev));
-  routed_gemm_kernel<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(tm_a, tm_rows, tm_w, args);
+  // upper bound of pair tiles: ceil(tiles0 / 2) + ceil(tiles1 / 2) <= (ceil(T / 128) + 1) / 2 + 1
+  const int64_t pairs_max = ((int64_t(T) + BM - 1) / BM + 1) / 2 + 1;
+  const int64_t work_max = pairs_max * int64_t(N / BN);
+  const int64_t clusters = work_max < max_active_pairs<EPI>(dev) ? work_max : max_active_pairs<EPI>(dev);
+  routed_gemm_kernel<EPI><<<unsigned(2 * clusters), THREADS, SMEM_BYTES, s>>>(tm_a, tm_rows, tm_w, args);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
