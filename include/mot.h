@@ -66,6 +66,12 @@ extern "C" {
 /* epilogues of mot_routed_gemm */
 #define MOT_EPI_CAST   0  /* out = bf16(acc) */
 #define MOT_EPI_SWIGLU 1  /* out = bf16(silu(bf16(acc_gate)) * bf16(acc_up)) */
+/* row-order flags, OR-ed into mot_routed_gemm's epilogue argument. "Plan order" is the row
+ * order of the routing plan: the und rows in ascending order, then the gen rows (the order
+ * mot_gather_rows produces). The flags change where rows are read and written, never their
+ * values. */
+#define MOT_A_PLAN_ORDER   0x100  /* row i of `a` is the plan's i-th row */
+#define MOT_OUT_PLAN_ORDER 0x200  /* row i of `out` is the plan's i-th row */
 
 /* largest packed batch the library accepts */
 #define MOT_MAX_TOKENS (1 << 24)
@@ -164,6 +170,8 @@ int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv, const mot
  *                             mot_swiglu_interleave (N = 2 I); out [T][I] =
  *                             bf16(g / (1 + expf(-g)) * u), g = bf16(acc_gate),
  *                             u = bf16(acc_up), fp32 arithmetic.
+ * With MOT_A_PLAN_ORDER every 128-row tile of `a` is contiguous and is read with one tiled
+ * copy; without it, tiles whose rows are not consecutive are gathered four rows at a time.
  * Geometry: N a multiple of 256, K a multiple of 64.
  */
 int mot_routed_gemm(const mot_bf16* a, const mot_bf16* w, int64_t T, int N, int K, int epilogue,
@@ -191,6 +199,17 @@ int mot_routed_gemm(const mot_bf16* a, const mot_bf16* w, int64_t T, int N, int 
  */
 int mot_routed_gemm_noalloc(const mot_bf16* a, const mot_bf16* w, const uint8_t* mod, int64_t T, int N, int K,
                             int epilogue, mot_bf16* out, uint32_t* device_flags, void* stream);
+
+/*
+ * mot_gather_rows -- reorders the rows of a [T][K] bf16 tensor into plan order:
+ * dst[i] = src[perm[i]], perm being the plan's row list (und rows ascending, then gen rows).
+ * Feeding a routed GEMM with MOT_A_PLAN_ORDER this way reads each row once instead of
+ * gathering it for every K block of every output tile when the modality is scattered.
+ *   src, dst  [T][K] bf16 device arrays (distinct).   ws  workspace holding the plan for T.
+ * Geometry: K a multiple of 8.
+ */
+int mot_gather_rows(const mot_bf16* src, int64_t T, int K, void* ws, size_t ws_bytes, mot_bf16* dst,
+                    void* stream);
 
 /*
  * mot_swiglu_interleave -- one-time layout step for the gate/up weights.

@@ -23,12 +23,14 @@ __all__ = [
     "mot_abi_version", "mot_status_string", "mot_workspace_bytes", "mot_route_plan",
     "mot_fused_add_rmsnorm", "mot_routed_qkv_norm_rope", "mot_routed_gemm",
     "mot_swiglu_interleave", "mot_rope_table_fill_host", "mot_device_status", "mot_routed_gemm_noalloc",
-    "NOALLOC_MAX_TOKENS",
+    "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows",
 ]
 
 ABI_VERSION = 1
 EPI_CAST = 0
 EPI_SWIGLU = 1
+A_PLAN_ORDER = 0x100
+OUT_PLAN_ORDER = 0x200
 DEV_BAD_MODALITY = 0x1
 DEV_TIMEOUT = 0x2
 DEV_PLAN_MISMATCH = 0x4
@@ -55,6 +57,7 @@ _SIGNATURES = {
     "mot_routed_gemm": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_noalloc": (_c_i, [_c_p, _c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_p, _c_p]),
     "mot_swiglu_interleave": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_p]),
+    "mot_gather_rows": (_c_i, [_c_p, _c_i64, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_rope_table_fill_host": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
 }
@@ -204,7 +207,8 @@ def mot_routed_qkv_norm_rope(x, w_qkv, q_norm_w, k_norm_w, pos, rope_cs, Hq: int
 
 
 def mot_routed_gemm(a, w, ws, epilogue: int = EPI_CAST, out=None, stream=None):
-    """Routed GEMM: out[T][N] = bf16(a W^T) (cast) or out[T][N/2] = SwiGLU (interleaved gate/up w)."""
+    """Routed GEMM: out[T][N] = bf16(a W^T) (cast) or out[T][N/2] = SwiGLU (interleaved gate/up w).
+    `epilogue` may carry A_PLAN_ORDER / OUT_PLAN_ORDER (rows of a / out in the plan's order)."""
     T, K = a.shape
     _dev(a, "a", torch.bfloat16, 2)
     _dev(w, "w", torch.bfloat16, 3)
@@ -212,7 +216,7 @@ def mot_routed_gemm(a, w, ws, epilogue: int = EPI_CAST, out=None, stream=None):
     if w.shape[0] != 2 or w.shape[2] != K:
         raise ValueError("w must be [2, N, K]")
     N = w.shape[1]
-    ncols = N // 2 if epilogue == EPI_SWIGLU else N
+    ncols = N // 2 if (epilogue & 0xFF) == EPI_SWIGLU else N
     if out is None:
         out = torch.empty((T, ncols), dtype=torch.bfloat16, device=a.device)
     _dev(out, "out", torch.bfloat16, 2)
@@ -243,6 +247,19 @@ def mot_routed_gemm_noalloc(a, w, mod, epilogue: int = EPI_CAST, out=None, devic
     fp = _dev(device_flags, "device_flags", torch.int32, 1) if device_flags is not None else None
     _check("mot_routed_gemm_noalloc", _lib().mot_routed_gemm_noalloc(
         a.data_ptr(), w.data_ptr(), mod.data_ptr(), T, N, K, epilogue, out.data_ptr(), fp, _stream(a, stream)))
+    return out
+
+
+def mot_gather_rows(src, ws, out=None, stream=None):
+    """Rows of src [T][K] in the plan's order (und rows ascending, then gen rows)."""
+    T, K = src.shape
+    _dev(src, "src", torch.bfloat16, 2)
+    _dev(ws, "ws", torch.uint8, 1)
+    if out is None:
+        out = torch.empty_like(src)
+    _dev(out, "out", torch.bfloat16, 2)
+    _check("mot_gather_rows", _lib().mot_gather_rows(src.data_ptr(), T, K, ws.data_ptr(), ws.numel(), out.data_ptr(),
+                                                     _stream(src, stream)))
     return out
 
 

@@ -48,11 +48,12 @@ constexpr int BK = 64, STAGES = 6;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = BN_HALF * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;  // producer, MMA, 8 epilogue warps
+constexpr int EPI_WARPS = 8;
 constexpr uint32_t ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256 + 1024;  // + QK-norm weights
 
 enum Epi { EPI_CAST = 0, EPI_SWIGLU = 1, EPI_QKV64 = 2, EPI_QKV128 = 3 };
 
@@ -71,6 +72,8 @@ struct Args {
   int P;
   int Hq, Hkv;
   float eps;
+  int a_plan_order;      // rows of A are in plan order
+  int out_plan_order;    // rows of out are written in plan order
 };
 
 __device__ __forceinline__ void store_row_u4(uint16_t* dst, const uint32_t* pk, int n_u4) {
@@ -79,13 +82,16 @@ __device__ __forceinline__ void store_row_u4(uint16_t* dst, const uint32_t* pk, 
   for (int i = 0; i < n_u4; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
 }
 
-// out = bf16(acc), 256 columns
-__device__ __forceinline__ void epi_cast(const Args& a, uint32_t taddr, bool valid, int grow, int nt) {
-  uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * BN;
+// Epilogue warps: two per TMEM lane quarter; warp "half" h handles the tile's columns
+// [128 h, 128 h + 128) of its 32 rows.
+
+// out = bf16(acc): 128 columns
+__device__ __forceinline__ void epi_cast(const Args& a, uint32_t taddr, bool valid, int grow, int nt, int half) {
+  uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * BN + half * 128;
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = 0; c < 4; ++c) {
     float v[32];
-    tmem_ld32(taddr + c * 32, v);
+    tmem_ld32(taddr + half * 128 + c * 32, v);
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
@@ -93,14 +99,15 @@ __device__ __forceinline__ void epi_cast(const Args& a, uint32_t taddr, bool val
   }
 }
 
-// gate columns 0..127 and up columns 128..255 of the tile -> 128 outputs
-__device__ __forceinline__ void epi_swiglu(const Args& a, uint32_t taddr, bool valid, int grow, int nt) {
-  uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * (BN / 2);
+// gate columns 0..127 and up columns 128..255 of the tile -> 128 outputs; half h makes outputs
+// [64 h, 64 h + 64) from gate columns 64 h + i and up columns 128 + 64 h + i
+__device__ __forceinline__ void epi_swiglu(const Args& a, uint32_t taddr, bool valid, int grow, int nt, int half) {
+  uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * (BN / 2) + half * 64;
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < 2; ++c) {
     float g[32], u[32];
-    tmem_ld32(taddr + c * 32, g);
-    tmem_ld32(taddr + 128 + c * 32, u);
+    tmem_ld32(taddr + half * 64 + c * 32, g);
+    tmem_ld32(taddr + 128 + half * 64 + c * 32, u);
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
@@ -118,92 +125,139 @@ __device__ __forceinline__ void epi_swiglu(const Args& a, uint32_t taddr, bool v
   }
 }
 
-// Per-head QK RMSNorm (fp32, fixed chunk tree) and BF16 RoPE; V heads pass through.
+// bf16x2 arithmetic with one round-to-nearest-even of the exact result (the product of two
+// bf16 numbers, and the sum of two, are exact in fp32, so this equals the fp32 operation
+// followed by a bf16 cast)
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_neg(uint32_t a) { return a ^ 0x80008000u; }
+
+// The RoPE (cos, sin) words of the row's position for the head dimension D, loaded before the
+// accumulator is ready. Word i holds (cos_i, sin_i).
 template <int D>
-__device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool valid, int grow, int e, int nt) {
-  constexpr int HEADS = BN / D;
-  constexpr int NP = D / 2;  // packed pairs per head
-  uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * BN;
+__device__ __forceinline__ void load_cs_row(const Args& a, bool valid, int grow, uint32_t (&cw)[D / 2]) {
   int p = valid ? a.pos[grow] : 0;
   if (p < 0 || p >= a.P) {
     atomicOr(a.err, MOT_DEV_BAD_POSITION);
     p = 0;
   }
-  const uint16_t* csrow = a.cs + int64_t(p) * D;  // D/2 (cos, sin) pairs
+  const uint4* src = reinterpret_cast<const uint4*>(a.cs + int64_t(p) * D);
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) {
+    const uint4 v = __ldg(src + i);
+    cw[4 * i] = v.x;
+    cw[4 * i + 1] = v.y;
+    cw[4 * i + 2] = v.z;
+    cw[4 * i + 3] = v.w;
+  }
+}
+
+// Adds the bias of columns [col, col + n) (n a multiple of 8) to v when a bias is given.
+template <int NV>
+__device__ __forceinline__ void add_bias(const Args& a, int e, int64_t col, float (&v)[NV]) {
+  if (a.bias == nullptr) return;
+  const uint4* bp = reinterpret_cast<const uint4*>(a.bias + int64_t(e) * a.N + col);
+#pragma unroll
+  for (int q4 = 0; q4 < NV / 8; ++q4) {
+    const uint4 bb = __ldg(bp + q4);
+    const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[8 * q4 + 2 * k] = __fadd_rn(v[8 * q4 + 2 * k], bf_lo(bw[k]));
+      v[8 * q4 + 2 * k + 1] = __fadd_rn(v[8 * q4 + 2 * k + 1], bf_hi(bw[k]));
+    }
+  }
+}
+
+// Per-head QK RMSNorm (fp32, fixed chunk tree) and BF16 RoPE on this warp's half of the tile;
+// V heads pass through. gs: the norm weights in shared memory, [q / k][expert][D/2] words;
+// cw: the (cos, sin) words of the row's position. Pass 1 reads the head from TMEM for its sum
+// of squares; pass 2 reads it again, 16 columns of each rotation pair (i, i + D/2) at a time,
+// and writes the outputs.
+template <int D>
+__device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool valid, int grow, int e, int nt, int half,
+                                        const uint32_t* gs, const uint32_t (&cw)[D / 2]) {
+  constexpr int HEADS = 128 / D;  // heads in this half
+  constexpr int NP = D / 2;       // packed words per head
+  uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * BN + half * 128;
 #pragma unroll 1
   for (int hh = 0; hh < HEADS; ++hh) {
-    const int h = nt * HEADS + hh;
+    const int h = nt * (BN / D) + half * HEADS + hh;
     const int kind = h < a.Hq ? 0 : (h < a.Hq + a.Hkv ? 1 : 2);  // q, k, v
-    uint32_t qp[NP];
-    float csum[D / 32];
+    const int col0 = half * 128 + hh * D;
+    const int64_t gcol0 = int64_t(nt) * BN + col0;  // column in the full output
+    uint16_t* ohead = orow + hh * D;
+    if (kind == 2) {
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float v[32];
+        tmem_ld32(taddr + col0 + c * 32, v);
+        add_bias<32>(a, e, gcol0 + c * 32, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
+        if (valid) store_row_u4(ohead + c * 32, pk, 4);
+      }
+      continue;
+    }
+    // pass 1: q = bf16(acc + b); chunk sums of q^2, folded left to right
+    float ss = 0.0f;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       float v[32];
-      tmem_ld32(taddr + hh * D + c * 32, v);
-      if (a.bias != nullptr) {
-        const uint4* bp =
-            reinterpret_cast<const uint4*>(a.bias + int64_t(e) * a.N + int64_t(nt) * BN + hh * D + c * 32);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 bb = __ldg(bp + q4);
-          const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            v[8 * q4 + 2 * k] = __fadd_rn(v[8 * q4 + 2 * k], bf_lo(bw[k]));
-            v[8 * q4 + 2 * k + 1] = __fadd_rn(v[8 * q4 + 2 * k + 1], bf_hi(bw[k]));
-          }
-        }
-      }
+      tmem_ld32(taddr + col0 + c * 32, v);
+      add_bias<32>(a, e, gcol0 + c * 32, v);
       float part = 0.0f;
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
         const uint32_t pk = pack_bf2(v[i], v[i + 1]);
-        qp[c * 16 + i / 2] = pk;
         const float q0 = bf_lo(pk), q1 = bf_hi(pk);
         part = __fadd_rn(part, __fmul_rn(q0, q0));
         part = __fadd_rn(part, __fmul_rn(q1, q1));
       }
-      csum[c] = part;
+      ss = c == 0 ? part : __fadd_rn(ss, part);
     }
-    if (kind != 2) {
-      float ss = csum[0];
+    const float ms = __fdiv_rn(ss, float(D));
+    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+    const uint32_t* g = gs + (kind * 2 + e) * NP;
+    // pass 2: u = bf16((q * rstd) * g); out_i = bf16(bf16(u_i c) + bf16(-u_{i+D/2} s)),
+    // out_{i+D/2} = bf16(bf16(u_{i+D/2} c) + bf16(u_i s)); two neighbouring i per word
 #pragma unroll
-      for (int c = 1; c < D / 32; ++c) ss = __fadd_rn(ss, csum[c]);
-      const float ms = __fdiv_rn(ss, float(D));
-      const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
-      const uint16_t* g = (kind == 0 ? a.qn : a.kn) + e * D;
-      // blocks of 8 rotation pairs (i, i + D/2)
+    for (int c = 0; c < NP / 16; ++c) {
+      float v1[16], v2[16];
+      tmem_ld16(taddr + col0 + c * 16, v1);
+      tmem_ld16(taddr + col0 + NP + c * 16, v2);
+      add_bias<16>(a, e, gcol0 + c * 16, v1);
+      add_bias<16>(a, e, gcol0 + NP + c * 16, v2);
+      uint32_t o1[8], o2[8];
 #pragma unroll
-      for (int m = 0; m < D / 16; ++m) {
-        const uint4 glo = __ldg(reinterpret_cast<const uint4*>(g + 8 * m));
-        const uint4 ghi = __ldg(reinterpret_cast<const uint4*>(g + NP + 8 * m));
-        const uint4 cs0 = __ldg(reinterpret_cast<const uint4*>(csrow + 16 * m));
-        const uint4 cs1 = __ldg(reinterpret_cast<const uint4*>(csrow + 16 * m + 8));
-        const uint32_t gl[4] = {glo.x, glo.y, glo.z, glo.w};
-        const uint32_t gh[4] = {ghi.x, ghi.y, ghi.z, ghi.w};
-        const uint32_t cw[8] = {cs0.x, cs0.y, cs0.z, cs0.w, cs1.x, cs1.y, cs1.z, cs1.w};  // (cos, sin) per pair
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t qa = qp[4 * m + k], qb = qp[NP / 2 + 4 * m + k];
-          float o1[2], o2[2];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const float xa = t ? bf_hi(qa) : bf_lo(qa);
-            const float xb = t ? bf_hi(qb) : bf_lo(qb);
-            const float ga = t ? bf_hi(gl[k]) : bf_lo(gl[k]);
-            const float gb = t ? bf_hi(gh[k]) : bf_lo(gh[k]);
-            const float c = bf_lo(cw[2 * k + t]), s = bf_hi(cw[2 * k + t]);
-            const float ua = bf_round(__fmul_rn(__fmul_rn(xa, rstd), ga));
-            const float ub = bf_round(__fmul_rn(__fmul_rn(xb, rstd), gb));
-            o1[t] = __fadd_rn(bf_round(__fmul_rn(ua, c)), bf_round(__fmul_rn(-ub, s)));
-            o2[t] = __fadd_rn(bf_round(__fmul_rn(ub, c)), bf_round(__fmul_rn(ua, s)));
-          }
-          qp[4 * m + k] = pack_bf2(o1[0], o1[1]);
-          qp[NP / 2 + 4 * m + k] = pack_bf2(o2[0], o2[1]);
-        }
+      for (int j = 0; j < 8; ++j) {
+        const int w = c * 8 + j;  // word index within the head's first half
+        const uint32_t q1 = pack_bf2(v1[2 * j], v1[2 * j + 1]);
+        const uint32_t q2 = pack_bf2(v2[2 * j], v2[2 * j + 1]);
+        const uint32_t g1 = g[w], g2 = g[NP / 2 + w];
+        const uint32_t u1 = pack_bf2(__fmul_rn(__fmul_rn(bf_lo(q1), rstd), bf_lo(g1)),
+                                     __fmul_rn(__fmul_rn(bf_hi(q1), rstd), bf_hi(g1)));
+        const uint32_t u2 = pack_bf2(__fmul_rn(__fmul_rn(bf_lo(q2), rstd), bf_lo(g2)),
+                                     __fmul_rn(__fmul_rn(bf_hi(q2), rstd), bf_hi(g2)));
+        const uint32_t c2 = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x5410);  // (cos_2w, cos_2w+1)
+        const uint32_t s2 = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x7632);  // (sin_2w, sin_2w+1)
+        o1[j] = bf2_add(bf2_mul(u1, c2), bf2_mul(bf2_neg(u2), s2));
+        o2[j] = bf2_add(bf2_mul(u2, c2), bf2_mul(u1, s2));
+      }
+      if (valid) {
+        store_row_u4(ohead + c * 16, o1, 2);
+        store_row_u4(ohead + NP + c * 16, o2, 2);
       }
     }
-    if (valid) store_row_u4(orow + hh * D, qp, NP / 4);
   }
 }
 
@@ -249,6 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* drain = bars + 2 * STAGES + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  uint32_t* gnorm = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES + 256);  // [2][2][D/2] words
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -273,7 +328,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), 8);
+      mbar_init(smem_u32(&tempty[b]), 2 * EPI_WARPS);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0u;
@@ -304,7 +359,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const PairTile pt = decode_pair(u, P0, P, nt0, nt1, rank);
       const Tile tl = tiles[pt.mt];
       const int wrow = pt.expert * args.N + pt.nt * BN + int(rank) * BN_HALF;
-      const bool gather = tl.row0 < 0;
+      const int arow0 = args.a_plan_order ? tl.list_begin : tl.row0;
+      const bool gather = arow0 < 0;
       int r[4] = {0, 0, 0, 0};
       if (gather) {
         const int last = tl.n_rows - 1;
@@ -320,7 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           // on the leader's barrier (a phase cannot complete before the leader's arrival)
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * STAGE_BYTES);
           tma_load_2d_pair(smem_u32(sb + stage * B_BYTES), &tm_w, kb * BK, wrow, fb);
-          if (!gather) tma_load_2d_pair(smem_u32(sa + stage * A_BYTES), &tm_a, kb * BK, tl.row0, fb);
+          if (!gather) tma_load_2d_pair(smem_u32(sa + stage * A_BYTES), &tm_a, kb * BK, arow0, fb);
         }
         __syncwarp();
         if (gather)
@@ -384,25 +440,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else {
     // ---------------- epilogue (both CTAs) ----------------
-    const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
+    constexpr int D = EPI == EPI_QKV64 ? 64 : 128;
+    const int quarter = warp & 3;          // the TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;      // which 128 columns of the tile
     const int row_in_tile = quarter * 32 + lane;
+    const int et = threadIdx.x - 64;       // 0 .. 255 among the epilogue threads
+    if constexpr (EPI == EPI_QKV64 || EPI == EPI_QKV128) {
+      // both experts' q and k norm weights, once per CTA
+      for (int i = et; i < 2 * D; i += 32 * EPI_WARPS) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(i < D ? args.qn : args.kn);
+        gnorm[i] = __ldg(src + (i % D));
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
+    }
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cluster; u < total; u += nclusters) {
       const PairTile pt = decode_pair(u, P0, P, nt0, nt1, rank);
       const Tile tl = tiles[pt.mt];
       const bool valid = pt.has_rows && row_in_tile < tl.n_rows;
-      const int grow = valid ? perm[tl.list_begin + row_in_tile] : 0;
+      const int grow = !valid ? 0 : (args.out_plan_order ? tl.list_begin + row_in_tile : perm[tl.list_begin + row_in_tile]);
+      uint32_t cw[D / 2];
+      bool rope = false;
+      if constexpr (EPI == EPI_QKV64 || EPI == EPI_QKV128) {
+        rope = pt.nt * (BN / D) + half * (128 / D) < args.Hq + args.Hkv;  // this half holds a q or k head
+        if (rope) load_cs_row<D>(args, valid, grow, cw);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16);
-      if constexpr (EPI == EPI_CAST) epi_cast(args, taddr, valid, grow, pt.nt);
-      if constexpr (EPI == EPI_SWIGLU) epi_swiglu(args, taddr, valid, grow, pt.nt);
-      if constexpr (EPI == EPI_QKV64) epi_qkv<64>(args, taddr, valid, grow, pt.expert, pt.nt);
-      if constexpr (EPI == EPI_QKV128) epi_qkv<128>(args, taddr, valid, grow, pt.expert, pt.nt);
+      if constexpr (EPI == EPI_CAST) epi_cast(args, taddr, valid, grow, pt.nt, half);
+      if constexpr (EPI == EPI_SWIGLU) epi_swiglu(args, taddr, valid, grow, pt.nt, half);
+      if constexpr (EPI == EPI_QKV64 || EPI == EPI_QKV128) epi_qkv<D>(args, taddr, valid, grow, pt.expert, pt.nt, half, gnorm, cw);
+      (void)rope;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&tempty[acc]), 0));
+      // the accumulator's TMEM reads have completed (tcgen05.wait::ld), so a relaxed arrive suffices
+      if (lane == 0) mbar_arrive_cluster_relaxed(map_to_rank(smem_u32(&tempty[acc]), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -512,6 +586,8 @@ extern "C" int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv
 extern "C" int mot_routed_gemm(const mot_bf16* a_in, const mot_bf16* w, int64_t T, int N, int K, int epilogue,
                                void* ws, size_t ws_bytes, mot_bf16* out, void* stream) {
   if (!a_in || !w || !ws || !out) return MOT_ERR_NULL;
+  const int order_flags = epilogue & (MOT_A_PLAN_ORDER | MOT_OUT_PLAN_ORDER);
+  epilogue &= ~(MOT_A_PLAN_ORDER | MOT_OUT_PLAN_ORDER);
   if (epilogue != MOT_EPI_CAST && epilogue != MOT_EPI_SWIGLU) return MOT_ERR_ARG;
   if (T < 1 || T > MOT_MAX_TOKENS) return MOT_ERR_GEOMETRY;
   if (N < gemm::BN || N % gemm::BN != 0 || N > (1 << 20)) return MOT_ERR_GEOMETRY;
@@ -533,6 +609,8 @@ extern "C" int mot_routed_gemm(const mot_bf16* a_in, const mot_bf16* w, int64_t 
   a.n_tiles = N / gemm::BN;
   a.out = out;
   a.ldo = epilogue == MOT_EPI_SWIGLU ? N / 2 : N;
+  a.a_plan_order = (order_flags & MOT_A_PLAN_ORDER) != 0;
+  a.out_plan_order = (order_flags & MOT_OUT_PLAN_ORDER) != 0;
   if (epilogue == MOT_EPI_SWIGLU) return gemm::launch<gemm::EPI_SWIGLU>(a_in, w, int(T), N, K, a, dev, s);
   return gemm::launch<gemm::EPI_CAST>(a_in, w, int(T), N, K, a, dev, s);
 }

@@ -267,6 +267,25 @@ static cudaError_t launch_norm(const NormArgs& a, int grid, size_t smem, cudaStr
   return cudaGetLastError();
 }
 
+// dst[i] = src[perm[i]]: one warp per row, 16-byte vectors, persistent grid
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src, int T, int K8,
+                                                          const uint8_t* __restrict__ ws, uint4* __restrict__ dst) {
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(ws);
+  if (hdr->magic != kPlanMagic || hdr->T != T) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(const_cast<uint32_t*>(&hdr->error), MOT_DEV_PLAN_MISMATCH);
+    return;
+  }
+  if (hdr->count[0] + hdr->count[1] != T) return;  // no plan (bad modality): nothing is defined
+  const int32_t* perm = reinterpret_cast<const int32_t*>(ws + perm_offset());
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < T; i += warps) {
+    const uint4* s = src + int64_t(perm[i]) * K8;
+    uint4* d = dst + i * K8;
+    for (int k = lane; k < K8; k += 32) __stcs(d + k, __ldcs(s + k));
+  }
+}
+
 int enqueue_route_plan(const uint8_t* mod, int T, uint8_t* ws, cudaStream_t s) {
   route_plan_kernel<<<1, kRouteThreads, 0, s>>>(mod, T, ws);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
@@ -338,4 +357,23 @@ extern "C" int mot_fused_add_rmsnorm(const mot_bf16* x, const mot_bf16* res, con
   else
     e = launch_norm<32>(a, grid, smem, s);
   return e == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+}
+
+extern "C" int mot_gather_rows(const mot_bf16* src, int64_t T, int K, void* ws, size_t ws_bytes, mot_bf16* dst,
+                               void* stream) {
+  if (!src || !ws || !dst) return MOT_ERR_NULL;
+  if (T < 1 || T > MOT_MAX_TOKENS || K < 8 || K % 8 != 0 || K > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (!aligned16(src) || !aligned16(ws) || !aligned16(dst)) return MOT_ERR_ALIGN;
+  if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
+  if (src == dst) return MOT_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {src, ws, dst};
+  int dev = -1;
+  int st = check_device(s, ptrs, 3, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  const int grid = 4 * sm_count(dev);
+  gather_rows_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), int(T), K / 8,
+                                          static_cast<const uint8_t*>(ws), reinterpret_cast<uint4*>(dst));
+  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }

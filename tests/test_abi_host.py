@@ -146,6 +146,21 @@ def test_noalloc_rejects_before_touching_cuda(lib):
     assert f(MIS, A, A, 8, 256, 64, 0, C, None, None) == MOT_ERR_ALIGN
 
 
+def test_gather_rows_rejects(lib):
+    f = lib.mot_gather_rows
+    assert f(None, 10, 64, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert f(A, 10, 60, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, 0, 64, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, 10, 64, MIS, 1 << 20, C, None) == MOT_ERR_ALIGN
+    assert f(A, 1000, 64, B, 100, C, None) == MOT_ERR_WORKSPACE
+    assert f(A, 10, 64, B, 1 << 20, A, None) == MOT_ERR_ARG
+
+
+def test_routed_gemm_order_flags_checked(lib):
+    assert lib.mot_routed_gemm(A, A, 8, 256, 64, 0x400, B, 1 << 20, C, None) == MOT_ERR_ARG
+    assert lib.mot_routed_gemm(A, A, 8, 256, 64, 0x2 | 0x100, B, 1 << 20, C, None) == MOT_ERR_ARG
+
+
 def test_interleave_and_status_reject(lib):
     assert lib.mot_swiglu_interleave(A, A, 100, 64, B, None) == MOT_ERR_GEOMETRY
     assert lib.mot_swiglu_interleave(None, A, 128, 64, B, None) == MOT_ERR_NULL

@@ -185,6 +185,45 @@ def test_routed_gemm_plan_mismatch_fails_closed():
     assert torch.all(out == 3.0)
 
 
+def test_gather_rows_is_plan_order():
+    T, K = 1000, 520
+    src = W.bf16_normal(W.rng_for(3, 80), (T, K)).cuda()
+    mod = W.modality_bernoulli(W.rng_for(3, 81), T, 0.3).cuda()
+    ws = mot.mot_route_plan(mod)
+    dst = mot.mot_gather_rows(src, ws)
+    assert mot.mot_device_status(ws) == 0
+    m = mod.cpu().numpy()
+    perm = np.concatenate([np.nonzero(m == 0)[0], np.nonzero(m == 1)[0]])
+    assert_bitwise(dst, src.cpu()[torch.from_numpy(perm)], "gathered rows")
+
+
+@pytest.mark.parametrize("epi", ["cast", "swiglu"])
+def test_plan_order_flags_give_the_same_bits(epi):
+    # reading A in plan order and/or writing out in plan order moves rows, never changes them
+    T, K = 777, 512
+    a = W.bf16_normal(W.rng_for(4, 82), (T, K)).cuda()
+    mod = W.modality_scattered(W.rng_for(4, 83), T, 200).cuda()
+    ws = mot.mot_route_plan(mod)
+    if epi == "cast":
+        w = W.bf16_normal(W.rng_for(4, 84), (2, 512, K), std=0.02).cuda()
+        e = mot.EPI_CAST
+    else:
+        w = mot.mot_swiglu_interleave(W.bf16_normal(W.rng_for(4, 85), (2, 256, K), std=0.02).cuda(),
+                                      W.bf16_normal(W.rng_for(4, 86), (2, 256, K), std=0.02).cuda())
+        e = mot.EPI_SWIGLU
+    m = mod.cpu().numpy()
+    perm = torch.from_numpy(np.concatenate([np.nonzero(m == 0)[0], np.nonzero(m == 1)[0]]))
+    ref = mot.mot_routed_gemm(a, w, ws, e).cpu()                         # token order in and out
+    a_plan = mot.mot_gather_rows(a, ws)
+    in_plan = mot.mot_routed_gemm(a_plan, w, ws, e | mot.A_PLAN_ORDER).cpu()
+    both = mot.mot_routed_gemm(a_plan, w, ws, e | mot.A_PLAN_ORDER | mot.OUT_PLAN_ORDER).cpu()
+    out_plan = mot.mot_routed_gemm(a, w, ws, e | mot.OUT_PLAN_ORDER).cpu()
+    assert mot.mot_device_status(ws) == 0
+    assert_bitwise(in_plan, ref, "A in plan order")
+    assert_bitwise(both, ref[perm], "A and out in plan order")
+    assert_bitwise(out_plan, ref[perm], "out in plan order")
+
+
 def test_swiglu_interleave_layout():
     I, K = 256, 64
     wg = W.bf16_normal(W.rng_for(2, 69), (2, I, K))
