@@ -1,19 +1,22 @@
 #!/usr/bin/env python
 """Benchmark of the MoT token-routed projection step on GB300.
 
-One step is one pass of the projection path over a packed batch: the routing pre-pass,
-the fused residual-add RMSNorm and the routed QKV GEMM with its per-head QK RMSNorm and BF16
-RoPE epilogue. The workload is the BAGEL-shaped layer: T = 4096 packed bf16 tokens, hidden
-3584, Q 28 x 128, KV 4 x 128 (QKV out 4608), und/gen weight sets W ~ N(0, 0.02), the first 3072
-tokens und then a contiguous 1024-token gen block, positions 0..4095, eps 1e-6, theta 1e6.
-Inputs are synthetic and seeded (one pack per rank); L2 is flushed (a write and a read of twice its
-size) before every timed step, outside the timed events.
+One step is one pass of the projection path over a packed batch: the fused residual-add
+RMSNorm (whose launch also builds the routing plan) and the routed QKV GEMM with its per-head
+QK RMSNorm and BF16 RoPE epilogue. The workload is the BAGEL-shaped layer: T = 4096 packed bf16
+tokens, hidden 3584, Q 28 x 128, KV 4 x 128 (QKV out 4608), und/gen weight sets W ~ N(0, 0.02),
+the first 3072 tokens und then a contiguous 1024-token gen block, positions 0..4095, eps 1e-6,
+theta 1e6. Inputs are synthetic and seeded (one pack per rank); L2 is flushed (a write and a
+read of twice its size) before every timed step, outside the timed events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0). `value` is whole-job TFLOP/s of the routed QKV projection
-(2 T H N flops per rank) over the whole step time, max over ranks. `--impl reference` times
-the CPU oracle on the host cores instead (rank 0 only).
+(2 T H N flops per rank) over the whole step time, max over ranks. The line also carries
+secondary measurements of the other rows of the path on their own workloads (the routed
+SwiGLU MLP at T = 8192 with scattered gen rows, and the CFG pack at T = 36864 with the routed
+O projection), each against its roofline. `--impl reference` times the CPU oracle on the host
+cores instead (rank 0 only).
 """
 
 from __future__ import annotations
@@ -36,7 +39,12 @@ WORKLOAD = "bagel_layer_T4096_H3584_q28x128_kv4x128_und3072_gen1024"
 T, H, HQ, HKV, D = 4096, 3584, 28, 4, 128
 N_QKV = (HQ + 2 * HKV) * D
 QKV_FLOPS = 2 * T * H * N_QKV                     # 135.29 GFLOP per step
-NORM_BYTES = 8 * T * H + 4 * H + T                # read x, res; write y, res_out; weights; modality
+
+
+def norm_bytes(t: int, h: int) -> int:
+    """Algorithmic bytes of the fused add-RMSNorm: read x, res; write y, res_out; weights; modality."""
+    return 8 * t * h + 4 * h + t
+
 
 # DRAM traffic of one QKV kernel launch from an ncu capture of this workload, keyed by the
 # hash of the kernel source it was taken on (null once the kernel has changed).
@@ -55,6 +63,27 @@ def peaks() -> dict:
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "of measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "of fallback"}
+
+
+# ---------------------------------------------------------------------------
+# ranks: one pack per GPU, no collective on the data path
+# ---------------------------------------------------------------------------
+
+def reduce_max(values, world: int, device=None) -> list:
+    """Element-wise maximum over ranks (identity on one rank)."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world: int, work_per_rank: float, seconds: float) -> float:
+    """Work of all ranks over the slowest rank's time (weak scaling: per-rank work is fixed)."""
+    return world * work_per_rank / seconds
 
 
 # ---------------------------------------------------------------------------
@@ -112,18 +141,55 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# our arm
+# device timing
 # ---------------------------------------------------------------------------
 
-def make_inputs(seed: int, dev):
+class L2Flush:
+    """Writes and then reads a buffer of twice the L2 size, so a timed region starts with a cold
+    L2 holding only clean lines (a write-only flush would leave dirty lines whose write-back
+    lands inside the timed kernels)."""
+
+    def __init__(self, dev):
+        import torch
+
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.buf = torch.empty(2 * max(l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
+        self.i = 0
+
+    def __call__(self):
+        self.i += 1
+        self.buf.fill_(self.i)
+        self.buf.sum()
+
+
+def time_stages(stages, steps: int, warmup: int, flush, stream) -> dict:
+    """Runs the list of (name, fn) as one step `warmup + steps` times with an L2 flush before
+    every step; returns the mean device time of each stage and of the step, in seconds."""
     import torch
 
-    from mixture_transformers_token_gb300 import workloads as W
+    for _ in range(warmup):
+        flush()
+        for _, fn in stages:
+            fn()
+    torch.cuda.synchronize()
+    if steps == 0:
+        return {}
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        for j, (_, fn) in enumerate(stages):
+            fn()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    out = {name: statistics.fmean(e[j].elapsed_time(e[j + 1]) for e in ev) / 1e3 for j, (name, _) in enumerate(stages)}
+    out["step"] = statistics.fmean(e[0].elapsed_time(e[-1]) for e in ev) / 1e3
+    return out
 
-    shape, inp = W.bagel_layer(seed=seed, T=T)
-    d = {k: v.to(dev) for k, v in inp.items() if isinstance(v, torch.Tensor)}
-    return shape, inp, d
 
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
 
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -131,6 +197,7 @@ def run_ours(args, rank, world, local_rank):
 
     import mixture_transformers_token_gb300 as mot
     from mixture_transformers_token_gb300 import build as mot_build
+    from mixture_transformers_token_gb300 import workloads as W
 
     if rank == 0 or world == 1:
         mot_build.build()
@@ -139,36 +206,27 @@ def run_ours(args, rank, world, local_rank):
     mot.load_library()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    shape, inp, d = make_inputs(1 + rank, dev)
+    shape, inp = W.bagel_layer(seed=1 + rank, T=T)
+    d = {k: v.to(dev) for k, v in inp.items() if isinstance(v, torch.Tensor)}
     stream = torch.cuda.current_stream(dev)
     cs = mot.mot_rope_table_fill_host(shape.theta, D, T).to(dev)
     ws = torch.empty(mot.mot_workspace_bytes(T), dtype=torch.uint8, device=dev)
     y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     ro = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, N_QKV), dtype=torch.bfloat16, device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * max(l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
 
-    def flush_l2(i):
-        # write twice L2 (evicts everything, our outputs' dirty lines are written back here),
-        # then read it back so the timed step starts with only clean lines in L2
-        flush.fill_(i)
-        flush.sum()
+    def norm():  # its launch also writes the routing plan of mod into ws (one extra CTA)
+        mot.mot_fused_add_rmsnorm(d["x"], d["res"], d["w_norm"], d["mod"], shape.eps, y=y, res_out=ro, ws=ws)
 
-    def step(x, res):
-        # the norm launch also writes the routing plan of mod into ws (one extra CTA)
-        mot.mot_fused_add_rmsnorm(x, res, d["w_norm"], d["mod"], shape.eps, y=y, res_out=ro, ws=ws)
+    def qkv():
         mot.mot_routed_qkv_norm_rope(y, d["w_qkv"], d["q_norm"], d["k_norm"], d["pos"], cs, HQ, HKV, D, shape.eps,
                                      ws, out=out)
 
-    for i in range(args.warmup):
-        flush_l2(i)
-        step(d["x"], d["res"])
-    torch.cuda.synchronize()
+    stages = [("add_rmsnorm_and_route_plan", norm), ("qkv_norm_rope", qkv)]
+    time_stages(stages, 0, args.warmup, flush, stream)
     if mot.mot_device_status(ws) != 0:
         raise RuntimeError("device error flags set during warm-up")
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -178,16 +236,7 @@ def run_ours(args, rank, world, local_rank):
     if sampler:
         sampler.mark("start")
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush_l2(i)
-        e = ev[i]
-        e[0].record(stream)
-        mot.mot_fused_add_rmsnorm(d["x"], d["res"], d["w_norm"], d["mod"], shape.eps, y=y, res_out=ro, ws=ws)
-        e[1].record(stream)
-        mot.mot_routed_qkv_norm_rope(y, d["w_qkv"], d["q_norm"], d["k_norm"], d["pos"], cs, HQ, HKV, D, shape.eps,
-                                     ws, out=out)
-        e[2].record(stream)
-    torch.cuda.synchronize()
+    times = time_stages(stages, args.steps, 0, flush, stream)
     wall = time.perf_counter() - t_wall
     if sampler:
         sampler.mark("end")
@@ -197,29 +246,25 @@ def run_ours(args, rank, world, local_rank):
     flags = mot.mot_device_status(ws)
     if flags != 0:
         raise RuntimeError(f"device error flags {flags:#x} in the timed region")
+    step_s, qkv_s, norm_s = reduce_max([times["step"], times["qkv_norm_rope"], times["add_rmsnorm_and_route_plan"]],
+                                       world, dev)
 
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    norm_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    qkv_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    mean = statistics.fmean
-    local = torch.tensor([mean(step_ms), mean(qkv_ms), mean(norm_ms)], dtype=torch.float64, device=dev)
+    e2e = run_e2e(args, shape, d, cs, ws, dev, world)
+    secondary = None
+    if rank == 0 and args.secondary:
+        secondary = {"swiglu_mlp_T8192": run_mlp(dev, flush), "cfg_pack_T36864": run_cfg_pack(dev, flush)}
     if world > 1:
-        dist.all_reduce(local, op=dist.ReduceOp.MAX)
-    step_s, qkv_s, norm_s = (v / 1e3 for v in local.tolist())
-
-    # end to end through the public API: host (pinned) inputs in, results back to the host
-    e2e = run_e2e(args, shape, d, cs, ws, stream, dev, world)
-
+        dist.barrier()
     if rank != 0:
         return None
+
     pk = peaks()
     qkv_tflops = QKV_FLOPS / qkv_s / 1e12
-    norm_gbs = NORM_BYTES / norm_s / 1e9
+    norm_gbs = norm_bytes(T, H) / norm_s / 1e9
     h = src_hash("mot_gemm.cu")
-    traffic = NCU_TRAFFIC.get(h)
     res = {
         "metric": METRIC,
-        "value": round(world * QKV_FLOPS / step_s / 1e12, 2),
+        "value": round(whole_job_rate(world, QKV_FLOPS, step_s) / 1e12, 2),
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -237,12 +282,12 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world} (one pack per GPU, no collective)"},
         "roofline": {"kernel": "routed_gemm_kernel<QKV128>", "bound": "tensor", "achieved": round(qkv_tflops, 2),
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(qkv_tflops / pk["bf16_tflops"], 4),
-                     "peak_source": pk["source"] + " (bf16 dense, burst)", "traffic": traffic,
+                     "peak_source": pk["source"] + " (bf16 dense, burst)", "traffic": NCU_TRAFFIC.get(h),
                      "algorithmic": "2*T*H*N flops per launch = 1.3529e11"},
         "roofline_norm": {"kernel": "add_rmsnorm_kernel (+ routing-plan CTA)", "bound": "hbm",
-                          "achieved": round(norm_gbs, 1),
-                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(norm_gbs / pk["hbm_gbs"], 4),
-                          "peak_source": pk["source"], "algorithmic": "8*T*H + 4*H + T bytes per launch"},
+                          "achieved": round(norm_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(norm_gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"],
+                          "algorithmic": "8*T*H + 4*H + T bytes per launch"},
         "kernels_us": {"add_rmsnorm_and_route_plan": round(norm_s * 1e6, 2), "qkv_norm_rope": round(qkv_s * 1e6, 2)},
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
@@ -250,56 +295,195 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed_loop": round(wall, 3),
         "kernel_src": h,
     }
+    if secondary is not None:
+        res["secondary"] = secondary
     if args.cpu_baseline and world == 1:
         res["cpu_baseline"] = cpu_baseline(rows=args.cpu_rows)
     return res
 
 
-def run_e2e(args, shape, d, cs, ws, stream, dev, world):
+def run_e2e(args, shape, d, cs, ws, dev, world):
+    """The same step through the public API from pinned host buffers: every step copies its
+    inputs (x, res) to the device and reads its results (qkv, res_out) back. Copies run on their
+    own streams with two device buffer sets, so the copies of neighbouring steps overlap the
+    compute; the rate is the steps' total device time over the timed steps."""
     import torch
     import torch.distributed as dist
 
     import mixture_transformers_token_gb300 as mot
 
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     x_h = d["x"].cpu().pin_memory()
     r_h = d["res"].cpu().pin_memory()
-    out_h = torch.empty((T, N_QKV), dtype=torch.bfloat16).pin_memory()
-    ro_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(d["x"])
-    r_d = torch.empty_like(d["res"])
+    out_h = [torch.empty((T, N_QKV), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    ro_h = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(d["x"]) for _ in range(2)]
+    r_d = [torch.empty_like(d["res"]) for _ in range(2)]
+    ro_d = [torch.empty_like(d["x"]) for _ in range(2)]
+    out_d = [torch.empty((T, N_QKV), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     y = torch.empty_like(d["x"])
-    ro = torch.empty_like(d["x"])
-    out = torch.empty((T, N_QKV), dtype=torch.bfloat16, device=dev)
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
     steps = max(3, min(args.steps, 200))
 
-    def one():
-        x_d.copy_(x_h, non_blocking=True)
-        r_d.copy_(r_h, non_blocking=True)
-        mot.mot_fused_add_rmsnorm(x_d, r_d, d["w_norm"], d["mod"], shape.eps, y=y, res_out=ro, ws=ws)
+    def one(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(comp_done[b])            # the slot's inputs are consumed
+            x_d[b].copy_(x_h, non_blocking=True)
+            r_d[b].copy_(r_h, non_blocking=True)
+            in_done[b].record(s_in)
+        comp.wait_event(in_done[b])
+        if i >= 2:
+            comp.wait_event(out_done[b])                 # the slot's outputs are read back
+        mot.mot_fused_add_rmsnorm(x_d[b], r_d[b], d["w_norm"], d["mod"], shape.eps, y=y, res_out=ro_d[b], ws=ws,
+                                  stream=comp)
         mot.mot_routed_qkv_norm_rope(y, d["w_qkv"], d["q_norm"], d["k_norm"], d["pos"], cs, HQ, HKV, D, shape.eps,
-                                     ws, out=out)
-        out_h.copy_(out, non_blocking=True)
-        ro_h.copy_(ro, non_blocking=True)
+                                     ws, out=out_d[b], stream=comp)
+        comp_done[b].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            out_h[b].copy_(out_d[b], non_blocking=True)
+            ro_h[b].copy_(ro_d[b], non_blocking=True)
+            out_done[b].record(s_out)
 
-    for _ in range(3):
-        one()
+    for i in range(4):
+        one(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
+    a.record(s_in)
+    for i in range(steps):
+        one(i)
+    s_out.wait_stream(comp)
+    b.record(s_out)
     torch.cuda.synchronize()
-    s = a.elapsed_time(b) / 1e3 / steps
-    t = torch.tensor([s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    s = float(t.item())
-    return {"value": round(world * QKV_FLOPS / s / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(s * 1e3, 4),
-            "steps": steps, "h2d_bytes_per_step": 2 * T * H * 2, "d2h_bytes_per_step": T * N_QKV * 2 + T * H * 2}
+    if mot.mot_device_status(ws) != 0:
+        raise RuntimeError("device error flags set in the end-to-end loop")
+    s = reduce_max([a.elapsed_time(b) / 1e3 / steps], world, dev)[0]
+    return {"value": round(whole_job_rate(world, QKV_FLOPS, s) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(s * 1e3, 4), "steps": steps, "h2d_bytes_per_step": 2 * T * H * 2,
+            "d2h_bytes_per_step": T * N_QKV * 2 + T * H * 2,
+            "note": "pinned host inputs copied in and results read back every step; copies overlap neighbouring steps"}
+
+
+def _tflops(flops, s):
+    return round(flops / s / 1e12, 2)
+
+
+def run_mlp(dev, flush) -> dict:
+    """Routed SwiGLU MLP, T = 8192, hidden 3584, intermediate 18944, 2048 gen rows scattered:
+    add-RMSNorm (+ plan) -> rows into plan order -> gate/up + SwiGLU (plan order in and out) ->
+    down (plan order in, token order out)."""
+    import torch
+
+    import mixture_transformers_token_gb300 as mot
+    from mixture_transformers_token_gb300 import workloads as W
+
+    t, h, i = W.MLP_T, W.MLP_H, W.MLP_I
+    stream = torch.cuda.current_stream(dev)
+    x = W.bf16_normal_device(3, 1, (t, h), dev)
+    res = W.bf16_normal_device(3, 2, (t, h), dev)
+    w_norm = W.bf16_normal_device(3, 3, (2, h), dev, mean=1.0, std=0.1)
+    w_gu = mot.mot_swiglu_interleave(W.bf16_normal_device(3, 4, (2, i, h), dev, std=0.02),
+                                     W.bf16_normal_device(3, 5, (2, i, h), dev, std=0.02))
+    w_down = W.bf16_normal_device(3, 6, (2, h, i), dev, std=0.02)
+    mod = W.modality_scattered(W.rng_for(3, 7), t, 2048).to(dev)
+    ws = torch.empty(mot.mot_workspace_bytes(t), dtype=torch.uint8, device=dev)
+    y, ro, y_plan = (torch.empty((t, h), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    hid = torch.empty((t, i), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((t, h), dtype=torch.bfloat16, device=dev)
+    stages = [
+        ("add_rmsnorm_and_route_plan", lambda: mot.mot_fused_add_rmsnorm(x, res, w_norm, mod, 1e-6, y=y, res_out=ro,
+                                                                         ws=ws)),
+        ("gather_rows", lambda: mot.mot_gather_rows(y, ws, out=y_plan)),
+        ("gate_up_swiglu", lambda: mot.mot_routed_gemm(y_plan, w_gu, ws, mot.EPI_SWIGLU | mot.A_PLAN_ORDER
+                                                       | mot.OUT_PLAN_ORDER, out=hid)),
+        ("down", lambda: mot.mot_routed_gemm(hid, w_down, ws, mot.EPI_CAST | mot.A_PLAN_ORDER, out=out)),
+    ]
+    r = time_stages(stages, 5, 2, flush, stream)
+    if mot.mot_device_status(ws) != 0:
+        raise RuntimeError("device error flags set in the MLP workload")
+    pk = peaks()
+    f_gu, f_dn = 2 * t * h * 2 * i, 2 * t * i * h
+    nb = norm_bytes(t, h)
+    result = {
+        "workload": "T8192_H3584_I18944_gen2048_scattered",
+        "add_rmsnorm_us": round(r["add_rmsnorm_and_route_plan"] * 1e6, 2),
+        "add_rmsnorm_gbs": round(nb / r["add_rmsnorm_and_route_plan"] / 1e9, 1),
+        "add_rmsnorm_frac_hbm": round(nb / r["add_rmsnorm_and_route_plan"] / 1e9 / pk["hbm_gbs"], 4),
+        "gather_rows_us": round(r["gather_rows"] * 1e6, 2),
+        "gather_rows_gbs": round(2 * t * h * 2 / r["gather_rows"] / 1e9, 1),
+        "gate_up_swiglu_us": round(r["gate_up_swiglu"] * 1e6, 2),
+        "gate_up_swiglu_tflops": _tflops(f_gu, r["gate_up_swiglu"]),
+        "gate_up_swiglu_frac": round(f_gu / r["gate_up_swiglu"] / 1e12 / pk["bf16_tflops"], 4),
+        "down_us": round(r["down"] * 1e6, 2),
+        "down_tflops": _tflops(f_dn, r["down"]),
+        "down_frac": round(f_dn / r["down"] / 1e12 / pk["bf16_tflops"], 4),
+        "step_us": round(r["step"] * 1e6, 2),
+        "peaks": f"{pk['source']}: bf16 {pk['bf16_tflops']} TFLOP/s (burst), HBM {pk['hbm_gbs']} GB/s",
+    }
+    del w_gu, w_down, hid
+    return result
+
+
+def run_cfg_pack(dev, flush) -> dict:
+    """CFG pack: 12 sequences of 2048 und + 1024 gen rows (T = 36864), positions restarting per
+    sequence: add-RMSNorm (+ plan), routed QKV + QK-norm + RoPE, routed O projection 3584 -> 3584
+    (its input stands in for the attention output)."""
+    import torch
+
+    import mixture_transformers_token_gb300 as mot
+    from mixture_transformers_token_gb300 import workloads as W
+
+    s = W.CFG_PACK
+    t, h = s.T, s.H
+    stream = torch.cuda.current_stream(dev)
+    mod, pos = W.cfg_pack_layout()
+    mod, pos = mod.to(dev), pos.to(dev)
+    x = W.bf16_normal_device(5, 1, (t, h), dev)
+    res = W.bf16_normal_device(5, 2, (t, h), dev)
+    attn = W.bf16_normal_device(5, 3, (t, h), dev)
+    w_norm = W.bf16_normal_device(5, 4, (2, h), dev, mean=1.0, std=0.1)
+    w_qkv = W.bf16_normal_device(5, 5, (2, s.n_qkv, h), dev, std=0.02)
+    qn = W.bf16_normal_device(5, 6, (2, s.D), dev, mean=1.0, std=0.1)
+    kn = W.bf16_normal_device(5, 7, (2, s.D), dev, mean=1.0, std=0.1)
+    w_o = W.bf16_normal_device(5, 8, (2, h, h), dev, std=0.02)
+    cs = mot.mot_rope_table_fill_host(s.theta, s.D, 3072).to(dev)
+    ws = torch.empty(mot.mot_workspace_bytes(t), dtype=torch.uint8, device=dev)
+    y, ro, o = (torch.empty((t, h), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    qkv = torch.empty((t, s.n_qkv), dtype=torch.bfloat16, device=dev)
+    stages = [
+        ("add_rmsnorm_and_route_plan", lambda: mot.mot_fused_add_rmsnorm(x, res, w_norm, mod, s.eps, y=y, res_out=ro,
+                                                                         ws=ws)),
+        ("qkv_norm_rope", lambda: mot.mot_routed_qkv_norm_rope(y, w_qkv, qn, kn, pos, cs, s.Hq, s.Hkv, s.D, s.eps, ws,
+                                                               out=qkv)),
+        ("o_proj", lambda: mot.mot_routed_gemm(attn, w_o, ws, mot.EPI_CAST, out=o)),
+    ]
+    r = time_stages(stages, 5, 2, flush, stream)
+    if mot.mot_device_status(ws) != 0:
+        raise RuntimeError("device error flags set in the CFG-pack workload")
+    pk = peaks()
+    f_qkv, f_o = 2 * t * h * s.n_qkv, 2 * t * h * h
+    nb = norm_bytes(t, h)
+    return {
+        "workload": "T36864_12x(2048und+1024gen)_H3584_q28x128_kv4x128",
+        "add_rmsnorm_us": round(r["add_rmsnorm_and_route_plan"] * 1e6, 2),
+        "add_rmsnorm_gbs": round(nb / r["add_rmsnorm_and_route_plan"] / 1e9, 1),
+        "add_rmsnorm_frac_hbm": round(nb / r["add_rmsnorm_and_route_plan"] / 1e9 / pk["hbm_gbs"], 4),
+        "qkv_us": round(r["qkv_norm_rope"] * 1e6, 2),
+        "qkv_tflops": _tflops(f_qkv, r["qkv_norm_rope"]),
+        "qkv_frac": round(f_qkv / r["qkv_norm_rope"] / 1e12 / pk["bf16_tflops"], 4),
+        "o_proj_us": round(r["o_proj"] * 1e6, 2),
+        "o_proj_tflops": _tflops(f_o, r["o_proj"]),
+        "o_proj_frac": round(f_o / r["o_proj"] / 1e12 / pk["bf16_tflops"], 4),
+        "step_us": round(r["step"] * 1e6, 2),
+    }
 
 
 # ---------------------------------------------------------------------------
@@ -392,6 +576,8 @@ def main():
     ap.add_argument("--cpu-baseline", dest="cpu_baseline", action="store_true", default=True)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--secondary", dest="secondary", action="store_true", default=True)
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--cpu-baseline-child", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_baseline_child is not None:

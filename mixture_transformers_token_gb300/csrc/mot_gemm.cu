@@ -267,10 +267,27 @@ struct PairTile {
   bool has_rows;       // false for the empty half of an expert's last pair
 };
 
-__device__ __forceinline__ PairTile decode_pair(int u, int P0, int P, int nt0, int nt1, uint32_t rank) {
+// Raster order of the pair tiles: bands of `band` pairs; within a band the pair index varies
+// fastest, then the N tile. When every pair's A rows fit in L2 the band is all pairs (A is read
+// once, each weight tile is shared by all pairs at once); otherwise a band holds about 32 MB of
+// A rows, so they stay in L2 while the band sweeps all N tiles. The order never changes a
+// tile's arithmetic.
+__device__ __forceinline__ int band_pairs(int P, int K) {
+  const int64_t a_pair_bytes = int64_t(2 * BM) * K * 2;
+  if (int64_t(P) * a_pair_bytes <= (int64_t(64) << 20)) return P;
+  const int b = int((int64_t(32) << 20) / a_pair_bytes);
+  return b < 2 ? 2 : b;
+}
+
+__device__ __forceinline__ PairTile decode_pair(int u, int P0, int P, int band, int n_tiles, int nt0, int nt1,
+                                                uint32_t rank) {
   PairTile t;
-  const int p = u % P;
-  t.nt = u / P;
+  const int per_band = band * n_tiles;
+  const int first_pair = (u / per_band) * band;
+  const int bp = P - first_pair < band ? P - first_pair : band;
+  const int r = u % per_band;
+  const int p = first_pair + r % bp;
+  t.nt = r / bp;
   int first, count;
   if (p < P0) {
     t.expert = 0;
@@ -318,6 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
   const int P0 = (nt0 + 1) / 2, P = P0 + (nt1 + 1) / 2;
   const int total = P * args.n_tiles;
+  const int band = P > 0 ? band_pairs(P, args.K) : 1;
   const int cluster = int(blockIdx.x >> 1), nclusters = int(gridDim.x >> 1);
   if (cluster >= total) return;  // uniform across the pair
 
@@ -356,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int u = cluster; u < total && ok; u += nclusters) {
-      const PairTile pt = decode_pair(u, P0, P, nt0, nt1, rank);
+      const PairTile pt = decode_pair(u, P0, P, band, args.n_tiles, nt0, nt1, rank);
       const Tile tl = tiles[pt.mt];
       const int wrow = pt.expert * args.N + pt.nt * BN + int(rank) * BN_HALF;
       const int arow0 = args.a_plan_order ? tl.list_begin : tl.row0;
@@ -456,7 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cluster; u < total; u += nclusters) {
-      const PairTile pt = decode_pair(u, P0, P, nt0, nt1, rank);
+      const PairTile pt = decode_pair(u, P0, P, band, args.n_tiles, nt0, nt1, rank);
       const Tile tl = tiles[pt.mt];
       const bool valid = pt.has_rows && row_in_tile < tl.n_rows;
       const int grow = !valid ? 0 : (args.out_plan_order ? tl.list_begin + row_in_tile : perm[tl.list_begin + row_in_tile]);

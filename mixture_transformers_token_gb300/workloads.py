@@ -40,6 +40,22 @@ def bf16_normal(rng: np.random.Generator, shape, mean: float = 0.0, std: float =
     return torch.from_numpy(a).to(torch.bfloat16)
 
 
+def bf16_normal_device(seed: int, stream: int, shape, device, mean: float = 0.0, std: float = 1.0) -> torch.Tensor:
+    """A device bf16 tensor of N(mean, std^2) draws from torch's seeded generator on `device`.
+
+    Used for the large weights of throughput-only workloads, where drawing on the host would
+    dominate the run; inputs that the oracle also sees come from the host generators above.
+    """
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1_000_003 + stream)
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    if mean != 0.0:
+        t.add_(mean)
+    return t.to(torch.bfloat16)
+
+
 def bf16_integers(rng: np.random.Generator, shape, lo: int, hi: int) -> torch.Tensor:
     """A CPU bf16 tensor of small integers in [lo, hi] (exact in bf16 when |v| <= 256)."""
     a = rng.integers(lo, hi + 1, size=shape).astype(np.float32)
