@@ -387,13 +387,9 @@ def run_mlp(dev, flush) -> dict:
 
     t, h, i = W.MLP_T, W.MLP_H, W.MLP_I
     stream = torch.cuda.current_stream(dev)
-    x = W.bf16_normal_device(3, 1, (t, h), dev)
-    res = W.bf16_normal_device(3, 2, (t, h), dev)
-    w_norm = W.bf16_normal_device(3, 3, (2, h), dev, mean=1.0, std=0.1)
-    w_gu = mot.mot_swiglu_interleave(W.bf16_normal_device(3, 4, (2, i, h), dev, std=0.02),
-                                     W.bf16_normal_device(3, 5, (2, i, h), dev, std=0.02))
-    w_down = W.bf16_normal_device(3, 6, (2, h, i), dev, std=0.02)
-    mod = W.modality_scattered(W.rng_for(3, 7), t, 2048).to(dev)
+    m = W.mlp_device_inputs(dev)
+    x, res, w_norm, mod, w_down = m["x"], m["res"], m["w_norm"], m["mod"], m["w_down"]
+    w_gu = mot.mot_swiglu_interleave(m.pop("w_gate"), m.pop("w_up"))
     ws = torch.empty(mot.mot_workspace_bytes(t), dtype=torch.uint8, device=dev)
     y, ro, y_plan = (torch.empty((t, h), dtype=torch.bfloat16, device=dev) for _ in range(3))
     hid = torch.empty((t, i), dtype=torch.bfloat16, device=dev)
@@ -444,16 +440,9 @@ def run_cfg_pack(dev, flush) -> dict:
     s = W.CFG_PACK
     t, h = s.T, s.H
     stream = torch.cuda.current_stream(dev)
-    mod, pos = W.cfg_pack_layout()
-    mod, pos = mod.to(dev), pos.to(dev)
-    x = W.bf16_normal_device(5, 1, (t, h), dev)
-    res = W.bf16_normal_device(5, 2, (t, h), dev)
-    attn = W.bf16_normal_device(5, 3, (t, h), dev)
-    w_norm = W.bf16_normal_device(5, 4, (2, h), dev, mean=1.0, std=0.1)
-    w_qkv = W.bf16_normal_device(5, 5, (2, s.n_qkv, h), dev, std=0.02)
-    qn = W.bf16_normal_device(5, 6, (2, s.D), dev, mean=1.0, std=0.1)
-    kn = W.bf16_normal_device(5, 7, (2, s.D), dev, mean=1.0, std=0.1)
-    w_o = W.bf16_normal_device(5, 8, (2, h, h), dev, std=0.02)
+    c = W.cfg_pack_device_inputs(dev)
+    mod, pos, x, res, attn = c["mod"], c["pos"], c["x"], c["res"], c["attn"]
+    w_norm, w_qkv, qn, kn, w_o = c["w_norm"], c["w_qkv"], c["q_norm"], c["k_norm"], c["w_o"]
     cs = mot.mot_rope_table_fill_host(s.theta, s.D, 3072).to(dev)
     ws = torch.empty(mot.mot_workspace_bytes(t), dtype=torch.uint8, device=dev)
     y, ro, o = (torch.empty((t, h), dtype=torch.bfloat16, device=dev) for _ in range(3))

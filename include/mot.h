@@ -234,6 +234,16 @@ int mot_swiglu_interleave(const mot_bf16* w_gate, const mot_bf16* w_up, int I, i
 int mot_rope_table_fill_host(double theta, int D, int P, mot_bf16* host_cs);
 
 /*
+ * mot_selftest_wait_timeout -- exercises the bounded wait that every pipeline wait of the
+ * library uses ([RFC-435] §3: fail closed instead of hanging). One thread waits on an mbarrier
+ * that nothing signals; after about one second the wait gives up, MOT_DEV_TIMEOUT is OR-ed into
+ * the workspace error word (read it with mot_device_status) and the kernel returns normally,
+ * leaving the context usable. No fault, trap or unbounded wait is involved.
+ *   ws   device workspace of at least 64 bytes (its error word receives the bit).
+ */
+int mot_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream);
+
+/*
  * mot_device_status -- synchronizes `stream` and copies the workspace error word
  * (MOT_DEV_* bits, 0 = clean) to *flags.
  */

@@ -23,7 +23,7 @@ __all__ = [
     "mot_abi_version", "mot_status_string", "mot_workspace_bytes", "mot_route_plan",
     "mot_fused_add_rmsnorm", "mot_routed_qkv_norm_rope", "mot_routed_gemm",
     "mot_swiglu_interleave", "mot_rope_table_fill_host", "mot_device_status", "mot_routed_gemm_noalloc",
-    "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows",
+    "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows", "mot_selftest_wait_timeout",
 ]
 
 ABI_VERSION = 1
@@ -58,6 +58,7 @@ _SIGNATURES = {
     "mot_routed_gemm_noalloc": (_c_i, [_c_p, _c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_p, _c_p]),
     "mot_swiglu_interleave": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_p]),
     "mot_gather_rows": (_c_i, [_c_p, _c_i64, _c_i, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_selftest_wait_timeout": (_c_i, [_c_p, _c_sz, _c_p]),
     "mot_rope_table_fill_host": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
 }
@@ -283,6 +284,12 @@ def mot_rope_table_fill_host(theta: float, D: int, P: int) -> torch.Tensor:
     t = torch.empty((P, D // 2, 2), dtype=torch.bfloat16)
     _check("mot_rope_table_fill_host", _lib().mot_rope_table_fill_host(theta, D, P, t.data_ptr()))
     return t
+
+
+def mot_selftest_wait_timeout(ws, stream=None) -> None:
+    """Runs a bounded wait that nothing satisfies; afterwards ws's error word has DEV_TIMEOUT."""
+    _dev(ws, "ws", torch.uint8, 1)
+    _check("mot_selftest_wait_timeout", _lib().mot_selftest_wait_timeout(ws.data_ptr(), ws.numel(), _stream(ws, stream)))
 
 
 def mot_device_status(ws, stream=None) -> int:

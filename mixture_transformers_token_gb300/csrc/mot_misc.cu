@@ -37,6 +37,21 @@ __global__ void swiglu_interleave_kernel(const uint4* __restrict__ wg, const uin
   }
 }
 
+// Waits on an mbarrier that nothing ever signals, through the same bounded wait as every
+// pipeline wait of the library: after the limit the wait gives up, records MOT_DEV_TIMEOUT in
+// the error word and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, err);
+}
+
 }  // namespace mot
 
 using namespace mot;
@@ -115,5 +130,19 @@ extern "C" int mot_swiglu_interleave(const mot_bf16* w_gate, const mot_bf16* w_u
   swiglu_interleave_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(w_gate),
                                                  reinterpret_cast<const uint4*>(w_up), I, K / 8,
                                                  reinterpret_cast<uint4*>(w_gu));
+  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+}
+
+extern "C" int mot_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr) return MOT_ERR_NULL;
+  if (!aligned16(ws)) return MOT_ERR_ALIGN;
+  if (ws_bytes < sizeof(PlanHeader)) return MOT_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {ws};
+  int dev = -1;
+  int st = check_device(s, ptrs, 1, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(&static_cast<PlanHeader*>(ws)->error);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }

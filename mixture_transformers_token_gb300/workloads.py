@@ -166,3 +166,38 @@ def mlp_inputs(T: int, H: int, I: int, n_gen: int, seed: int) -> dict:
         "w_down": bf16_normal(rng_for(seed, 16), (2, H, I), std=0.02),
         "mod": modality_scattered(rng_for(seed, 10), T, n_gen),
     }
+
+
+def mlp_device_inputs(device, seed: int = 3) -> dict:
+    """Routed SwiGLU MLP at T = 8192, hidden 3584, intermediate 18944, exactly 2048 gen rows
+    scattered uniformly: x, res, norm weights and separate gate / up / down weights drawn on the
+    device (the modality index on the host)."""
+    t, h, i = MLP_T, MLP_H, MLP_I
+    return {
+        "x": bf16_normal_device(seed, 1, (t, h), device),
+        "res": bf16_normal_device(seed, 2, (t, h), device),
+        "w_norm": bf16_normal_device(seed, 3, (2, h), device, mean=1.0, std=0.1),
+        "w_gate": bf16_normal_device(seed, 4, (2, i, h), device, std=0.02),
+        "w_up": bf16_normal_device(seed, 5, (2, i, h), device, std=0.02),
+        "w_down": bf16_normal_device(seed, 6, (2, h, i), device, std=0.02),
+        "mod": modality_scattered(rng_for(seed, 7), t, 2048).to(device),
+    }
+
+
+def cfg_pack_device_inputs(device, seed: int = 5) -> dict:
+    """CFG pack: 12 sequences of 2048 und + 1024 gen rows (T = 36864), positions restarting per
+    sequence; `attn` stands in for the attention output that feeds the routed O projection."""
+    s = CFG_PACK
+    t, h = s.T, s.H
+    mod, pos = cfg_pack_layout()
+    return {
+        "mod": mod.to(device), "pos": pos.to(device),
+        "x": bf16_normal_device(seed, 1, (t, h), device),
+        "res": bf16_normal_device(seed, 2, (t, h), device),
+        "attn": bf16_normal_device(seed, 3, (t, h), device),
+        "w_norm": bf16_normal_device(seed, 4, (2, h), device, mean=1.0, std=0.1),
+        "w_qkv": bf16_normal_device(seed, 5, (2, s.n_qkv, h), device, std=0.02),
+        "q_norm": bf16_normal_device(seed, 6, (2, s.D), device, mean=1.0, std=0.1),
+        "k_norm": bf16_normal_device(seed, 7, (2, s.D), device, mean=1.0, std=0.1),
+        "w_o": bf16_normal_device(seed, 8, (2, h, h), device, std=0.02),
+    }

@@ -161,6 +161,12 @@ def test_routed_gemm_order_flags_checked(lib):
     assert lib.mot_routed_gemm(A, A, 8, 256, 64, 0x2 | 0x100, B, 1 << 20, C, None) == MOT_ERR_ARG
 
 
+def test_selftest_rejects(lib):
+    assert lib.mot_selftest_wait_timeout(None, 64, None) == MOT_ERR_NULL
+    assert lib.mot_selftest_wait_timeout(MIS, 64, None) == MOT_ERR_ALIGN
+    assert lib.mot_selftest_wait_timeout(A, 8, None) == MOT_ERR_WORKSPACE
+
+
 def test_interleave_and_status_reject(lib):
     assert lib.mot_swiglu_interleave(A, A, 100, 64, B, None) == MOT_ERR_GEOMETRY
     assert lib.mot_swiglu_interleave(None, A, 128, 64, B, None) == MOT_ERR_NULL

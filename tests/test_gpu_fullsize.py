@@ -1,0 +1,101 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py times.
+
+Same inputs (workloads.mlp_device_inputs / cfg_pack_device_inputs) and the same sequence of
+entry points as the secondary workloads of bench.py. Each stage is checked on outputs the
+oracle can compute one by one, with the previous stage's GPU output as its input:
+  - add-RMSNorm on sampled rows, bit for bit against the fp32 emulator;
+  - routed GEMMs on sampled rows x sampled columns, against the fp64 golden within the
+    tolerance (max |diff| <= 2e-2, or half a bf16 step where |value| >= 8; rel-L2 <= 4e-3);
+  - the QK-norm + RoPE epilogue on sampled whole rows, bit for bit against the emulator fed
+    the GPU's own cast GEMM output.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_transformers_token_gb300 as mot
+from mixture_transformers_token_gb300 import workloads as W
+from oracle import mot_oracle as O
+
+from _util import assert_bitwise, assert_tolerance, f64, need_gpu, np_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _plan_positions(mod: np.ndarray) -> np.ndarray:
+    """Position of every row in plan order (und rows ascending, then gen rows)."""
+    perm = np.concatenate([np.nonzero(mod == 0)[0], np.nonzero(mod == 1)[0]])
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(len(perm))
+    return inv
+
+
+def test_swiglu_mlp_T8192_sampled():
+    need_gpu()
+    dev = torch.device("cuda")
+    m = W.mlp_device_inputs(dev)
+    t, h, i = W.MLP_T, W.MLP_H, W.MLP_I
+    w_gu = mot.mot_swiglu_interleave(m["w_gate"], m["w_up"])
+    ws = torch.empty(mot.mot_workspace_bytes(t), dtype=torch.uint8, device=dev)
+    y, ro = mot.mot_fused_add_rmsnorm(m["x"], m["res"], m["w_norm"], m["mod"], 1e-6, ws=ws)
+    y_plan = mot.mot_gather_rows(y, ws)
+    hid = mot.mot_routed_gemm(y_plan, w_gu, ws, mot.EPI_SWIGLU | mot.A_PLAN_ORDER | mot.OUT_PLAN_ORDER)
+    out = mot.mot_routed_gemm(hid, m["w_down"], ws, mot.EPI_CAST | mot.A_PLAN_ORDER)
+    assert mot.mot_device_status(ws) == 0
+
+    mod = m["mod"].cpu().numpy()
+    rng = W.rng_for(41, 1)
+    rows = np.sort(np.concatenate([rng.choice(np.nonzero(mod == 0)[0], 12, replace=False),
+                                   rng.choice(np.nonzero(mod == 1)[0], 12, replace=False)]))
+    inv = _plan_positions(mod)
+    r_t = torch.from_numpy(rows).to(dev)
+    p_t = torch.from_numpy(inv[rows]).to(dev)
+
+    e = O.e_fused_add_rmsnorm(f64(m["x"][r_t]), f64(m["res"][r_t]), f64(m["w_norm"]), mod[rows], 1e-6)
+    assert_bitwise(y[r_t], np_bits(e["y"]), "add-RMSNorm y (sampled rows)")
+    assert_bitwise(ro[r_t], np_bits(e["res_out"]), "add-RMSNorm res_out (sampled rows)")
+    assert_bitwise(y_plan[p_t], y[r_t], "rows in plan order")
+
+    cols = torch.from_numpy(np.sort(rng.choice(i, 128, replace=False))).to(dev)
+    g = O.g_routed_swiglu(f64(y[r_t]), f64(m["w_gate"][:, cols, :]), f64(m["w_up"][:, cols, :]), mod[rows])
+    assert_tolerance(f64(hid[p_t][:, cols]), g["h_pre"], "gate/up + SwiGLU (sampled rows x columns)")
+
+    ocols = torch.from_numpy(np.sort(rng.choice(h, 128, replace=False))).to(dev)
+    ref = O.g_routed_gemm_cast(f64(hid[p_t]), f64(m["w_down"][:, ocols, :]), mod[rows])
+    assert_tolerance(f64(out[r_t][:, ocols]), ref["out_pre"], "down projection (sampled rows x columns)")
+
+
+def test_cfg_pack_T36864_sampled():
+    need_gpu()
+    dev = torch.device("cuda")
+    s = W.CFG_PACK
+    c = W.cfg_pack_device_inputs(dev)
+    cs = mot.mot_rope_table_fill_host(s.theta, s.D, 3072).to(dev)
+    ws = torch.empty(mot.mot_workspace_bytes(s.T), dtype=torch.uint8, device=dev)
+    y, ro = mot.mot_fused_add_rmsnorm(c["x"], c["res"], c["w_norm"], c["mod"], s.eps, ws=ws)
+    qkv = mot.mot_routed_qkv_norm_rope(y, c["w_qkv"], c["q_norm"], c["k_norm"], c["pos"], cs, s.Hq, s.Hkv, s.D,
+                                       s.eps, ws)
+    o = mot.mot_routed_gemm(c["attn"], c["w_o"], ws, mot.EPI_CAST)
+    q = mot.mot_routed_gemm(y, c["w_qkv"], ws, mot.EPI_CAST)       # the unfused GEMM output
+    assert mot.mot_device_status(ws) == 0
+
+    mod = c["mod"].cpu().numpy()
+    pos = c["pos"].cpu().numpy()
+    rng = W.rng_for(42, 1)
+    rows = np.unique(np.concatenate([[0, 2047, 2048, 3071, 3072, s.T - 1], rng.choice(s.T, 18, replace=False)]))
+    r_t = torch.from_numpy(rows).to(dev)
+
+    e = O.e_fused_add_rmsnorm(f64(c["x"][r_t]), f64(c["res"][r_t]), f64(c["w_norm"]), mod[rows], s.eps)
+    assert_bitwise(y[r_t], np_bits(e["y"]), "add-RMSNorm y (sampled rows)")
+
+    acc = O.g_routed_matmul(f64(y[r_t]), f64(c["w_qkv"]), mod[rows])
+    assert_tolerance(f64(q[r_t]), acc, "routed QKV GEMM (bf16 cast, sampled rows)")
+    cc, ss = O.rope_cos_sin(s.theta, s.D, pos[rows])
+    e_out = O.e_qk_norm_rope(f64(q[r_t]), f64(c["q_norm"]), f64(c["k_norm"]), cc, ss, mod[rows], s.Hq, s.Hkv, s.D,
+                             s.eps)
+    assert_bitwise(qkv[r_t], np_bits(e_out), "QK-norm + RoPE epilogue (sampled rows)")
+
+    ocols = torch.from_numpy(np.sort(rng.choice(s.H, 128, replace=False))).to(dev)
+    ref = O.g_routed_gemm_cast(f64(c["attn"][r_t]), f64(c["w_o"][:, ocols, :]), mod[rows])
+    assert_tolerance(f64(o[r_t][:, ocols]), ref["out_pre"], "routed O projection (sampled rows x columns)")

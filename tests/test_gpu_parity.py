@@ -6,10 +6,12 @@
   - the routed GEMMs are compared with G within the tolerance (bit for bit on integer-valued
     inputs, where every sum is exact), and their epilogues bit for bit with E fed the GPU's own
     bf16 GEMM output ("fused equals unfused").
-Tolerance on bf16 outputs: max |diff| <= 2e-2 and relative L2 <= 4e-3 against G's value
-before its final cast. Sizes span several tiles and a ragged tail; the full-size cases check
+Tolerance on bf16 outputs: max |diff| <= 2e-2 (or half a bf16 step where |value| >= 8, as no bf16
+number lies closer) and relative L2 <= 4e-3 against G's value before its final cast. Sizes span several tiles and a ragged tail; the full-size cases check
 sampled rows against G (rows are independent) and every row against E.
 """
+
+import time
 
 import numpy as np
 import pytest
@@ -19,7 +21,7 @@ import mixture_transformers_token_gb300 as mot
 from mixture_transformers_token_gb300 import workloads as W
 from oracle import mot_oracle as O
 
-from _util import assert_bitwise, assert_tolerance, decode_plan, f64, need_gpu, np_bits
+from _util import allowed_abs, assert_bitwise, assert_tolerance, decode_plan, f64, need_gpu, np_bits
 
 pytestmark = pytest.mark.gpu
 EPS = 1e-6
@@ -174,6 +176,25 @@ def test_routed_gemm_cast_tolerance(T, K, N, p_gen, seed):
     assert_tolerance(f64(out), g["out_pre"], "routed GEMM vs G")
 
 
+def test_bounded_wait_times_out_and_context_stays_usable():
+    # a wait that nothing satisfies gives up after about a second and reports a device error
+    ws = torch.zeros(mot.mot_workspace_bytes(64), dtype=torch.uint8, device="cuda")
+    t0 = time.time()
+    mot.mot_selftest_wait_timeout(ws)
+    flags = mot.mot_device_status(ws)
+    dt = time.time() - t0
+    assert flags & mot.DEV_TIMEOUT
+    assert 0.5 < dt < 30.0
+    # the context is still usable: a routed GEMM runs and is exact on integer inputs
+    a = W.bf16_integers(W.rng_for(5, 90), (64, 128), -1, 1)
+    w = W.bf16_integers(W.rng_for(5, 91), (2, 256, 128), -1, 1)
+    mod = W.modality_bernoulli(W.rng_for(5, 92), 64)
+    ws2 = mot.mot_route_plan(mod.cuda())
+    out = mot.mot_routed_gemm(a.cuda(), w.cuda(), ws2, mot.EPI_CAST)
+    assert mot.mot_device_status(ws2) == 0
+    assert_bitwise(out, np_bits(O.g_routed_gemm_cast(f64(a), f64(w), mod.numpy())["out"]), "GEMM after a timeout")
+
+
 def test_routed_gemm_plan_mismatch_fails_closed():
     a = W.bf16_normal(W.rng_for(1, 67), (100, 128)).cuda()
     w = W.bf16_normal(W.rng_for(1, 68), (2, 256, 128)).cuda()
@@ -298,7 +319,7 @@ def _check_end_to_end(out, g, q_gpu, u_e, acc_abs, shape, what):
     allowed = 0.5 * _bf16_step(q_gpu) + 2.0 * K * 2.0 ** -24 * acc_abs
     assert np.all(gemm_err <= allowed), f"{what}: GEMM output outside half a step plus the accumulation bound"
     flips = q_gpu != g["q"]
-    bad = np.argwhere(d > 2e-2)
+    bad = np.argwhere(d > allowed_abs(ref))
     unexplained = []
     for r, c in bad:
         h, i = divmod(int(c), D)
