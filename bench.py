@@ -48,7 +48,7 @@ def norm_bytes(t: int, h: int) -> int:
 
 # DRAM traffic of one QKV kernel launch from an ncu capture of this workload, keyed by the
 # hash of the kernel source it was taken on (null once the kernel has changed).
-NCU_TRAFFIC = {"b2d0b5f87d477e24": 119274496}   # profiles/routed_gemm_qkv128_bagel_layer_T4096.md
+NCU_TRAFFIC = {"8ca99383883bd4a3": 122876416}   # profiles/routed_gemm_qkv128_bagel_layer_T4096.md
 
 
 def src_hash(name: str) -> str:
@@ -567,10 +567,26 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=512)
     ap.add_argument("--secondary", dest="secondary", action="store_true", default=True)
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
+    ap.add_argument("--profile", choices=["mlp", "cfg"], default=None,
+                    help="run only one secondary workload (2 warm-up + 5 timed steps) and print its figures; "
+                         "a short command for profiler captures")
     ap.add_argument("--cpu-baseline-child", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_baseline_child is not None:
         cpu_baseline_child(args.cpu_baseline_child)
+        return
+    if args.profile is not None:
+        import torch
+
+        import mixture_transformers_token_gb300 as mot
+        from mixture_transformers_token_gb300 import build as mot_build
+
+        mot_build.build()
+        mot.load_library()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        fn = run_mlp if args.profile == "mlp" else run_cfg_pack
+        print(json.dumps({args.profile: fn(dev, L2Flush(dev))}), flush=True)
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
