@@ -164,7 +164,8 @@ class L2Flush:
 
 def time_stages(stages, steps: int, warmup: int, flush, stream) -> dict:
     """Runs the list of (name, fn) as one step `warmup + steps` times with an L2 flush before
-    every step; returns the mean device time of each stage and of the step, in seconds."""
+    every step; returns the mean device time of each stage and of the step, in seconds, and
+    under "dist" their median, 10th and 90th percentiles in microseconds."""
     import torch
 
     for _ in range(warmup):
@@ -182,9 +183,86 @@ def time_stages(stages, steps: int, warmup: int, flush, stream) -> dict:
             fn()
             ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
-    out = {name: statistics.fmean(e[j].elapsed_time(e[j + 1]) for e in ev) / 1e3 for j, (name, _) in enumerate(stages)}
-    out["step"] = statistics.fmean(e[0].elapsed_time(e[-1]) for e in ev) / 1e3
+    samples = {name: [e[j].elapsed_time(e[j + 1]) / 1e3 for e in ev] for j, (name, _) in enumerate(stages)}
+    samples["step"] = [e[0].elapsed_time(e[-1]) / 1e3 for e in ev]
+    out = {name: statistics.fmean(v) for name, v in samples.items()}
+    out["dist"] = {name: percentiles_us(v) for name, v in samples.items()}
     return out
+
+
+def percentiles_us(seconds: list) -> dict:
+    v = sorted(seconds)
+
+    def q(f):  # nearest-rank percentile
+        return round(v[min(len(v) - 1, max(0, int(round(f * (len(v) - 1)))))] * 1e6, 2)
+
+    return {"median": q(0.5), "p10": q(0.1), "p90": q(0.9)}
+
+
+def time_warm(fn, iters: int, stream) -> float:
+    """Mean device time of `fn` run back to back with no flush (inputs left in L2 by the
+    previous call), in seconds."""
+    import torch
+
+    for _ in range(3):
+        fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / iters
+
+
+def _cmd(argv: list) -> str | None:
+    try:
+        r = subprocess.run(argv, capture_output=True, text=True, timeout=20)
+        return r.stdout.strip() if r.returncode == 0 else None
+    except (OSError, subprocess.SubprocessError):
+        return None
+
+
+def provenance(dev) -> dict:
+    """Where the numbers came from: source revision, toolchain, device and the peak figures."""
+    import torch
+
+    commit = _cmd(["git", "-C", ROOT, "rev-parse", "HEAD"])
+    dirty = None
+    if commit is not None:
+        st = _cmd(["git", "-C", ROOT, "status", "--porcelain", "--untracked-files=no"])
+        dirty = None if st is None else bool(st)
+    nvcc = _cmd(["nvcc", "--version"])
+    props = torch.cuda.get_device_properties(dev)
+    return {
+        "git_commit": commit, "git_dirty": dirty,
+        "kernel_src": {n: src_hash(n) for n in ("mot_gemm.cu", "mot_route_norm.cu", "mot_misc.cu")},
+        "nvcc": nvcc.splitlines()[-1] if nvcc else None,
+        "driver": _cmd(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader", "-i",
+                        str(dev.index or 0)]),
+        "torch": torch.__version__, "torch_cuda": torch.version.cuda,
+        "gpu": props.name, "sm_count": props.multi_processor_count, "cc": f"{props.major}.{props.minor}",
+        "l2_bytes": props.L2_cache_size, "peaks": peaks(),
+    }
+
+
+def host_cpu() -> dict:
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    if model is None:
+        out = _cmd(["lscpu"])
+        for line in (out or "").splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    return {"model": model, "affinity_cores": len(os.sched_getaffinity(0))}
 
 
 # ---------------------------------------------------------------------------
@@ -249,6 +327,7 @@ def run_ours(args, rank, world, local_rank):
     step_s, qkv_s, norm_s = reduce_max([times["step"], times["qkv_norm_rope"], times["add_rmsnorm_and_route_plan"]],
                                        world, dev)
 
+    warm_qkv = time_warm(qkv, 50, stream)
     e2e = run_e2e(args, shape, d, cs, ws, dev, world)
     secondary = None
     if rank == 0 and args.secondary:
@@ -289,11 +368,16 @@ def run_ours(args, rank, world, local_rank):
                           "frac": round(norm_gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"],
                           "algorithmic": "8*T*H + 4*H + T bytes per launch"},
         "kernels_us": {"add_rmsnorm_and_route_plan": round(norm_s * 1e6, 2), "qkv_norm_rope": round(qkv_s * 1e6, 2)},
+        "distribution_us": times["dist"],
+        "l2_warm": {"qkv_norm_rope_us": round(warm_qkv * 1e6, 2),
+                    "qkv_tflops": round(QKV_FLOPS / warm_qkv / 1e12, 2),
+                    "note": "QKV launches back to back with no flush (L2-warm), rank 0; not the headline"},
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "wall_s_timed_loop": round(wall, 3),
         "kernel_src": h,
+        "provenance": provenance(dev),
     }
     if secondary is not None:
         res["secondary"] = secondary
@@ -402,7 +486,7 @@ def run_mlp(dev, flush) -> dict:
                                                        | mot.OUT_PLAN_ORDER, out=hid)),
         ("down", lambda: mot.mot_routed_gemm(hid, w_down, ws, mot.EPI_CAST | mot.A_PLAN_ORDER, out=out)),
     ]
-    r = time_stages(stages, 5, 2, flush, stream)
+    r = time_stages(stages, 50, 5, flush, stream)
     if mot.mot_device_status(ws) != 0:
         raise RuntimeError("device error flags set in the MLP workload")
     pk = peaks()
@@ -454,7 +538,7 @@ def run_cfg_pack(dev, flush) -> dict:
                                                                out=qkv)),
         ("o_proj", lambda: mot.mot_routed_gemm(attn, w_o, ws, mot.EPI_CAST, out=o)),
     ]
-    r = time_stages(stages, 5, 2, flush, stream)
+    r = time_stages(stages, 50, 5, flush, stream)
     if mot.mot_device_status(ws) != 0:
         raise RuntimeError("device error flags set in the CFG-pack workload")
     pk = peaks()
@@ -523,6 +607,7 @@ def cpu_baseline(rows: int) -> dict:
     d = json.loads(r.stdout.strip().splitlines()[-1])
     flops = QKV_FLOPS * d["rows"] / T
     return {"value": round(flops / d["seconds"] / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "host": host_cpu(),
             "sample": f"{d['rows']} of {T} rows of the same pack (fp64 golden: add-RMSNorm + routed QKV + QK-norm "
                       f"+ RoPE), {d['seconds']:.1f} s single-threaded; rows are independent, so the rate scales"}
 
@@ -551,7 +636,7 @@ def run_reference(args, rank, world) -> dict | None:
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "step": "oracle fp64 golden on a row sample, scaled to the full pack"},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": int(threads) if threads.isdigit()
-                             else threads, "kind": "oracle",
+                             else threads, "kind": "oracle", "host": host_cpu(),
                              "sample": f"{rows_per_step} random rows of {T} per step, scaled to the pack"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -568,7 +653,7 @@ def main():
     ap.add_argument("--secondary", dest="secondary", action="store_true", default=True)
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--profile", choices=["mlp", "cfg"], default=None,
-                    help="run only one secondary workload (2 warm-up + 5 timed steps) and print its figures; "
+                    help="run only one secondary workload (5 warm-up + 50 timed steps) and print its figures; "
                          "a short command for profiler captures")
     ap.add_argument("--cpu-baseline-child", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
