@@ -149,20 +149,28 @@ def rope_inv_freq(theta: float, D: int) -> np.ndarray:
     return np.power(float(theta), -2.0 * i / D).astype(F32)
 
 
-def rope_cos_sin(theta: float, D: int, pos) -> tuple[np.ndarray, np.ndarray]:
-    """bf16 cos/sin of the angle pos * inv_i, for each position and i < D/2.
+def rope_cos_sin_f32(theta: float, D: int, pos) -> tuple[np.ndarray, np.ndarray]:
+    """fp32 cos/sin of the angle pos * inv_i, for each position and i < D/2.
 
     The angle is the fp32 product of the position and inv_i; cos and sin are evaluated
-    in fp64 of that fp32 angle, stored in fp32, and cast to bf16 at the RoPE boundary
-    ([RFC-435] §2 Reference hazards: "QK norm runs in FP32, then RoPE and Q/K in BF16").
-    Returns float64 arrays [len(pos)][D/2] holding bf16 values.
+    in fp64 of that fp32 angle and stored in fp32 ([RFC-435] §3 BAGEL-specific rules:
+    tables built in FP64, stored in FP32). Returns float64 arrays [len(pos)][D/2] holding
+    fp32 values.
     """
     inv = rope_inv_freq(theta, D)
     ang = np.asarray(pos).astype(F32)[:, None] * inv[None, :]
     ang64 = ang.astype(np.float64)
-    c = bf16(np.cos(ang64).astype(F32))
-    s = bf16(np.sin(ang64).astype(F32))
-    return c, s
+    return np.cos(ang64).astype(F32).astype(np.float64), np.sin(ang64).astype(F32).astype(np.float64)
+
+
+def rope_cos_sin(theta: float, D: int, pos) -> tuple[np.ndarray, np.ndarray]:
+    """bf16 cos/sin for the BF16 RoPE profile: the fp32 table values of rope_cos_sin_f32,
+    cast to bf16 at the RoPE boundary ([RFC-435] §2 Reference hazards: "QK norm runs in
+    FP32, then RoPE and Q/K in BF16"). Returns float64 arrays [len(pos)][D/2] holding bf16
+    values.
+    """
+    c, s = rope_cos_sin_f32(theta, D, pos)
+    return bf16(c), bf16(s)
 
 
 def g_rope_bf16(u, c, s):
@@ -182,6 +190,22 @@ def g_rope_bf16(u, c, s):
     return bf16(pre), pre
 
 
+def g_rope_f32(u, c, s):
+    """RoPE of the FP32 profile on a head u[..., D]: the rotation of g_rope_bf16 (same
+    half-split pairing and direction) evaluated exactly on the unrounded normalized head
+    and the fp32 table values, then one bf16 cast.
+
+    [RFC-435] open question 4 (keep the reference BF16 RoPE, or define an FP32 profile):
+    the FP32 profile rotates the fp32 normalized q/k and casts once.
+      out_i = bf16( u_i * c_i' + partner_i * s_i' ),  i' = i mod D/2
+    Returns (out, pre) with pre the value before the cast.
+    """
+    h = u.shape[-1] // 2
+    u1, u2 = u[..., :h], u[..., h:]
+    pre = np.concatenate([u1 * c - u2 * s, u2 * c + u1 * s], axis=-1)
+    return bf16(pre), pre
+
+
 def g_rope_exact(u, pos, theta: float, D: int):
     """Cast-free RoPE in fp64 (same pairing and direction as g_rope_bf16).
 
@@ -196,23 +220,34 @@ def g_rope_exact(u, pos, theta: float, D: int):
     return np.concatenate([u1 * c - u2 * s, u2 * c + u1 * s], axis=-1)
 
 
-def g_qk_norm_rope(q, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta):
-    """Per-head QK RMSNorm and BF16 RoPE on the bf16 GEMM output q (fp64 statistics).
+ROPE_PROFILES = ("bf16", "fp32")
+
+
+def g_qk_norm_rope(q, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta, rope_profile: str = "bf16"):
+    """Per-head QK RMSNorm and RoPE on the bf16 GEMM output q (fp64 statistics).
 
     [RFC-435] §2 Reference hazards: QK norm in FP32 (here fp64), then RoPE and Q/K in BF16.
-      Q, K heads:  u = bf16(q * rstd_head * g[mod]),  rstd_head = 1/sqrt(sum q^2 / D + eps)
-                   out = RoPE_bf16(u, cos, sin of pos)
+      Q, K heads:  rstd_head = 1/sqrt(sum q^2 / D + eps)
+                   BF16 profile (the reference):  u = bf16(q * rstd_head * g[mod]),
+                                                  out = RoPE_bf16(u, bf16 cos, sin of pos)
+                   FP32 profile ([RFC-435] open question 4):  u = q * rstd_head * g[mod],
+                                                  out = bf16(rotation of u by the fp32 cos, sin)
       V heads:     out = q
     The per-head norm weight g is q_norm or k_norm, [2][D], one vector per expert shared by
     all heads of that kind. Returns out, out_pre (value before the final cast) and u, the
     normalized heads [T][Hq+Hkv][D].
     """
+    if rope_profile not in ROPE_PROFILES:
+        raise ValueError(f"rope_profile must be one of {ROPE_PROFILES}")
     mod = _check_mod(mod)
     eps = _eps32(eps)
     q = np.asarray(q, np.float64)
     out = q.copy()
     out_pre = q.copy()
-    c, s = rope_cos_sin(theta, D, pos)
+    if rope_profile == "bf16":
+        c, s = rope_cos_sin(theta, D, pos)
+    else:
+        c, s = rope_cos_sin_f32(theta, D, pos)
     q_norm = np.asarray(q_norm, np.float64)
     k_norm = np.asarray(k_norm, np.float64)
     us = np.zeros((q.shape[0], Hq + Hkv, D))
@@ -222,22 +257,26 @@ def g_qk_norm_rope(q, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta):
         qh = q[:, cols]
         ms = np.sum(qh * qh, axis=1) / D
         rstd = 1.0 / np.sqrt(ms + eps)
-        u = bf16(qh * rstd[:, None] * g[mod])
-        o, pre = g_rope_bf16(u, c, s)
+        if rope_profile == "bf16":
+            u = bf16(qh * rstd[:, None] * g[mod])
+            o, pre = g_rope_bf16(u, c, s)
+        else:
+            u = qh * rstd[:, None] * g[mod]
+            o, pre = g_rope_f32(u, c, s)
         out[:, cols] = o
         out_pre[:, cols] = pre
         us[:, h] = u
     return {"out": out, "out_pre": out_pre, "u": us}
 
 
-def g_qkv_norm_rope(y, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta):
+def g_qkv_norm_rope(y, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta, rope_profile: str = "bf16"):
     """Routed QKV projection, per-head QK RMSNorm in fp32, RoPE and Q/K in BF16.
 
     [PR-1402] "What does this PR do?": MoT dual-branch routed Q/K/V projections with
     fused qkv_proj_{und,gen} weights, per-head QK RMSNorm and packed RoPE.
       acc  = routed(y, w_qkv) (+ b_qkv[mod] if given)       columns ordered q, k, v heads
       q    = bf16(acc)                                      (GEMM output boundary)
-      out  = g_qk_norm_rope(q)
+      out  = g_qk_norm_rope(q)                              (BF16 or FP32 RoPE profile)
     For V columns the value before the final cast is acc itself. Returns out, out_pre, q,
     acc and u (the normalized Q/K heads).
     """
@@ -246,7 +285,7 @@ def g_qkv_norm_rope(y, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, 
     if b_qkv is not None:
         acc = acc + np.asarray(b_qkv, np.float64)[mod]
     q = bf16(acc)
-    r = g_qk_norm_rope(q, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta)
+    r = g_qk_norm_rope(q, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta, rope_profile)
     out_pre = r["out_pre"]
     v0 = (Hq + Hkv) * D
     out_pre[:, v0:] = acc[:, v0:]
@@ -271,10 +310,11 @@ def g_routed_swiglu(a, w_gate, w_up, mod):
     return g_swiglu(g_routed_matmul(a, w_gate, mod), g_routed_matmul(a, w_up, mod))
 
 
-def g_layer(x, res, w_norm, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta):
+def g_layer(x, res, w_norm, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta,
+            rope_profile: str = "bf16"):
     """The whole projection step: fused add-RMSNorm, then the routed QKV with norm and RoPE."""
     n = g_fused_add_rmsnorm(x, res, w_norm, mod, eps)
-    r = g_qkv_norm_rope(n["y"], w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta)
+    r = g_qkv_norm_rope(n["y"], w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, eps, theta, rope_profile)
     r.update({"y": n["y"], "y_pre": n["y_pre"], "res_out": n["res_out"]})
     return r
 
@@ -353,13 +393,30 @@ def e_rope_bf16(u, c, s):
     return np.concatenate([o1, o2], axis=-1)
 
 
-def e_qk_norm_rope(q, q_norm, k_norm, cos, sin, mod, Hq, Hkv, D, eps, return_stats: bool = False):
-    """Teacher-forced epilogue check: per-head QK RMSNorm and BF16 RoPE on a given q.
-
-    q is the bf16 GEMM output (float values), [T][(Hq+2Hkv)*D]; cos and sin are the bf16
-    table rows of each token's position, [T][D/2]. Q and K heads become
-    RoPE_bf16(bf16((q * rstd) * g[mod])); V heads pass through unchanged.
+def e_rope_f32(u, c, s):
+    """fp32 restatement of g_rope_f32: each product and the sum rounded to fp32 (no fused
+    multiply-add), then one bf16 cast.
+      out_i = bf16( fp32( fp32(u_i * c) + fp32(partner_i * s) ) )
     """
+    h = u.shape[-1] // 2
+    u1, u2 = u[..., :h], u[..., h:]
+    o1 = bf16_f32((u1 * c) + (-u2 * s))
+    o2 = bf16_f32((u2 * c) + (u1 * s))
+    return np.concatenate([o1, o2], axis=-1)
+
+
+def e_qk_norm_rope(q, q_norm, k_norm, cos, sin, mod, Hq, Hkv, D, eps, return_stats: bool = False,
+                   rope_profile: str = "bf16"):
+    """Teacher-forced epilogue check: per-head QK RMSNorm and RoPE on a given q.
+
+    q is the bf16 GEMM output (float values), [T][(Hq+2Hkv)*D]; cos and sin are the table
+    rows of each token's position, [T][D/2] (bf16 values for the BF16 profile, fp32 values
+    for the FP32 profile). Q and K heads become RoPE_bf16(bf16((q * rstd) * g[mod])) in the
+    BF16 profile and e_rope_f32((q * rstd) * g[mod]) in the FP32 profile; V heads pass
+    through unchanged.
+    """
+    if rope_profile not in ROPE_PROFILES:
+        raise ValueError(f"rope_profile must be one of {ROPE_PROFILES}")
     mod = _check_mod(mod)
     q32 = np.asarray(q, np.float64).astype(F32)
     c32 = np.asarray(cos, np.float64).astype(F32)
@@ -374,8 +431,12 @@ def e_qk_norm_rope(q, q_norm, k_norm, cos, sin, mod, Hq, Hkv, D, eps, return_sta
         cols = slice(h * D, (h + 1) * D)
         qh = q32[:, cols]
         rstd, ss = e_head_rstd(qh, eps)
-        u = bf16_f32((qh * rstd[:, None]) * g[mod])
-        out[:, cols] = e_rope_bf16(u, c32, s32)
+        if rope_profile == "bf16":
+            u = bf16_f32((qh * rstd[:, None]) * g[mod])
+            out[:, cols] = e_rope_bf16(u, c32, s32)
+        else:
+            u = (qh * rstd[:, None]) * g[mod]
+            out[:, cols] = e_rope_f32(u, c32, s32)
         stats.append(ss)
         us[:, h] = u
     if return_stats:

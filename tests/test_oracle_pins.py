@@ -230,8 +230,9 @@ def _onehot_qkv(c_q, c_k, Hq, Hkv, D):
     return y, w
 
 
+@pytest.mark.parametrize("profile", ["bf16", "fp32"])
 @pytest.mark.parametrize("c_q,c_k", [(1.5, -3.0), (2.0 ** -10, -(2.0 ** -11))])
-def test_qk_norm_constant_head_closed_form_at_position_zero(c_q, c_k):
+def test_qk_norm_constant_head_closed_form_at_position_zero(c_q, c_k, profile):
     # A head of equal values c normalizes to g * c / sqrt(c^2 + eps); small c makes eps visible.
     Hq, Hkv, D = 2, 1, 128
     eps = float(F32(1e-6))
@@ -239,9 +240,10 @@ def test_qk_norm_constant_head_closed_form_at_position_zero(c_q, c_k):
     qn = np.stack([np.full(D, 0.75), np.full(D, 1.25)])
     kn = np.stack([np.full(D, 1.5), np.full(D, 0.5)])
     mod = np.array([0, 1])
-    g = O.g_qkv_norm_rope(y, w, None, qn, kn, np.array([0, 0]), mod, Hq, Hkv, D, 1e-6, 1e6)
-    c, s = O.rope_cos_sin(1e6, D, np.array([0, 0]))
-    e_out = O.e_qk_norm_rope(g["q"], qn, kn, c, s, mod, Hq, Hkv, D, 1e-6)
+    g = O.g_qkv_norm_rope(y, w, None, qn, kn, np.array([0, 0]), mod, Hq, Hkv, D, 1e-6, 1e6, rope_profile=profile)
+    table = O.rope_cos_sin if profile == "bf16" else O.rope_cos_sin_f32
+    c, s = table(1e6, D, np.array([0, 0]))
+    e_out = O.e_qk_norm_rope(g["q"], qn, kn, c, s, mod, Hq, Hkv, D, 1e-6, rope_profile=profile)
     for r, e in ((0, 0), (1, 1)):
         qv = O.bf16(qn[e, 0] * c_q / math.sqrt(c_q * c_q + eps))
         kv = O.bf16(kn[e, 0] * c_k / math.sqrt(c_k * c_k + eps))
@@ -375,6 +377,137 @@ def test_e_qk_epilogue_matches_g_on_same_q():
 # ---------------------------------------------------------------------------
 # SwiGLU
 # ---------------------------------------------------------------------------
+
+# ---------------------------------------------------------------------------
+# FP32 RoPE profile
+# ---------------------------------------------------------------------------
+
+def test_rope_f32_table_hand_values():
+    gd = GOLDEN["rope_fp32"]
+    c, s = O.rope_cos_sin_f32(1e6, 128, np.array([0, 1]))
+    assert np.all(c[0] == 1.0) and np.all(s[0] == 0.0)
+    assert c[1, 0] == _hex(gd["pos1_i0_cos"]) and s[1, 0] == _hex(gd["pos1_i0_sin"])
+    # the angle is the fp32 product of the position and the fp32 frequency
+    a = gd["angle_case"]
+    assert O.rope_inv_freq(a["theta"], a["D"])[1] == _hex(a["inv_1"])
+    _, s3 = O.rope_cos_sin_f32(a["theta"], a["D"], np.array([a["pos"]]))
+    assert s3[0, 1] == _hex(a["sin_1"])
+
+
+def test_rope_f32_single_cast_and_fp32_sum_hand_values():
+    # G rounds the exact rotation once; E rounds the fp32 sum, which lands on a bf16 tie.
+    gd = GOLDEN["rope_fp32"]
+    D = 4
+    u = np.array([[_hex(gd["u_i"]), 0.0, _hex(gd["u_partner"]), 0.0]])
+    c = np.ones((1, D // 2))
+    s = np.ones((1, D // 2))
+    out, pre = O.g_rope_f32(u, c, s)
+    assert out[0, 0] == _hex(gd["exact_profile_out"]) and out[0, 2] == _hex(gd["partner_out"])
+    assert out[0, 1] == 0.0 and out[0, 3] == 0.0
+    e = O.e_rope_f32(u.astype(F32), c.astype(F32), s.astype(F32))
+    assert e[0, 0] == _hex(gd["fp32_sum_out"]) and e[0, 2] == _hex(gd["partner_out"])
+
+
+def _table_bound(u, pos, theta, D):
+    """Bound on |rotation with the fp32 table - exact rotation| per element: the fp32 angle
+    (two roundings of pos * theta^(-2i/D), relative 2^-23 together) and the fp32 rounding
+    of cos and sin (2^-24 each), times |u_i| + |u_partner|."""
+    h = D // 2
+    i = np.arange(h)
+    ang = np.asarray(pos, np.float64)[:, None] * np.power(float(theta), -2.0 * i / D)[None, :]
+    per = 1.01 * ang * 2.0 ** -23 + 2.0 ** -23
+    mag = np.abs(u[..., :h]) + np.abs(u[..., h:])
+    b = mag * per
+    return np.concatenate([b, b], axis=-1)
+
+
+def _complex_rotation(u, pos, theta, D):
+    h = D // 2
+    i = np.arange(h)
+    z = (u[:, :h] + 1j * u[:, h:]) * np.exp(1j * np.asarray(pos)[:, None] * theta ** (-2.0 * i / D))
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def test_rope_f32_is_rotation_within_table_error():
+    rng = np.random.default_rng(36)
+    D, theta = 128, 1e6
+    u = rng.standard_normal((64, D))
+    pos = rng.integers(0, 4096, 64)
+    c, s = O.rope_cos_sin_f32(theta, D, pos)
+    out, pre = O.g_rope_f32(u, c, s)
+    exact = _complex_rotation(u, pos, theta, D)
+    assert np.all(np.abs(pre - exact) <= _table_bound(u, pos, theta, D) + 1e-15)
+    h = D // 2
+    np.testing.assert_allclose(pre[:, :h] ** 2 + pre[:, h:] ** 2, u[:, :h] ** 2 + u[:, h:] ** 2, rtol=2.0 ** -21)
+
+
+def _half_step(v):
+    _, ex = np.frexp(np.maximum(np.abs(v), 2.0 ** -126))
+    return np.ldexp(1.0, ex - 9)
+
+
+@pytest.mark.parametrize("c_q,c_k", [(1.5, -3.0), (0.25, 7.0)])
+def test_rope_f32_profile_on_constant_heads_is_one_rounding(c_q, c_k):
+    # A constant head c normalizes to g * c / sqrt(c^2 + eps) (closed form); the FP32
+    # profile then rotates it with the fp32 table and rounds once, so every output lies
+    # within half a bf16 step (plus the table error) of the exact rotation of that closed
+    # form. The BF16 profile rounds u, both products and the sum, and misses this bound.
+    Hq, Hkv, D, theta = 2, 1, 128, 1e6
+    eps = float(F32(1e-6))
+    y, w = _onehot_qkv(c_q, c_k, Hq, Hkv, D)
+    rng = np.random.default_rng(37)
+    qn = O.bf16(1 + 0.2 * rng.standard_normal((2, D)))
+    kn = O.bf16(1 + 0.2 * rng.standard_normal((2, D)))
+    mod = np.array([0, 1])
+    pos = np.array([1234, 3001])
+    outs = {}
+    for profile in ("fp32", "bf16"):
+        outs[profile] = O.g_qkv_norm_rope(y, w, None, qn, kn, pos, mod, Hq, Hkv, D, 1e-6, theta,
+                                          rope_profile=profile)["out"]
+    c32, s32 = O.rope_cos_sin_f32(theta, D, pos)
+    e32 = O.e_qk_norm_rope(O.bf16(np.einsum("tk,tnk->tn", y, w[mod])), qn, kn, c32, s32, mod, Hq, Hkv, D, 1e-6,
+                           rope_profile="fp32")
+    miss_bf16 = 0
+    for h in range(Hq + Hkv):
+        cv = c_q if h < Hq else c_k
+        g = (qn if h < Hq else kn)[mod]
+        u = g * (cv / math.sqrt(cv * cv + eps))
+        exact = _complex_rotation(u, pos, theta, D)
+        bound = _half_step(exact) + _table_bound(u, pos, theta, D) + 1e-12
+        cols = slice(h * D, (h + 1) * D)
+        assert np.all(np.abs(outs["fp32"][:, cols] - exact) <= bound)
+        # E: fp32 u, products and sum add a few fp32 roundings before the one cast
+        e_bound = bound + 8 * 2.0 ** -24 * (np.abs(u) + np.abs(np.roll(u, D // 2, axis=1)))
+        e_diff = np.abs(e32[:, cols] - exact)
+        assert np.all((e_diff <= e_bound) | (e_diff <= 2 * _half_step(exact)))
+        miss_bf16 += int(np.sum(np.abs(outs["bf16"][:, cols] - exact) > bound))
+    assert miss_bf16 > 0
+
+
+def test_e_qk_epilogue_fp32_profile_matches_g_on_same_q():
+    rng = np.random.default_rng(38)
+    Hq, Hkv, D, T = 4, 2, 64, 40
+    N = (Hq + 2 * Hkv) * D
+    y = O.bf16(rng.standard_normal((T, 256)))
+    w = O.bf16(0.02 * rng.standard_normal((2, N, 256)))
+    qn = O.bf16(1 + 0.1 * rng.standard_normal((2, D)))
+    kn = O.bf16(1 + 0.1 * rng.standard_normal((2, D)))
+    mod = rng.integers(0, 2, T)
+    pos = rng.integers(0, 4096, T)
+    g = O.g_qkv_norm_rope(y, w, None, qn, kn, pos, mod, Hq, Hkv, D, 1e-6, 1e6, rope_profile="fp32")
+    c, s = O.rope_cos_sin_f32(1e6, D, pos)
+    e = O.e_qk_norm_rope(g["q"], qn, kn, c, s, mod, Hq, Hkv, D, 1e-6, rope_profile="fp32")
+    # same q in: one cast on each side, so they differ by at most one step, rarely
+    _, ex = np.frexp(np.maximum(np.abs(g["out"]), 2.0 ** -100))
+    step = np.ldexp(1.0, ex - 8)
+    diff = np.abs(e - g["out"])
+    assert np.all(diff <= step)
+    assert np.mean(diff > 0) < 0.01
+    # the two profiles are different fingerprints of the same rotation
+    gb = O.g_qkv_norm_rope(y, w, None, qn, kn, pos, mod, Hq, Hkv, D, 1e-6, 1e6)
+    assert np.any(gb["out"] != g["out"])
+    assert np.max(np.abs(gb["out"] - g["out"])) < 0.1
+
 
 def test_swiglu_hand_values():
     for c in GOLDEN["swiglu"]["cases"]:
