@@ -331,7 +331,8 @@ def run_ours(args, rank, world, local_rank):
     e2e = run_e2e(args, shape, d, cs, ws, dev, world)
     secondary = None
     if rank == 0 and args.secondary:
-        secondary = {"swiglu_mlp_T8192": run_mlp(dev, flush), "cfg_pack_T36864": run_cfg_pack(dev, flush)}
+        secondary = {"swiglu_mlp_T8192": run_mlp(dev, flush), "cfg_pack_T36864": run_cfg_pack(dev, flush),
+                     "fp32_rope_profile_T4096": run_qkv_fp32_rope(dev, flush)}
     if world > 1:
         dist.barrier()
     if rank != 0:
@@ -512,6 +513,33 @@ def run_mlp(dev, flush) -> dict:
     return result
 
 
+def run_qkv_fp32_rope(dev, flush) -> dict:
+    """The FP32 RoPE profile of the QKV projection on the bench workload (T = 4096): add-RMSNorm
+    (+ plan) once, then the routed QKV with QK-norm and RoPE in fp32 (fp32 table, one cast)."""
+    import torch
+
+    import mixture_transformers_token_gb300 as mot
+    from mixture_transformers_token_gb300 import workloads as W
+
+    stream = torch.cuda.current_stream(dev)
+    shape, inp = W.bagel_layer(seed=1, T=T)
+    d = {k: v.to(dev) for k, v in inp.items() if isinstance(v, torch.Tensor)}
+    cs32 = mot.mot_rope_table_fill_host_fp32(shape.theta, D, T).to(dev)
+    ws = torch.empty(mot.mot_workspace_bytes(T), dtype=torch.uint8, device=dev)
+    y, ro = mot.mot_fused_add_rmsnorm(d["x"], d["res"], d["w_norm"], d["mod"], shape.eps, ws=ws)
+    out = torch.empty((T, N_QKV), dtype=torch.bfloat16, device=dev)
+    stages = [("qkv_fp32_rope", lambda: mot.mot_routed_qkv_norm_rope_fp32(
+        y, d["w_qkv"], d["q_norm"], d["k_norm"], d["pos"], cs32, HQ, HKV, D, shape.eps, ws, out=out))]
+    r = time_stages(stages, 200, 5, flush, stream)
+    if mot.mot_device_status(ws) != 0:
+        raise RuntimeError("device error flags set in the FP32 RoPE workload")
+    pk = peaks()
+    return {"workload": WORKLOAD, "qkv_fp32_rope_us": round(r["qkv_fp32_rope"] * 1e6, 2),
+            "qkv_fp32_rope_tflops": _tflops(QKV_FLOPS, r["qkv_fp32_rope"]),
+            "qkv_fp32_rope_frac": round(QKV_FLOPS / r["qkv_fp32_rope"] / 1e12 / pk["bf16_tflops"], 4),
+            "distribution_us": r["dist"]["qkv_fp32_rope"]}
+
+
 def run_cfg_pack(dev, flush) -> dict:
     """CFG pack: 12 sequences of 2048 und + 1024 gen rows (T = 36864), positions restarting per
     sequence: add-RMSNorm (+ plan), routed QKV + QK-norm + RoPE, routed O projection 3584 -> 3584
@@ -652,9 +680,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=512)
     ap.add_argument("--secondary", dest="secondary", action="store_true", default=True)
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
-    ap.add_argument("--profile", choices=["mlp", "cfg"], default=None,
-                    help="run only one secondary workload (5 warm-up + 50 timed steps) and print its figures; "
-                         "a short command for profiler captures")
+    ap.add_argument("--profile", choices=["mlp", "cfg", "qkv_fp32"], default=None,
+                    help="run only one secondary workload (mlp, cfg: 5 warm-up + 50 timed steps; qkv_fp32: "
+                         "5 + 200) and print its figures; a short command for profiler captures")
     ap.add_argument("--cpu-baseline-child", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_baseline_child is not None:
@@ -670,7 +698,7 @@ def main():
         mot.load_library()
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        fn = run_mlp if args.profile == "mlp" else run_cfg_pack
+        fn = {"mlp": run_mlp, "cfg": run_cfg_pack, "qkv_fp32": run_qkv_fp32_rope}[args.profile]
         print(json.dumps({args.profile: fn(dev, L2Flush(dev))}), flush=True)
         return
     if args.warmup < 3:

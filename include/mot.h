@@ -159,6 +159,22 @@ int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv, const mot
                              void* ws, size_t ws_bytes, mot_bf16* qkv_out, void* stream);
 
 /*
+ * mot_routed_qkv_norm_rope_fp32 -- the same projection with the FP32 RoPE profile
+ * ([RFC-435] open question 4: keep the reference BF16 RoPE or define an FP32 profile; §3: a
+ * profile change is a new numeric fingerprint). Arguments as mot_routed_qkv_norm_rope except
+ *   rope_cs_f32  [P][D/2][2] fp32   (cos, sin) table, see mot_rope_table_fill_host_fp32.
+ * Per Q/K head: u = (q * rstd) * g[e] in fp32 without a cast, then
+ * out_i = bf16(fp32(u_i c) + fp32(partner_i s)): both products and the sum rounded to fp32,
+ * one bf16 cast. q = bf16(acc + b), the statistics and V heads are those of the BF16 profile.
+ * Errors and ownership as mot_routed_qkv_norm_rope; rope_cs_f32 must be 16-byte aligned.
+ */
+int mot_routed_qkv_norm_rope_fp32(const mot_bf16* x, const mot_bf16* w_qkv, const mot_bf16* b_qkv,
+                                  const mot_bf16* q_norm_w, const mot_bf16* k_norm_w,
+                                  const int32_t* pos, const float* rope_cs_f32, int P,
+                                  int64_t T, int H, int Hq, int Hkv, int D, float eps,
+                                  void* ws, size_t ws_bytes, mot_bf16* qkv_out, void* stream);
+
+/*
  * mot_routed_gemm -- routed dense projection for the O, gate/up and down projections
  * ([RFC-435] §5 mot_routed_gemm and mot_swiglu_mlp; [PR-503] grouped expert GEMM commit:
  * one writer per row, grouped result equal to the per-expert GEMM).
@@ -232,6 +248,15 @@ int mot_swiglu_interleave(const mot_bf16* w_gate, const mot_bf16* w_up, int I, i
  * Geometry: D even, 2 <= D <= 1024; 1 <= P <= MOT_MAX_TOKENS; theta > 1.
  */
 int mot_rope_table_fill_host(double theta, int D, int P, mot_bf16* host_cs);
+
+/*
+ * mot_rope_table_fill_host_fp32 -- the fp32 table of the FP32 RoPE profile: the same fp32
+ * values as mot_rope_table_fill_host before its bf16 cast ([RFC-435] §3: tables built in
+ * FP64, stored in FP32).
+ *   host_cs  host array of P * D/2 * 2 floats, entry [p][i] = (cos, sin).
+ * Geometry and errors as mot_rope_table_fill_host.
+ */
+int mot_rope_table_fill_host_fp32(double theta, int D, int P, float* host_cs);
 
 /*
  * mot_selftest_wait_timeout -- exercises the bounded wait that every pipeline wait of the

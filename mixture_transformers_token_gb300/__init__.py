@@ -23,6 +23,7 @@ __all__ = [
     "mot_abi_version", "mot_status_string", "mot_workspace_bytes", "mot_route_plan",
     "mot_fused_add_rmsnorm", "mot_routed_qkv_norm_rope", "mot_routed_gemm",
     "mot_swiglu_interleave", "mot_rope_table_fill_host", "mot_device_status", "mot_routed_gemm_noalloc",
+    "mot_routed_qkv_norm_rope_fp32", "mot_rope_table_fill_host_fp32",
     "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows", "mot_selftest_wait_timeout",
 ]
 
@@ -54,12 +55,15 @@ _SIGNATURES = {
     "mot_fused_add_rmsnorm": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i, _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "mot_routed_qkv_norm_rope": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i64, _c_i, _c_i, _c_i,
                                         _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_routed_qkv_norm_rope_fp32": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i64, _c_i, _c_i,
+                                             _c_i, _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_noalloc": (_c_i, [_c_p, _c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_p, _c_p]),
     "mot_swiglu_interleave": (_c_i, [_c_p, _c_p, _c_i, _c_i, _c_p, _c_p]),
     "mot_gather_rows": (_c_i, [_c_p, _c_i64, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_selftest_wait_timeout": (_c_i, [_c_p, _c_sz, _c_p]),
     "mot_rope_table_fill_host": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
+    "mot_rope_table_fill_host_fp32": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
 }
 
@@ -176,7 +180,9 @@ def mot_fused_add_rmsnorm(x, res, w, mod, eps: float, y=None, res_out=None, ws=N
 
 def mot_routed_qkv_norm_rope(x, w_qkv, q_norm_w, k_norm_w, pos, rope_cs, Hq: int, Hkv: int, D: int, eps: float,
                              ws, b_qkv=None, out=None, stream=None):
-    """Routed QKV GEMM + per-head QK RMSNorm + BF16 RoPE; `ws` must hold the plan for T rows."""
+    """Routed QKV GEMM + per-head QK RMSNorm + RoPE; `ws` must hold the plan for T rows.
+    A bf16 `rope_cs` selects the BF16 RoPE profile (mot_routed_qkv_norm_rope), an fp32 one
+    the FP32 profile (mot_routed_qkv_norm_rope_fp32)."""
     T, H = x.shape
     N = (Hq + 2 * Hkv) * D
     _dev(x, "x", torch.bfloat16, 2)
@@ -184,7 +190,8 @@ def mot_routed_qkv_norm_rope(x, w_qkv, q_norm_w, k_norm_w, pos, rope_cs, Hq: int
     _dev(q_norm_w, "q_norm_w", torch.bfloat16, 2)
     _dev(k_norm_w, "k_norm_w", torch.bfloat16, 2)
     _dev(pos, "pos", torch.int32, 1)
-    _dev(rope_cs, "rope_cs", torch.bfloat16, 3)
+    fp32 = rope_cs.dtype == torch.float32
+    _dev(rope_cs, "rope_cs", torch.float32 if fp32 else torch.bfloat16, 3)
     _dev(ws, "ws", torch.uint8, 1)
     if tuple(w_qkv.shape) != (2, N, H):
         raise ValueError(f"w_qkv must be [2, {N}, {H}]")
@@ -200,11 +207,21 @@ def mot_routed_qkv_norm_rope(x, w_qkv, q_norm_w, k_norm_w, pos, rope_cs, Hq: int
     if out is None:
         out = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
     _dev(out, "out", torch.bfloat16, 2)
-    _check("mot_routed_qkv_norm_rope", _lib().mot_routed_qkv_norm_rope(
+    name = "mot_routed_qkv_norm_rope_fp32" if fp32 else "mot_routed_qkv_norm_rope"
+    _check(name, getattr(_lib(), name)(
         x.data_ptr(), w_qkv.data_ptr(), bp, q_norm_w.data_ptr(), k_norm_w.data_ptr(), pos.data_ptr(),
         rope_cs.data_ptr(), rope_cs.shape[0], T, H, Hq, Hkv, D, eps, ws.data_ptr(), ws.numel(), out.data_ptr(),
         _stream(x, stream)))
     return out
+
+
+def mot_routed_qkv_norm_rope_fp32(x, w_qkv, q_norm_w, k_norm_w, pos, rope_cs_f32, Hq: int, Hkv: int, D: int,
+                                  eps: float, ws, b_qkv=None, out=None, stream=None):
+    """The FP32 RoPE profile of mot_routed_qkv_norm_rope; `rope_cs_f32` is the fp32 table."""
+    if rope_cs_f32.dtype != torch.float32:
+        raise TypeError("rope_cs_f32 must be float32 (mot_rope_table_fill_host_fp32)")
+    return mot_routed_qkv_norm_rope(x, w_qkv, q_norm_w, k_norm_w, pos, rope_cs_f32, Hq, Hkv, D, eps, ws,
+                                    b_qkv=b_qkv, out=out, stream=stream)
 
 
 def mot_routed_gemm(a, w, ws, epilogue: int = EPI_CAST, out=None, stream=None):
@@ -283,6 +300,13 @@ def mot_rope_table_fill_host(theta: float, D: int, P: int) -> torch.Tensor:
     """Host (cos, sin) table [P][D/2][2] as a CPU bf16 tensor (copy it to the device once)."""
     t = torch.empty((P, D // 2, 2), dtype=torch.bfloat16)
     _check("mot_rope_table_fill_host", _lib().mot_rope_table_fill_host(theta, D, P, t.data_ptr()))
+    return t
+
+
+def mot_rope_table_fill_host_fp32(theta: float, D: int, P: int) -> torch.Tensor:
+    """Host fp32 (cos, sin) table [P][D/2][2] of the FP32 RoPE profile, as a CPU tensor."""
+    t = torch.empty((P, D // 2, 2), dtype=torch.float32)
+    _check("mot_rope_table_fill_host_fp32", _lib().mot_rope_table_fill_host_fp32(theta, D, P, t.data_ptr()))
     return t
 
 

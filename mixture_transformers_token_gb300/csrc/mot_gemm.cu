@@ -2,6 +2,8 @@
 //   cast          out = bf16(acc)                                  (O and down projections)
 //   SwiGLU        out = bf16(silu(bf16(acc_gate)) * bf16(acc_up))  (gate/up projection)
 //   QK-norm+RoPE  per-head fp32 RMSNorm, then BF16 RoPE           (fused QKV projection)
+//                 or, in the FP32 RoPE profile, RoPE in fp32 on the fp32 normalized head
+//                 with one bf16 cast (open question 4 of the roadmap below)
 //
 // Sources: [RFC][BAGEL-7B-MoT][CUDA/ROCm] WS1/WS2 kernel roadmap and integration plan #435
 // (§1 item 1: per-token weight sets; §2 Reference hazards: QK norm in FP32, then RoPE and Q/K
@@ -23,8 +25,9 @@
 //               CTA); in the leader CTA one thread issues tcgen05.mma.cta_group::2 (M 256,
 //               N 256, K 16), K blocks in ascending order, and multicasts its commits to both
 //               CTAs.
-//   warps 2-5   epilogue of each CTA: one thread per accumulator row (its TMEM lane), read with
-//               tcgen05.ld, written to the row's original position.
+//   warps 2-9   epilogue of each CTA: two warps per TMEM lane quarter, one per 128-column half;
+//               one thread per accumulator row (its TMEM lane), read with tcgen05.ld, written
+//               to the row's original position (or its plan position).
 // Every tile of every pack uses the same tile shape, K order and instruction sequence, so a
 // row's bits depend only on the row and its expert's weights.
 
@@ -55,7 +58,11 @@ constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 constexpr int NUM_BARS = 2 * STAGES + 5;
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256 + 1024;  // + QK-norm weights
 
-enum Epi { EPI_CAST = 0, EPI_SWIGLU = 1, EPI_QKV64 = 2, EPI_QKV128 = 3 };
+enum Epi { EPI_CAST = 0, EPI_SWIGLU = 1, EPI_QKV64 = 2, EPI_QKV128 = 3, EPI_QKV64_F32 = 4, EPI_QKV128_F32 = 5 };
+
+__host__ __device__ constexpr bool is_qkv(int epi) { return epi >= EPI_QKV64; }
+__host__ __device__ constexpr bool rope_f32(int epi) { return epi == EPI_QKV64_F32 || epi == EPI_QKV128_F32; }
+__host__ __device__ constexpr int head_dim(int epi) { return epi == EPI_QKV64 || epi == EPI_QKV64_F32 ? 64 : 128; }
 
 struct Args {
   const uint8_t* ws;  // routing plan
@@ -68,7 +75,8 @@ struct Args {
   const uint16_t* qn;    // [2][D]
   const uint16_t* kn;    // [2][D]
   const int32_t* pos;    // [T]
-  const uint16_t* cs;    // [P][D/2][2]
+  const uint16_t* cs;    // [P][D/2][2] bf16 (BF16 RoPE profile)
+  const float* cs32;     // [P][D/2][2] fp32 (FP32 RoPE profile)
   int P;
   int Hq, Hkv;
   float eps;
@@ -160,6 +168,18 @@ __device__ __forceinline__ void load_cs_row(const Args& a, bool valid, int grow,
   }
 }
 
+// The fp32 (cos, sin) row of the row's position (FP32 RoPE profile): D floats, pairs
+// (cos_i, sin_i). Read chunk by chunk in pass 2; the table stays in L2.
+template <int D>
+__device__ __forceinline__ const float4* cs32_row(const Args& a, bool valid, int grow) {
+  int p = valid ? a.pos[grow] : 0;
+  if (p < 0 || p >= a.P) {
+    atomicOr(a.err, MOT_DEV_BAD_POSITION);
+    p = 0;
+  }
+  return reinterpret_cast<const float4*>(a.cs32 + int64_t(p) * D);
+}
+
 // Adds the bias of columns [col, col + n) (n a multiple of 8) to v when a bias is given.
 template <int NV>
 __device__ __forceinline__ void add_bias(const Args& a, int e, int64_t col, float (&v)[NV]) {
@@ -177,14 +197,15 @@ __device__ __forceinline__ void add_bias(const Args& a, int e, int64_t col, floa
   }
 }
 
-// Per-head QK RMSNorm (fp32, fixed chunk tree) and BF16 RoPE on this warp's half of the tile;
+// Per-head QK RMSNorm (fp32, fixed chunk tree) and RoPE on this warp's half of the tile;
 // V heads pass through. gs: the norm weights in shared memory, [q / k][expert][D/2] words;
-// cw: the (cos, sin) words of the row's position. Pass 1 reads the head from TMEM for its sum
-// of squares; pass 2 reads it again, 16 columns of each rotation pair (i, i + D/2) at a time,
+// cw: the bf16 (cos, sin) words of the row's position (BF16 profile); crow: the fp32 table
+// row of the row's position (FP32 profile). Pass 1 reads the head from TMEM for its sum of
+// squares; pass 2 reads it again, 16 columns of each rotation pair (i, i + D/2) at a time,
 // and writes the outputs.
-template <int D>
+template <int D, bool F32>
 __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool valid, int grow, int e, int nt, int half,
-                                        const uint32_t* gs, const uint32_t (&cw)[D / 2]) {
+                                        const uint32_t* gs, const uint32_t (&cw)[D / 2], const float4* crow) {
   constexpr int HEADS = 128 / D;  // heads in this half
   constexpr int NP = D / 2;       // packed words per head
   uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * BN + half * 128;
@@ -228,6 +249,43 @@ __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool vali
     const float ms = __fdiv_rn(ss, float(D));
     const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
     const uint32_t* g = gs + (kind * 2 + e) * NP;
+    if constexpr (F32) {
+      // pass 2, FP32 profile: u = (q * rstd) * g in fp32, not rounded;
+      // out_i = bf16(u_i c + (-u_{i+D/2}) s), out_{i+D/2} = bf16(u_{i+D/2} c + u_i s), each
+      // product and the sum rounded to fp32, one cast
+#pragma unroll
+      for (int c = 0; c < NP / 16; ++c) {
+        float4 t[8];  // (cos, sin) of frequencies 16c + 2j and 16c + 2j + 1 in t[j]
+#pragma unroll
+        for (int j = 0; j < 8; ++j) t[j] = __ldg(crow + c * 8 + j);
+        float v1[16], v2[16];
+        tmem_ld16(taddr + col0 + c * 16, v1);
+        tmem_ld16(taddr + col0 + NP + c * 16, v2);
+        add_bias<16>(a, e, gcol0 + c * 16, v1);
+        add_bias<16>(a, e, gcol0 + NP + c * 16, v2);
+        uint32_t o1[8], o2[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int w = c * 8 + j;
+          const uint32_t q1 = pack_bf2(v1[2 * j], v1[2 * j + 1]);
+          const uint32_t q2 = pack_bf2(v2[2 * j], v2[2 * j + 1]);
+          const uint32_t g1 = g[w], g2 = g[NP / 2 + w];
+          const float u1a = __fmul_rn(__fmul_rn(bf_lo(q1), rstd), bf_lo(g1));
+          const float u1b = __fmul_rn(__fmul_rn(bf_hi(q1), rstd), bf_hi(g1));
+          const float u2a = __fmul_rn(__fmul_rn(bf_lo(q2), rstd), bf_lo(g2));
+          const float u2b = __fmul_rn(__fmul_rn(bf_hi(q2), rstd), bf_hi(g2));
+          o1[j] = pack_bf2(__fadd_rn(__fmul_rn(u1a, t[j].x), __fmul_rn(-u2a, t[j].y)),
+                           __fadd_rn(__fmul_rn(u1b, t[j].z), __fmul_rn(-u2b, t[j].w)));
+          o2[j] = pack_bf2(__fadd_rn(__fmul_rn(u2a, t[j].x), __fmul_rn(u1a, t[j].y)),
+                           __fadd_rn(__fmul_rn(u2b, t[j].z), __fmul_rn(u1b, t[j].w)));
+        }
+        if (valid) {
+          store_row_u4(ohead + c * 16, o1, 2);
+          store_row_u4(ohead + NP + c * 16, o2, 2);
+        }
+      }
+      continue;
+    }
     // pass 2: u = bf16((q * rstd) * g); out_i = bf16(bf16(u_i c) + bf16(-u_{i+D/2} s)),
     // out_{i+D/2} = bf16(bf16(u_{i+D/2} c) + bf16(u_i s)); two neighbouring i per word
 #pragma unroll
@@ -458,12 +516,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else {
     // ---------------- epilogue (both CTAs) ----------------
-    constexpr int D = EPI == EPI_QKV64 ? 64 : 128;
+    constexpr int D = head_dim(EPI);
     const int quarter = warp & 3;          // the TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;      // which 128 columns of the tile
     const int row_in_tile = quarter * 32 + lane;
     const int et = threadIdx.x - 64;       // 0 .. 255 among the epilogue threads
-    if constexpr (EPI == EPI_QKV64 || EPI == EPI_QKV128) {
+    if constexpr (is_qkv(EPI)) {
       // both experts' q and k norm weights, once per CTA
       for (int i = et; i < 2 * D; i += 32 * EPI_WARPS) {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(i < D ? args.qn : args.kn);
@@ -479,18 +537,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const bool valid = pt.has_rows && row_in_tile < tl.n_rows;
       const int grow = !valid ? 0 : (args.out_plan_order ? tl.list_begin + row_in_tile : perm[tl.list_begin + row_in_tile]);
       uint32_t cw[D / 2];
-      bool rope = false;
-      if constexpr (EPI == EPI_QKV64 || EPI == EPI_QKV128) {
-        rope = pt.nt * (BN / D) + half * (128 / D) < args.Hq + args.Hkv;  // this half holds a q or k head
-        if (rope) load_cs_row<D>(args, valid, grow, cw);
+      const float4* crow = nullptr;
+      if constexpr (is_qkv(EPI)) {
+        // this half holds a q or k head
+        if (pt.nt * (BN / D) + half * (128 / D) < args.Hq + args.Hkv) {
+          if constexpr (rope_f32(EPI))
+            crow = cs32_row<D>(args, valid, grow);
+          else
+            load_cs_row<D>(args, valid, grow, cw);
+        }
       }
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16);
       if constexpr (EPI == EPI_CAST) epi_cast(args, taddr, valid, grow, pt.nt, half);
       if constexpr (EPI == EPI_SWIGLU) epi_swiglu(args, taddr, valid, grow, pt.nt, half);
-      if constexpr (EPI == EPI_QKV64 || EPI == EPI_QKV128) epi_qkv<D>(args, taddr, valid, grow, pt.expert, pt.nt, half, gnorm, cw);
-      (void)rope;
+      if constexpr (is_qkv(EPI))
+        epi_qkv<D, rope_f32(EPI)>(args, taddr, valid, grow, pt.expert, pt.nt, half, gnorm, cw, crow);
       tc_fence_before();
       __syncwarp();
       // the accumulator's TMEM reads have completed (tcgen05.wait::ld), so a relaxed arrive suffices
@@ -556,11 +619,14 @@ static int launch(const void* a, const void* w, int T, int N, int K, const Args&
 
 using namespace mot;
 
-extern "C" int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv, const mot_bf16* b_qkv,
-                                        const mot_bf16* q_norm_w, const mot_bf16* k_norm_w, const int32_t* pos,
-                                        const mot_bf16* rope_cs, int P, int64_t T, int H, int Hq, int Hkv, int D,
-                                        float eps, void* ws, size_t ws_bytes, mot_bf16* qkv_out, void* stream) {
-  if (!x || !w_qkv || !q_norm_w || !k_norm_w || !pos || !rope_cs || !ws || !qkv_out) return MOT_ERR_NULL;
+// Shared by both RoPE profiles: validation, then one launch. table_bf16 / table_f32: the
+// (cos, sin) table of the profile (the other is null).
+static int routed_qkv_entry(const mot_bf16* x, const mot_bf16* w_qkv, const mot_bf16* b_qkv, const mot_bf16* q_norm_w,
+                            const mot_bf16* k_norm_w, const int32_t* pos, const mot_bf16* table_bf16,
+                            const float* table_f32, int P, int64_t T, int H, int Hq, int Hkv, int D, float eps,
+                            void* ws, size_t ws_bytes, mot_bf16* qkv_out, void* stream) {
+  const void* table = table_f32 ? static_cast<const void*>(table_f32) : static_cast<const void*>(table_bf16);
+  if (!x || !w_qkv || !q_norm_w || !k_norm_w || !pos || !table || !ws || !qkv_out) return MOT_ERR_NULL;
   if (T < 1 || T > MOT_MAX_TOKENS) return MOT_ERR_GEOMETRY;
   if (D != 64 && D != 128) return MOT_ERR_GEOMETRY;
   if (Hq < 1 || Hkv < 1 || Hq > 1024 || Hkv > 1024) return MOT_ERR_GEOMETRY;
@@ -570,11 +636,11 @@ extern "C" int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv
   if (P < 1 || P > MOT_MAX_TOKENS) return MOT_ERR_ARG;
   if (!(eps > 0.0f) || !(eps < 3.0e38f)) return MOT_ERR_ARG;
   if (!aligned16(x) || !aligned16(w_qkv) || (b_qkv && !aligned16(b_qkv)) || !aligned16(q_norm_w) ||
-      !aligned16(k_norm_w) || !aligned16(pos) || !aligned16(rope_cs) || !aligned16(ws) || !aligned16(qkv_out))
+      !aligned16(k_norm_w) || !aligned16(pos) || !aligned16(table) || !aligned16(ws) || !aligned16(qkv_out))
     return MOT_ERR_ALIGN;
   if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const void* ptrs[] = {x, w_qkv, b_qkv, q_norm_w, k_norm_w, pos, rope_cs, ws, qkv_out};
+  const void* ptrs[] = {x, w_qkv, b_qkv, q_norm_w, k_norm_w, pos, table, ws, qkv_out};
   int dev = -1;
   int st = check_device(s, ptrs, 9, &dev);
   if (st != MOT_OK) return st;
@@ -592,13 +658,37 @@ extern "C" int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv
   a.qn = q_norm_w;
   a.kn = k_norm_w;
   a.pos = pos;
-  a.cs = rope_cs;
+  a.cs = table_bf16;
+  a.cs32 = table_f32;
   a.P = P;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.eps = eps;
+  if (table_f32) {
+    if (D == 64) return gemm::launch<gemm::EPI_QKV64_F32>(x, w_qkv, int(T), int(N), H, a, dev, s);
+    return gemm::launch<gemm::EPI_QKV128_F32>(x, w_qkv, int(T), int(N), H, a, dev, s);
+  }
   if (D == 64) return gemm::launch<gemm::EPI_QKV64>(x, w_qkv, int(T), int(N), H, a, dev, s);
   return gemm::launch<gemm::EPI_QKV128>(x, w_qkv, int(T), int(N), H, a, dev, s);
+}
+
+extern "C" int mot_routed_qkv_norm_rope(const mot_bf16* x, const mot_bf16* w_qkv, const mot_bf16* b_qkv,
+                                        const mot_bf16* q_norm_w, const mot_bf16* k_norm_w, const int32_t* pos,
+                                        const mot_bf16* rope_cs, int P, int64_t T, int H, int Hq, int Hkv, int D,
+                                        float eps, void* ws, size_t ws_bytes, mot_bf16* qkv_out, void* stream) {
+  if (rope_cs == nullptr) return MOT_ERR_NULL;
+  return routed_qkv_entry(x, w_qkv, b_qkv, q_norm_w, k_norm_w, pos, rope_cs, nullptr, P, T, H, Hq, Hkv, D, eps, ws,
+                          ws_bytes, qkv_out, stream);
+}
+
+extern "C" int mot_routed_qkv_norm_rope_fp32(const mot_bf16* x, const mot_bf16* w_qkv, const mot_bf16* b_qkv,
+                                             const mot_bf16* q_norm_w, const mot_bf16* k_norm_w, const int32_t* pos,
+                                             const float* rope_cs_f32, int P, int64_t T, int H, int Hq, int Hkv,
+                                             int D, float eps, void* ws, size_t ws_bytes, mot_bf16* qkv_out,
+                                             void* stream) {
+  if (rope_cs_f32 == nullptr) return MOT_ERR_NULL;
+  return routed_qkv_entry(x, w_qkv, b_qkv, q_norm_w, k_norm_w, pos, nullptr, rope_cs_f32, P, T, H, Hq, Hkv, D, eps,
+                          ws, ws_bytes, qkv_out, stream);
 }
 
 extern "C" int mot_routed_gemm(const mot_bf16* a_in, const mot_bf16* w, int64_t T, int N, int K, int epilogue,

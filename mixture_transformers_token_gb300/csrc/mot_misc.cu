@@ -79,8 +79,10 @@ extern "C" size_t mot_workspace_bytes(int64_t T) {
   return size_t(plan_bytes(T));
 }
 
-extern "C" int mot_rope_table_fill_host(double theta, int D, int P, mot_bf16* host_cs) {
-  if (host_cs == nullptr) return MOT_ERR_NULL;
+// (cos_i, sin_i) of positions 0 .. P-1 in fp32: inv_i = theta^(-2i/D) in fp64 stored fp32,
+// angle = fp32(p) * inv_i in fp32, cos and sin in fp64 of that angle, stored fp32.
+template <typename Store>
+static int rope_table_fill(double theta, int D, int P, Store store) {
   if (D < 2 || D > 1024 || D % 2 != 0 || P < 1 || P > MOT_MAX_TOKENS) return MOT_ERR_GEOMETRY;
   if (!(theta > 1.0) || !std::isfinite(theta)) return MOT_ERR_ARG;
   const int half = D / 2;
@@ -90,13 +92,26 @@ extern "C" int mot_rope_table_fill_host(double theta, int D, int P, mot_bf16* ho
     const float fp = float(p);
     for (int i = 0; i < half; ++i) {
       const float ang = fp * inv[i];
-      const float c = float(std::cos(double(ang)));
-      const float s = float(std::sin(double(ang)));
-      host_cs[(int64_t(p) * half + i) * 2] = host_f32_to_bf16(c);
-      host_cs[(int64_t(p) * half + i) * 2 + 1] = host_f32_to_bf16(s);
+      store((int64_t(p) * half + i) * 2, float(std::cos(double(ang))), float(std::sin(double(ang))));
     }
   }
   return MOT_OK;
+}
+
+extern "C" int mot_rope_table_fill_host(double theta, int D, int P, mot_bf16* host_cs) {
+  if (host_cs == nullptr) return MOT_ERR_NULL;
+  return rope_table_fill(theta, D, P, [host_cs](int64_t k, float c, float s) {
+    host_cs[k] = host_f32_to_bf16(c);
+    host_cs[k + 1] = host_f32_to_bf16(s);
+  });
+}
+
+extern "C" int mot_rope_table_fill_host_fp32(double theta, int D, int P, float* host_cs) {
+  if (host_cs == nullptr) return MOT_ERR_NULL;
+  return rope_table_fill(theta, D, P, [host_cs](int64_t k, float c, float s) {
+    host_cs[k] = c;
+    host_cs[k + 1] = s;
+  });
 }
 
 extern "C" int mot_device_status(const void* ws, uint32_t* flags, void* stream) {

@@ -124,6 +124,25 @@ def test_qkv_rejects(lib):
     assert call(wsb=100) == MOT_ERR_WORKSPACE
 
 
+def test_qkv_fp32_profile_rejects(lib):
+    f = lib.mot_routed_qkv_norm_rope_fp32
+
+    def call(**kw):
+        a = dict(x=A, w=A, b=None, qn=A, kn=A, pos=A, cs=A, P=64, T=64, H=256, Hq=4, Hkv=2, D=64, eps=1e-6, ws=B,
+                 wsb=1 << 20, out=C)
+        a.update(kw)
+        return f(a["x"], a["w"], a["b"], a["qn"], a["kn"], a["pos"], a["cs"], a["P"], a["T"], a["H"], a["Hq"],
+                 a["Hkv"], a["D"], a["eps"], a["ws"], a["wsb"], a["out"], None)
+
+    assert call(cs=None) == MOT_ERR_NULL
+    assert call(cs=MIS) == MOT_ERR_ALIGN
+    assert call(D=32) == MOT_ERR_GEOMETRY
+    assert call(T=(1 << 24) + 1) == MOT_ERR_GEOMETRY
+    assert call(P=0) == MOT_ERR_ARG
+    assert call(eps=float("inf")) == MOT_ERR_ARG
+    assert call(wsb=16) == MOT_ERR_WORKSPACE
+
+
 def test_routed_gemm_rejects(lib):
     f = lib.mot_routed_gemm
     assert f(None, A, 8, 256, 64, 0, B, 1 << 20, C, None) == MOT_ERR_NULL
@@ -190,8 +209,24 @@ def test_rope_table_matches_oracle(D, P, theta):
     np.testing.assert_array_equal(got[:, :, 1], s)
 
 
+@pytest.mark.parametrize("D,P,theta", [(64, 64, 1e6), (128, 4096, 1e6), (128, 300, 1e4), (4, 8, 9.0)])
+def test_rope_table_fp32_matches_oracle(D, P, theta):
+    t = mot.mot_rope_table_fill_host_fp32(theta, D, P)
+    c, s = O.rope_cos_sin_f32(theta, D, np.arange(P))
+    got = t.numpy().astype(np.float64)
+    np.testing.assert_array_equal(got[:, :, 0], c)
+    np.testing.assert_array_equal(got[:, :, 1], s)
+    # the bf16 table is this table rounded to bf16
+    b = mot.mot_rope_table_fill_host(theta, D, P)
+    assert torch.equal(b, t.to(torch.bfloat16))
+
+
 def test_rope_table_rejects(lib):
     buf = (ctypes.c_uint16 * 16)()
     assert lib.mot_rope_table_fill_host(1e6, 3, 2, buf) == MOT_ERR_GEOMETRY
     assert lib.mot_rope_table_fill_host(0.5, 4, 2, buf) == MOT_ERR_ARG
     assert lib.mot_rope_table_fill_host(1e6, 4, 2, None) == MOT_ERR_NULL
+    fbuf = (ctypes.c_float * 16)()
+    assert lib.mot_rope_table_fill_host_fp32(1e6, 3, 2, fbuf) == MOT_ERR_GEOMETRY
+    assert lib.mot_rope_table_fill_host_fp32(float("nan"), 4, 2, fbuf) == MOT_ERR_ARG
+    assert lib.mot_rope_table_fill_host_fp32(1e6, 4, 2, None) == MOT_ERR_NULL

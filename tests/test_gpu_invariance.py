@@ -5,14 +5,16 @@ Motivation item 1 (a row's bytes must not depend on the modality mix of the pack
 Reference hazards (sequential, CFG-parallel, SP and step-batched paths pack rows differently);
 the sweep follows the methodology of [WS1][CUDA][Qwen3-Next] MoE route/combine contract #503
 (each item alone and inside sub-batches of 2, 7 and 64 at other offsets, and in a shuffled
-order) and compares raw bits (signed zero distinct).
+order) and compares raw bits (signed zero distinct). Both RoPE profiles of the QKV projection
+are swept.
 
 2048 reference rows of the tiny layer shape (hidden 256, 4 Q / 2 KV heads of 64), each with
 its own modality, position and data, are re-packed into packs of 8192 rows whose gen fraction
 is 0, 1/8, 1/4, 1/2, 3/4 or 1 (at 0 and 1 only the reference rows of that modality take
 part), with contiguous (und block then gen block) and interleaved routing and a shuffled
-order. Every reference row's outputs of all four entry points must be bit-identical to its
-outputs in the reference pack.
+order. Every reference row's outputs -- y and res_out of the norm, the QKV projection in both
+RoPE profiles, the cast and the SwiGLU GEMM -- must be bit-identical to its outputs in the
+reference pack.
 """
 
 import numpy as np
@@ -48,6 +50,7 @@ def setup():
         "k_norm": W.bf16_normal(W.rng_for(21, 8), (2, D), mean=1.0, std=0.1).to(dev),
         "w_o": W.bf16_normal(W.rng_for(21, 9), (2, 512, H), std=0.02).to(dev),
         "cs": mot.mot_rope_table_fill_host(THETA, D, P).to(dev),
+        "cs32": mot.mot_rope_table_fill_host_fp32(THETA, D, P).to(dev),
     }
     weights["w_gu"] = mot.mot_swiglu_interleave(W.bf16_normal(W.rng_for(21, 10), (2, 256, H), std=0.02).to(dev),
                                                 W.bf16_normal(W.rng_for(21, 11), (2, 256, H), std=0.02).to(dev))
@@ -61,10 +64,13 @@ def run_pack(pack, wt):
     ws = mot.mot_route_plan(mod)
     y, ro = mot.mot_fused_add_rmsnorm(x, res, wt["w_norm"], mod, EPS, ws=ws)
     qkv = mot.mot_routed_qkv_norm_rope(y, wt["w_qkv"], wt["q_norm"], wt["k_norm"], pos, wt["cs"], HQ, HKV, D, EPS, ws)
+    qkv32 = mot.mot_routed_qkv_norm_rope_fp32(y, wt["w_qkv"], wt["q_norm"], wt["k_norm"], pos, wt["cs32"], HQ, HKV, D,
+                                              EPS, ws)
     o = mot.mot_routed_gemm(y, wt["w_o"], ws, mot.EPI_CAST)
     h = mot.mot_routed_gemm(y, wt["w_gu"], ws, mot.EPI_SWIGLU)
     assert mot.mot_device_status(ws) == 0
-    return {k: bits(v) for k, v in (("y", y), ("res_out", ro), ("qkv", qkv), ("o", o), ("h", h))}
+    return {k: bits(v) for k, v in (("y", y), ("res_out", ro), ("qkv", qkv), ("qkv_fp32_rope", qkv32), ("o", o),
+                                    ("h", h))}
 
 
 def build_pack(ref, sel, slots, T, filler_mod, seed):
