@@ -323,18 +323,37 @@ def g_layer(x, res, w_norm, w_qkv, b_qkv, q_norm, k_norm, pos, mod, Hq, Hkv, D, 
 # E: fp32 contract emulator
 # ---------------------------------------------------------------------------
 
+def e_row_tree_sum(terms):
+    """Row sums of fp32 terms [T][H] over the fixed 32-wide chunked tree of the add-RMSNorm.
+
+    ([PR-503] zero-centred RMSNorm commit, "On exactness against vLLM": the fixed 32-wide
+    chunked sum is what buys batch invariance), defined here as:
+      lane l in [0, 32) owns columns 256*j + 8*l + t, j = 0 .. H/256-1, t = 0 .. 7;
+      p_l = sequential fp32 sum of its terms from 0.0, j outer, t inner;
+      the 32 partials combine by an xor butterfly with offsets 16, 8, 4, 2, 1,
+      each step p_l <- p_l + p_(l xor off)  (every lane ends with the same value).
+    Returns (sums [T], lane partials after the butterfly [T][32]).
+    """
+    terms = np.asarray(terms, F32)
+    T, H = terms.shape
+    if H % 256:
+        raise ValueError("the reduction tree is defined for H a multiple of 256")
+    lanes = np.arange(32)
+    p = np.zeros((T, 32), F32)
+    for j in range(H // 256):
+        for t in range(8):
+            p = p + terms[:, 256 * j + 8 * lanes + t]
+    for off in (16, 8, 4, 2, 1):
+        p = p + p[:, lanes ^ off]
+    return p[:, 0], p
+
+
 def e_fused_add_rmsnorm(x, res, w, mod, eps, return_stats: bool = False):
     """fp32 restatement of the fused add-RMSNorm with its fixed reduction tree.
 
-    The reduction is a fixed 32-wide chunked sum ([PR-503] zero-centred RMSNorm commit,
-    "On exactness against vLLM": the fixed 32-wide chunked sum is what buys batch
-    invariance), defined here as:
-      lane l in [0, 32) owns columns 256*j + 8*l + t, j = 0 .. H/256-1, t = 0 .. 7;
-      p_l = sequential fp32 sum of s^2 from 0.0, j outer, t inner;
-      the 32 partials combine by an xor butterfly with offsets 16, 8, 4, 2, 1,
-      each step p_l <- p_l + p_(l xor off)  (every lane ends with the same value).
-    Then ms = p / H (IEEE division), rstd = 1 / sqrt(ms + eps) (IEEE sqrt and division),
-    y = bf16((s * rstd) * w[mod]) left to right, each operation rounded on its own.
+    The sum of s^2 runs over e_row_tree_sum's fixed tree. Then ms = p / H (IEEE division),
+    rstd = 1 / sqrt(ms + eps) (IEEE sqrt and division), y = bf16((s * rstd) * w[mod]) left
+    to right, each operation rounded on its own.
     """
     mod = _check_mod(mod)
     x32 = np.asarray(x, np.float64).astype(F32)
@@ -344,15 +363,7 @@ def e_fused_add_rmsnorm(x, res, w, mod, eps, return_stats: bool = False):
     if H % 256:
         raise ValueError("the reduction tree is defined for H a multiple of 256")
     s = bf16_f32(x32 + r32)
-    lanes = np.arange(32)
-    p = np.zeros((T, 32), F32)
-    for j in range(H // 256):
-        for t in range(8):
-            v = s[:, 256 * j + 8 * lanes + t]
-            p = p + v * v
-    for off in (16, 8, 4, 2, 1):
-        p = p + p[:, lanes ^ off]
-    ss = p[:, 0]
+    ss, p = e_row_tree_sum(s * s)
     ms = ss / F32(H)
     rstd = F32(1.0) / np.sqrt(ms + F32(eps))
     y = bf16_f32((s * rstd[:, None]) * w32[mod])
@@ -454,3 +465,122 @@ def e_swiglu(g, u):
     u32 = np.asarray(u, np.float64).astype(F32)
     silu = g32 / (F32(1.0) + np.exp(-g32))
     return bf16_f32(silu * u32)
+
+
+# ---------------------------------------------------------------------------
+# Backward of the routed projection path
+# ---------------------------------------------------------------------------
+#
+# [RFC-435] §3 BAGEL-specific rules: phase A trains only the gen expert, but the frozen und
+# operators still need dX for marker rows, so dX runs through both weight sets while the
+# weight gradient is needed for the gen set. [PR-503] gated-norm commit: the backward is
+# assembled from deterministic pieces -- a dx kernel and a weight gradient taken as per-row
+# fp32 partials folded in ascending row order. The cast of a forward output to bf16 is
+# treated as the identity when differentiating (its gradient is the incoming gradient).
+
+def g_routed_gemm_dx(dout, w, mod):
+    """Input gradient of the routed GEMM out = a W[mod]^T, in float64, then one bf16 cast.
+
+      dA[r, k] = sum_n dout[r, n] * w[mod[r], n, k]
+    Both weight sets take part (each row through its own). Returns dx and dx_pre.
+    """
+    mod = _check_mod(mod)
+    dout = np.asarray(dout, np.float64)
+    w = np.asarray(w, np.float64)
+    acc = np.zeros((dout.shape[0], w.shape[2]), np.float64)
+    for e in (0, 1):
+        rows = np.nonzero(mod == e)[0]
+        if rows.size:
+            acc[rows] = dout[rows] @ w[e]
+    return {"dx": bf16(acc), "dx_pre": acc}
+
+
+def g_routed_gemm_dw(dout, a, mod, expert: int):
+    """Weight gradient of one weight set of the routed GEMM, in float64 (no cast).
+
+      dW[n, k] = sum over rows r with mod[r] = expert of dout[r, n] * a[r, k]
+    Rows of the other weight set do not contribute.
+    """
+    mod = _check_mod(mod)
+    dout = np.asarray(dout, np.float64)
+    a = np.asarray(a, np.float64)
+    rows = np.nonzero(mod == expert)[0]
+    return dout[rows].T @ a[rows]
+
+
+def g_add_rmsnorm_backward(dy, s, w, mod, eps, d_res_out=None):
+    """Gradient of the fused add-RMSNorm, in float64.
+
+    Forward (g_fused_add_rmsnorm): s = bf16(x + res), rstd = 1/sqrt(mean(s^2) + eps),
+    y_pre = s * rstd * w[mod]. With xh = s * rstd and g = dy * w[mod]:
+      ds  = rstd * (g - xh * mean(g * xh))  (+ d_res_out, the gradient reaching res_out)
+      dx  = dres = bf16(ds)                 (s = x + res passes ds to both inputs)
+      dw[e, j] = sum over rows r with mod[r] = e of dy[r, j] * xh[r, j]
+    Returns dx, dx_pre, dw [2][H] and rstd.
+    """
+    mod = _check_mod(mod)
+    dy = np.asarray(dy, np.float64)
+    s = np.asarray(s, np.float64)
+    w = np.asarray(w, np.float64)
+    H = s.shape[1]
+    rstd = 1.0 / np.sqrt(np.sum(s * s, axis=1) / H + _eps32(eps))
+    xh = s * rstd[:, None]
+    g = dy * w[mod]
+    c = np.sum(g * xh, axis=1) / H
+    ds = rstd[:, None] * (g - xh * c[:, None])
+    if d_res_out is not None:
+        ds = ds + np.asarray(d_res_out, np.float64)
+    dw = np.zeros((2, H))
+    for e in (0, 1):
+        rows = np.nonzero(mod == e)[0]
+        dw[e] = np.sum(dy[rows] * xh[rows], axis=0)
+    return {"dx": bf16(ds), "dx_pre": ds, "dw": dw, "rstd": rstd}
+
+
+def e_left_fold_rows(partials, mod, expert: int):
+    """Ascending-row fp32 left fold of per-row partials [T][H] over the rows of one weight
+    set ([PR-503] gated-norm commit: per-row fp32 dweight rows, then an ascending-row fp32
+    left fold): ((p_r0 + p_r1) + p_r2) + ... for r0 < r1 < r2 < ... with mod[r] = expert.
+    The fold starts from the first row's partial; no rows give zeros.
+    """
+    mod = _check_mod(mod)
+    partials = np.asarray(partials, F32)
+    rows = np.nonzero(mod == expert)[0]
+    if rows.size == 0:
+        return np.zeros(partials.shape[1], F32)
+    acc = partials[rows[0]].copy()
+    for r in rows[1:]:
+        acc = acc + partials[r]
+    return acc
+
+
+def e_add_rmsnorm_backward(dy, s, w, mod, eps, d_res_out=None):
+    """fp32 restatement of g_add_rmsnorm_backward, every operation rounded on its own.
+
+      rstd   as in the forward (e_row_tree_sum of s^2, IEEE division and square root)
+      xh_j   = s_j * rstd
+      g_j    = dy_j * w[mod]_j
+      dot    = e_row_tree_sum of g_j * xh_j      (the forward's fixed tree)
+      c      = dot / H
+      ds_j   = rstd * (g_j - xh_j * c)           (+ d_res_out_j)
+      dx_j   = bf16(ds_j)
+      p_r[j] = dy_j * xh_j,  dw[e] = e_left_fold_rows(p, mod, e)
+    Returns dx, dw [2][H] (fp32), rstd and dot.
+    """
+    mod = _check_mod(mod)
+    dy32 = np.asarray(dy, np.float64).astype(F32)
+    s32 = np.asarray(s, np.float64).astype(F32)
+    w32 = np.asarray(w, np.float64).astype(F32)
+    T, H = s32.shape
+    ss, _ = e_row_tree_sum(s32 * s32)
+    rstd = F32(1.0) / np.sqrt(ss / F32(H) + F32(eps))
+    xh = s32 * rstd[:, None]
+    g = dy32 * w32[mod]
+    dot, _ = e_row_tree_sum(g * xh)
+    c = dot / F32(H)
+    ds = rstd[:, None] * (g - xh * c[:, None])
+    if d_res_out is not None:
+        ds = ds + np.asarray(d_res_out, np.float64).astype(F32)
+    p = dy32 * xh
+    dw = np.stack([e_left_fold_rows(p, mod, 0), e_left_fold_rows(p, mod, 1)])
+    return {"dx": bf16_f32(ds), "dw": dw, "rstd": rstd, "dot": dot}

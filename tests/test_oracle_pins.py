@@ -542,3 +542,120 @@ def test_layer_composition():
                           shape.Hq, shape.Hkv, shape.D, shape.eps, shape.theta)
     np.testing.assert_array_equal(lay["out"], q["out"])
     assert np.isfinite(lay["out"]).all()
+
+
+# ---------------------------------------------------------------------------
+# backward: routed GEMM dX / dW, add-RMSNorm dx / dw
+# ---------------------------------------------------------------------------
+
+def test_routed_dx_dw_brute_force_integers():
+    rng = np.random.default_rng(41)
+    T, N, K = 7, 5, 3
+    dout = rng.integers(-3, 4, (T, N)).astype(np.float64)
+    a = rng.integers(-3, 4, (T, K)).astype(np.float64)
+    w = rng.integers(-3, 4, (2, N, K)).astype(np.float64)
+    mod = np.array([0, 1, 1, 0, 1, 0, 0])
+    dx = O.g_routed_gemm_dx(dout, w, mod)["dx_pre"]
+    for r in range(T):
+        for k in range(K):
+            assert dx[r, k] == sum(dout[r, n] * w[mod[r], n, k] for n in range(N))
+    for e in (0, 1):
+        dw = O.g_routed_gemm_dw(dout, a, mod, e)
+        for n in range(N):
+            for k in range(K):
+                assert dw[n, k] == sum(dout[r, n] * a[r, k] for r in range(T) if mod[r] == e)
+
+
+def test_routed_dx_dw_adjoint_identities():
+    # <dout, routed(a, W)> = <dA, a> = sum_e <dW_e, W_e>  (the backward is the adjoint of the forward)
+    rng = np.random.default_rng(42)
+    T, N, K = 40, 24, 16
+    dout = rng.standard_normal((T, N))
+    a = rng.standard_normal((T, K))
+    w = rng.standard_normal((2, N, K))
+    mod = rng.integers(0, 2, T)
+    lhs = float(np.sum(dout * O.g_routed_matmul(a, w, mod)))
+    via_dx = float(np.sum(O.g_routed_gemm_dx(dout, w, mod)["dx_pre"] * a))
+    via_dw = sum(float(np.sum(O.g_routed_gemm_dw(dout, a, mod, e) * w[e])) for e in (0, 1))
+    assert abs(via_dw - lhs) <= 1e-9 * (1 + abs(lhs))
+    assert abs(via_dx - lhs) <= 1e-9 * (1 + abs(lhs))
+    # a weight set's gradient ignores the other set's rows
+    d2 = dout.copy()
+    d2[mod == 1] = rng.standard_normal((int(np.sum(mod == 1)), N))
+    np.testing.assert_array_equal(O.g_routed_gemm_dw(d2, a, mod, 0), O.g_routed_gemm_dw(dout, a, mod, 0))
+
+
+def _norm_forward_pre(s, w, mod, eps):
+    """The cast-free add-RMSNorm forward as a function of the residual sum s (for finite differences)."""
+    rstd = 1.0 / np.sqrt(np.mean(s * s, axis=1) + eps)
+    return s * rstd[:, None] * w[mod]
+
+
+def test_norm_backward_is_the_gradient():
+    # directional derivatives by central differences of F(s, w) = <dy, y_pre(s, w)> + <dro, s>
+    rng = np.random.default_rng(43)
+    T, H = 6, 256
+    eps = float(F32(1e-6))
+    s = rng.standard_normal((T, H))
+    s[2] *= 1e-3                                       # a row where eps matters
+    w = 1 + 0.1 * rng.standard_normal((2, H))
+    dy = rng.standard_normal((T, H))
+    dro = rng.standard_normal((T, H))
+    mod = np.array([0, 1, 1, 0, 1, 0])
+    g = O.g_add_rmsnorm_backward(dy, s, w, mod, 1e-6, d_res_out=dro)
+
+    def F(s_, w_):
+        return float(np.sum(dy * _norm_forward_pre(s_, w_, mod, eps)) + np.sum(dro * s_))
+
+    h = 1e-6
+    for seed in range(3):
+        v = np.random.default_rng(100 + seed).standard_normal((T, H))
+        num = (F(s + h * v, w) - F(s - h * v, w)) / (2 * h)
+        assert abs(num - float(np.sum(g["dx_pre"] * v))) <= 1e-5 * (1 + abs(num))
+        V = np.random.default_rng(200 + seed).standard_normal((2, H))
+        num_w = (F(s, w + h * V) - F(s, w - h * V)) / (2 * h)
+        assert abs(num_w - float(np.sum(g["dw"] * V))) <= 1e-5 * (1 + abs(num_w))
+
+
+def test_left_fold_hand_value():
+    gd = GOLDEN["dweight_left_fold"]
+    p = np.array(gd["partials"], F32)[:, None]
+    mod = np.array(gd["mod"])
+    assert O.e_left_fold_rows(p, mod, 1)[0] == gd["dw_gen"]
+    assert O.e_left_fold_rows(p, mod, 0)[0] == gd["dw_und"]
+    assert O.e_left_fold_rows(p[:0], mod[:0], 0).shape == (1,)
+
+
+def test_norm_backward_e_dot_uses_the_forward_tree():
+    # s = 1, w = 1, eps = 0: rstd = 1 and xh = 1, so the dot's terms are dy itself; dy set to
+    # row A of the forward tree fixture (2^24 at column 0, 1 at columns 1..7 and at 8l) sums
+    # to the fixture's hand value on the fixed tree
+    gd = GOLDEN["add_rmsnorm_tree_sum"]
+    H = 512
+    dy = np.zeros((1, H))
+    dy[0, 0] = 2.0 ** 24
+    dy[0, 1:8] = 1.0
+    dy[0, 8 * np.arange(1, 32)] = 1.0
+    e = O.e_add_rmsnorm_backward(dy, np.ones((1, H)), np.ones((2, H)), np.array([0]), 0.0)
+    assert e["rstd"][0] == 1.0
+    assert e["dot"][0] == gd["row_A_sum_of_squares"]
+
+
+def test_norm_backward_e_matches_g():
+    rng = np.random.default_rng(44)
+    T, H = 48, 512
+    s = O.bf16(rng.standard_normal((T, H)))
+    dy = O.bf16(rng.standard_normal((T, H)))
+    dro = O.bf16(rng.standard_normal((T, H)))
+    w = O.bf16(1 + 0.1 * rng.standard_normal((2, H)))
+    mod = rng.integers(0, 2, T)
+    for d_res in (None, dro):
+        g = O.g_add_rmsnorm_backward(dy, s, w, mod, 1e-6, d_res_out=d_res)
+        e = O.e_add_rmsnorm_backward(dy, s, w, mod, 1e-6, d_res_out=d_res)
+        # one cast on each side: equal or one bf16 step apart, rarely
+        _, ex = np.frexp(np.maximum(np.abs(g["dx"]), 2.0 ** -100))
+        step = np.ldexp(1.0, ex - 8)
+        diff = np.abs(e["dx"] - g["dx"])
+        assert np.all(diff <= step) and np.mean(diff > 0) < 0.02
+        np.testing.assert_allclose(e["dw"], g["dw"], rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(e["rstd"], g["rstd"], rtol=1e-6)
