@@ -259,6 +259,80 @@ int mot_rope_table_fill_host(double theta, int D, int P, mot_bf16* host_cs);
 int mot_rope_table_fill_host_fp32(double theta, int D, int P, float* host_cs);
 
 /*
+ * mot_routed_gemm_dx -- input gradient of the routed GEMM out = a W[mod]^T through both
+ * weight sets ([RFC-435] §3 BAGEL-specific rules: phase A trains only the gen set, but the
+ * frozen und operators still need dX; §3 Numerical contract: fixed accumulation order).
+ *   dout  [T][N] bf16        gradient of the forward output (rows in token order, or in the
+ *                            plan's order with MOT_A_PLAN_ORDER).
+ *   w     [2][N][K] bf16     the forward's weights, unchanged (nn.Linear layout).
+ *   flags MOT_A_PLAN_ORDER | MOT_OUT_PLAN_ORDER or 0; no epilogue bits.
+ *   ws    the routing plan of mod for this T.
+ *   dx    [T][K] bf16        out: dx[r][k] = bf16(sum_n dout[r][n] W[mod[r]][n][k]), fp32
+ *                            accumulation over n in ascending 64-wide blocks, one cast.
+ * The weight is read as the MN-major operand of the same tensor-core pipeline, so no
+ * transposed copy is made. Geometry: K a multiple of 256, N a multiple of 64. Errors as
+ * mot_routed_gemm.
+ */
+int mot_routed_gemm_dx(const mot_bf16* dout, const mot_bf16* w, int64_t T, int N, int K, int flags,
+                       void* ws, size_t ws_bytes, mot_bf16* dx, void* stream);
+
+/*
+ * mot_routed_gemm_dw -- gradient of one weight set of the routed GEMM out = a W[mod]^T
+ * ([RFC-435] §3 BAGEL-specific rules: phase A trains the gen set; §3 Numerical contract:
+ * fixed accumulation order, no split-K or atomics).
+ *   dout_plan [T][N] bf16    gradient of the forward output, rows in the plan's order
+ *                            (mot_gather_rows, or a GEMM run with MOT_OUT_PLAN_ORDER).
+ *   a_plan    [T][K] bf16    the forward GEMM's input, rows in the plan's order.
+ *   expert    0 (und) or 1 (gen): the weight set whose gradient is formed.
+ *   ws        the routing plan of mod for this T.
+ *   dw        [N][K] fp32    out: dw[n][k] = sum over the set's rows r of dout[r][n] a[r][k],
+ *                            accumulated in fp32 on the tensor cores over the rows in
+ *                            ascending order (blocks of 64, then 16), one accumulator per
+ *                            output element, no cast; zeros for a set without rows.
+ * Geometry: N and K multiples of 256. A plan for another T sets MOT_DEV_PLAN_MISMATCH; a plan
+ * that failed (bad modality) leaves dw undefined. Other errors as mot_routed_gemm.
+ */
+int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_plan, int64_t T, int N, int K,
+                       int expert, void* ws, size_t ws_bytes, float* dw, void* stream);
+
+/*
+ * mot_add_rmsnorm_backward -- input gradient of mot_fused_add_rmsnorm ([RFC-435] §3
+ * BAGEL-specific rules: the frozen und operators still need dX, so both weight sets take
+ * part; [PR-503] gated-norm commit: the backward is assembled from deterministic pieces,
+ * a dx kernel first).
+ *   dy        [T][H] bf16      gradient of y.
+ *   d_res_out [T][H] bf16      gradient reaching res_out (the residual stream), or NULL.
+ *   s         [T][H] bf16      the forward's res_out (s = bf16(x + res)).
+ *   w         [2][H] bf16      the forward's norm weights; mod [T] uint8 as in the forward.
+ *   ws        workspace of at least mot_workspace_bytes(T); its error word receives device
+ *             errors (a modality other than 0/1). The plan it holds is not read here.
+ *   dx        [T][H] bf16      out: the gradient of x and of res (s = x + res passes it to both).
+ *   rstd      [T] fp32         out: each row's rstd (the forward's), for mot_rmsnorm_dweight.
+ * Per row, every operation rounded on its own in fp32: rstd on the forward's fixed tree;
+ * xh = s * rstd; g = dy * w[e]; dot = sum of g * xh on the same tree; c = dot / H;
+ * dx = bf16(rstd * (g - xh * c) (+ d_res_out)). Geometry as mot_fused_add_rmsnorm; all
+ * pointers 16-byte aligned device memory of the stream's device (mod: any alignment).
+ */
+int mot_add_rmsnorm_backward(const mot_bf16* dy, const mot_bf16* d_res_out, const mot_bf16* s,
+                             const mot_bf16* w, const uint8_t* mod, int64_t T, int H, float eps,
+                             void* ws, size_t ws_bytes, mot_bf16* dx, float* rstd, void* stream);
+
+/*
+ * mot_rmsnorm_dweight -- gradient of both norm weight sets ([PR-503] gated-norm commit:
+ * per-row fp32 partials, then the ascending-row fp32 left fold).
+ *   dy, s     [T][H] bf16      as in mot_add_rmsnorm_backward; rstd [T] fp32 its output.
+ *   ws        workspace holding the routing plan of mod for this T (mot_route_plan or the
+ *             forward norm); the rows of each set are taken from it in ascending order.
+ *   dw        [2][H] fp32      out: dw[e][j] = ((p_r0 + p_r1) + p_r2) + ... over the rows
+ *             r0 < r1 < ... of set e, p_r = dy[r][j] * (s[r][j] * rstd[r]); 0 for a set
+ *             without rows.
+ * A plan for another T sets MOT_DEV_PLAN_MISMATCH; a plan that failed (bad modality) leaves
+ * dw undefined. Geometry: 256 <= H <= 8192, H a multiple of 256.
+ */
+int mot_rmsnorm_dweight(const mot_bf16* dy, const mot_bf16* s, const float* rstd, int64_t T, int H,
+                        void* ws, size_t ws_bytes, float* dw, void* stream);
+
+/*
  * mot_selftest_wait_timeout -- exercises the bounded wait that every pipeline wait of the
  * library uses ([RFC-435] §3: fail closed instead of hanging). One thread waits on an mbarrier
  * that nothing signals; after about one second the wait gives up, MOT_DEV_TIMEOUT is OR-ed into

@@ -23,7 +23,8 @@ __all__ = [
     "mot_abi_version", "mot_status_string", "mot_workspace_bytes", "mot_route_plan",
     "mot_fused_add_rmsnorm", "mot_routed_qkv_norm_rope", "mot_routed_gemm",
     "mot_swiglu_interleave", "mot_rope_table_fill_host", "mot_device_status", "mot_routed_gemm_noalloc",
-    "mot_routed_qkv_norm_rope_fp32", "mot_rope_table_fill_host_fp32",
+    "mot_routed_qkv_norm_rope_fp32", "mot_rope_table_fill_host_fp32", "mot_add_rmsnorm_backward",
+    "mot_rmsnorm_dweight", "mot_routed_gemm_dx", "mot_routed_gemm_dw",
     "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows", "mot_selftest_wait_timeout",
 ]
 
@@ -64,6 +65,11 @@ _SIGNATURES = {
     "mot_selftest_wait_timeout": (_c_i, [_c_p, _c_sz, _c_p]),
     "mot_rope_table_fill_host": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
     "mot_rope_table_fill_host_fp32": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
+    "mot_add_rmsnorm_backward": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p,
+                                        _c_p]),
+    "mot_rmsnorm_dweight": (_c_i, [_c_p, _c_p, _c_p, _c_i64, _c_i, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_routed_gemm_dx": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_routed_gemm_dw": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
 }
 
@@ -294,6 +300,94 @@ def mot_swiglu_interleave(w_gate, w_up, out=None, stream=None):
     _check("mot_swiglu_interleave", _lib().mot_swiglu_interleave(
         w_gate.data_ptr(), w_up.data_ptr(), I, K, out.data_ptr(), _stream(w_gate, stream)))
     return out
+
+
+def mot_routed_gemm_dx(dout, w, ws, flags: int = 0, out=None, stream=None):
+    """Input gradient of the routed GEMM through both weight sets: dx[T][K] = bf16(dout W[mod]).
+    `w` is the forward's [2][N][K] weight; `flags` may carry A_PLAN_ORDER / OUT_PLAN_ORDER."""
+    T, N = dout.shape
+    _dev(dout, "dout", torch.bfloat16, 2)
+    _dev(w, "w", torch.bfloat16, 3)
+    _dev(ws, "ws", torch.uint8, 1)
+    if w.shape[0] != 2 or w.shape[1] != N:
+        raise ValueError(f"w must be [2, {N}, K]")
+    K = w.shape[2]
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.bfloat16, device=dout.device)
+    _dev(out, "out", torch.bfloat16, 2)
+    if tuple(out.shape) != (T, K):
+        raise ValueError(f"out must be [{T}, {K}]")
+    _check("mot_routed_gemm_dx", _lib().mot_routed_gemm_dx(
+        dout.data_ptr(), w.data_ptr(), T, N, K, flags, ws.data_ptr(), ws.numel(), out.data_ptr(),
+        _stream(dout, stream)))
+    return out
+
+
+def mot_routed_gemm_dw(dout_plan, a_plan, ws, expert: int = 1, out=None, stream=None):
+    """Gradient [N][K] fp32 of weight set `expert` from plan-order rows of dout [T][N] and a [T][K]."""
+    T, N = dout_plan.shape
+    _dev(dout_plan, "dout_plan", torch.bfloat16, 2)
+    _dev(a_plan, "a_plan", torch.bfloat16, 2)
+    _dev(ws, "ws", torch.uint8, 1)
+    if a_plan.shape[0] != T:
+        raise ValueError("dout_plan and a_plan must have the same rows")
+    K = a_plan.shape[1]
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=dout_plan.device)
+    _dev(out, "out", torch.float32, 2)
+    if tuple(out.shape) != (N, K):
+        raise ValueError(f"out must be [{N}, {K}]")
+    _check("mot_routed_gemm_dw", _lib().mot_routed_gemm_dw(
+        dout_plan.data_ptr(), a_plan.data_ptr(), T, N, K, expert, ws.data_ptr(), ws.numel(), out.data_ptr(),
+        _stream(dout_plan, stream)))
+    return out
+
+
+def mot_add_rmsnorm_backward(dy, s, w, mod, eps: float, ws, d_res_out=None, dx=None, rstd=None, stream=None):
+    """Input gradient of the fused add-RMSNorm: returns (dx [T][H] bf16, rstd [T] fp32).
+    `s` is the forward's res_out; `ws` (>= mot_workspace_bytes(T)) receives device errors."""
+    T, H = dy.shape
+    _dev(dy, "dy", torch.bfloat16, 2)
+    _dev(s, "s", torch.bfloat16, 2)
+    _dev(w, "w", torch.bfloat16, 2)
+    _dev(mod, "mod", torch.uint8, 1)
+    _dev(ws, "ws", torch.uint8, 1)
+    if tuple(s.shape) != (T, H) or tuple(w.shape) != (2, H) or mod.numel() != T:
+        raise ValueError("s must be [T, H], w [2, H] and mod [T]")
+    rp = None
+    if d_res_out is not None:
+        _dev(d_res_out, "d_res_out", torch.bfloat16, 2)
+        if tuple(d_res_out.shape) != (T, H):
+            raise ValueError("d_res_out must be [T, H]")
+        rp = d_res_out.data_ptr()
+    if dx is None:
+        dx = torch.empty((T, H), dtype=torch.bfloat16, device=dy.device)
+    if rstd is None:
+        rstd = torch.empty((T,), dtype=torch.float32, device=dy.device)
+    _dev(dx, "dx", torch.bfloat16, 2)
+    _dev(rstd, "rstd", torch.float32, 1)
+    _check("mot_add_rmsnorm_backward", _lib().mot_add_rmsnorm_backward(
+        dy.data_ptr(), rp, s.data_ptr(), w.data_ptr(), mod.data_ptr(), T, H, eps, ws.data_ptr(), ws.numel(),
+        dx.data_ptr(), rstd.data_ptr(), _stream(dy, stream)))
+    return dx, rstd
+
+
+def mot_rmsnorm_dweight(dy, s, rstd, ws, dw=None, stream=None):
+    """Gradient of both norm weight sets, [2][H] fp32, as an ascending-row fp32 left fold per set."""
+    T, H = dy.shape
+    _dev(dy, "dy", torch.bfloat16, 2)
+    _dev(s, "s", torch.bfloat16, 2)
+    _dev(rstd, "rstd", torch.float32, 1)
+    _dev(ws, "ws", torch.uint8, 1)
+    if tuple(s.shape) != (T, H) or rstd.numel() != T:
+        raise ValueError("s must be [T, H] and rstd [T]")
+    if dw is None:
+        dw = torch.empty((2, H), dtype=torch.float32, device=dy.device)
+    _dev(dw, "dw", torch.float32, 2)
+    _check("mot_rmsnorm_dweight", _lib().mot_rmsnorm_dweight(
+        dy.data_ptr(), s.data_ptr(), rstd.data_ptr(), T, H, ws.data_ptr(), ws.numel(), dw.data_ptr(),
+        _stream(dy, stream)))
+    return dw
 
 
 def mot_rope_table_fill_host(theta: float, D: int, P: int) -> torch.Tensor:

@@ -282,6 +282,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle layout: an atom is
+// 8 rows of 128 B, each row 64 consecutive M (or N) elements of one K index, the 8 rows 8
+// consecutive K. The next 8 K rows follow at 1024 B (stride-dimension offset); the next 64
+// M/N elements at `mn_stride` bytes (leading-dimension offset).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);               // start address
+  d |= uint64_t((mn_stride >> 4) & 0x3FFFu) << 16;      // leading-dimension byte offset: next 64 M/N
+  d |= uint64_t(1024 >> 4) << 32;                       // stride-dimension byte offset: next 8 K rows
+  d |= uint64_t(1) << 46;                               // descriptor version for tcgen05
+  d |= uint64_t(2) << 61;                               // layout: 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                      // accumulator format: f32
@@ -290,6 +304,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (uint32_t(N >> 3) << 17)     // N / 8
          | (uint32_t(M >> 4) << 24);    // M / 16
 }
+constexpr uint32_t kIdescAMnMajor = 1u << 15;  // A operand MN-major
+constexpr uint32_t kIdescBMnMajor = 1u << 16;  // B operand MN-major
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {

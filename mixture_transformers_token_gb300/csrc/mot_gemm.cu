@@ -362,7 +362,10 @@ __device__ __forceinline__ PairTile decode_pair(int u, int P0, int P, int band, 
   return t;
 }
 
-template <int EPI>
+// B_MN: the weight is read as an MN-major operand -- w is [2][K][N] with N contiguous, the
+// reduction running over its rows. This gives the input gradient of a forward GEMM whose
+// weight is [2][N_fwd][K_fwd] (here K = N_fwd, N = K_fwd) without a transposed copy.
+template <int EPI, bool B_MN = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     routed_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_rows,
                        const __grid_constant__ CUtensorMap tm_w, const Args args) {
@@ -451,7 +454,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           // the leader arrives once for both CTAs' bytes; the peer's copies only complete bytes
           // on the leader's barrier (a phase cannot complete before the leader's arrival)
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * STAGE_BYTES);
-          tma_load_2d_pair(smem_u32(sb + stage * B_BYTES), &tm_w, kb * BK, wrow, fb);
+          if constexpr (B_MN) {
+            // this CTA's 128 output columns as two 64-column boxes of the stage's 64 weight rows
+            const int bx = pt.nt * BN + int(rank) * BN_HALF, by = pt.expert * args.K + kb * BK;
+            tma_load_2d_pair(smem_u32(sb + stage * B_BYTES), &tm_w, bx, by, fb);
+            tma_load_2d_pair(smem_u32(sb + stage * B_BYTES + B_BYTES / 2), &tm_w, bx + 64, by, fb);
+          } else {
+            tma_load_2d_pair(smem_u32(sb + stage * B_BYTES), &tm_w, kb * BK, wrow, fb);
+          }
           if (!gather) tma_load_2d_pair(smem_u32(sa + stage * A_BYTES), &tm_a, kb * BK, arow0, fb);
         }
         __syncwarp();
@@ -477,7 +487,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer (leader CTA only) ----------------
     if (rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN) | (B_MN ? kIdescBMnMajor : 0u);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -494,7 +504,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
-              mma_bf16_pair(d, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+              mma_bf16_pair(d, smem_desc_sw128(a0 + k * 32),
+                            B_MN ? smem_desc_mn_sw128(b0 + k * 2048, B_BYTES / 2) : smem_desc_sw128(b0 + k * 32),
+                            idesc, (kb | k) != 0);
             mma_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
           }
           __syncwarp();
@@ -570,8 +582,225 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Weight gradient of one weight set: dW[n][k] = sum over its rows r (ascending) of
+// dout[r][n] * a[r][k], fp32, no cast.
+// ---------------------------------------------------------------------------
+// Both operands are MN-major (the reduction runs over rows): A' = dout^T, 128 n per CTA, and
+// B' = a^T, 128 k per CTA, each staged as two 64-column boxes of 64 rows. The inputs are in
+// the plan's order, so the set's rows are one contiguous run; full 64-row blocks are tiled
+// loads, the last partial block is gathered four rows at a time with rows past the run
+// pointed outside the tensor, which the copy fills with zeros. Pair tiles cover 256 n x 256 k;
+// each accumulates its 64-row blocks in ascending order into one fp32 accumulator (no split
+// of the reduction), and the epilogue stores fp32 rows of dW.
+struct DwArgs {
+  const uint8_t* ws;
+  uint32_t* err;
+  int T, N, K;  // dout [T][N], a [T][K], dw [N][K]
+  int expert;
+  float* dw;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    routed_gemm_dw_kernel(const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_d_rows,
+                          const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_rows,
+                          const DwArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* drain = bars + 2 * STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(args.ws);
+  if (hdr->magic != kPlanMagic || hdr->T != args.T) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.err, MOT_DEV_PLAN_MISMATCH);
+    return;  // uniform across the grid
+  }
+  if (hdr->count[0] + hdr->count[1] != args.T) return;  // no plan (bad modality): nothing is defined
+  const int row_start = args.expert == 0 ? 0 : hdr->count[0];
+  const int count = hdr->count[args.expert];
+  const int kblocks = (count + BK - 1) / BK;
+  const int m_tiles = args.N / BN, n_tiles = args.K / BN;
+  const int total = m_tiles * n_tiles;
+  if (kblocks == 0) {
+    // a set without rows: its gradient is zero
+    const int64_t n4 = int64_t(args.N) * args.K / 4;
+    float4* o = reinterpret_cast<float4*>(args.dw);
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x)
+      o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int cluster = int(blockIdx.x >> 1), nclusters = int(gridDim.x >> 1);
+  if (cluster >= total) return;  // uniform across the pair
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 2 * EPI_WARPS);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_d);
+    tma_prefetch_desc(&tm_d_rows);
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_a_rows);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = cluster; u < total && ok; u += nclusters) {
+      const int mt = u % m_tiles, nt = u / m_tiles;
+      const int n0 = mt * BN + int(rank) * BN_HALF;  // this CTA's 128 rows of dW
+      const int k0 = nt * BN + int(rank) * BN_HALF;  // this CTA's 128 columns of the B' operand
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err));
+        if (!ok) break;
+        const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
+        const int row0 = row_start + kb * BK;
+        const int valid = count - kb * BK;
+        const uint32_t da = smem_u32(sa + stage * A_BYTES), db = smem_u32(sb + stage * B_BYTES);
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * STAGE_BYTES);
+          if (valid >= BK) {
+            tma_load_2d_pair(da, &tm_d, n0, row0, fb);
+            tma_load_2d_pair(da + A_BYTES / 2, &tm_d, n0 + 64, row0, fb);
+            tma_load_2d_pair(db, &tm_a, k0, row0, fb);
+            tma_load_2d_pair(db + B_BYTES / 2, &tm_a, k0 + 64, row0, fb);
+          }
+        }
+        __syncwarp();
+        if (valid < BK) {
+          // 4 boxes x 16 four-row groups, two per lane; rows past the run read as zeros
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int idx = lane + 32 * q;
+            const int box = idx >> 4, quad = idx & 15;
+            int r[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r[i] = quad * 4 + i < valid ? row0 + quad * 4 + i : args.T;
+            const uint32_t dst = (box < 2 ? da : db) + (box & 1) * (A_BYTES / 2) + quad * 512;
+            const int x = (box < 2 ? n0 : k0) + 64 * (box & 1);
+            tma_gather4_pair(dst, box < 2 ? static_cast<const void*>(&tm_d_rows) : static_cast<const void*>(&tm_a_rows),
+                             x, r[0], r[1], r[2], r[3], fb);
+          }
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (ok) {
+      for (int i = 0; i < STAGES; ++i) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err))) break;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader CTA only) ----------------
+    if (rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN) | kIdescAMnMajor | kIdescBMnMajor;
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = cluster; u < total && ok; u += nclusters) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * ACC_COLS;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              mma_bf16_pair(d, smem_desc_mn_sw128(a0 + k * 2048, A_BYTES / 2),
+                            smem_desc_mn_sw128(b0 + k * 2048, B_BYTES / 2), idesc, (kb | k) != 0);
+            mma_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit_pair_multicast(smem_u32(&tfull[acc]), 0x3);
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (lane == 0) mma_commit_pair(smem_u32(drain));
+      __syncwarp();
+      mbar_drain(smem_u32(drain), 0);
+    }
+  } else {
+    // ---------------- epilogue (both CTAs): fp32 rows of dW ----------------
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = cluster; u < total; u += nclusters) {
+      const int mt = u % m_tiles, nt = u / m_tiles;
+      const int n = mt * BN + int(rank) * BN_HALF + quarter * 32 + lane;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err))) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16) + half * 128;
+      float4* orow = reinterpret_cast<float4*>(args.dw + int64_t(n) * args.K + nt * BN + half * 128);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) orow[c * 8 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(map_to_rank(smem_u32(&tempty[acc]), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 // Clusters of the pair kernel that fit on the device at once (computed once per device).
-template <int EPI>
+template <int EPI, bool B_MN = false>
 static int max_active_pairs(int dev) {
   static std::atomic<int> cache[kMaxDevices];
   int v = cache[dev].load();
@@ -588,7 +817,7 @@ static int max_active_pairs(int dev) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, routed_gemm_kernel<EPI>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, routed_gemm_kernel<EPI, B_MN>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = sm_count(dev) / 2;
   }
@@ -596,21 +825,23 @@ static int max_active_pairs(int dev) {
   return n;
 }
 
-template <int EPI>
+template <int EPI, bool B_MN = false>
 static int launch(const void* a, const void* w, int T, int N, int K, const Args& args, int dev, cudaStream_t s) {
   CUtensorMap tm_a, tm_rows, tm_w;
+  const bool w_ok = B_MN ? make_tmap_bf16(&tm_w, w, uint64_t(N), uint64_t(2) * K, 64, BK)
+                         : make_tmap_bf16(&tm_w, w, uint64_t(K), uint64_t(2) * N, BK, BN_HALF);
   if (!make_tmap_bf16(&tm_a, a, uint64_t(K), uint64_t(T), BK, BM) ||
-      !make_tmap_bf16(&tm_rows, a, uint64_t(K), uint64_t(T), BK, 1) ||
-      !make_tmap_bf16(&tm_w, w, uint64_t(K), uint64_t(2) * N, BK, BN_HALF))
+      !make_tmap_bf16(&tm_rows, a, uint64_t(K), uint64_t(T), BK, 1) || !w_ok)
     return MOT_ERR_CUDA;
-  if (cudaFuncSetAttribute(routed_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES)) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(routed_gemm_kernel<EPI, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(SMEM_BYTES)) != cudaSuccess)
     return MOT_ERR_CUDA;
   // upper bound of pair tiles: ceil(tiles0 / 2) + ceil(tiles1 / 2) <= (ceil(T / 128) + 1) / 2 + 1
   const int64_t pairs_max = ((int64_t(T) + BM - 1) / BM + 1) / 2 + 1;
   const int64_t work_max = pairs_max * int64_t(N / BN);
-  const int64_t clusters = work_max < max_active_pairs<EPI>(dev) ? work_max : max_active_pairs<EPI>(dev);
-  routed_gemm_kernel<EPI><<<unsigned(2 * clusters), THREADS, SMEM_BYTES, s>>>(tm_a, tm_rows, tm_w, args);
+  const int64_t cap = max_active_pairs<EPI, B_MN>(dev);
+  const int64_t clusters = work_max < cap ? work_max : cap;
+  routed_gemm_kernel<EPI, B_MN><<<unsigned(2 * clusters), THREADS, SMEM_BYTES, s>>>(tm_a, tm_rows, tm_w, args);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
@@ -689,6 +920,77 @@ extern "C" int mot_routed_qkv_norm_rope_fp32(const mot_bf16* x, const mot_bf16* 
   if (rope_cs_f32 == nullptr) return MOT_ERR_NULL;
   return routed_qkv_entry(x, w_qkv, b_qkv, q_norm_w, k_norm_w, pos, nullptr, rope_cs_f32, P, T, H, Hq, Hkv, D, eps,
                           ws, ws_bytes, qkv_out, stream);
+}
+
+extern "C" int mot_routed_gemm_dx(const mot_bf16* dout, const mot_bf16* w, int64_t T, int N, int K, int flags,
+                                  void* ws, size_t ws_bytes, mot_bf16* dx, void* stream) {
+  if (!dout || !w || !ws || !dx) return MOT_ERR_NULL;
+  if ((flags & ~(MOT_A_PLAN_ORDER | MOT_OUT_PLAN_ORDER)) != 0) return MOT_ERR_ARG;
+  if (T < 1 || T > MOT_MAX_TOKENS) return MOT_ERR_GEOMETRY;
+  // the forward's K is the output width (tiles of 256), its N the reduction (blocks of 64)
+  if (K < gemm::BN || K % gemm::BN != 0 || K > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (N < gemm::BK || N % gemm::BK != 0 || N > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (!aligned16(dout) || !aligned16(w) || !aligned16(ws) || !aligned16(dx)) return MOT_ERR_ALIGN;
+  if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {dout, w, ws, dx};
+  int dev = -1;
+  int st = check_device(s, ptrs, 4, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  gemm::Args a{};
+  a.ws = static_cast<const uint8_t*>(ws);
+  a.err = &static_cast<PlanHeader*>(ws)->error;
+  a.T = int(T);
+  a.N = K;
+  a.K = N;
+  a.n_tiles = K / gemm::BN;
+  a.out = dx;
+  a.ldo = K;
+  a.a_plan_order = (flags & MOT_A_PLAN_ORDER) != 0;
+  a.out_plan_order = (flags & MOT_OUT_PLAN_ORDER) != 0;
+  return gemm::launch<gemm::EPI_CAST, true>(dout, w, int(T), K, N, a, dev, s);
+}
+
+extern "C" int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_plan, int64_t T, int N, int K,
+                                  int expert, void* ws, size_t ws_bytes, float* dw, void* stream) {
+  if (!dout_plan || !a_plan || !ws || !dw) return MOT_ERR_NULL;
+  if (expert != 0 && expert != 1) return MOT_ERR_ARG;
+  if (T < 1 || T > MOT_MAX_TOKENS) return MOT_ERR_GEOMETRY;
+  if (N < gemm::BN || N % gemm::BN != 0 || N > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (K < gemm::BN || K % gemm::BN != 0 || K > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (!aligned16(dout_plan) || !aligned16(a_plan) || !aligned16(ws) || !aligned16(dw)) return MOT_ERR_ALIGN;
+  if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {dout_plan, a_plan, ws, dw};
+  int dev = -1;
+  int st = check_device(s, ptrs, 4, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  CUtensorMap tm_d, tm_d_rows, tm_a, tm_a_rows;
+  if (!make_tmap_bf16(&tm_d, dout_plan, uint64_t(N), uint64_t(T), 64, gemm::BK) ||
+      !make_tmap_bf16(&tm_d_rows, dout_plan, uint64_t(N), uint64_t(T), 64, 1) ||
+      !make_tmap_bf16(&tm_a, a_plan, uint64_t(K), uint64_t(T), 64, gemm::BK) ||
+      !make_tmap_bf16(&tm_a_rows, a_plan, uint64_t(K), uint64_t(T), 64, 1))
+    return MOT_ERR_CUDA;
+  if (cudaFuncSetAttribute(gemm::routed_gemm_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(gemm::SMEM_BYTES)) != cudaSuccess)
+    return MOT_ERR_CUDA;
+  gemm::DwArgs a{};
+  a.ws = static_cast<const uint8_t*>(ws);
+  a.err = &static_cast<PlanHeader*>(ws)->error;
+  a.T = int(T);
+  a.N = N;
+  a.K = K;
+  a.expert = expert;
+  a.dw = dw;
+  const int64_t total = int64_t(N / gemm::BN) * (K / gemm::BN);
+  // same threads, shared memory and cluster shape as the routed kernel, so the same residency
+  const int64_t cap = gemm::max_active_pairs<gemm::EPI_CAST, true>(dev);
+  const int64_t clusters = total < cap ? total : cap;
+  gemm::routed_gemm_dw_kernel<<<unsigned(2 * clusters), gemm::THREADS, gemm::SMEM_BYTES, s>>>(tm_d, tm_d_rows, tm_a,
+                                                                                               tm_a_rows, a);
+  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
 extern "C" int mot_routed_gemm(const mot_bf16* a_in, const mot_bf16* w, int64_t T, int N, int K, int epilogue,

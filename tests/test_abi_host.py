@@ -143,6 +143,42 @@ def test_qkv_fp32_profile_rejects(lib):
     assert call(wsb=16) == MOT_ERR_WORKSPACE
 
 
+def test_norm_backward_rejects(lib):
+    f = lib.mot_add_rmsnorm_backward
+    assert f(None, None, A, A, A, 8, 256, 1e-6, B, 1 << 20, C, C, None) == MOT_ERR_NULL
+    assert f(A, None, A, A, A, 8, 256, 1e-6, None, 1 << 20, C, C, None) == MOT_ERR_NULL
+    assert f(A, None, A, A, A, 8, 256, 1e-6, B, 1 << 20, C, None, None) == MOT_ERR_NULL
+    assert f(A, None, A, A, A, 8, 200, 1e-6, B, 1 << 20, C, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, None, A, A, A, 8, 8448, 1e-6, B, 1 << 20, C, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, None, A, A, A, 0, 256, 1e-6, B, 1 << 20, C, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, None, A, A, A, 8, 256, 0.0, B, 1 << 20, C, C, None) == MOT_ERR_ARG
+    assert f(A, MIS, A, A, A, 8, 256, 1e-6, B, 1 << 20, C, C, None) == MOT_ERR_ALIGN
+    assert f(A, None, A, A, A, 8, 256, 1e-6, B, 1 << 20, C, MIS, None) == MOT_ERR_ALIGN
+    assert f(A, None, A, A, A, 1000, 256, 1e-6, B, 100, C, C, None) == MOT_ERR_WORKSPACE
+    g = lib.mot_rmsnorm_dweight
+    assert g(None, A, A, 8, 256, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert g(A, A, A, 8, 255, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert g(A, A, MIS, 8, 256, B, 1 << 20, C, None) == MOT_ERR_ALIGN
+    assert g(A, A, A, 1000, 256, B, 100, C, None) == MOT_ERR_WORKSPACE
+
+
+def test_gemm_backward_rejects(lib):
+    dx = lib.mot_routed_gemm_dx
+    assert dx(None, A, 8, 64, 256, 0, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert dx(A, A, 8, 64, 256, 0x1, B, 1 << 20, C, None) == MOT_ERR_ARG          # no epilogue bits
+    assert dx(A, A, 8, 64, 320, 0, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY       # output K % 256
+    assert dx(A, A, 8, 96, 256, 0, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY       # reduction N % 64
+    assert dx(A, MIS, 8, 64, 256, 0, B, 1 << 20, C, None) == MOT_ERR_ALIGN
+    assert dx(A, A, 1000, 64, 256, 0, B, 100, C, None) == MOT_ERR_WORKSPACE
+    dw = lib.mot_routed_gemm_dw
+    assert dw(None, A, 8, 256, 256, 1, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert dw(A, A, 8, 256, 256, 2, B, 1 << 20, C, None) == MOT_ERR_ARG
+    assert dw(A, A, 8, 128, 256, 1, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert dw(A, A, 8, 256, 320, 1, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert dw(A, A, 8, 256, 256, 1, B, 1 << 20, MIS, None) == MOT_ERR_ALIGN
+    assert dw(A, A, 1000, 256, 256, 1, B, 100, C, None) == MOT_ERR_WORKSPACE
+
+
 def test_routed_gemm_rejects(lib):
     f = lib.mot_routed_gemm
     assert f(None, A, 8, 256, 64, 0, B, 1 << 20, C, None) == MOT_ERR_NULL

@@ -1,0 +1,234 @@
+"""Backward of the routed projection path on the GPU, through the C ABI, against the oracle.
+
+add-RMSNorm backward ([RFC][BAGEL-7B-MoT][CUDA/ROCm] WS1/WS2 kernel roadmap #435, §3 BAGEL
+rules: the frozen und operators still need dX; [WS1][CUDA][Qwen3-Next] MoE route/combine
+contract #503, gated-norm commit: a dx kernel and the weight gradient as an ascending-row fp32
+left fold of per-row partials): dx, rstd and dw must equal the fp32 emulator E bit for bit,
+and stay within the tolerance of the fp64 golden G.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_transformers_token_gb300 as mot
+from mixture_transformers_token_gb300 import workloads as W
+from oracle import mot_oracle as O
+
+from _util import assert_bitwise, assert_tolerance, f64, need_gpu, np_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _norm_bwd_inputs(T, H, seed, mod=None, with_dres=True):
+    rng = W.rng_for(seed, 300)
+    if mod is None:
+        mod = W.modality_bernoulli(rng, T, 0.3)
+    return {
+        "dy": W.bf16_normal(W.rng_for(seed, 301), (T, H)),
+        "s": W.bf16_normal(W.rng_for(seed, 302), (T, H)),
+        "dro": W.bf16_normal(W.rng_for(seed, 303), (T, H)) if with_dres else None,
+        "w": W.bf16_normal(W.rng_for(seed, 304), (2, H), mean=1.0, std=0.1),
+        "mod": mod,
+    }
+
+
+def _run_norm_bwd(inp, eps=1e-6):
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    ws = mot.mot_route_plan(d["mod"])
+    dx, rstd = mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], d["mod"], eps, ws, d_res_out=d["dro"])
+    dw = mot.mot_rmsnorm_dweight(d["dy"], d["s"], rstd, ws)
+    assert mot.mot_device_status(ws) == 0
+    return dx, rstd, dw
+
+
+@pytest.mark.parametrize("T,H,seed,with_dres", [(64, 256, 1, True), (1, 256, 2, True), (333, 3584, 3, True),
+                                                (1000, 768, 4, False), (300, 5120, 5, True),
+                                                (4096, 3584, 6, True)])
+def test_add_rmsnorm_backward_bitwise_vs_emulator(T, H, seed, with_dres):
+    inp = _norm_bwd_inputs(T, H, seed, with_dres=with_dres)
+    dx, rstd, dw = _run_norm_bwd(inp)
+    dro = f64(inp["dro"]) if with_dres else None
+    e = O.e_add_rmsnorm_backward(f64(inp["dy"]), f64(inp["s"]), f64(inp["w"]), inp["mod"].numpy(), 1e-6,
+                                 d_res_out=dro)
+    assert_bitwise(dx, np_bits(e["dx"]), "dx vs E")
+    assert np.array_equal(rstd.cpu().numpy().view(np.uint32), e["rstd"].view(np.uint32)), "rstd vs E"
+    assert np.array_equal(dw.cpu().numpy().view(np.uint32), e["dw"].view(np.uint32)), "dw vs E"
+    g = O.g_add_rmsnorm_backward(f64(inp["dy"]), f64(inp["s"]), f64(inp["w"]), inp["mod"].numpy(), 1e-6,
+                                 d_res_out=dro)
+    assert_tolerance(f64(dx), g["dx_pre"], "dx vs G")
+    # fp32 fold of T products against the exact sum: within T * 2^-23 of the sum of |partials|
+    mod = inp["mod"].numpy()
+    xh = f64(inp["s"]) * g["rstd"][:, None]
+    for ex in (0, 1):
+        r = mod == ex
+        bound = (max(1, int(r.sum())) * 2.0 ** -23 + 1e-6) * np.sum(np.abs(f64(inp["dy"])[r] * xh[r]), axis=0)
+        assert np.all(np.abs(dw.cpu().numpy()[ex].astype(np.float64) - g["dw"][ex]) <= bound + 1e-30)
+
+
+def test_add_rmsnorm_backward_single_modality_and_empty_set():
+    T, H = 200, 512
+    inp = _norm_bwd_inputs(T, H, 7, mod=torch.zeros(T, dtype=torch.uint8))
+    dx, rstd, dw = _run_norm_bwd(inp)
+    e = O.e_add_rmsnorm_backward(f64(inp["dy"]), f64(inp["s"]), f64(inp["w"]), inp["mod"].numpy(), 1e-6,
+                                 d_res_out=f64(inp["dro"]))
+    assert_bitwise(dx, np_bits(e["dx"]), "dx vs E (all und)")
+    dwn = dw.cpu().numpy()
+    assert np.array_equal(dwn[0].view(np.uint32), e["dw"][0].view(np.uint32))
+    assert np.all(dwn[1].view(np.uint32) == 0)      # +0.0 for the set without rows
+
+
+def test_add_rmsnorm_backward_rows_are_batch_invariant():
+    # a row's dx and rstd do not depend on the pack; dw of a sub-pack is the fold of its rows only
+    T, H = 600, 1024
+    inp = _norm_bwd_inputs(T, H, 8)
+    dx, rstd, _ = _run_norm_bwd(inp)
+    sel = np.sort(W.rng_for(8, 310).choice(T, 77, replace=False))
+    sub = {k: (v[sel] if (v is not None and k != "w") else v) for k, v in inp.items()}
+    dx2, rstd2, _ = _run_norm_bwd(sub)
+    assert_bitwise(dx2, dx[torch.from_numpy(sel).cuda()], "dx of a sub-pack")
+    assert torch.equal(rstd2, rstd[torch.from_numpy(sel).cuda()])
+
+
+def test_add_rmsnorm_backward_flags():
+    T, H = 64, 256
+    inp = _norm_bwd_inputs(T, H, 9)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    ws = mot.mot_route_plan(d["mod"])
+    bad = d["mod"].clone()
+    bad[5] = 2
+    mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], bad, 1e-6, ws)
+    assert mot.mot_device_status(ws) & mot.DEV_BAD_MODALITY
+    ws2 = torch.empty(mot.mot_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    mot.mot_route_plan(d["mod"][:50].contiguous(), ws=ws2)       # a plan of another T
+    _, rstd = mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], d["mod"], 1e-6, ws2)
+    mot.mot_rmsnorm_dweight(d["dy"], d["s"], rstd, ws2)
+    assert mot.mot_device_status(ws2) & mot.DEV_PLAN_MISMATCH
+
+
+# ---------------------------------------------------------------------------
+# routed GEMM input gradient (both weight sets, MN-major weight operand)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,N,K,mode", [(300, 128, 256, "scatter"), (129, 512, 512, "gen"), (1, 64, 256, "scatter"),
+                                        (640, 4608, 3584, "blocks")])
+def test_routed_gemm_dx_integer_inputs_exact(T, N, K, mode):
+    # small integers: every fp32 partial sum is exact, so the result is the exact gradient
+    rng = W.rng_for(11, T + N)
+    if mode == "scatter":
+        mod = W.modality_bernoulli(rng, T, 0.4)
+    elif mode == "gen":
+        mod = torch.ones(T, dtype=torch.uint8)
+    else:
+        mod = W.modality_blocks([(0, T // 2), (1, T - T // 2)])
+    dout = W.bf16_integers(W.rng_for(11, 1), (T, N), -2, 2)
+    w = W.bf16_integers(W.rng_for(11, 2), (2, N, K), -2, 2)
+    ws = mot.mot_route_plan(mod.cuda())
+    dx = mot.mot_routed_gemm_dx(dout.cuda(), w.cuda(), ws)
+    assert mot.mot_device_status(ws) == 0
+    g = O.g_routed_gemm_dx(f64(dout), f64(w), mod.numpy())
+    assert_bitwise(dx, np_bits(g["dx"]), "routed dX (integers)")
+
+
+@pytest.mark.parametrize("T,N,K,p_gen,seed", [(777, 1024, 768, 0.3, 1), (4096, 4608, 3584, 0.25, 2),
+                                              (500, 3584, 18944, 0.5, 3)])
+def test_routed_gemm_dx_tolerance(T, N, K, p_gen, seed):
+    mod = W.modality_bernoulli(W.rng_for(seed, 320), T, p_gen)
+    dout = W.bf16_normal(W.rng_for(seed, 321), (T, N))
+    w = W.bf16_normal(W.rng_for(seed, 322), (2, N, K), std=0.02)
+    ws = mot.mot_route_plan(mod.cuda())
+    dx = mot.mot_routed_gemm_dx(dout.cuda(), w.cuda(), ws)
+    assert mot.mot_device_status(ws) == 0
+    rows = np.arange(T) if T <= 1000 else np.unique(np.concatenate(
+        [np.sort(W.rng_for(seed, 323).choice(T, 128, replace=False)), [0, T - 1]]))
+    g = O.g_routed_gemm_dx(f64(dout)[rows], f64(w), mod.numpy()[rows])
+    assert_tolerance(f64(dx)[rows], g["dx_pre"], "routed dX vs G")
+
+
+def test_routed_gemm_dx_plan_order_flags_give_the_same_bits():
+    T, N, K = 333, 512, 768
+    mod = W.modality_bernoulli(W.rng_for(12, 330), T, 0.5)
+    dout = W.bf16_normal(W.rng_for(12, 331), (T, N)).cuda()
+    w = W.bf16_normal(W.rng_for(12, 332), (2, N, K), std=0.02).cuda()
+    ws = mot.mot_route_plan(mod.cuda())
+    ref = mot.mot_routed_gemm_dx(dout, w, ws)
+    perm = torch.from_numpy(np.concatenate([np.nonzero(mod.numpy() == 0)[0], np.nonzero(mod.numpy() == 1)[0]])).cuda()
+    dout_plan = mot.mot_gather_rows(dout, ws)
+    a_plan = mot.mot_routed_gemm_dx(dout_plan, w, ws, flags=mot.A_PLAN_ORDER)
+    both = mot.mot_routed_gemm_dx(dout_plan, w, ws, flags=mot.A_PLAN_ORDER | mot.OUT_PLAN_ORDER)
+    out_plan = mot.mot_routed_gemm_dx(dout, w, ws, flags=mot.OUT_PLAN_ORDER)
+    assert mot.mot_device_status(ws) == 0
+    assert_bitwise(a_plan, ref, "dX, plan-order input")
+    assert_bitwise(both, ref[perm], "dX, plan order in and out")
+    assert_bitwise(out_plan, ref[perm], "dX, plan-order output")
+
+
+# ---------------------------------------------------------------------------
+# routed GEMM weight gradient (one weight set, rows ascending, fp32)
+# ---------------------------------------------------------------------------
+
+def _dw_run(dout, a, mod, expert):
+    ws = mot.mot_route_plan(mod.cuda())
+    dp = mot.mot_gather_rows(dout.cuda(), ws)
+    ap = mot.mot_gather_rows(a.cuda(), ws)
+    dw = mot.mot_routed_gemm_dw(dp, ap, ws, expert=expert)
+    assert mot.mot_device_status(ws) == 0
+    return dw
+
+
+@pytest.mark.parametrize("T,N,K,mode,expert", [(300, 256, 512, "scatter", 1), (300, 256, 512, "scatter", 0),
+                                               (129, 512, 256, "gen", 1), (64, 256, 256, "scatter", 0),
+                                               (1000, 768, 1024, "blocks", 0)])
+def test_routed_gemm_dw_integer_inputs_exact(T, N, K, mode, expert):
+    rng = W.rng_for(13, T + N + expert)
+    if mode == "scatter":
+        mod = W.modality_bernoulli(rng, T, 0.4)
+    elif mode == "gen":
+        mod = torch.ones(T, dtype=torch.uint8)
+    else:
+        mod = W.modality_blocks([(0, 700), (1, T - 700)])
+    dout = W.bf16_integers(W.rng_for(13, 1), (T, N), -2, 2)
+    a = W.bf16_integers(W.rng_for(13, 2), (T, K), -2, 2)
+    dw = _dw_run(dout, a, mod, expert)
+    g = O.g_routed_gemm_dw(f64(dout), f64(a), mod.numpy(), expert)
+    np.testing.assert_array_equal(dw.cpu().numpy().astype(np.float64), g)
+
+
+def test_routed_gemm_dw_set_without_rows_is_zero():
+    T, N, K = 200, 256, 256
+    mod = torch.zeros(T, dtype=torch.uint8)
+    dw = _dw_run(W.bf16_normal(W.rng_for(14, 1), (T, N)), W.bf16_normal(W.rng_for(14, 2), (T, K)), mod, 1)
+    assert torch.all(dw.view(torch.int32) == 0)
+
+
+@pytest.mark.parametrize("T,N,K,p_gen,expert,seed", [(777, 1024, 768, 0.3, 1, 1), (777, 1024, 768, 0.3, 0, 1),
+                                                     (4096, 4608, 3584, 0.25, 1, 2)])
+def test_routed_gemm_dw_tolerance(T, N, K, p_gen, expert, seed):
+    mod = W.modality_bernoulli(W.rng_for(seed, 340), T, p_gen)
+    dout = W.bf16_normal(W.rng_for(seed, 341), (T, N))
+    a = W.bf16_normal(W.rng_for(seed, 342), (T, K))
+    dw = _dw_run(dout, a, mod, expert)
+    rows = mod.numpy() == expert
+    g = O.g_routed_gemm_dw(f64(dout), f64(a), mod.numpy(), expert)
+    absum = np.abs(f64(dout)[rows]).T @ np.abs(f64(a)[rows])
+    n = int(rows.sum())
+    err = np.abs(dw.cpu().numpy().astype(np.float64) - g)
+    # fp32 accumulation of n products (each exact in fp32) plus the final fp32 value
+    assert np.all(err <= 2 * n * 2.0 ** -24 * absum + 2.0 ** -24 * np.abs(g)), float(np.max(err / (absum + 1e-30)))
+    rel = float(np.linalg.norm(dw.cpu().numpy() - g) / np.linalg.norm(g))
+    assert rel <= 1e-5, rel
+
+
+def test_routed_gemm_dw_is_deterministic():
+    T, N, K = 1500, 512, 512
+    mod = W.modality_bernoulli(W.rng_for(15, 350), T, 0.6)
+    dout = W.bf16_normal(W.rng_for(15, 351), (T, N))
+    a = W.bf16_normal(W.rng_for(15, 352), (T, K))
+    d1 = _dw_run(dout, a, mod, 1)
+    d2 = _dw_run(dout, a, mod, 1)
+    assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))
