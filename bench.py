@@ -332,7 +332,8 @@ def run_ours(args, rank, world, local_rank):
     secondary = None
     if rank == 0 and args.secondary:
         secondary = {"swiglu_mlp_T8192": run_mlp(dev, flush), "cfg_pack_T36864": run_cfg_pack(dev, flush),
-                     "fp32_rope_profile_T4096": run_qkv_fp32_rope(dev, flush)}
+                     "fp32_rope_profile_T4096": run_qkv_fp32_rope(dev, flush),
+                     "backward_T4096": run_backward(dev, flush)}
     if world > 1:
         dist.barrier()
     if rank != 0:
@@ -540,6 +541,70 @@ def run_qkv_fp32_rope(dev, flush) -> dict:
             "distribution_us": r["dist"]["qkv_fp32_rope"]}
 
 
+def run_backward(dev, flush) -> dict:
+    """Backward of the bench layer's projection step (T = 4096, hidden 3584, QKV out 4608):
+    add-RMSNorm backward (dx, rstd and the per-row weight partials), the norm-weight fold, the
+    QKV GEMM's input gradient
+    through both weight sets, the rows of dqkv and y into plan order, and the gen set's weight
+    gradient (1024 rows)."""
+    import torch
+
+    import mixture_transformers_token_gb300 as mot
+    from mixture_transformers_token_gb300 import workloads as W
+
+    stream = torch.cuda.current_stream(dev)
+    shape, inp = W.bagel_layer(seed=1, T=T)
+    d = {k: v.to(dev) for k, v in inp.items() if isinstance(v, torch.Tensor)}
+    ws = torch.empty(mot.mot_workspace_bytes(T), dtype=torch.uint8, device=dev)
+    y, s_res = mot.mot_fused_add_rmsnorm(d["x"], d["res"], d["w_norm"], d["mod"], shape.eps, ws=ws)
+    dqkv = W.bf16_normal_device(1, 400, (T, N_QKV), dev)
+    dres = W.bf16_normal_device(1, 401, (T, H), dev)
+    dy = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    dxn = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    rstd = torch.empty((T,), dtype=torch.float32, device=dev)
+    dwn = torch.empty((2, H), dtype=torch.float32, device=dev)
+    part = torch.empty((H // 64, T, 64), dtype=torch.float32, device=dev)
+    dq_plan = torch.empty_like(dqkv)
+    y_plan = torch.empty_like(y)
+    dw_gen = torch.empty((N_QKV, H), dtype=torch.float32, device=dev)
+    stages = [
+        ("qkv_dx", lambda: mot.mot_routed_gemm_dx(dqkv, d["w_qkv"], ws, out=dy)),
+        ("add_rmsnorm_dx", lambda: mot.mot_add_rmsnorm_backward(dy, s_res, d["w_norm"], shape.eps, ws,
+                                                                d_res_out=dres, dx=dxn, rstd=rstd,
+                                                                dw_partials=part)),
+        ("rmsnorm_dweight", lambda: mot.mot_rmsnorm_dweight(part, ws, dw=dwn)),
+        ("gather_dqkv_y", lambda: (mot.mot_gather_rows(dqkv, ws, out=dq_plan), mot.mot_gather_rows(y, ws, out=y_plan))),
+        ("qkv_dw_gen", lambda: mot.mot_routed_gemm_dw(dq_plan, y_plan, ws, expert=1, out=dw_gen)),
+    ]
+    r = time_stages(stages, 50, 5, flush, stream)
+    if mot.mot_device_status(ws) != 0:
+        raise RuntimeError("device error flags set in the backward workload")
+    pk = peaks()
+    n_gen = int(inp["mod"].sum())
+    f_dx, f_dw = 2 * T * N_QKV * H, 2 * n_gen * N_QKV * H
+    b_dx = 12 * T * H + 8 * T + 4 * H         # dy, s, d_res_out read; dx, fp32 partials, rstd written; plan; w
+    b_dw = 4 * T * H + 8 * H                  # fp32 partials read; dw written
+
+    def gbs(b, name):
+        return round(b / r[name] / 1e9, 1)
+
+    return {
+        "workload": WORKLOAD + "_backward",
+        "qkv_dx_us": round(r["qkv_dx"] * 1e6, 2), "qkv_dx_tflops": _tflops(f_dx, r["qkv_dx"]),
+        "qkv_dx_frac": round(f_dx / r["qkv_dx"] / 1e12 / pk["bf16_tflops"], 4),
+        "add_rmsnorm_dx_us": round(r["add_rmsnorm_dx"] * 1e6, 2),
+        "add_rmsnorm_dx_gbs": gbs(b_dx, "add_rmsnorm_dx"),
+        "add_rmsnorm_dx_frac_hbm": round(b_dx / r["add_rmsnorm_dx"] / 1e9 / pk["hbm_gbs"], 4),
+        "rmsnorm_dweight_us": round(r["rmsnorm_dweight"] * 1e6, 2),
+        "rmsnorm_dweight_gbs": gbs(b_dw, "rmsnorm_dweight"),
+        "rmsnorm_dweight_frac_hbm": round(b_dw / r["rmsnorm_dweight"] / 1e9 / pk["hbm_gbs"], 4),
+        "gather_dqkv_y_us": round(r["gather_dqkv_y"] * 1e6, 2),
+        "qkv_dw_gen_us": round(r["qkv_dw_gen"] * 1e6, 2), "qkv_dw_gen_tflops": _tflops(f_dw, r["qkv_dw_gen"]),
+        "qkv_dw_gen_frac": round(f_dw / r["qkv_dw_gen"] / 1e12 / pk["bf16_tflops"], 4),
+        "gen_rows": n_gen, "step_us": round(r["step"] * 1e6, 2),
+    }
+
+
 def run_cfg_pack(dev, flush) -> dict:
     """CFG pack: 12 sequences of 2048 und + 1024 gen rows (T = 36864), positions restarting per
     sequence: add-RMSNorm (+ plan), routed QKV + QK-norm + RoPE, routed O projection 3584 -> 3584
@@ -680,9 +745,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=512)
     ap.add_argument("--secondary", dest="secondary", action="store_true", default=True)
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
-    ap.add_argument("--profile", choices=["mlp", "cfg", "qkv_fp32"], default=None,
-                    help="run only one secondary workload (mlp, cfg: 5 warm-up + 50 timed steps; qkv_fp32: "
-                         "5 + 200) and print its figures; a short command for profiler captures")
+    ap.add_argument("--profile", choices=["mlp", "cfg", "qkv_fp32", "backward"], default=None,
+                    help="run only one secondary workload (mlp, cfg, backward: 5 warm-up + 50 timed steps; "
+                         "qkv_fp32: 5 + 200) and print its figures; a short command for profiler captures")
     ap.add_argument("--cpu-baseline-child", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_baseline_child is not None:
@@ -698,7 +763,7 @@ def main():
         mot.load_library()
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        fn = {"mlp": run_mlp, "cfg": run_cfg_pack, "qkv_fp32": run_qkv_fp32_rope}[args.profile]
+        fn = {"mlp": run_mlp, "cfg": run_cfg_pack, "qkv_fp32": run_qkv_fp32_rope, "backward": run_backward}[args.profile]
         print(json.dumps({args.profile: fn(dev, L2Flush(dev))}), flush=True)
         return
     if args.warmup < 3:

@@ -299,38 +299,41 @@ int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_plan, int64_
  * mot_add_rmsnorm_backward -- input gradient of mot_fused_add_rmsnorm ([RFC-435] §3
  * BAGEL-specific rules: the frozen und operators still need dX, so both weight sets take
  * part; [PR-503] gated-norm commit: the backward is assembled from deterministic pieces,
- * a dx kernel first).
+ * a dx kernel and the per-row weight-gradient partials).
  *   dy        [T][H] bf16      gradient of y.
  *   d_res_out [T][H] bf16      gradient reaching res_out (the residual stream), or NULL.
  *   s         [T][H] bf16      the forward's res_out (s = bf16(x + res)).
- *   w         [2][H] bf16      the forward's norm weights; mod [T] uint8 as in the forward.
- *   ws        workspace of at least mot_workspace_bytes(T); its error word receives device
- *             errors (a modality other than 0/1). The plan it holds is not read here.
+ *   w         [2][H] bf16      the forward's norm weights.
+ *   ws        the routing plan of the forward's mod for this T (mot_route_plan, or the
+ *             forward norm's); it selects each row's weight set, and its error word receives
+ *             device errors (a plan for another T: MOT_DEV_PLAN_MISMATCH).
  *   dx        [T][H] bf16      out: the gradient of x and of res (s = x + res passes it to both).
- *   rstd      [T] fp32         out: each row's rstd (the forward's), for mot_rmsnorm_dweight.
+ *   rstd      [T] fp32         out: each row's rstd (the forward's).
+ *   dw_partials  [H/64][T][64] fp32, or NULL: out: the weight-gradient partials
+ *             p[r][j] = dy[r][j] * (s[r][j] * rstd[r]) in blocks of 64 columns, rows in the
+ *             plan's order: element (j / 64, i, j % 64) belongs to row perm[i] -- so each weight
+ *             set's rows are one contiguous run in ascending order. mot_rmsnorm_dweight folds them.
  * Per row, every operation rounded on its own in fp32: rstd on the forward's fixed tree;
  * xh = s * rstd; g = dy * w[e]; dot = sum of g * xh on the same tree; c = dot / H;
  * dx = bf16(rstd * (g - xh * c) (+ d_res_out)). Geometry as mot_fused_add_rmsnorm; all
- * pointers 16-byte aligned device memory of the stream's device (mod: any alignment).
+ * pointers 16-byte aligned device memory of the stream's device. A plan that failed (bad
+ * modality) leaves every output undefined.
  */
 int mot_add_rmsnorm_backward(const mot_bf16* dy, const mot_bf16* d_res_out, const mot_bf16* s,
-                             const mot_bf16* w, const uint8_t* mod, int64_t T, int H, float eps,
-                             void* ws, size_t ws_bytes, mot_bf16* dx, float* rstd, void* stream);
+                             const mot_bf16* w, int64_t T, int H, float eps, void* ws, size_t ws_bytes,
+                             mot_bf16* dx, float* rstd, float* dw_partials, void* stream);
 
 /*
  * mot_rmsnorm_dweight -- gradient of both norm weight sets ([PR-503] gated-norm commit:
  * per-row fp32 partials, then the ascending-row fp32 left fold).
- *   dy, s     [T][H] bf16      as in mot_add_rmsnorm_backward; rstd [T] fp32 its output.
- *   ws        workspace holding the routing plan of mod for this T (mot_route_plan or the
- *             forward norm); the rows of each set are taken from it in ascending order.
+ *   dw_partials  [H/64][T][64] fp32  mot_add_rmsnorm_backward's partials (plan order).
+ *   ws        the same routing plan.
  *   dw        [2][H] fp32      out: dw[e][j] = ((p_r0 + p_r1) + p_r2) + ... over the rows
- *             r0 < r1 < ... of set e, p_r = dy[r][j] * (s[r][j] * rstd[r]); 0 for a set
- *             without rows.
- * A plan for another T sets MOT_DEV_PLAN_MISMATCH; a plan that failed (bad modality) leaves
- * dw undefined. Geometry: 256 <= H <= 8192, H a multiple of 256.
+ *             r0 < r1 < ... of set e; +0 for a set without rows.
+ * Geometry: 256 <= H <= 8192, H a multiple of 256. Errors as mot_add_rmsnorm_backward.
  */
-int mot_rmsnorm_dweight(const mot_bf16* dy, const mot_bf16* s, const float* rstd, int64_t T, int H,
-                        void* ws, size_t ws_bytes, float* dw, void* stream);
+int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, void* ws, size_t ws_bytes, float* dw,
+                        void* stream);
 
 /*
  * mot_selftest_wait_timeout -- exercises the bounded wait that every pipeline wait of the

@@ -65,9 +65,9 @@ _SIGNATURES = {
     "mot_selftest_wait_timeout": (_c_i, [_c_p, _c_sz, _c_p]),
     "mot_rope_table_fill_host": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
     "mot_rope_table_fill_host_fp32": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
-    "mot_add_rmsnorm_backward": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p,
+    "mot_add_rmsnorm_backward": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p, _c_p,
                                         _c_p]),
-    "mot_rmsnorm_dweight": (_c_i, [_c_p, _c_p, _c_p, _c_i64, _c_i, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_rmsnorm_dweight": (_c_i, [_c_p, _c_i64, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_dx": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_dw": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
@@ -343,23 +343,31 @@ def mot_routed_gemm_dw(dout_plan, a_plan, ws, expert: int = 1, out=None, stream=
     return out
 
 
-def mot_add_rmsnorm_backward(dy, s, w, mod, eps: float, ws, d_res_out=None, dx=None, rstd=None, stream=None):
+def mot_add_rmsnorm_backward(dy, s, w, eps: float, ws, d_res_out=None, dx=None, rstd=None, dw_partials=None,
+                             stream=None):
     """Input gradient of the fused add-RMSNorm: returns (dx [T][H] bf16, rstd [T] fp32).
-    `s` is the forward's res_out; `ws` (>= mot_workspace_bytes(T)) receives device errors."""
+    `s` is the forward's res_out and `ws` holds the routing plan of the forward's mod. If
+    `dw_partials` (fp32 [H/64][T][64]) is given, the per-row weight-gradient partials are
+    written there in the plan's row order."""
     T, H = dy.shape
     _dev(dy, "dy", torch.bfloat16, 2)
     _dev(s, "s", torch.bfloat16, 2)
     _dev(w, "w", torch.bfloat16, 2)
-    _dev(mod, "mod", torch.uint8, 1)
     _dev(ws, "ws", torch.uint8, 1)
-    if tuple(s.shape) != (T, H) or tuple(w.shape) != (2, H) or mod.numel() != T:
-        raise ValueError("s must be [T, H], w [2, H] and mod [T]")
+    if tuple(s.shape) != (T, H) or tuple(w.shape) != (2, H):
+        raise ValueError("s must be [T, H] and w [2, H]")
     rp = None
     if d_res_out is not None:
         _dev(d_res_out, "d_res_out", torch.bfloat16, 2)
         if tuple(d_res_out.shape) != (T, H):
             raise ValueError("d_res_out must be [T, H]")
         rp = d_res_out.data_ptr()
+    pp = None
+    if dw_partials is not None:
+        _dev(dw_partials, "dw_partials", torch.float32, 3)
+        if tuple(dw_partials.shape) != (H // 64, T, 64):
+            raise ValueError(f"dw_partials must be [{H // 64}, {T}, 64]")
+        pp = dw_partials.data_ptr()
     if dx is None:
         dx = torch.empty((T, H), dtype=torch.bfloat16, device=dy.device)
     if rstd is None:
@@ -367,26 +375,25 @@ def mot_add_rmsnorm_backward(dy, s, w, mod, eps: float, ws, d_res_out=None, dx=N
     _dev(dx, "dx", torch.bfloat16, 2)
     _dev(rstd, "rstd", torch.float32, 1)
     _check("mot_add_rmsnorm_backward", _lib().mot_add_rmsnorm_backward(
-        dy.data_ptr(), rp, s.data_ptr(), w.data_ptr(), mod.data_ptr(), T, H, eps, ws.data_ptr(), ws.numel(),
-        dx.data_ptr(), rstd.data_ptr(), _stream(dy, stream)))
+        dy.data_ptr(), rp, s.data_ptr(), w.data_ptr(), T, H, eps, ws.data_ptr(), ws.numel(), dx.data_ptr(),
+        rstd.data_ptr(), pp, _stream(dy, stream)))
     return dx, rstd
 
 
-def mot_rmsnorm_dweight(dy, s, rstd, ws, dw=None, stream=None):
-    """Gradient of both norm weight sets, [2][H] fp32, as an ascending-row fp32 left fold per set."""
-    T, H = dy.shape
-    _dev(dy, "dy", torch.bfloat16, 2)
-    _dev(s, "s", torch.bfloat16, 2)
-    _dev(rstd, "rstd", torch.float32, 1)
+def mot_rmsnorm_dweight(dw_partials, ws, dw=None, stream=None):
+    """Gradient of both norm weight sets, [2][H] fp32: the ascending-row fp32 left fold of the
+    partials of mot_add_rmsnorm_backward over each set's rows."""
+    nb, T, c64 = dw_partials.shape
+    _dev(dw_partials, "dw_partials", torch.float32, 3)
     _dev(ws, "ws", torch.uint8, 1)
-    if tuple(s.shape) != (T, H) or rstd.numel() != T:
-        raise ValueError("s must be [T, H] and rstd [T]")
+    if c64 != 64:
+        raise ValueError("dw_partials must be [H/64, T, 64]")
+    H = nb * 64
     if dw is None:
-        dw = torch.empty((2, H), dtype=torch.float32, device=dy.device)
+        dw = torch.empty((2, H), dtype=torch.float32, device=dw_partials.device)
     _dev(dw, "dw", torch.float32, 2)
     _check("mot_rmsnorm_dweight", _lib().mot_rmsnorm_dweight(
-        dy.data_ptr(), s.data_ptr(), rstd.data_ptr(), T, H, ws.data_ptr(), ws.numel(), dw.data_ptr(),
-        _stream(dy, stream)))
+        dw_partials.data_ptr(), T, H, ws.data_ptr(), ws.numel(), dw.data_ptr(), _stream(dw_partials, stream)))
     return dw
 
 

@@ -15,13 +15,17 @@
 //   dw[e][j] = ((p_r0 + p_r1) + p_r2) + ... over the rows r0 < r1 < ... of weight set e,
 //   p_r = dy[r][j] * xh[r][j].
 //
-// add_rmsnorm_bwd_kernel   one warp per row; lane l holds columns 256 j + 8 l + t (the
-//                          forward's tree layout) of s and dy in registers for three passes
-//                          (sum of s^2, dot, output), writes dx and the row's rstd.
-// rmsnorm_dw_fold_kernel   one CTA per (weight set, 64-column block): its 128 threads stream
-//                          the set's rows (ascending, from the routing plan) through a ring of
-//                          shared-memory stages with cp.async; 64 of them fold one column each.
+// add_rmsnorm_bwd_kernel   persistent, one CTA per SM, rows in the routing plan's order: a
+//                          producer warp bulk-copies whole rows of s, dy (and d_res_out) into
+//                          shared-memory slots; one consumer warp per slot runs the three passes
+//                          (sum of s^2, dot, output) with lane l on columns 256 j + 8 l + t (the
+//                          forward's tree layout), writes dx, the row's rstd and its partials.
+// rmsnorm_dw_fold_kernel   one CTA per (weight set, 64-column block): the set's partials, left
+//                          by the backward kernel as one contiguous run per column block,
+//                          stream in by TMA tiles; two warps fold one column per thread over
+//                          the set's rows in ascending order.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "mot.h"
@@ -32,16 +36,18 @@ namespace mot {
 namespace bwd {
 
 struct NormBwdArgs {
-  const uint4* dy;
-  const uint4* s;
-  const uint4* dro;  // may be null
-  const uint4* w;    // [2][H/8]
-  const uint8_t* mod;
+  const uint16_t* dy;
+  const uint16_t* s;
+  const uint16_t* dro;  // may be null
+  const uint16_t* w;    // [2][H]
   int T, H;
   float eps;
   uint4* dx;
   float* rstd;
+  float* part;          // [H/64][T][64] per-row dweight partials by plan position, or null
+  const uint8_t* ws;    // the routing plan: rows are visited in its order
   uint32_t* err;
+  int consumers;        // consumer warps = row slots
 };
 
 __device__ __forceinline__ float elem(const uint4& v, int t) {
@@ -55,200 +61,286 @@ __device__ __forceinline__ float warp_tree(float p) {
   return p;
 }
 
+// One CTA per SM, persistent over the plan positions b + k G (b = blockIdx.x), so the
+// weight-gradient partials of each weight set come out as one contiguous run. Warp 0 streams
+// the whole rows of s, dy (and d_res_out) of those positions into C shared-memory slots with
+// 1D bulk copies; consumer warp c owns slot c and takes every C-th position of the CTA. A consumer keeps the row's s in registers
+// after the first pass, reads dy, the weights and d_res_out from shared memory, writes dx
+// and rstd, and hands the slot back after the last pass.
+constexpr int kBwdMaxConsumers = 8;
+constexpr size_t kBwdSlotBudget = 180 * 1024;
+
 template <int NJ>  // NJ >= H / 256
-__global__ void __launch_bounds__(256) add_rmsnorm_bwd_kernel(const NormBwdArgs a) {
-  extern __shared__ uint4 sw[];  // both weight sets, [2][H/8]
-  const int h8 = a.H / 8, nj = a.H / 256;
-  for (int i = threadIdx.x; i < 2 * h8; i += blockDim.x) sw[i] = __ldg(a.w + i);
+__global__ void __launch_bounds__(32 * (1 + kBwdMaxConsumers), 1) add_rmsnorm_bwd_kernel(const NormBwdArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int C = a.consumers;
+  const uint32_t row_bytes = uint32_t(a.H) * 2;
+  const int nrows = a.dro ? 3 : 2;  // rows per slot: s, dy (, d_res_out)
+  uint8_t* wbuf = smem;                   // [2][H] norm weights
+  uint8_t* slots = smem + 2 * row_bytes;  // C x nrows rows
+  uint64_t* full = reinterpret_cast<uint64_t*>(slots + size_t(C) * nrows * row_bytes);
+  uint64_t* empty = full + kBwdMaxConsumers;
+  uint64_t* wbar = empty + kBwdMaxConsumers;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(wbar + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = int(blockIdx.x), G = int(gridDim.x);
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < C; ++c) {
+      mbar_init(smem_u32(&full[c]), 1);
+      mbar_init(smem_u32(&empty[c]), 1);
+    }
+    mbar_init(smem_u32(wbar), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws);
+  if (hdr->magic != kPlanMagic || hdr->T != a.T) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.err, MOT_DEV_PLAN_MISMATCH);
+    return;  // uniform across the grid
+  }
+  if (hdr->count[0] + hdr->count[1] != a.T) return;  // no plan (bad modality): nothing is defined
+  const int32_t* perm = reinterpret_cast<const int32_t*>(a.ws + perm_offset());
+  const int count0 = hdr->count[0];
+
+  if (warp == 0) {
+    // ---------------- producer: plan positions b + k G, their rows read 32 ahead ----------------
+    if (lane == 0) {
+      mbar_arrive_expect_tx(smem_u32(wbar), 2 * row_bytes);
+      bulk_load(smem_u32(wbuf), a.w, 2 * row_bytes, smem_u32(wbar));
+    }
+    int issued = 0;
+    bool ok = true;
+    for (int k0 = 0; ok; k0 += 32) {
+      const int64_t mine = int64_t(b) + int64_t(k0 + lane) * G;
+      const int my_row = mine < a.T ? perm[mine] : -1;
+      for (int q = 0; q < 32; ++q) {
+        const int k = k0 + q;
+        const int row = __shfl_sync(0xffffffffu, my_row, q);
+        if (row < 0) {
+          ok = false;
+          break;
+        }
+        const int c = k % C;
+        const uint32_t round = uint32_t(k / C);
+        if (lane == 0) {
+          if (!mbar_wait(smem_u32(&empty[c]), (round & 1u) ^ 1u, abort_flag, a.err)) {
+            ok = false;
+          } else {
+            uint8_t* slot = slots + size_t(c) * nrows * row_bytes;
+            const uint32_t fb = smem_u32(&full[c]);
+            const int64_t off = int64_t(row) * a.H;  // elements
+            mbar_arrive_expect_tx(fb, uint32_t(nrows) * row_bytes);
+            bulk_load(smem_u32(slot), a.s + off, row_bytes, fb);
+            bulk_load(smem_u32(slot + row_bytes), a.dy + off, row_bytes, fb);
+            if (a.dro) bulk_load(smem_u32(slot + 2 * row_bytes), a.dro + off, row_bytes, fb);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        issued = k + 1;
+      }
+    }
+    // no copy may still be landing when the CTA exits: wait for the last fill of every slot
+    if (lane == 0) {
+      mbar_drain(smem_u32(wbar), 0);
+      for (int k = issued - C > 0 ? issued - C : 0; k < issued; ++k)
+        mbar_drain(smem_u32(&full[k % C]), uint32_t(k / C) & 1u);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int c = warp - 1;
+  if (c >= C) return;
+  const int nj = a.H >> 8, h8 = a.H >> 3;
   const float fH = float(a.H);
-  for (int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < a.T; row += warps) {
-    const int e = a.mod[row];
-    if (e > 1) {
-      if (lane == 0) atomicOr(a.err, MOT_DEV_BAD_MODALITY);
-      continue;
-    }
-    const uint4* srow = a.s + row * h8 + lane;
-    const uint4* drow = a.dy + row * h8 + lane;
-    // rows wider than 4096 keep only s in registers and read dy again in passes 2 and 3
-    constexpr bool kHoldDy = NJ <= 16;
-    uint4 sv[NJ], dv[kHoldDy ? NJ : 1];
+  const uint4* ss4 = reinterpret_cast<const uint4*>(slots + size_t(c) * nrows * row_bytes);
+  const uint4* sd4 = ss4 + h8;
+  const uint4* sr4 = ss4 + 2 * h8;
+  if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(wbar), 0, abort_flag, a.err))) return;
+  for (int k = c;; k += C) {
+    const int64_t pos = int64_t(b) + int64_t(k) * G;  // plan position
+    if (pos >= a.T) break;
+    const int64_t row = perm[pos];
+    const int e = pos < count0 ? 0 : 1;
+    const uint32_t round = uint32_t(k / C);
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[c]), round & 1u, abort_flag, a.err))) break;
+    {
+      // pass 1: sum of s^2 on the forward's tree; s stays in registers (rows up to 4096 wide;
+      // wider rows read it from the slot again)
+      constexpr bool kHoldS = NJ <= 16;
+      uint4 sv[kHoldS ? NJ : 1];
+      auto s_at = [&](int j) { if constexpr (kHoldS) return sv[j]; else return ss4[32 * j + lane]; };
+      float ss = 0.0f;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (j < nj) {
-        sv[j] = __ldcs(srow + j * 32);
-        if constexpr (kHoldDy) dv[j] = __ldcs(drow + j * 32);
-      }
-    }
-    // pass 1: sum of s^2 on the forward's tree
-    float ss = 0.0f;
+      for (int j = 0; j < NJ; ++j) {
+        if (j < nj) {
+          const uint4 s1 = ss4[32 * j + lane];
+          if constexpr (kHoldS) sv[j] = s1;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (j < nj) {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float v = elem(sv[j], t);
-          ss = __fadd_rn(ss, __fmul_rn(v, v));
+          for (int t = 0; t < 8; ++t) {
+            const float v = elem(s1, t);
+            ss = __fadd_rn(ss, __fmul_rn(v, v));
+          }
         }
       }
-    }
-    ss = warp_tree(ss);
-    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, fH), a.eps)));
-    // pass 2: dot = sum of (dy * w) * (s * rstd) on the same tree
-    const uint4* wrow = sw + e * h8 + lane;
-    float dot = 0.0f;
+      ss = warp_tree(ss);
+      const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, fH), a.eps)));
+      // pass 2: dot = sum of (dy * w) * (s * rstd) on the same tree
+      const uint4* wrow = reinterpret_cast<const uint4*>(wbuf + size_t(e) * row_bytes);
+      float dot = 0.0f;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (j < nj) {
-        const uint4 wv = wrow[j * 32];
-        uint4 d;
-        if constexpr (kHoldDy) d = dv[j]; else d = __ldg(drow + j * 32);
+      for (int j = 0; j < NJ; ++j) {
+        if (j < nj) {
+          const uint4 wv = wrow[32 * j + lane], d = sd4[32 * j + lane], sj = s_at(j);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float xh = __fmul_rn(elem(sv[j], t), rstd);
-          const float g = __fmul_rn(elem(d, t), elem(wv, t));
-          dot = __fadd_rn(dot, __fmul_rn(g, xh));
+          for (int t = 0; t < 8; ++t) {
+            const float xh = __fmul_rn(elem(sj, t), rstd);
+            const float g = __fmul_rn(elem(d, t), elem(wv, t));
+            dot = __fadd_rn(dot, __fmul_rn(g, xh));
+          }
         }
       }
-    }
-    dot = warp_tree(dot);
-    const float c = __fdiv_rn(dot, fH);
-    // pass 3: ds = rstd * (g - xh * c) (+ d_res_out), one cast
-    uint4* orow = a.dx + row * h8 + lane;
-    const uint4* rrow = a.dro ? a.dro + row * h8 + lane : nullptr;
+      dot = warp_tree(dot);
+      const float cc = __fdiv_rn(dot, fH);
+      // pass 3: ds = rstd * (g - xh * c) (+ d_res_out), one cast
+      uint4* orow = a.dx + row * h8 + lane;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (j < nj) {
-        const uint4 wv = wrow[j * 32];
-        uint4 d;
-        if constexpr (kHoldDy) d = dv[j]; else d = __ldg(drow + j * 32);
-        uint4 rv = make_uint4(0u, 0u, 0u, 0u);
-        if (rrow) rv = __ldcs(rrow + j * 32);
-        float o[8];
+      for (int j = 0; j < NJ; ++j) {
+        if (j < nj) {
+          const uint4 wv = wrow[32 * j + lane], d = sd4[32 * j + lane], sj = s_at(j);
+          const uint4 rv = a.dro ? sr4[32 * j + lane] : make_uint4(0u, 0u, 0u, 0u);
+          float o[8], pp[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float xh = __fmul_rn(elem(sv[j], t), rstd);
-          const float g = __fmul_rn(elem(d, t), elem(wv, t));
-          float ds = __fmul_rn(rstd, __fsub_rn(g, __fmul_rn(xh, c)));
-          if (rrow) ds = __fadd_rn(ds, elem(rv, t));
-          o[t] = ds;
+          for (int t = 0; t < 8; ++t) {
+            const float xh = __fmul_rn(elem(sj, t), rstd);
+            const float g = __fmul_rn(elem(d, t), elem(wv, t));
+            float ds = __fmul_rn(rstd, __fsub_rn(g, __fmul_rn(xh, cc)));
+            if (a.dro) ds = __fadd_rn(ds, elem(rv, t));
+            o[t] = ds;
+            pp[t] = __fmul_rn(elem(d, t), xh);
+          }
+          if (a.part) {
+            // columns 256 j + 8 lane + t: block 4 j + lane / 8, offset 8 (lane % 8) + t
+            float4* pd = reinterpret_cast<float4*>(a.part + ((int64_t(4 * j + (lane >> 3)) * a.T + pos) << 6) +
+                                                   8 * (lane & 7));
+            __stcs(pd, make_float4(pp[0], pp[1], pp[2], pp[3]));
+            __stcs(pd + 1, make_float4(pp[4], pp[5], pp[6], pp[7]));
+          }
+          __stcs(orow + 32 * j, make_uint4(pack_bf2(o[0], o[1]), pack_bf2(o[2], o[3]), pack_bf2(o[4], o[5]),
+                                           pack_bf2(o[6], o[7])));
         }
-        __stcs(orow + j * 32, make_uint4(pack_bf2(o[0], o[1]), pack_bf2(o[2], o[3]), pack_bf2(o[4], o[5]),
-                                         pack_bf2(o[6], o[7])));
       }
+      if (lane == 0) a.rstd[row] = rstd;
     }
-    if (lane == 0) a.rstd[row] = rstd;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[c]));
   }
 }
 
-constexpr int kFoldCols = 64, kFoldRows = 32, kFoldStages = 12, kFoldThreads = 128;
-constexpr size_t kFoldStageBytes = size_t(2) * kFoldRows * kFoldCols * 2 + kFoldRows * 4;
-constexpr size_t kFoldSmem = kFoldStages * kFoldStageBytes;
+// Weight-gradient fold. The backward kernel leaves the per-row partials p = dy * (s * rstd)
+// in fp32 blocks of 64 columns by plan position, part[cb][i][64], so the rows of a weight set
+// in a column block are one contiguous run in ascending row order. One CTA per (set, block):
+// warp 0 streams 64-row tiles of the run (16 KB) with TMA into a ring of kFoldStages slots;
+// warps 1 and 2 fold 32 columns each, one column per thread.
+constexpr int kFoldCols = 64, kFoldRows = 64, kFoldStages = 8;
+constexpr int kFoldThreads = 32 * 3;
+constexpr uint32_t kFoldPartBytes = kFoldRows * kFoldCols * 4;  // 16 KB
+constexpr size_t kFoldSmem = 128 + kFoldStages * size_t(kFoldPartBytes) + 2 * kFoldStages * 8 + 16;
 
 struct FoldArgs {
-  const uint16_t* dy;
-  const uint16_t* s;
-  const float* rstd;
   const uint8_t* ws;
   int T, H;
   float* dw;
+  uint32_t* err;
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void tma_load_2d_cta(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
-__global__ void __launch_bounds__(kFoldThreads) rmsnorm_dw_fold_kernel(const FoldArgs a) {
-  extern __shared__ __align__(16) uint8_t fsm[];
-  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws);
+__global__ void __launch_bounds__(kFoldThreads) rmsnorm_dw_fold_kernel(const __grid_constant__ CUtensorMap tm_part,
+                                                                      const FoldArgs a) {
+  extern __shared__ __align__(128) uint8_t fraw[];
+  uint8_t* fsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fraw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(fsm + kFoldStages * size_t(kFoldPartBytes));
+  uint64_t* empty = full + kFoldStages;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + kFoldStages);
   const int ncb = a.H / kFoldCols;
   const int e = int(blockIdx.x) / ncb, cb = int(blockIdx.x) % ncb;
-  const int tid = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws);
   if (hdr->magic != kPlanMagic || hdr->T != a.T) {
-    if (blockIdx.x == 0 && tid == 0) atomicOr(const_cast<uint32_t*>(&hdr->error), MOT_DEV_PLAN_MISMATCH);
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.err, MOT_DEV_PLAN_MISMATCH);
     return;
   }
   if (hdr->count[0] + hdr->count[1] != a.T) return;  // no plan (bad modality): nothing is defined
+  const int start = e == 0 ? 0 : hdr->count[0];
   const int count = hdr->count[e];
-  const int32_t* rows = reinterpret_cast<const int32_t*>(a.ws + perm_offset()) + (e ? hdr->count[0] : 0);
   const int nst = (count + kFoldRows - 1) / kFoldRows;
-  const int col0 = cb * kFoldCols;
-  auto stage_dy = [&](int slot) { return fsm + size_t(slot) * kFoldStageBytes; };
-  auto stage_s = [&](int slot) { return fsm + size_t(slot) * kFoldStageBytes + kFoldRows * kFoldCols * 2; };
-  auto stage_r = [&](int slot) { return fsm + size_t(slot) * kFoldStageBytes + 2 * kFoldRows * kFoldCols * 2; };
-  auto load_stage = [&](int k, int slot) {
-    // 32 rows x 64 columns of dy and of s (8 chunks of 16 B per row), and the rows' rstd
-    for (int c = tid; c < 2 * kFoldRows * 8; c += kFoldThreads) {
-      const int arr = c / (kFoldRows * 8), rr = (c / 8) % kFoldRows, part = c % 8;
-      const int i = k * kFoldRows + rr;
-      if (i < count) {
-        const int64_t r = rows[i];
-        const uint16_t* src = (arr ? a.s : a.dy) + r * a.H + col0 + part * 8;
-        uint8_t* dst = (arr ? stage_s(slot) : stage_dy(slot)) + (rr * kFoldCols + part * 8) * 2;
-        cp_async16(smem_u32(dst), src);
-      }
+  if (threadIdx.x == 0) {
+    for (int sl = 0; sl < kFoldStages; ++sl) {
+      mbar_init(smem_u32(&full[sl]), 1);
+      mbar_init(smem_u32(&empty[sl]), 2);  // the two fold warps
     }
-    if (tid < kFoldRows) {
-      const int i = k * kFoldRows + tid;
-      if (i < count) cp_async4(smem_u32(stage_r(slot) + tid * 4), a.rstd + rows[i]);
-    }
-  };
-#pragma unroll 1
-  for (int k = 0; k < kFoldStages - 1; ++k) {
-    if (k < nst) load_stage(k, k);
-    cp_async_commit();
+    *abort_flag = 0u;
+    fence_mbar_init();
   }
-  float acc = -0.0f;  // -0 + p = p for every p: the fold starts with the first row's partial
-#pragma unroll 1
+  __syncthreads();
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int k = 0; k < nst; ++k) {
+        const int slot = k % kFoldStages;
+        const uint32_t round = uint32_t(k / kFoldStages);
+        if (!mbar_wait(smem_u32(&empty[slot]), (round & 1u) ^ 1u, abort_flag, a.err)) break;
+        const uint32_t fb = smem_u32(&full[slot]);
+        mbar_arrive_expect_tx(fb, kFoldPartBytes);
+        tma_load_2d_cta(smem_u32(fsm + size_t(slot) * kFoldPartBytes), &tm_part, 0,
+                        cb * a.T + start + k * kFoldRows, fb);
+        issued = k + 1;
+      }
+      for (int k = issued - kFoldStages > 0 ? issued - kFoldStages : 0; k < issued; ++k)
+        mbar_drain(smem_u32(&full[k % kFoldStages]), uint32_t(k / kFoldStages) & 1u);
+    }
+    return;
+  }
+  // ---------------- folds: warp 1 columns 0..31, warp 2 columns 32..63 ----------------
+  const int col = (warp - 1) * 32 + lane;
+  float acc = -0.0f;  // -0 + p = p for every p: the fold starts with the set's first partial
+  bool ok = true;
   for (int k = 0; k < nst; ++k) {
-    cp_async_wait<kFoldStages - 2>();
-    __syncthreads();  // stage k landed for every thread; stage k - 1 is no longer read
-    const int kn = k + kFoldStages - 1;
-    if (kn < nst) load_stage(kn, kn % kFoldStages);
-    cp_async_commit();
-    if (tid < kFoldCols) {
-      const int slot = k % kFoldStages;
-      const uint16_t* sdy = reinterpret_cast<const uint16_t*>(stage_dy(slot));
-      const uint16_t* ssv = reinterpret_cast<const uint16_t*>(stage_s(slot));
-      const float* srs = reinterpret_cast<const float*>(stage_r(slot));
-      const int n = count - k * kFoldRows < kFoldRows ? count - k * kFoldRows : kFoldRows;
-#pragma unroll 4
-      for (int rr = 0; rr < n; ++rr) {
-        const float xh = __fmul_rn(bf_to_f(ssv[rr * kFoldCols + tid]), srs[rr]);
-        acc = __fadd_rn(acc, __fmul_rn(bf_to_f(sdy[rr * kFoldCols + tid]), xh));
-      }
+    const int slot = k % kFoldStages;
+    const uint32_t round = uint32_t(k / kFoldStages);
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[slot]), round & 1u, abort_flag, a.err));
+    if (!ok) break;
+    const float* sp = reinterpret_cast<const float*>(fsm + size_t(slot) * kFoldPartBytes);
+    const int n = count - k * kFoldRows < kFoldRows ? count - k * kFoldRows : kFoldRows;
+    if (n == kFoldRows) {
+#pragma unroll
+      for (int rr = 0; rr < kFoldRows; ++rr) acc = __fadd_rn(acc, sp[rr * kFoldCols + col]);
+    } else {
+      for (int rr = 0; rr < n; ++rr) acc = __fadd_rn(acc, sp[rr * kFoldCols + col]);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
   }
-  cp_async_wait<0>();
-  if (tid < kFoldCols) a.dw[int64_t(e) * a.H + col0 + tid] = count > 0 ? acc : 0.0f;
+  if (ok) a.dw[int64_t(e) * a.H + cb * kFoldCols + col] = count > 0 ? acc : 0.0f;
 }
 
 template <int NJ>
-static cudaError_t launch_bwd(const NormBwdArgs& a, int dev, cudaStream_t s) {
-  const size_t smem = size_t(a.H) * 2 * 2;
+static cudaError_t launch_bwd(const NormBwdArgs& a, int grid, size_t smem, cudaStream_t s) {
   cudaError_t st = cudaFuncSetAttribute(add_rmsnorm_bwd_kernel<NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         int(smem));
   if (st != cudaSuccess) return st;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, add_rmsnorm_bwd_kernel<NJ>, 256, smem) != cudaSuccess ||
-      per_sm < 1) {
-    cudaGetLastError();
-    per_sm = 1;
-  }
-  const int64_t want = (int64_t(a.T) + 7) / 8;
-  const int64_t cap = int64_t(per_sm) * sm_count(dev);
-  const int grid = int(want < cap ? want : cap);
-  add_rmsnorm_bwd_kernel<NJ><<<grid, 256, smem, s>>>(a);
+  add_rmsnorm_bwd_kernel<NJ><<<grid, 32 * (1 + a.consumers), smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -258,70 +350,89 @@ static cudaError_t launch_bwd(const NormBwdArgs& a, int dev, cudaStream_t s) {
 using namespace mot;
 
 extern "C" int mot_add_rmsnorm_backward(const mot_bf16* dy, const mot_bf16* d_res_out, const mot_bf16* s,
-                                        const mot_bf16* w, const uint8_t* mod, int64_t T, int H, float eps,
-                                        void* ws, size_t ws_bytes, mot_bf16* dx, float* rstd, void* stream) {
-  if (!dy || !s || !w || !mod || !ws || !dx || !rstd) return MOT_ERR_NULL;
+                                        const mot_bf16* w, int64_t T, int H, float eps, void* ws, size_t ws_bytes,
+                                        mot_bf16* dx, float* rstd, float* dw_partials, void* stream) {
+  if (!dy || !s || !w || !ws || !dx || !rstd) return MOT_ERR_NULL;
   if (T < 1 || T > MOT_MAX_TOKENS || H < 256 || H > 8192 || H % 256 != 0) return MOT_ERR_GEOMETRY;
   if (!(eps > 0.0f) || !(eps < 3.0e38f)) return MOT_ERR_ARG;
   if (!aligned16(dy) || (d_res_out && !aligned16(d_res_out)) || !aligned16(s) || !aligned16(w) || !aligned16(ws) ||
-      !aligned16(dx) || !aligned16(rstd))
+      !aligned16(dx) || !aligned16(rstd) || (dw_partials && !aligned16(dw_partials)))
     return MOT_ERR_ALIGN;
   if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const void* ptrs[] = {dy, d_res_out, s, w, mod, ws, dx, rstd};
+  const void* ptrs[] = {dy, d_res_out, s, w, ws, dx, rstd, dw_partials};
   int dev = -1;
   int rc = check_device(st, ptrs, 8, &dev);
   if (rc != MOT_OK) return rc;
   DeviceGuard guard(dev);
   bwd::NormBwdArgs a{};
-  a.dy = reinterpret_cast<const uint4*>(dy);
-  a.s = reinterpret_cast<const uint4*>(s);
-  a.dro = reinterpret_cast<const uint4*>(d_res_out);
-  a.w = reinterpret_cast<const uint4*>(w);
-  a.mod = mod;
+  a.dy = dy;
+  a.s = s;
+  a.dro = d_res_out;
+  a.w = w;
   a.T = int(T);
   a.H = H;
   a.eps = eps;
   a.dx = reinterpret_cast<uint4*>(dx);
   a.rstd = rstd;
+  a.part = dw_partials;
+  a.ws = static_cast<const uint8_t*>(ws);
   a.err = &static_cast<PlanHeader*>(ws)->error;
+  const size_t row_bytes = size_t(H) * 2;
+  const int nrows = d_res_out ? 3 : 2;
+  int C = int(bwd::kBwdSlotBudget / (nrows * row_bytes));
+  C = C > bwd::kBwdMaxConsumers ? bwd::kBwdMaxConsumers : C;
+  a.consumers = C;
+  const size_t smem =
+      2 * row_bytes + size_t(C) * nrows * row_bytes + (2 * bwd::kBwdMaxConsumers + 2) * sizeof(uint64_t);
+  const int sms = sm_count(dev);
+  const int grid = int(T < sms ? T : sms);
   const int nj = H / 256;
   cudaError_t e;
   if (nj <= 4)
-    e = bwd::launch_bwd<4>(a, dev, st);
+    e = bwd::launch_bwd<4>(a, grid, smem, st);
   else if (nj <= 8)
-    e = bwd::launch_bwd<8>(a, dev, st);
+    e = bwd::launch_bwd<8>(a, grid, smem, st);
   else if (nj <= 16)
-    e = bwd::launch_bwd<16>(a, dev, st);
+    e = bwd::launch_bwd<16>(a, grid, smem, st);
   else
-    e = bwd::launch_bwd<32>(a, dev, st);
+    e = bwd::launch_bwd<32>(a, grid, smem, st);
   return e == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
-extern "C" int mot_rmsnorm_dweight(const mot_bf16* dy, const mot_bf16* s, const float* rstd, int64_t T, int H,
-                                   void* ws, size_t ws_bytes, float* dw, void* stream) {
-  if (!dy || !s || !rstd || !ws || !dw) return MOT_ERR_NULL;
+extern "C" int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, void* ws, size_t ws_bytes, float* dw,
+                                   void* stream) {
+  if (!dw_partials || !ws || !dw) return MOT_ERR_NULL;
   if (T < 1 || T > MOT_MAX_TOKENS || H < 256 || H > 8192 || H % 256 != 0) return MOT_ERR_GEOMETRY;
-  if (!aligned16(dy) || !aligned16(s) || !aligned16(rstd) || !aligned16(ws) || !aligned16(dw)) return MOT_ERR_ALIGN;
+  if (!aligned16(dw_partials) || !aligned16(ws) || !aligned16(dw)) return MOT_ERR_ALIGN;
   if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const void* ptrs[] = {dy, s, rstd, ws, dw};
+  const void* ptrs[] = {dw_partials, ws, dw};
   int dev = -1;
-  int rc = check_device(st, ptrs, 5, &dev);
+  int rc = check_device(st, ptrs, 3, &dev);
   if (rc != MOT_OK) return rc;
   DeviceGuard guard(dev);
   if (cudaFuncSetAttribute(bwd::rmsnorm_dw_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(bwd::kFoldSmem)) != cudaSuccess)
     return MOT_ERR_CUDA;
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return MOT_ERR_CUDA;
+  // the partials as a 2D fp32 tensor of (H / 64) * T rows of 64 columns
+  CUtensorMap tm_part;
+  cuuint64_t dims[2] = {uint64_t(bwd::kFoldCols), uint64_t(H / bwd::kFoldCols) * uint64_t(T)};
+  cuuint64_t strides[1] = {uint64_t(bwd::kFoldCols) * 4};
+  cuuint32_t box[2] = {uint32_t(bwd::kFoldCols), uint32_t(bwd::kFoldRows)};
+  cuuint32_t estr[2] = {1, 1};
+  if (enc(&tm_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(dw_partials), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MOT_ERR_CUDA;
   bwd::FoldArgs a{};
-  a.dy = dy;
-  a.s = s;
-  a.rstd = rstd;
   a.ws = static_cast<const uint8_t*>(ws);
   a.T = int(T);
   a.H = H;
   a.dw = dw;
-  const int grid = 2 * (H / bwd::kFoldCols);
-  bwd::rmsnorm_dw_fold_kernel<<<grid, bwd::kFoldThreads, bwd::kFoldSmem, st>>>(a);
+  a.err = &static_cast<PlanHeader*>(ws)->error;
+  bwd::rmsnorm_dw_fold_kernel<<<2 * (H / bwd::kFoldCols), bwd::kFoldThreads, bwd::kFoldSmem, st>>>(tm_part, a);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }

@@ -592,7 +592,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // loads, the last partial block is gathered four rows at a time with rows past the run
 // pointed outside the tensor, which the copy fills with zeros. Pair tiles cover 256 n x 256 k;
 // each accumulates its 64-row blocks in ascending order into one fp32 accumulator (no split
-// of the reduction), and the epilogue stores fp32 rows of dW.
+// of the reduction), and the epilogue stores fp32 rows of dW through a per-warp transpose in
+// shared memory (five pipeline stages leave room for it).
+constexpr int kDwStages = 5;  // one stage fewer than the routed kernel: room for the store staging
+constexpr int kDwBars = 2 * kDwStages + 5;
+constexpr int kDwStageFloats = 32 * 36;  // a warp's 32 x 32 fp32 block, rows padded to 36
+constexpr size_t kDwSmem = 1024 + size_t(kDwStages) * STAGE_BYTES + 256 + size_t(EPI_WARPS) * kDwStageFloats * 4;
+
 struct DwArgs {
   const uint8_t* ws;
   uint32_t* err;
@@ -607,6 +613,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                           const DwArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int STAGES = kDwStages;
   uint8_t* sa = smem;
   uint8_t* sb = smem + STAGES * A_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -615,8 +622,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = bars + 2 * STAGES + 2;
   uint64_t* drain = bars + 2 * STAGES + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kDwBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  float* stagebuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -766,23 +774,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else {
     // ---------------- epilogue (both CTAs): fp32 rows of dW ----------------
+    // Each warp turns its 32 rows x 32 columns blocks around in shared memory, so one store
+    // instruction writes four whole 128-byte row segments instead of 32 scattered pieces.
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
+    float* buf = stagebuf + (warp - 2) * kDwStageFloats;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cluster; u < total; u += nclusters) {
       const int mt = u % m_tiles, nt = u / m_tiles;
-      const int n = mt * BN + int(rank) * BN_HALF + quarter * 32 + lane;
+      const int n_base = mt * BN + int(rank) * BN_HALF + quarter * 32;  // this warp's first dW row
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16) + half * 128;
-      float4* orow = reinterpret_cast<float4*>(args.dw + int64_t(n) * args.K + nt * BN + half * 128);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float v[32];
-        tmem_ld32(taddr + c * 32, v);
+        tmem_ld32(taddr + c * 32, v);  // row n_base + lane, columns 32 c .. 32 c + 31 of this half
 #pragma unroll
-        for (int i = 0; i < 8; ++i) orow[c * 8 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4*>(buf + lane * 36 + 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2],
+                                                                            v[4 * i + 3]);
+        __syncwarp();
+        const int col4 = lane & 7;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int r = q * 4 + (lane >> 3);
+          const float4 val = *reinterpret_cast<const float4*>(buf + r * 36 + 4 * col4);
+          *reinterpret_cast<float4*>(args.dw + int64_t(n_base + r) * args.K + nt * BN + half * 128 + c * 32 +
+                                     4 * col4) = val;
+        }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
@@ -974,7 +996,7 @@ extern "C" int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_p
       !make_tmap_bf16(&tm_a_rows, a_plan, uint64_t(K), uint64_t(T), 64, 1))
     return MOT_ERR_CUDA;
   if (cudaFuncSetAttribute(gemm::routed_gemm_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(gemm::SMEM_BYTES)) != cudaSuccess)
+                           int(gemm::kDwSmem)) != cudaSuccess)
     return MOT_ERR_CUDA;
   gemm::DwArgs a{};
   a.ws = static_cast<const uint8_t*>(ws);
@@ -985,11 +1007,12 @@ extern "C" int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_p
   a.expert = expert;
   a.dw = dw;
   const int64_t total = int64_t(N / gemm::BN) * (K / gemm::BN);
-  // same threads, shared memory and cluster shape as the routed kernel, so the same residency
+  // same threads and cluster shape as the routed kernel and more shared memory than half an
+  // SM: one pair per two SMs, the same residency
   const int64_t cap = gemm::max_active_pairs<gemm::EPI_CAST, true>(dev);
   const int64_t clusters = total < cap ? total : cap;
-  gemm::routed_gemm_dw_kernel<<<unsigned(2 * clusters), gemm::THREADS, gemm::SMEM_BYTES, s>>>(tm_d, tm_d_rows, tm_a,
-                                                                                               tm_a_rows, a);
+  gemm::routed_gemm_dw_kernel<<<unsigned(2 * clusters), gemm::THREADS, gemm::kDwSmem, s>>>(tm_d, tm_d_rows, tm_a,
+                                                                                            tm_a_rows, a);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 

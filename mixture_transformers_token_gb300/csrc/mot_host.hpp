@@ -114,7 +114,7 @@ inline EncodeTiledFn encode_tiled_fn() {
 
 // 2D bf16 tensor map over a row-major [rows][cols] array with the 128-byte swizzle.
 inline bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                           uint32_t box_rows) {
+                           uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -122,7 +122,7 @@ inline bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -40,9 +40,11 @@ def _norm_bwd_inputs(T, H, seed, mod=None, with_dres=True):
 
 def _run_norm_bwd(inp, eps=1e-6):
     d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    T, H = d["dy"].shape
     ws = mot.mot_route_plan(d["mod"])
-    dx, rstd = mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], d["mod"], eps, ws, d_res_out=d["dro"])
-    dw = mot.mot_rmsnorm_dweight(d["dy"], d["s"], rstd, ws)
+    part = torch.empty((H // 64, T, 64), dtype=torch.float32, device="cuda")
+    dx, rstd = mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], eps, ws, d_res_out=d["dro"], dw_partials=part)
+    dw = mot.mot_rmsnorm_dweight(part, ws)
     assert mot.mot_device_status(ws) == 0
     return dx, rstd, dw
 
@@ -95,20 +97,31 @@ def test_add_rmsnorm_backward_rows_are_batch_invariant():
     assert torch.equal(rstd2, rstd[torch.from_numpy(sel).cuda()])
 
 
-def test_add_rmsnorm_backward_flags():
+def test_add_rmsnorm_backward_flags_and_partials_layout():
     T, H = 64, 256
     inp = _norm_bwd_inputs(T, H, 9)
     d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    # a plan for another T is refused on the device
+    ws_other = torch.empty(mot.mot_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    mot.mot_route_plan(d["mod"][:50].contiguous(), ws=ws_other)
+    mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], 1e-6, ws_other)
+    assert mot.mot_device_status(ws_other) & mot.DEV_PLAN_MISMATCH
+    part0 = torch.empty((H // 64, T, 64), dtype=torch.float32, device="cuda")
+    ws_other2 = torch.empty(mot.mot_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    mot.mot_route_plan(d["mod"][:50].contiguous(), ws=ws_other2)
+    mot.mot_rmsnorm_dweight(part0, ws_other2)
+    assert mot.mot_device_status(ws_other2) & mot.DEV_PLAN_MISMATCH
+    # the partials are p[r][j] = dy * (s * rstd) in blocks of 64 columns, rows in plan order
     ws = mot.mot_route_plan(d["mod"])
-    bad = d["mod"].clone()
-    bad[5] = 2
-    mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], bad, 1e-6, ws)
-    assert mot.mot_device_status(ws) & mot.DEV_BAD_MODALITY
-    ws2 = torch.empty(mot.mot_workspace_bytes(T), dtype=torch.uint8, device="cuda")
-    mot.mot_route_plan(d["mod"][:50].contiguous(), ws=ws2)       # a plan of another T
-    _, rstd = mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], d["mod"], 1e-6, ws2)
-    mot.mot_rmsnorm_dweight(d["dy"], d["s"], rstd, ws2)
-    assert mot.mot_device_status(ws2) & mot.DEV_PLAN_MISMATCH
+    part = torch.empty((H // 64, T, 64), dtype=torch.float32, device="cuda")
+    _, rstd = mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], 1e-6, ws, dw_partials=part)
+    assert mot.mot_device_status(ws) == 0
+    mod = inp["mod"].numpy()
+    perm = np.concatenate([np.nonzero(mod == 0)[0], np.nonzero(mod == 1)[0]])
+    dy32 = inp["dy"].float().numpy()
+    xh = (inp["s"].float().numpy() * rstd.cpu().numpy()[:, None]).astype(np.float32)
+    want = (dy32 * xh).astype(np.float32)[perm].reshape(T, H // 64, 64).transpose(1, 0, 2)
+    assert np.array_equal(part.cpu().numpy().view(np.uint32), np.ascontiguousarray(want).view(np.uint32))
 
 
 # ---------------------------------------------------------------------------
