@@ -48,7 +48,7 @@ def norm_bytes(t: int, h: int) -> int:
 
 # DRAM traffic of one QKV kernel launch from an ncu capture of this workload, keyed by the
 # hash of the kernel source it was taken on (null once the kernel has changed).
-NCU_TRAFFIC = {"8ca99383883bd4a3": 122876416}   # profiles/routed_gemm_qkv128_bagel_layer_T4096.md
+NCU_TRAFFIC = {"84872c0adfe57465": 122135808}   # profiles/routed_gemm_qkv128_bagel_layer_T4096.md
 
 
 def src_hash(name: str) -> str:
@@ -742,7 +742,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-baseline", dest="cpu_baseline", action="store_true", default=True)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--secondary", dest="secondary", action="store_true", default=True)
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--profile", choices=["mlp", "cfg", "qkv_fp32", "backward"], default=None,
