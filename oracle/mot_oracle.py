@@ -584,3 +584,53 @@ def e_add_rmsnorm_backward(dy, s, w, mod, eps, d_res_out=None):
     p = dy32 * xh
     dw = np.stack([e_left_fold_rows(p, mod, 0), e_left_fold_rows(p, mod, 1)])
     return {"dx": bf16_f32(ds), "dw": dw, "rstd": rstd, "dot": dot}
+
+
+# ---------------------------------------------------------------------------
+# Joint attention of the packed sequences
+# ---------------------------------------------------------------------------
+#
+# [RFC-435] §1 Motivation item 2: latent tokens query the prompt KV non-causally at every
+# step; §2 Reference hazards: cached prefill needs a bottom-right causal mask (a top-left
+# aligned causal mask is wrong when the queries are the last rows of a longer key range);
+# §3 Numerical contract: no split-KV. The pages give no formula beyond that; the attention
+# is the textbook scaled dot-product softmax attention with grouped KV heads.
+
+def g_joint_attention(qkv, seqs, Hq: int, Hkv: int, D: int, scale: float | None = None):
+    """Attention over packed sequences, in float64, one bf16 cast.
+
+    qkv   [T][(Hq + 2 Hkv) D]: per row the q heads, then k heads, then v heads (the fused QKV
+          output after QK-norm and RoPE). Query head h reads KV head h // (Hq / Hkv).
+    seqs  rows (q_start, k_start, nq, nk, n_causal): the sequence's queries are rows
+          q_start .. q_start + nq - 1 and its keys rows k_start .. k_start + nk - 1; the
+          queries are the last nq key positions (bottom-right alignment), so query i sits at
+          key position nk - nq + i. Query rows i < n_causal are causal: they see keys
+          j <= nk - nq + i. The other query rows see all nk keys (latent rows).
+    scale defaults to 1 / sqrt(D).
+    Returns out [T][Hq D] (bf16 values; rows that are no sequence's query are 0) and out_pre.
+    """
+    qkv = np.asarray(qkv, np.float64)
+    T = qkv.shape[0]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    grp = Hq // Hkv
+    sc = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    out = np.zeros((T, Hq * D))
+    for q0, k0, nq, nk, nc in np.asarray(seqs, np.int64):
+        if nq < 0 or nk < 1 or not 0 <= nc <= nq or (nc > 0 and nk < nq):
+            raise ValueError("bad sequence descriptor")
+        i = np.arange(nq)[:, None]
+        j = np.arange(nk)[None, :]
+        allowed = np.where(i < nc, j <= nk - nq + i, True)
+        for h in range(Hq):
+            g = h // grp
+            q = qkv[q0:q0 + nq, h * D:(h + 1) * D]
+            k = qkv[k0:k0 + nk, (Hq + g) * D:(Hq + g + 1) * D]
+            v = qkv[k0:k0 + nk, (Hq + Hkv + g) * D:(Hq + Hkv + g + 1) * D]
+            s = (q @ k.T) * sc
+            s = np.where(allowed, s, -np.inf)
+            m = np.max(s, axis=1, keepdims=True)
+            p = np.exp(s - m)
+            p = p / np.sum(p, axis=1, keepdims=True)
+            out[q0:q0 + nq, h * D:(h + 1) * D] = p @ v
+    return {"out": bf16(out), "out_pre": out}

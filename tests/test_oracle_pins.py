@@ -659,3 +659,88 @@ def test_norm_backward_e_matches_g():
         assert np.all(diff <= step) and np.mean(diff > 0) < 0.02
         np.testing.assert_allclose(e["dw"], g["dw"], rtol=1e-5, atol=1e-5)
         np.testing.assert_allclose(e["rstd"], g["rstd"], rtol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# joint attention
+# ---------------------------------------------------------------------------
+
+def _qkv_rows(q, k, v):
+    """Pack per-row q [T][Hq][D], k and v [T][Hkv][D] into the fused QKV layout."""
+    T = q.shape[0]
+    return np.concatenate([q.reshape(T, -1), k.reshape(T, -1), v.reshape(T, -1)], axis=1)
+
+
+def test_joint_attention_scale_and_softmax_hand_value():
+    gd = GOLDEN["joint_attention"]
+    D = 4
+    q = np.zeros((2, 1, D))
+    k = np.zeros((2, 1, D))
+    v = np.zeros((2, 1, D))
+    q[1, 0, 0] = 2.0          # the query is row 1; rows 0 and 1 are the keys
+    k[1, 0, 0] = 1.0
+    v[1, 0, :] = 1.0
+    r = O.g_joint_attention(_qkv_rows(q, k, v), [(1, 0, 1, 2, 0)], 1, 1, D)
+    assert np.allclose(r["out_pre"][1], gd["sigmoid_1"], rtol=0, atol=1e-15)
+    assert np.all(r["out"][1] == gd["sigmoid_1_bf16"])
+    assert np.all(r["out"][0] == 0.0)        # not a query row of any sequence
+
+
+def test_joint_attention_bottom_right_alignment_and_closed_forms():
+    rng = np.random.default_rng(51)
+    D, nk = 8, 3
+    v = O.bf16(rng.standard_normal((nk, 1, D)))
+    qkv = _qkv_rows(np.zeros((nk, 1, D)), O.bf16(rng.standard_normal((nk, 1, D))), v)
+    # one causal query at the bottom right sees all three keys; q = 0 gives their mean
+    r = O.g_joint_attention(qkv, [(2, 0, 1, nk, 1)], 1, 1, D)
+    np.testing.assert_allclose(r["out_pre"][2], v[:, 0].mean(axis=0), rtol=0, atol=1e-15)
+    # the first causal row of a full-length sequence sees key 0 only: out = v0 exactly
+    qkv2 = _qkv_rows(O.bf16(rng.standard_normal((nk, 1, D))), O.bf16(rng.standard_normal((nk, 1, D))), v)
+    r2 = O.g_joint_attention(qkv2, [(0, 0, nk, nk, nk)], 1, 1, D)
+    np.testing.assert_array_equal(r2["out"][0], v[0, 0])
+    # q = 0: a causal row i averages v_0..v_i, a latent row averages all values
+    r3 = O.g_joint_attention(qkv, [(0, 0, nk, nk, 2)], 1, 1, D)
+    np.testing.assert_allclose(r3["out_pre"][1], v[:2, 0].mean(axis=0), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(r3["out_pre"][2], v[:, 0].mean(axis=0), rtol=0, atol=1e-15)
+
+
+def test_joint_attention_grouped_heads():
+    # query heads 0, 1 read KV head 0 (values 1); heads 2, 3 read KV head 1 (values 2)
+    rng = np.random.default_rng(52)
+    T, D, Hq, Hkv = 5, 8, 4, 2
+    q = rng.standard_normal((T, Hq, D))
+    k = rng.standard_normal((T, Hkv, D))
+    v = np.zeros((T, Hkv, D))
+    v[:, 0] = 1.0
+    v[:, 1] = 2.0
+    r = O.g_joint_attention(_qkv_rows(q, k, v), [(0, 0, T, T, 3)], Hq, Hkv, D)
+    out = r["out_pre"].reshape(T, Hq, D)
+    np.testing.assert_allclose(out[:, :2], 1.0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out[:, 2:], 2.0, rtol=0, atol=1e-12)
+
+
+def test_joint_attention_brute_force_and_sequence_independence():
+    rng = np.random.default_rng(53)
+    Hq, Hkv, D = 4, 2, 8
+    T = 13
+    qkv = O.bf16(rng.standard_normal((T, (Hq + 2 * Hkv) * D)))
+    seqs = [(0, 0, 6, 6, 4), (6, 6, 3, 7, 3), (10, 6, 3, 7, 0)]  # the last two share keys (cached prefix)
+    r = O.g_joint_attention(qkv, seqs, Hq, Hkv, D)
+    for q0, k0, nq, nk, nc in seqs:
+        for i in range(nq):
+            for h in range(Hq):
+                g = h // (Hq // Hkv)
+                qv = qkv[q0 + i, h * D:(h + 1) * D]
+                keys = [j for j in range(nk) if i >= nc or j <= nk - nq + i]
+                sc = [math.fsum(qv[d] * qkv[k0 + j, (Hq + g) * D + d] for d in range(D)) / math.sqrt(D) for j in keys]
+                mx = max(sc)
+                w = [math.exp(x - mx) for x in sc]
+                tot = math.fsum(w)
+                for d in range(D):
+                    want = math.fsum(w[n] * qkv[k0 + j, (Hq + Hkv + g) * D + d] for n, j in enumerate(keys)) / tot
+                    assert abs(r["out_pre"][q0 + i, h * D + d] - want) <= 1e-12
+    # changing another sequence's rows leaves a sequence's output bit for bit
+    qkv2 = qkv.copy()
+    qkv2[:6] = O.bf16(rng.standard_normal((6, qkv.shape[1])))
+    r2 = O.g_joint_attention(qkv2, seqs, Hq, Hkv, D)
+    np.testing.assert_array_equal(r2["out_pre"][6:], r["out_pre"][6:])
