@@ -333,7 +333,8 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and args.secondary:
         secondary = {"swiglu_mlp_T8192": run_mlp(dev, flush), "cfg_pack_T36864": run_cfg_pack(dev, flush),
                      "fp32_rope_profile_T4096": run_qkv_fp32_rope(dev, flush),
-                     "backward_T4096": run_backward(dev, flush)}
+                     "backward_T4096": run_backward(dev, flush),
+                     "joint_attention": run_attention(dev, flush)}
     if world > 1:
         dist.barrier()
     if rank != 0:
@@ -605,6 +606,47 @@ def run_backward(dev, flush) -> dict:
     }
 
 
+def attention_flops(seqs, Hq: int, D: int) -> int:
+    """4 D flops per visible (query, key) pair and query head: Q K^T and P V."""
+    pairs = 0
+    for q0, k0, nq, nk, nc in seqs:
+        c = min(nc, nq)
+        # causal rows i < c see nk - nq + i + 1 keys; the others see nk
+        pairs += c * (nk - nq) + c * (c + 1) // 2 + (nq - c) * nk
+    return 4 * D * Hq * pairs
+
+
+def run_attention(dev, flush) -> dict:
+    """Joint attention on the BAGEL layer's pack (one sequence: 3072 causal prompt rows, then
+    1024 latent rows seeing all 4096 keys) and on the CFG pack (12 x (2048 prompt + 1024 latent)
+    rows, T = 36864), Q/K/V from the fused QKV layout (28 q heads, 4 kv heads of 128)."""
+    import torch
+
+    import mixture_transformers_token_gb300 as mot
+    from mixture_transformers_token_gb300 import workloads as W
+
+    stream = torch.cuda.current_stream(dev)
+    pk = peaks()
+    res = {}
+    for name, t, seqs in (
+            ("bagel_layer_T4096", T, [(0, 0, T, T, 3072)]),
+            ("cfg_pack_T36864", 36864, [(3072 * i, 3072 * i, 3072, 3072, 2048) for i in range(12)])):
+        qkv = W.bf16_normal_device(9, 600, (t, N_QKV), dev)
+        s = torch.tensor(seqs, dtype=torch.int32, device=dev)
+        ws = torch.zeros(64, dtype=torch.uint8, device=dev)
+        out = torch.empty((t, HQ * D), dtype=torch.bfloat16, device=dev)
+        r = time_stages([("attention", lambda: mot.mot_joint_attention(qkv, s, HQ, HKV, D, ws, out=out))], 20, 3,
+                        flush, stream)
+        if mot.mot_device_status(ws) != 0:
+            raise RuntimeError("device error flags set in the attention workload")
+        f = attention_flops(seqs, HQ, D)
+        res[name] = {"attention_us": round(r["attention"] * 1e6, 2), "tflops": _tflops(f, r["attention"]),
+                     "frac": round(f / r["attention"] / 1e12 / pk["bf16_tflops"], 4), "flops": f,
+                     "distribution_us": r["dist"]["attention"]}
+        del qkv, out
+    return res
+
+
 def run_cfg_pack(dev, flush) -> dict:
     """CFG pack: 12 sequences of 2048 und + 1024 gen rows (T = 36864), positions restarting per
     sequence: add-RMSNorm (+ plan), routed QKV + QK-norm + RoPE, routed O projection 3584 -> 3584
@@ -745,7 +787,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--secondary", dest="secondary", action="store_true", default=True)
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
-    ap.add_argument("--profile", choices=["mlp", "cfg", "qkv_fp32", "backward"], default=None,
+    ap.add_argument("--profile", choices=["mlp", "cfg", "qkv_fp32", "backward", "attention"], default=None,
                     help="run only one secondary workload (mlp, cfg, backward: 5 warm-up + 50 timed steps; "
                          "qkv_fp32: 5 + 200) and print its figures; a short command for profiler captures")
     ap.add_argument("--cpu-baseline-child", type=int, default=None, help=argparse.SUPPRESS)
@@ -763,7 +805,8 @@ def main():
         mot.load_library()
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        fn = {"mlp": run_mlp, "cfg": run_cfg_pack, "qkv_fp32": run_qkv_fp32_rope, "backward": run_backward}[args.profile]
+        fn = {"mlp": run_mlp, "cfg": run_cfg_pack, "qkv_fp32": run_qkv_fp32_rope, "backward": run_backward,
+              "attention": run_attention}[args.profile]
         print(json.dumps({args.profile: fn(dev, L2Flush(dev))}), flush=True)
         return
     if args.warmup < 3:

@@ -62,6 +62,7 @@ extern "C" {
 #define MOT_DEV_TIMEOUT       0x2u  /* a pipeline wait gave up after about one second */
 #define MOT_DEV_PLAN_MISMATCH 0x4u  /* the workspace holds no plan for this T */
 #define MOT_DEV_BAD_POSITION  0x8u  /* a RoPE position outside [0, P) (clamped to 0) */
+#define MOT_DEV_BAD_SEQUENCE  0x10u /* an attention sequence descriptor out of range */
 
 /* epilogues of mot_routed_gemm */
 #define MOT_EPI_CAST   0  /* out = bf16(acc) */
@@ -257,6 +258,32 @@ int mot_rope_table_fill_host(double theta, int D, int P, mot_bf16* host_cs);
  * Geometry and errors as mot_rope_table_fill_host.
  */
 int mot_rope_table_fill_host_fp32(double theta, int D, int P, float* host_cs);
+
+/*
+ * mot_joint_attention -- attention of packed sequences over the fused QKV output ([RFC-435]
+ * §1 Motivation item 2: latent tokens query the prompt KV non-causally at every step; §2
+ * Reference hazards: cached prefill needs a bottom-right causal mask; §3 Numerical contract:
+ * no split-KV, fixed accumulation order).
+ *   qkv   [T][(Hq + 2 Hkv) D] bf16   q heads, k heads, v heads per row (RoPE applied), the
+ *                                    output of mot_routed_qkv_norm_rope.
+ *   seqs  device int32 [n_seq][5] = (q_start, k_start, nq, nk, n_causal): queries are rows
+ *         q_start .. q_start + nq - 1, keys rows k_start .. k_start + nk - 1; the queries are
+ *         the last nq key positions (bottom-right alignment). Query row i < n_causal sees keys
+ *         j <= nk - nq + i (a prompt row); the others see all nk keys (latent rows). Requires
+ *         nk >= 1, 0 <= n_causal <= nq, nk >= nq when n_causal > 0, ranges inside [0, T) and
+ *         query ranges of different sequences that do not overlap; otherwise
+ *         MOT_DEV_BAD_SEQUENCE is set and the bad sequence's rows are not written.
+ *   scale  softmax scale (1 / sqrt(D) for the standard attention), > 0.
+ *   ws    at least 64 bytes (e.g. a routing plan); its error word receives device errors.
+ *   out   [T][Hq D] bf16   out: rows that are some sequence's query; other rows untouched.
+ * Query head h reads KV head h / (Hq / Hkv). Arithmetic: S = Q K^T in fp32 on the tensor
+ * cores; per row, 128-key blocks in ascending order from the sequence's first key: x = S *
+ * (scale * log2 e), running maximum m, p = exp2(x - m), running sum l (fp32, left to right),
+ * O = O * exp2(m_old - m) + bf16(p) V in fp32; out = bf16(O / l). D in {64, 128}, Hq a
+ * multiple of Hkv.
+ */
+int mot_joint_attention(const mot_bf16* qkv, int64_t T, int Hq, int Hkv, int D, const int32_t* seqs,
+                        int n_seq, float scale, void* ws, size_t ws_bytes, mot_bf16* out, void* stream);
 
 /*
  * mot_routed_gemm_dx -- input gradient of the routed GEMM out = a W[mod]^T through both

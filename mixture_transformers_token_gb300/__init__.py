@@ -13,6 +13,7 @@ the workspace.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
@@ -24,7 +25,7 @@ __all__ = [
     "mot_fused_add_rmsnorm", "mot_routed_qkv_norm_rope", "mot_routed_gemm",
     "mot_swiglu_interleave", "mot_rope_table_fill_host", "mot_device_status", "mot_routed_gemm_noalloc",
     "mot_routed_qkv_norm_rope_fp32", "mot_rope_table_fill_host_fp32", "mot_add_rmsnorm_backward",
-    "mot_rmsnorm_dweight", "mot_routed_gemm_dx", "mot_routed_gemm_dw",
+    "mot_rmsnorm_dweight", "mot_routed_gemm_dx", "mot_routed_gemm_dw", "mot_joint_attention", "DEV_BAD_SEQUENCE",
     "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows", "mot_selftest_wait_timeout",
 ]
 
@@ -37,6 +38,7 @@ DEV_BAD_MODALITY = 0x1
 DEV_TIMEOUT = 0x2
 DEV_PLAN_MISMATCH = 0x4
 DEV_BAD_POSITION = 0x8
+DEV_BAD_SEQUENCE = 0x10
 NOALLOC_MAX_TOKENS = 65536
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +72,7 @@ _SIGNATURES = {
     "mot_rmsnorm_dweight": (_c_i, [_c_p, _c_i64, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_dx": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_dw": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_joint_attention": (_c_i, [_c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
 }
 
@@ -340,6 +343,29 @@ def mot_routed_gemm_dw(dout_plan, a_plan, ws, expert: int = 1, out=None, stream=
     _check("mot_routed_gemm_dw", _lib().mot_routed_gemm_dw(
         dout_plan.data_ptr(), a_plan.data_ptr(), T, N, K, expert, ws.data_ptr(), ws.numel(), out.data_ptr(),
         _stream(dout_plan, stream)))
+    return out
+
+
+def mot_joint_attention(qkv, seqs, Hq: int, Hkv: int, D: int, ws, scale: float | None = None, out=None,
+                        stream=None):
+    """Attention of packed sequences over the fused QKV output [T][(Hq + 2 Hkv) D].
+    `seqs` is a device int32 [n_seq][5] of (q_start, k_start, nq, nk, n_causal); `ws` (>= 64
+    bytes) receives device errors. Returns out [T][Hq D] (rows that are no query untouched)."""
+    T = qkv.shape[0]
+    _dev(qkv, "qkv", torch.bfloat16, 2)
+    _dev(seqs, "seqs", torch.int32, 2)
+    _dev(ws, "ws", torch.uint8, 1)
+    if qkv.shape[1] != (Hq + 2 * Hkv) * D:
+        raise ValueError(f"qkv must be [T, {(Hq + 2 * Hkv) * D}]")
+    if seqs.shape[1] != 5:
+        raise ValueError("seqs must be [n_seq, 5]")
+    if out is None:
+        out = torch.zeros((T, Hq * D), dtype=torch.bfloat16, device=qkv.device)
+    _dev(out, "out", torch.bfloat16, 2)
+    sc = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check("mot_joint_attention", _lib().mot_joint_attention(
+        qkv.data_ptr(), T, Hq, Hkv, D, seqs.data_ptr(), seqs.shape[0], sc, ws.data_ptr(), ws.numel(),
+        out.data_ptr(), _stream(qkv, stream)))
     return out
 
 

@@ -180,6 +180,19 @@ def test_gemm_backward_rejects(lib):
     assert dw(A, A, 1000, 256, 256, 1, B, 100, C, None) == MOT_ERR_WORKSPACE
 
 
+def test_joint_attention_rejects(lib):
+    f = lib.mot_joint_attention
+    assert f(None, 64, 4, 2, 64, A, 1, 0.125, B, 64, C, None) == MOT_ERR_NULL
+    assert f(A, 64, 4, 2, 64, None, 1, 0.125, B, 64, C, None) == MOT_ERR_NULL
+    assert f(A, 64, 4, 2, 96, A, 1, 0.125, B, 64, C, None) == MOT_ERR_GEOMETRY      # D
+    assert f(A, 64, 4, 3, 64, A, 1, 0.125, B, 64, C, None) == MOT_ERR_GEOMETRY      # Hq % Hkv
+    assert f(A, 0, 4, 2, 64, A, 1, 0.125, B, 64, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, 64, 4, 2, 64, A, 0, 0.125, B, 64, C, None) == MOT_ERR_GEOMETRY      # no sequence
+    assert f(A, 64, 4, 2, 64, A, 1, 0.0, B, 64, C, None) == MOT_ERR_ARG
+    assert f(A, 64, 4, 2, 64, MIS, 1, 0.125, B, 64, C, None) == MOT_ERR_ALIGN
+    assert f(A, 64, 4, 2, 64, A, 1, 0.125, B, 8, C, None) == MOT_ERR_WORKSPACE
+
+
 def test_routed_gemm_rejects(lib):
     f = lib.mot_routed_gemm
     assert f(None, A, 8, 256, 64, 0, B, 1 << 20, C, None) == MOT_ERR_NULL
