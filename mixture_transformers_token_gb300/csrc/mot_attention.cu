@@ -11,18 +11,21 @@
 // in place from the fused QKV output (row stride (Hq + 2 Hkv) D).
 //
 // Arithmetic, the same for every tile of every pack: S = Q K^T in fp32 on the tensor cores;
-// per row, in 128-key blocks in ascending key order: x = S * (scale * log2 e) (masked keys
-// -inf), m' = max(m, max_block x), alpha = exp2(m - m'), p = exp2(x - m'), l = l * alpha +
-// (sum of the block's p, left to right), O = O * alpha + bf16(p) V (fp32, tensor cores); out =
-// bf16(O / l). Blocks start at the sequence's first key, so a row's bits do not depend on the
-// other sequences of the pack.
+// per row, in 128-key blocks in ascending key order, with c = scale * log2 e: the running
+// maximum m of S (masked keys excluded) moves to the block maximum only when that exceeds it
+// by more than 8 / c (then O and l are scaled by 2^((m_old - m) c)); p = 2^(S c - m c) (one
+// fused multiply-add and the SFU's exp2); l += the block's p (four interleaved partial sums);
+// O += bf16(p) V (fp32, tensor cores); out = bf16(O / l). Blocks start at the sequence's first
+// key, so a row's bits do not depend on the other sequences of the pack.
 //
-// One CTA per (128-row query tile, head); tiles of a sequence are visited last first (the
-// causal tiles near the end carry the most keys). Warp 0 loads Q once and K, V blocks into
-// two-stage rings (TMA, 128-byte swizzle); warp 1 issues S = Q K^T into one of two TMEM S
-// buffers one block ahead, then O += P V (V read as an MN-major operand); warps 2-5 hold one
-// query row per thread: they read S from TMEM, form p, rescale O in TMEM when the row maximum
-// moves, and write P (bf16, swizzled K-major) to shared memory for the next MMA.
+// One CTA per (pair of 128-row query tiles, head); pairs of a sequence are visited last first
+// (the causal tiles near the end carry the most keys). Warp 0 loads both Q tiles once, K
+// blocks into a two-stage ring and V blocks into one stage (TMA, 128-byte swizzle); warp 1
+// issues, per key block, S = Q K^T for both tiles, then O += P V of the previous block for
+// both (V read as an MN-major operand); warps 2-5 and 6-9 are the softmax warpgroups of the
+// two tiles, one query row per thread: they read S from TMEM, form p, rescale O in TMEM when
+// the row maximum moves, and write P (bf16, swizzled K-major) to shared memory. Each tile's
+// softmax runs while the tensor cores work on the other tile.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -35,20 +38,22 @@ namespace mot {
 namespace attn {
 
 constexpr int BQ = 128, BKV = 128;
-constexpr int THREADS = 192;  // producer, MMA, 4 softmax warps
-constexpr int KV_STAGES = 2;
+constexpr int TILES = 2;        // query tiles per CTA (ping-pong between two softmax warpgroups)
+constexpr int THREADS = 320;    // producer, MMA, 2 x 4 softmax warps
+constexpr int K_STAGES = 2;
 constexpr uint32_t SUB = 128 * 64 * 2;  // one [128 rows x 64 columns] bf16 swizzled sub-tile
 
 template <int D>
 struct Layout {
-  static constexpr uint32_t TILE = BQ * D * 2;  // Q tile, or one K or V block
-  static constexpr uint32_t Q = 0;
-  static constexpr uint32_t K = Q + TILE;
-  static constexpr uint32_t V = K + KV_STAGES * TILE;
-  static constexpr uint32_t P = V + KV_STAGES * TILE;  // [128 rows x 128 keys] bf16
-  static constexpr uint32_t BAR = P + BQ * BKV * 2;
+  static constexpr uint32_t TILE = BQ * D * 2;  // a Q tile, or one K or V block
+  static constexpr uint32_t Q = 0;                              // TILES Q tiles
+  static constexpr uint32_t K = Q + TILES * TILE;               // K_STAGES K blocks
+  static constexpr uint32_t V = K + K_STAGES * TILE;            // one V block
+  static constexpr uint32_t P = V + TILE;                       // TILES x [128 rows x 128 keys] bf16
+  static constexpr uint32_t BAR = P + TILES * BQ * BKV * 2;
   static constexpr size_t BYTES = 1024 + size_t(BAR) + 256;
-  static constexpr uint32_t TMEM_S0 = 0, TMEM_S1 = BKV, TMEM_O = 2 * BKV, TMEM_COLS = 512;
+  // tensor memory: S of tile t at 128 t, O of tile t at 256 + 128 t
+  static constexpr uint32_t TMEM_S = 0, TMEM_O = 2 * BKV, TMEM_COLS = 512;
 };
 
 struct Args {
@@ -60,31 +65,81 @@ struct Args {
   uint32_t* err;
 };
 
+// 2^x by the SFU instruction (relative error about 2^-22, subnormal results flushed to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The running maximum moves only when a block's maximum exceeds it by more than this many
+// powers of two: until then p = 2^(S c - m c) stays below 2^8, and O and l, which share m,
+// need no rescaling.
+constexpr float kLazyLog2 = 8.0f;
+
 __device__ __forceinline__ bool bad_seq(const int32_t* d, int T) {
   const int q0 = d[0], k0 = d[1], nq = d[2], nk = d[3], c = d[4];
   return q0 < 0 || k0 < 0 || nq < 0 || nk < 1 || c < 0 || c > nq || (c > 0 && nk < nq) ||
          int64_t(q0) + nq > T || int64_t(k0) + nk > T;
 }
 
-// The tile u of the grid: sequence s, first query row i0 of the tile (tiles of a sequence in
-// reverse order). Returns false past the last tile; a bad descriptor contributes no tiles.
-__device__ __forceinline__ bool find_tile(const Args& a, int u, int4& sq, int& nc, int& i0) {
-  int acc = 0;
-  for (int s = 0; s < a.n_seq; ++s) {
-    const int32_t* d = a.seqs + 5 * s;
-    const int nt = bad_seq(d, a.T) ? 0 : (d[2] + BQ - 1) / BQ;
-    if (u < acc + nt) {
-      sq = make_int4(d[0], d[1], d[2], d[3]);
-      nc = d[4];
-      i0 = (nt - 1 - (u - acc)) * BQ;
-      return true;
-    }
-    acc += nt;
-  }
-  return false;
+// The work items of a sequence are its 256-row pairs of query tiles; item r counts from the
+// end (r = 0 is the last pair, which sees the most keys). The grid visits items heaviest
+// first with the heads fastest: all heads of item 0 of every sequence, then item 1 of every
+// sequence, ... (for up to 64 sequences; beyond that, sequence by sequence), so the in-order
+// block dispatch balances the uneven causal work. CTA u takes head u % Hq of item u / Hq.
+// Returns false past the last item; a bad descriptor contributes none.
+constexpr int kSortedSeqs = 64;
+
+__device__ __forceinline__ int seq_items(const Args& a, int s) {
+  const int32_t* d = a.seqs + 5 * s;
+  return bad_seq(d, a.T) ? 0 : (d[2] + TILES * BQ - 1) / (TILES * BQ);
 }
 
-// CTA (0, 0) checks every descriptor, that the query ranges do not overlap (their rows sum to
+__device__ bool find_tile(const Args& a, int k, int4& sq, int& nc, int& i0) {
+  int found_s = -1, r = -1;
+  if (a.n_seq <= kSortedSeqs) {
+    int items[kSortedSeqs];
+    int most = 0;
+    for (int s = 0; s < a.n_seq; ++s) {
+      items[s] = seq_items(a, s);
+      most = items[s] > most ? items[s] : most;
+    }
+    int acc = 0;
+    for (int rr = 0; rr < most && found_s < 0; ++rr) {
+      for (int s = 0; s < a.n_seq; ++s) {
+        if (items[s] > rr) {
+          if (acc == k) {
+            found_s = s;
+            r = rr;
+            break;
+          }
+          ++acc;
+        }
+      }
+    }
+    if (found_s < 0) return false;
+  } else {
+    int acc = 0;
+    for (int s = 0; s < a.n_seq; ++s) {
+      const int nt = seq_items(a, s);
+      if (k < acc + nt) {
+        found_s = s;
+        r = k - acc;
+        break;
+      }
+      acc += nt;
+    }
+    if (found_s < 0) return false;
+  }
+  const int32_t* d = a.seqs + 5 * found_s;
+  sq = make_int4(d[0], d[1], d[2], d[3]);
+  nc = d[4];
+  i0 = (seq_items(a, found_s) - 1 - r) * (TILES * BQ);
+  return true;
+}
+
+// CTA 0 checks every descriptor, that the query ranges do not overlap (their rows sum to
 // at most T) and that the grid covers every tile; a failure sets MOT_DEV_BAD_SEQUENCE.
 __device__ void check_sequences(const Args& a) {
   int64_t tiles = 0, rows = 0;
@@ -95,10 +150,10 @@ __device__ void check_sequences(const Args& a) {
       bad = true;
       continue;
     }
-    tiles += (d[2] + BQ - 1) / BQ;
+    tiles += (d[2] + TILES * BQ - 1) / (TILES * BQ);
     rows += d[2];
   }
-  if (bad || rows > a.T || tiles > int64_t(gridDim.x)) atomicOr(a.err, MOT_DEV_BAD_SEQUENCE);
+  if (bad || rows > a.T || tiles * a.Hq > int64_t(gridDim.x)) atomicOr(a.err, MOT_DEV_BAD_SEQUENCE);
 }
 
 template <int D>
@@ -108,42 +163,56 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* v_full = bars + 3;   // [2]
-  uint64_t* k_empty = bars + 5;  // [2]
-  uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;   // [2]
-  uint64_t* s_free = bars + 11;  // [2]
-  uint64_t* p_full = bars + 13;
-  uint64_t* o_full = bars + 14;
+  uint64_t* q_full = bars;        // both Q tiles
+  uint64_t* k_full = bars + 1;    // [K_STAGES]
+  uint64_t* k_empty = bars + 3;   // [K_STAGES]: both tiles' S MMAs read the block
+  uint64_t* v_full = bars + 5;
+  uint64_t* v_empty = bars + 6;   // both tiles' P V MMAs read the block
+  uint64_t* s_full = bars + 7;    // [TILES]
+  uint64_t* s_free = bars + 9;    // [TILES]: the tile's softmax warps have read S
+  uint64_t* p_full = bars + 11;   // [TILES]
+  uint64_t* o_full = bars + 13;   // [TILES]: the tile's P V is done
   uint64_t* drain = bars + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) check_sequences(a);
-  int4 sq;
-  int nc, i0;
-  if (!find_tile(a, int(blockIdx.x), sq, nc, i0)) return;  // uniform across the CTA
-  const int q0 = sq.x, k0 = sq.y, nq = sq.z, nk = sq.w;
-  const int h = int(blockIdx.y), g = h / (a.Hq / a.Hkv);
-  const int i1 = i0 + BQ < nq ? i0 + BQ : nq;  // query rows [i0, i1) of the sequence
-  const int kmax = i1 > nc ? nk : nk - nq + i1;   // keys the tile needs
+  // thread 0 finds the CTA's work item; the others read it from shared memory
+  int* item = reinterpret_cast<int*>(tmem_slot + 2);  // found, q0, k0, nq, nk, n_causal, i0
+  if (threadIdx.x == 0) {
+    if (blockIdx.x == 0) check_sequences(a);
+    int4 sq4;
+    int c4 = 0, i04 = 0;
+    item[0] = find_tile(a, int(blockIdx.x) / a.Hq, sq4, c4, i04) ? 1 : 0;
+    item[1] = sq4.x;
+    item[2] = sq4.y;
+    item[3] = sq4.z;
+    item[4] = sq4.w;
+    item[5] = c4;
+    item[6] = i04;
+  }
+  __syncthreads();
+  if (!item[0]) return;  // uniform across the CTA
+  const int q0 = item[1], k0 = item[2], nq = item[3], nk = item[4], nc = item[5], i0 = item[6];
+  const int h = int(blockIdx.x) % a.Hq, g = h / (a.Hq / a.Hkv);
+  const int i1 = i0 + TILES * BQ < nq ? i0 + TILES * BQ : nq;  // query rows [i0, i1) of the sequence
+  const int kmax = i1 > nc ? nk : nk - nq + i1;                 // keys the pair needs
   const int nblk = (kmax + BKV - 1) / BKV;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < K_STAGES; ++i) {
       mbar_init(smem_u32(&k_full[i]), 1);
-      mbar_init(smem_u32(&v_full[i]), 1);
       mbar_init(smem_u32(&k_empty[i]), 1);
-      mbar_init(smem_u32(&v_empty[i]), 1);
-      mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_free[i]), 4);
     }
-    mbar_init(smem_u32(p_full), 4);
-    mbar_init(smem_u32(o_full), 1);
+    mbar_init(smem_u32(v_full), 1);
+    mbar_init(smem_u32(v_empty), 1);
+    for (int t = 0; t < TILES; ++t) {
+      mbar_init(smem_u32(&s_full[t]), 1);
+      mbar_init(smem_u32(&s_free[t]), 4);
+      mbar_init(smem_u32(&p_full[t]), 4);
+      mbar_init(smem_u32(&o_full[t]), 1);
+    }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -163,77 +232,82 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       bool ok = true;
       int kdone = 0, vdone = 0;  // blocks whose K / V copies were issued
-      mbar_arrive_expect_tx(smem_u32(q_full), L::TILE);
-      for (int b = 0; b < D / 64; ++b)
-        tma_load_2d(smem_u32(smem + L::Q + b * SUB), &tm_qkv, h * D + 64 * b, q0 + i0, smem_u32(q_full));
+      mbar_arrive_expect_tx(smem_u32(q_full), TILES * L::TILE);
+      for (int t = 0; t < TILES; ++t)
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_2d(smem_u32(smem + L::Q + t * L::TILE + b * SUB), &tm_qkv, h * D + 64 * b, q0 + i0 + t * BQ,
+                      smem_u32(q_full));
       for (int j = 0; j < nblk && ok; ++j) {
-        const int st = j % KV_STAGES;
-        const uint32_t ph = uint32_t(j / KV_STAGES) & 1u;
+        const int st = j % K_STAGES;
         const int y = k0 + j * BKV;
-        ok = mbar_wait(smem_u32(&k_empty[st]), ph ^ 1u, abort_flag, a.err);
+        ok = mbar_wait(smem_u32(&k_empty[st]), (uint32_t(j / K_STAGES) & 1u) ^ 1u, abort_flag, a.err);
         if (!ok) break;
         mbar_arrive_expect_tx(smem_u32(&k_full[st]), L::TILE);
         for (int b = 0; b < D / 64; ++b)
           tma_load_2d(smem_u32(smem + L::K + st * L::TILE + b * SUB), &tm_qkv, (a.Hq + g) * D + 64 * b, y,
                       smem_u32(&k_full[st]));
         kdone = j + 1;
-        ok = mbar_wait(smem_u32(&v_empty[st]), ph ^ 1u, abort_flag, a.err);
+        ok = mbar_wait(smem_u32(v_empty), (uint32_t(j) & 1u) ^ 1u, abort_flag, a.err);
         if (!ok) break;
-        mbar_arrive_expect_tx(smem_u32(&v_full[st]), L::TILE);
+        mbar_arrive_expect_tx(smem_u32(v_full), L::TILE);
         for (int b = 0; b < D / 64; ++b)
-          tma_load_2d(smem_u32(smem + L::V + st * L::TILE + b * SUB), &tm_qkv, (a.Hq + a.Hkv + g) * D + 64 * b, y,
-                      smem_u32(&v_full[st]));
+          tma_load_2d(smem_u32(smem + L::V + b * SUB), &tm_qkv, (a.Hq + a.Hkv + g) * D + 64 * b, y,
+                      smem_u32(v_full));
         vdone = j + 1;
       }
       // every issued copy has landed before the CTA can exit
       mbar_drain(smem_u32(q_full), 0);
-      for (int j = kdone - KV_STAGES > 0 ? kdone - KV_STAGES : 0; j < kdone; ++j)
-        mbar_drain(smem_u32(&k_full[j % KV_STAGES]), uint32_t(j / KV_STAGES) & 1u);
-      for (int j = vdone - KV_STAGES > 0 ? vdone - KV_STAGES : 0; j < vdone; ++j)
-        mbar_drain(smem_u32(&v_full[j % KV_STAGES]), uint32_t(j / KV_STAGES) & 1u);
+      for (int j = kdone - K_STAGES > 0 ? kdone - K_STAGES : 0; j < kdone; ++j)
+        mbar_drain(smem_u32(&k_full[j % K_STAGES]), uint32_t(j / K_STAGES) & 1u);
+      if (vdone > 0) mbar_drain(smem_u32(v_full), uint32_t(vdone - 1) & 1u);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // per block j: S_0(j), S_1(j), then P V of block j - 1 for both tiles, so that each tile's
+    // softmax overlaps the other tile's products
     constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV);
     constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, D) | kIdescBMnMajor;
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(q_full), 0, abort_flag, a.err));
     for (int j = 0; j <= nblk && ok; ++j) {
       if (j < nblk) {
-        const int st = j % KV_STAGES, sb = j & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&k_full[st]), uint32_t(j / KV_STAGES) & 1u, abort_flag,
+        const int st = j % K_STAGES;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&k_full[st]), uint32_t(j / K_STAGES) & 1u, abort_flag,
                                                a.err));
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_free[sb]), (uint32_t(j >> 1) & 1u) ^ 1u,
-                                                       abort_flag, a.err));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t qa = smem_u32(smem + L::Q), kb = smem_u32(smem + L::K + st * L::TILE);
+        for (int t = 0; t < TILES && ok; ++t) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_free[t]), (uint32_t(j) & 1u) ^ 1u, abort_flag, a.err));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t qa = smem_u32(smem + L::Q + t * L::TILE), kb = smem_u32(smem + L::K + st * L::TILE);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_bf16(tmem + (sb ? L::TMEM_S1 : L::TMEM_S0), smem_desc_sw128(qa + (kk / 4) * SUB + (kk % 4) * 32),
-                     smem_desc_sw128(kb + (kk / 4) * SUB + (kk % 4) * 32), idesc_s, kk > 0);
-          mma_commit(smem_u32(&s_full[sb]));
-          mma_commit(smem_u32(&k_empty[st]));
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_bf16(tmem + L::TMEM_S + t * BKV, smem_desc_sw128(qa + (kk / 4) * SUB + (kk % 4) * 32),
+                       smem_desc_sw128(kb + (kk / 4) * SUB + (kk % 4) * 32), idesc_s, kk > 0);
+            mma_commit(smem_u32(&s_full[t]));
+            if (t == TILES - 1) mma_commit(smem_u32(&k_empty[st]));
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        if (!ok) break;
       }
       if (j >= 1) {
-        const int jj = j - 1, st = jj % KV_STAGES;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(p_full), uint32_t(jj) & 1u, abort_flag, a.err));
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&v_full[st]), uint32_t(jj / KV_STAGES) & 1u,
-                                                       abort_flag, a.err));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t pa = smem_u32(smem + L::P), vb = smem_u32(smem + L::V + st * L::TILE);
+        const int jj = j - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(v_full), uint32_t(jj) & 1u, abort_flag, a.err));
+        for (int t = 0; t < TILES && ok; ++t) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_full[t]), uint32_t(jj) & 1u, abort_flag, a.err));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t pa = smem_u32(smem + L::P + t * (BQ * BKV * 2)), vb = smem_u32(smem + L::V);
 #pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk)
-            mma_bf16(tmem + L::TMEM_O, smem_desc_sw128(pa + (kk / 4) * SUB + (kk % 4) * 32),
-                     smem_desc_mn_sw128(vb + kk * 2048, SUB), idesc_o, (jj | kk) != 0);
-          mma_commit(smem_u32(o_full));
-          mma_commit(smem_u32(&v_empty[st]));
+            for (int kk = 0; kk < BKV / 16; ++kk)
+              mma_bf16(tmem + L::TMEM_O + t * 128, smem_desc_sw128(pa + (kk / 4) * SUB + (kk % 4) * 32),
+                       smem_desc_mn_sw128(vb + kk * 2048, SUB), idesc_o, (jj | kk) != 0);
+            mma_commit(smem_u32(&o_full[t]));
+            if (t == TILES - 1) mma_commit(smem_u32(v_empty));
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
     // every MMA issued has completed before tensor memory is released
@@ -241,97 +315,116 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
     mbar_drain(smem_u32(drain), 0);
   } else {
-    // ---------------- softmax: one query row per thread ----------------
+    // ---------------- softmax: warpgroup t = (warp - 2) / 4, one query row per thread ----------------
+    const int t = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int i = i0 + row;                                   // query row within the sequence
+    const int i = i0 + t * BQ + row;                             // query row within the sequence
     const bool valid = i < nq;
-    const int lim = (valid && i < nc) ? nk - nq + i + 1 : nk;  // keys [0, lim) are visible
+    const int lim = (valid && i < nc) ? nk - nq + i + 1 : nk;   // keys [0, lim) are visible
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    uint8_t* prow = smem + L::P + row * 128;  // row `row` of each 64-key sub-tile
+    const uint32_t ts = tmem + lane_off + L::TMEM_S + t * BKV, to = tmem + lane_off + L::TMEM_O + t * 128;
+    uint8_t* prow = smem + L::P + t * (BQ * BKV * 2) + row * 128;  // row `row` of each 64-key sub-tile
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[sb]), uint32_t(j >> 1) & 1u, abort_flag, a.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t]), uint32_t(j) & 1u, abort_flag, a.err));
       if (!ok) break;
       tc_fence_after();
-      float x[BKV];
-#pragma unroll
+      const bool masked = __any_sync(0xffffffffu, j * BKV + BKV > lim);  // the block reaches past a row's keys
+      // pass 1: block maximum of the raw scores (visible keys), four interleaved chains
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
       for (int c = 0; c < BKV / 32; ++c) {
         float v[32];
-        tmem_ld32(tmem + lane_off + (sb ? L::TMEM_S1 : L::TMEM_S0) + c * 32, v);
+        tmem_ld32(ts + c * 32, v);
+        if (masked) {
+          const int lim_c = lim - (j * BKV + c * 32);  // visible keys of this chunk: u < lim_c
 #pragma unroll
-        for (int t = 0; t < 32; ++t) x[c * 32 + t] = v[t];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_free[sb]));
-      // scale into the log2 domain, mask, block maximum
-      float bmax = -INFINITY;
+          for (int u = 0; u < 32; ++u) v[u] = u < lim_c ? v[u] : -INFINITY;
+        }
 #pragma unroll
-      for (int c = 0; c < BKV; ++c) {
-        const float xs = j * BKV + c < lim ? __fmul_rn(x[c], a.c) : -INFINITY;
-        x[c] = xs;
-        bmax = fmaxf(bmax, xs);
+        for (int u = 0; u < 32; ++u) mx[u & 3] = fmaxf(mx[u & 3], v[u]);
       }
-      const float m_new = fmaxf(m, bmax);
-      const float alpha = exp2f(__fsub_rn(m, m_new));  // 0 on the first block (m = -inf)
-      float psum = 0.0f;
-#pragma unroll
-      for (int c = 0; c < BKV; ++c) {
-        const float p = exp2f(__fsub_rn(x[c], m_new));
-        x[c] = p;
-        psum = __fadd_rn(psum, p);
+      const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      float alpha = 1.0f;
+      if (m == -INFINITY) {
+        m = bmax;  // the first block with a visible key (block 0 for every valid row)
+      } else if (__fmul_rn(__fsub_rn(bmax, m), a.c) > kLazyLog2) {
+        alpha = ex2(__fmul_rn(__fsub_rn(m, bmax), a.c));
+        m = bmax;
       }
-      l = __fadd_rn(__fmul_rn(l, alpha), psum);
-      m = m_new;
+      const float mc = m == -INFINITY ? 0.0f : __fmul_rn(m, a.c);
       if (j >= 1) {
         // the previous block's P V is done: the P buffer is free and O may be rescaled
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_full), uint32_t(j - 1) & 1u, abort_flag, a.err));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(j - 1) & 1u, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
-            tmem_ld32(tmem + lane_off + L::TMEM_O + c * 32, o);
+            tmem_ld32(to + c * 32, o);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) o[t] = __fmul_rn(o[t], alpha);
-            tmem_st32(tmem + lane_off + L::TMEM_O + c * 32, o);
+            for (int u = 0; u < 32; ++u) o[u] = __fmul_rn(o[u], alpha);
+            tmem_st32(to + c * 32, o);
           }
         }
       }
-      // P as bf16 into the swizzled K-major tile: keys 8 cc .. 8 cc + 7 of sub-tile b go to
-      // the 16-byte chunk cc ^ (row & 7) of the row
+      // pass 2: p = 2^(S c - m c) (four interleaved partial sums), written as bf16 into the
+      // swizzled K-major P tile: keys 8 cc .. 8 cc + 7 of sub-tile b go to the 16-byte chunk
+      // cc ^ (row & 7) of the row
+      float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+      for (int c = 0; c < BKV / 32; ++c) {
+        float v[32];
+        tmem_ld32(ts + c * 32, v);
+        if (masked) {
+          const int lim_c = lim - (j * BKV + c * 32);
 #pragma unroll
-      for (int cch = 0; cch < BKV / 8; ++cch) {
-        const int b = cch >> 3, cc = cch & 7;
-        const uint4 v = make_uint4(pack_bf2(x[8 * cch], x[8 * cch + 1]), pack_bf2(x[8 * cch + 2], x[8 * cch + 3]),
-                                   pack_bf2(x[8 * cch + 4], x[8 * cch + 5]), pack_bf2(x[8 * cch + 6], x[8 * cch + 7]));
-        *reinterpret_cast<uint4*>(prow + b * SUB + ((cc ^ (row & 7)) << 4)) = v;
+          for (int u = 0; u < 32; ++u) v[u] = u < lim_c ? v[u] : -INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const float p = ex2(fmaf(v[u], a.c, -mc));
+          v[u] = p;
+          ps[u & 3] = __fadd_rn(ps[u & 3], p);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cch = c * 4 + q;  // 8-key chunk of the block
+          const int b = cch >> 3, cc = cch & 7;
+          const uint4 pk = make_uint4(pack_bf2(v[8 * q], v[8 * q + 1]), pack_bf2(v[8 * q + 2], v[8 * q + 3]),
+                                      pack_bf2(v[8 * q + 4], v[8 * q + 5]), pack_bf2(v[8 * q + 6], v[8 * q + 7]));
+          *reinterpret_cast<uint4*>(prow + b * SUB + ((cc ^ (row & 7)) << 4)) = pk;
+        }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s_free[t]));  // S is read for the last time
+      const float psum = __fadd_rn(__fadd_rn(ps[0], ps[1]), __fadd_rn(ps[2], ps[3]));
+      l = __fadd_rn(__fmul_rn(l, alpha), psum);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(p_full));
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
     }
     if (ok && nblk > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_full), uint32_t(nblk - 1) & 1u, abort_flag, a.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(nblk - 1) & 1u, abort_flag, a.err));
       if (ok) {
         tc_fence_after();
         uint16_t* orow = a.out + int64_t(q0 + i) * (int64_t(a.Hq) * D) + int64_t(h) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
-          tmem_ld32(tmem + lane_off + L::TMEM_O + c * 32, o);
+          tmem_ld32(to + c * 32, o);
           if (valid) {
             uint32_t pk[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) pk[t] = pack_bf2(__fdiv_rn(o[2 * t], l), __fdiv_rn(o[2 * t + 1], l));
+            for (int u = 0; u < 16; ++u) pk[u] = pack_bf2(__fdiv_rn(o[2 * u], l), __fdiv_rn(o[2 * u + 1], l));
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+            for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
           }
         }
       }
@@ -357,7 +450,7 @@ static int launch(const mot_bf16* qkv, const Args& a, int n_tiles_max, cudaStrea
   if (cudaFuncSetAttribute(joint_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmemBytes)) != cudaSuccess)
     return MOT_ERR_CUDA;
-  joint_attention_kernel<D><<<dim3(unsigned(n_tiles_max), unsigned(a.Hq)), THREADS, kSmemBytes, s>>>(tm, a);
+  joint_attention_kernel<D><<<unsigned(int64_t(n_tiles_max) * a.Hq), THREADS, kSmemBytes, s>>>(tm, a);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
@@ -391,10 +484,10 @@ extern "C" int mot_joint_attention(const mot_bf16* qkv, int64_t T, int Hq, int H
   a.c = scale * 1.4426950408889634f;
   a.out = out;
   a.err = &static_cast<PlanHeader*>(ws)->error;
-  // every sequence has at most nq / 128 + 1 tiles and the query ranges do not overlap (checked
-  // on the device), so T / 128 + n_seq bounds the tile count
-  const int64_t tiles = (T + attn::BQ - 1) / attn::BQ + n_seq;
-  if (tiles > (int64_t(1) << 30)) return MOT_ERR_GEOMETRY;
+  // every sequence has at most nq / 256 + 1 work items (pairs of 128-row tiles) and the query
+  // ranges do not overlap (checked on the device), so T / 256 + n_seq bounds their count
+  const int64_t tiles = (T + attn::TILES * attn::BQ - 1) / (attn::TILES * attn::BQ) + n_seq;
+  if (tiles * Hq > (int64_t(1) << 31) - 1) return MOT_ERR_GEOMETRY;
   if (D == 64) return attn::launch<64>(qkv, a, int(tiles), s);
   return attn::launch<128>(qkv, a, int(tiles), s);
 }
