@@ -11,7 +11,7 @@
 // in place from the fused QKV output (row stride (Hq + 2 Hkv) D).
 //
 // Arithmetic, the same for every tile of every pack: S = Q K^T in fp32 on the tensor cores;
-// per row, in 128-key blocks in ascending key order, with c = scale * log2 e: the running
+// per row, in 64-key blocks in ascending key order, with c = scale * log2 e: the running
 // maximum m of S (masked keys excluded) moves to the block maximum only when that exceeds it
 // by more than 8 / c (then O and l are scaled by 2^((m_old - m) c)); p = 2^(S c - m c) (one
 // fused multiply-add and the SFU's exp2); l += the block's p (four interleaved partial sums);
@@ -19,13 +19,14 @@
 // key, so a row's bits do not depend on the other sequences of the pack.
 //
 // One CTA per (pair of 128-row query tiles, head); pairs of a sequence are visited last first
-// (the causal tiles near the end carry the most keys). Warp 0 loads both Q tiles once, K
-// blocks into a two-stage ring and V blocks into one stage (TMA, 128-byte swizzle); warp 1
-// issues, per key block, S = Q K^T for both tiles, then O += P V of the previous block for
-// both (V read as an MN-major operand); warps 2-5 and 6-9 are the softmax warpgroups of the
-// two tiles, one query row per thread: they read S from TMEM, form p, rescale O in TMEM when
-// the row maximum moves, and write P (bf16, swizzled K-major) to shared memory. Each tile's
-// softmax runs while the tensor cores work on the other tile.
+// (the causal tiles near the end carry the most keys). Warp 0 loads both Q tiles once and
+// 64-key K and V blocks into three-stage rings (TMA, 128-byte swizzle); warp 1 issues, per key
+// block, S = Q K^T for both tiles into their double-buffered TMEM S, then O += P V of the
+// previous block for both (V read as an MN-major operand); warps 2-5 and 6-9 are the softmax
+// warpgroups of the two tiles, one query row per thread: they read a block's S from TMEM once
+// (64 columns), form p, rescale O in TMEM when the row maximum moves, and write P (bf16,
+// swizzled K-major) into one of two shared-memory buffers. Each tile's softmax runs while the tensor cores work on
+// the other tile and on its own next block.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -37,23 +38,25 @@
 namespace mot {
 namespace attn {
 
-constexpr int BQ = 128, BKV = 128;
+constexpr int BQ = 128, BKV = 64;
 constexpr int TILES = 2;        // query tiles per CTA (ping-pong between two softmax warpgroups)
 constexpr int THREADS = 320;    // producer, MMA, 2 x 4 softmax warps
-constexpr int K_STAGES = 2;
-constexpr uint32_t SUB = 128 * 64 * 2;  // one [128 rows x 64 columns] bf16 swizzled sub-tile
+constexpr int KV_STAGES = 3;
+constexpr uint32_t SUB = 128 * 64 * 2;   // a [128 rows x 64 columns] bf16 swizzled tile (Q half, P)
+constexpr uint32_t KSUB = 64 * 64 * 2;   // a [64 keys x 64 columns] bf16 swizzled tile (K, V half)
 
 template <int D>
 struct Layout {
-  static constexpr uint32_t TILE = BQ * D * 2;  // a Q tile, or one K or V block
-  static constexpr uint32_t Q = 0;                              // TILES Q tiles
-  static constexpr uint32_t K = Q + TILES * TILE;               // K_STAGES K blocks
-  static constexpr uint32_t V = K + K_STAGES * TILE;            // one V block
-  static constexpr uint32_t P = V + TILE;                       // TILES x [128 rows x 128 keys] bf16
-  static constexpr uint32_t BAR = P + TILES * BQ * BKV * 2;
-  static constexpr size_t BYTES = 1024 + size_t(BAR) + 256;
-  // tensor memory: S of tile t at 128 t, O of tile t at 256 + 128 t
-  static constexpr uint32_t TMEM_S = 0, TMEM_O = 2 * BKV, TMEM_COLS = 512;
+  static constexpr uint32_t QTILE = BQ * D * 2;    // a Q tile
+  static constexpr uint32_t KVBLK = BKV * D * 2;   // one K or V block
+  static constexpr uint32_t Q = 0;                          // TILES Q tiles
+  static constexpr uint32_t K = Q + TILES * QTILE;          // KV_STAGES K blocks
+  static constexpr uint32_t V = K + KV_STAGES * KVBLK;      // KV_STAGES V blocks
+  static constexpr uint32_t P = V + KV_STAGES * KVBLK;      // TILES x 2 buffers x [128 rows x 64 keys] bf16
+  static constexpr uint32_t BAR = P + 2 * TILES * SUB;
+  static constexpr size_t BYTES = 1024 + size_t(BAR) + 512;  // barriers, tensor-memory slot, work item
+  // tensor memory: S of tile t, buffer b at 128 t + 64 b; O of tile t at 256 + 128 t
+  static constexpr uint32_t TMEM_S = 0, TMEM_O = 256, TMEM_COLS = 512;
 };
 
 struct Args {
@@ -158,22 +161,23 @@ __device__ void check_sequences(const Args& a) {
 
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
-    joint_attention_kernel(const __grid_constant__ CUtensorMap tm_qkv, const Args a) {
+    joint_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                           const Args a) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR);
   uint64_t* q_full = bars;        // both Q tiles
-  uint64_t* k_full = bars + 1;    // [K_STAGES]
-  uint64_t* k_empty = bars + 3;   // [K_STAGES]: both tiles' S MMAs read the block
-  uint64_t* v_full = bars + 5;
-  uint64_t* v_empty = bars + 6;   // both tiles' P V MMAs read the block
-  uint64_t* s_full = bars + 7;    // [TILES]
-  uint64_t* s_free = bars + 9;    // [TILES]: the tile's softmax warps have read S
-  uint64_t* p_full = bars + 11;   // [TILES]
-  uint64_t* o_full = bars + 13;   // [TILES]: the tile's P V is done
-  uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* k_full = bars + 1;    // [KV_STAGES]
+  uint64_t* k_empty = bars + 4;   // [KV_STAGES]: both tiles' S MMAs have read the block
+  uint64_t* v_full = bars + 7;    // [KV_STAGES]
+  uint64_t* v_empty = bars + 10;  // [KV_STAGES]: both tiles' P V MMAs have read the block
+  uint64_t* s_full = bars + 13;   // [TILES][2]
+  uint64_t* s_free = bars + 17;   // [TILES][2]: the tile's softmax warps have read the buffer
+  uint64_t* p_full = bars + 21;   // [TILES]
+  uint64_t* o_full = bars + 23;   // [TILES][2]: the tile's P V from P buffer b is done (and every earlier one)
+  uint64_t* drain = bars + 27;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 28);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   // thread 0 finds the CTA's work item; the others read it from shared memory
@@ -201,22 +205,26 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
-    for (int i = 0; i < K_STAGES; ++i) {
+    for (int i = 0; i < KV_STAGES; ++i) {
       mbar_init(smem_u32(&k_full[i]), 1);
       mbar_init(smem_u32(&k_empty[i]), 1);
+      mbar_init(smem_u32(&v_full[i]), 1);
+      mbar_init(smem_u32(&v_empty[i]), 1);
     }
-    mbar_init(smem_u32(v_full), 1);
-    mbar_init(smem_u32(v_empty), 1);
     for (int t = 0; t < TILES; ++t) {
-      mbar_init(smem_u32(&s_full[t]), 1);
-      mbar_init(smem_u32(&s_free[t]), 4);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(smem_u32(&s_full[2 * t + b]), 1);
+        mbar_init(smem_u32(&s_free[2 * t + b]), 4);
+      }
       mbar_init(smem_u32(&p_full[t]), 4);
-      mbar_init(smem_u32(&o_full[t]), 1);
+      mbar_init(smem_u32(&o_full[2 * t]), 1);
+      mbar_init(smem_u32(&o_full[2 * t + 1]), 1);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0u;
     fence_mbar_init();
-    tma_prefetch_desc(&tm_qkv);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
@@ -232,58 +240,60 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       bool ok = true;
       int kdone = 0, vdone = 0;  // blocks whose K / V copies were issued
-      mbar_arrive_expect_tx(smem_u32(q_full), TILES * L::TILE);
+      mbar_arrive_expect_tx(smem_u32(q_full), TILES * L::QTILE);
       for (int t = 0; t < TILES; ++t)
         for (int b = 0; b < D / 64; ++b)
-          tma_load_2d(smem_u32(smem + L::Q + t * L::TILE + b * SUB), &tm_qkv, h * D + 64 * b, q0 + i0 + t * BQ,
+          tma_load_2d(smem_u32(smem + L::Q + t * L::QTILE + b * SUB), &tm_q, h * D + 64 * b, q0 + i0 + t * BQ,
                       smem_u32(q_full));
       for (int j = 0; j < nblk && ok; ++j) {
-        const int st = j % K_STAGES;
+        const int st = j % KV_STAGES;
+        const uint32_t ph = uint32_t(j / KV_STAGES) & 1u;
         const int y = k0 + j * BKV;
-        ok = mbar_wait(smem_u32(&k_empty[st]), (uint32_t(j / K_STAGES) & 1u) ^ 1u, abort_flag, a.err);
+        ok = mbar_wait(smem_u32(&k_empty[st]), ph ^ 1u, abort_flag, a.err);
         if (!ok) break;
-        mbar_arrive_expect_tx(smem_u32(&k_full[st]), L::TILE);
+        mbar_arrive_expect_tx(smem_u32(&k_full[st]), L::KVBLK);
         for (int b = 0; b < D / 64; ++b)
-          tma_load_2d(smem_u32(smem + L::K + st * L::TILE + b * SUB), &tm_qkv, (a.Hq + g) * D + 64 * b, y,
+          tma_load_2d(smem_u32(smem + L::K + st * L::KVBLK + b * KSUB), &tm_kv, (a.Hq + g) * D + 64 * b, y,
                       smem_u32(&k_full[st]));
         kdone = j + 1;
-        ok = mbar_wait(smem_u32(v_empty), (uint32_t(j) & 1u) ^ 1u, abort_flag, a.err);
+        ok = mbar_wait(smem_u32(&v_empty[st]), ph ^ 1u, abort_flag, a.err);
         if (!ok) break;
-        mbar_arrive_expect_tx(smem_u32(v_full), L::TILE);
+        mbar_arrive_expect_tx(smem_u32(&v_full[st]), L::KVBLK);
         for (int b = 0; b < D / 64; ++b)
-          tma_load_2d(smem_u32(smem + L::V + b * SUB), &tm_qkv, (a.Hq + a.Hkv + g) * D + 64 * b, y,
-                      smem_u32(v_full));
+          tma_load_2d(smem_u32(smem + L::V + st * L::KVBLK + b * KSUB), &tm_kv, (a.Hq + a.Hkv + g) * D + 64 * b, y,
+                      smem_u32(&v_full[st]));
         vdone = j + 1;
       }
       // every issued copy has landed before the CTA can exit
       mbar_drain(smem_u32(q_full), 0);
-      for (int j = kdone - K_STAGES > 0 ? kdone - K_STAGES : 0; j < kdone; ++j)
-        mbar_drain(smem_u32(&k_full[j % K_STAGES]), uint32_t(j / K_STAGES) & 1u);
-      if (vdone > 0) mbar_drain(smem_u32(v_full), uint32_t(vdone - 1) & 1u);
+      for (int j = kdone - KV_STAGES > 0 ? kdone - KV_STAGES : 0; j < kdone; ++j)
+        mbar_drain(smem_u32(&k_full[j % KV_STAGES]), uint32_t(j / KV_STAGES) & 1u);
+      for (int j = vdone - KV_STAGES > 0 ? vdone - KV_STAGES : 0; j < vdone; ++j)
+        mbar_drain(smem_u32(&v_full[j % KV_STAGES]), uint32_t(j / KV_STAGES) & 1u);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    // per block j: S_0(j), S_1(j), then P V of block j - 1 for both tiles, so that each tile's
-    // softmax overlaps the other tile's products
+    // per block j: S of both tiles into their buffer j & 1, then P V of block j - 1 for both
     constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV);
     constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, D) | kIdescBMnMajor;
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(q_full), 0, abort_flag, a.err));
     for (int j = 0; j <= nblk && ok; ++j) {
       if (j < nblk) {
-        const int st = j % K_STAGES;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&k_full[st]), uint32_t(j / K_STAGES) & 1u, abort_flag,
+        const int st = j % KV_STAGES, sb = j & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&k_full[st]), uint32_t(j / KV_STAGES) & 1u, abort_flag,
                                                a.err));
         for (int t = 0; t < TILES && ok; ++t) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_free[t]), (uint32_t(j) & 1u) ^ 1u, abort_flag, a.err));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_free[2 * t + sb]), (uint32_t(j >> 1) & 1u) ^ 1u,
+                                                 abort_flag, a.err));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t qa = smem_u32(smem + L::Q + t * L::TILE), kb = smem_u32(smem + L::K + st * L::TILE);
+            const uint32_t qa = smem_u32(smem + L::Q + t * L::QTILE), kb = smem_u32(smem + L::K + st * L::KVBLK);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_bf16(tmem + L::TMEM_S + t * BKV, smem_desc_sw128(qa + (kk / 4) * SUB + (kk % 4) * 32),
-                       smem_desc_sw128(kb + (kk / 4) * SUB + (kk % 4) * 32), idesc_s, kk > 0);
-            mma_commit(smem_u32(&s_full[t]));
+              mma_bf16(tmem + L::TMEM_S + t * 128 + sb * BKV, smem_desc_sw128(qa + (kk / 4) * SUB + (kk % 4) * 32),
+                       smem_desc_sw128(kb + (kk / 4) * KSUB + (kk % 4) * 32), idesc_s, kk > 0);
+            mma_commit(smem_u32(&s_full[2 * t + sb]));
             if (t == TILES - 1) mma_commit(smem_u32(&k_empty[st]));
           }
           __syncwarp();
@@ -291,20 +301,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
       }
       if (j >= 1) {
-        const int jj = j - 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(v_full), uint32_t(jj) & 1u, abort_flag, a.err));
+        const int jj = j - 1, st = jj % KV_STAGES;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&v_full[st]), uint32_t(jj / KV_STAGES) & 1u, abort_flag,
+                                               a.err));
         for (int t = 0; t < TILES && ok; ++t) {
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_full[t]), uint32_t(jj) & 1u, abort_flag, a.err));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t pa = smem_u32(smem + L::P + t * (BQ * BKV * 2)), vb = smem_u32(smem + L::V);
+            const uint32_t pa = smem_u32(smem + L::P + (2 * t + (jj & 1)) * SUB);
+            const uint32_t vb = smem_u32(smem + L::V + st * L::KVBLK);
 #pragma unroll
             for (int kk = 0; kk < BKV / 16; ++kk)
-              mma_bf16(tmem + L::TMEM_O + t * 128, smem_desc_sw128(pa + (kk / 4) * SUB + (kk % 4) * 32),
-                       smem_desc_mn_sw128(vb + kk * 2048, SUB), idesc_o, (jj | kk) != 0);
-            mma_commit(smem_u32(&o_full[t]));
-            if (t == TILES - 1) mma_commit(smem_u32(v_empty));
+              mma_bf16(tmem + L::TMEM_O + t * 128, smem_desc_sw128(pa + kk * 32),
+                       smem_desc_mn_sw128(vb + kk * 2048, KSUB), idesc_o, (jj | kk) != 0);
+            mma_commit(smem_u32(&o_full[2 * t + (jj & 1)]));
+            if (t == TILES - 1) mma_commit(smem_u32(&v_empty[st]));
           }
           __syncwarp();
         }
@@ -323,29 +335,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool valid = i < nq;
     const int lim = (valid && i < nc) ? nk - nq + i + 1 : nk;   // keys [0, lim) are visible
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    const uint32_t ts = tmem + lane_off + L::TMEM_S + t * BKV, to = tmem + lane_off + L::TMEM_O + t * 128;
-    uint8_t* prow = smem + L::P + t * (BQ * BKV * 2) + row * 128;  // row `row` of each 64-key sub-tile
+    const uint32_t to = tmem + lane_off + L::TMEM_O + t * 128;
+    uint8_t* prow = smem + L::P + 2 * t * SUB + row * 128;  // the row of the tile's P buffer 0
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t]), uint32_t(j) & 1u, abort_flag, a.err));
+      const int sb = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[2 * t + sb]), uint32_t(j >> 1) & 1u, abort_flag,
+                                             a.err));
       if (!ok) break;
       tc_fence_after();
-      const bool masked = __any_sync(0xffffffffu, j * BKV + BKV > lim);  // the block reaches past a row's keys
-      // pass 1: block maximum of the raw scores (visible keys), four interleaved chains
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int c = 0; c < BKV / 32; ++c) {
-        float v[32];
-        tmem_ld32(ts + c * 32, v);
-        if (masked) {
-          const int lim_c = lim - (j * BKV + c * 32);  // visible keys of this chunk: u < lim_c
+      float x[BKV];
+      tmem_ld64(tmem + lane_off + L::TMEM_S + t * 128 + sb * BKV, x);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s_free[2 * t + sb]));  // the S buffer is free again
+      if (__any_sync(0xffffffffu, j * BKV + BKV > lim)) {  // the block reaches past a row's keys
+        const int lim_b = lim - j * BKV;
 #pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] = u < lim_c ? v[u] : -INFINITY;
-        }
-#pragma unroll
-        for (int u = 0; u < 32; ++u) mx[u & 3] = fmaxf(mx[u & 3], v[u]);
+        for (int c = 0; c < BKV; ++c) x[c] = c < lim_b ? x[c] : -INFINITY;
       }
+      // block maximum of the raw scores, four interleaved chains
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BKV; ++c) mx[c & 3] = fmaxf(mx[c & 3], x[c]);
       const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       float alpha = 1.0f;
       if (m == -INFINITY) {
@@ -355,62 +368,57 @@ __global__ void __launch_bounds__(THREADS, 1)
         m = bmax;
       }
       const float mc = m == -INFINITY ? 0.0f : __fmul_rn(m, a.c);
-      if (j >= 1) {
-        // the previous block's P V is done: the P buffer is free and O may be rescaled
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(j - 1) & 1u, abort_flag, a.err));
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32(to + c * 32, o);
-#pragma unroll
-            for (int u = 0; u < 32; ++u) o[u] = __fmul_rn(o[u], alpha);
-            tmem_st32(to + c * 32, o);
-          }
-        }
-      }
-      // pass 2: p = 2^(S c - m c) (four interleaved partial sums), written as bf16 into the
-      // swizzled K-major P tile: keys 8 cc .. 8 cc + 7 of sub-tile b go to the 16-byte chunk
-      // cc ^ (row & 7) of the row
+      // p = 2^(S c - m c), four interleaved partial sums, packed to bf16 pairs
       float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
-      for (int c = 0; c < BKV / 32; ++c) {
-        float v[32];
-        tmem_ld32(ts + c * 32, v);
-        if (masked) {
-          const int lim_c = lim - (j * BKV + c * 32);
+      uint32_t pk[BKV / 2];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] = u < lim_c ? v[u] : -INFINITY;
-        }
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float p = ex2(fmaf(v[u], a.c, -mc));
-          v[u] = p;
-          ps[u & 3] = __fadd_rn(ps[u & 3], p);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int cch = c * 4 + q;  // 8-key chunk of the block
-          const int b = cch >> 3, cc = cch & 7;
-          const uint4 pk = make_uint4(pack_bf2(v[8 * q], v[8 * q + 1]), pack_bf2(v[8 * q + 2], v[8 * q + 3]),
-                                      pack_bf2(v[8 * q + 4], v[8 * q + 5]), pack_bf2(v[8 * q + 6], v[8 * q + 7]));
-          *reinterpret_cast<uint4*>(prow + b * SUB + ((cc ^ (row & 7)) << 4)) = pk;
-        }
+      for (int c = 0; c < BKV; c += 2) {
+        const float p0 = ex2(fmaf(x[c], a.c, -mc)), p1 = ex2(fmaf(x[c + 1], a.c, -mc));
+        ps[c & 3] = __fadd_rn(ps[c & 3], p0);
+        ps[(c + 1) & 3] = __fadd_rn(ps[(c + 1) & 3], p1);
+        pk[c / 2] = pack_bf2(p0, p1);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_free[t]));  // S is read for the last time
       const float psum = __fadd_rn(__fadd_rn(ps[0], ps[1]), __fadd_rn(ps[2], ps[3]));
       l = __fadd_rn(__fmul_rn(l, alpha), psum);
+      // P buffer j & 1 was last read by the P V of block j - 2. The waits are per buffer, so a
+      // barrier never runs two phases ahead of its waiter (the next P V on a buffer needs this
+      // warpgroup's next P).
+      if (j >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[2 * t + (j & 1)]), uint32_t((j - 2) >> 1) & 1u,
+                                               abort_flag, a.err));
+        if (!ok) break;
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        // rescale O: every earlier P V (the last is block j - 1's) must be done
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[2 * t + ((j - 1) & 1)]),
+                                               uint32_t((j - 1) >> 1) & 1u, abort_flag, a.err));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(to + c * 32, o);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[u] = __fmul_rn(o[u], alpha);
+          tmem_st32(to + c * 32, o);
+        }
+      }
+      // P as bf16 into the swizzled K-major buffer j & 1: keys 8 cc .. 8 cc + 7 go to the
+      // 16-byte chunk cc ^ (row & 7) of the row
+      uint8_t* pb = prow + (j & 1) * SUB;
+#pragma unroll
+      for (int cc = 0; cc < BKV / 8; ++cc)
+        *reinterpret_cast<uint4*>(pb + ((cc ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
     }
     if (ok && nblk > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(nblk - 1) & 1u, abort_flag, a.err));
+      // the last P V (and with it every earlier one) is done
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[2 * t + ((nblk - 1) & 1)]),
+                                             uint32_t((nblk - 1) >> 1) & 1u, abort_flag, a.err));
       if (ok) {
         tc_fence_after();
         uint16_t* orow = a.out + int64_t(q0 + i) * (int64_t(a.Hq) * D) + int64_t(h) * D;
@@ -419,12 +427,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           float o[32];
           tmem_ld32(to + c * 32, o);
           if (valid) {
-            uint32_t pk[16];
+            uint32_t ok16[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) pk[u] = pack_bf2(__fdiv_rn(o[2 * u], l), __fdiv_rn(o[2 * u + 1], l));
+            for (int u = 0; u < 16; ++u) ok16[u] = pack_bf2(__fdiv_rn(o[2 * u], l), __fdiv_rn(o[2 * u + 1], l));
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            for (int u = 0; u < 4; ++u)
+              dst[u] = make_uint4(ok16[4 * u], ok16[4 * u + 1], ok16[4 * u + 2], ok16[4 * u + 3]);
           }
         }
       }
@@ -444,13 +453,15 @@ constexpr size_t kSmemBytes = Layout<128>::BYTES;
 
 template <int D>
 static int launch(const mot_bf16* qkv, const Args& a, int n_tiles_max, cudaStream_t s) {
-  CUtensorMap tm;
+  CUtensorMap tm_q, tm_kv;
   const uint64_t ncol = uint64_t(a.Hq + 2 * a.Hkv) * D;
-  if (!make_tmap_bf16(&tm, qkv, ncol, uint64_t(a.T), 64, BQ)) return MOT_ERR_CUDA;
+  if (!make_tmap_bf16(&tm_q, qkv, ncol, uint64_t(a.T), 64, BQ) ||
+      !make_tmap_bf16(&tm_kv, qkv, ncol, uint64_t(a.T), 64, BKV))
+    return MOT_ERR_CUDA;
   if (cudaFuncSetAttribute(joint_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmemBytes)) != cudaSuccess)
     return MOT_ERR_CUDA;
-  joint_attention_kernel<D><<<unsigned(int64_t(n_tiles_max) * a.Hq), THREADS, kSmemBytes, s>>>(tm, a);
+  joint_attention_kernel<D><<<unsigned(int64_t(n_tiles_max) * a.Hq), THREADS, kSmemBytes, s>>>(tm_q, tm_kv, a);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
