@@ -634,3 +634,153 @@ def g_joint_attention(qkv, seqs, Hq: int, Hkv: int, D: int, scale: float | None 
             p = p / np.sum(p, axis=1, keepdims=True)
             out[q0:q0 + nq, h * D:(h + 1) * D] = p @ v
     return {"out": bf16(out), "out_pre": out}
+
+
+# ---------------------------------------------------------------------------
+# Flow-matching sampler pieces: schedule, three-branch renormalised CFG, SDE step and logp
+# ---------------------------------------------------------------------------
+#
+# [RFC-435] §1 Motivation items 2 and 3 (the policy log-probability is the ODE-to-SDE transition
+# density; three-branch renormalised CFG with two scales, a timestep window and a norm-ratio
+# rescale) and §3 BAGEL-specific rules (schedule built in FP64 and stored in FP32 with the shift
+# s; SDE step and logp in FP32 with sigma = t and dt = t_i - t_{i+1} > 0; logp summed over all
+# latent elements in a fixed order; the CFG window compared on FP32 t; renorm per request).
+# The pages give no formulas: the readings are the rectified-flow path x_t = (1 - t) x_0 + t eps
+# (t = 1 is noise), velocity v = eps - x_0, the marginal-preserving reverse SDE, and CFG as
+# successive interpolations; each is stated in its docstring.
+
+LOG_SQRT_2PI = 0.5 * np.log(2.0 * np.pi)
+
+
+def flow_schedule(n: int, shift: float) -> np.ndarray:
+    """n times from 1 to 0 (n - 1 steps): t_i = s u / (1 + (s - 1) u) with u = 1 - i/(n-1),
+    built in float64 and stored in float32 ([RFC-435] §3: schedule built in FP64, stored and
+    traced in FP32; the shift s comes from the run config)."""
+    u = 1.0 - np.arange(n, dtype=np.float64) / (n - 1)
+    return (shift * u / (1.0 + (shift - 1.0) * u)).astype(F32)
+
+
+def cfg_guided(t, t_lo, t_hi) -> bool:
+    """Whether step time t lies in the CFG window, compared on fp32 values."""
+    return bool(F32(t_lo) <= F32(t) <= F32(t_hi))
+
+
+def g_cfg_combine_renorm(v_c, v_tu, v_iu, t, s_text, s_img, t_lo, t_hi, renorm_min):
+    """Three-branch renormalised CFG of one request, in float64.
+
+    v_c: the fully conditioned velocity; v_tu: text-unconditioned; v_iu: image-unconditioned
+    or None (two branches). Inside the window:
+      v1 = v_tu + s_text (v_c - v_tu);  v2 = v_iu + s_img (v1 - v_iu) (or v1);
+      r  = clamp(||v_c|| / ||v2||, renorm_min, 1) over all the request's elements (1 if v2 = 0);
+      v  = v2 r.
+    Outside the window v = v_c.
+    """
+    v_c = np.asarray(v_c, np.float64)
+    if not cfg_guided(t, t_lo, t_hi):
+        return v_c.copy()
+    v1 = np.asarray(v_tu, np.float64) + float(F32(s_text)) * (v_c - np.asarray(v_tu, np.float64))
+    if v_iu is not None:
+        v_iu = np.asarray(v_iu, np.float64)
+        v2 = v_iu + float(F32(s_img)) * (v1 - v_iu)
+    else:
+        v2 = v1
+    ng = np.sqrt(np.sum(v2 * v2))
+    r = 1.0 if ng == 0 else np.sqrt(np.sum(v_c * v_c)) / ng
+    r = min(max(r, float(F32(renorm_min))), 1.0)
+    return v2 * r
+
+
+def g_flow_sde_step(x, v, z, t_i, t_next):
+    """One SDE step from t_i down to t_next and its log-probability, in float64.
+
+    sigma = t_i, dt = t_i - t_next > 0. With eps_hat = x + (1 - t) v (the noise the velocity
+    implies) and the score -eps_hat / t, the reverse SDE that keeps the marginals of
+    dx/dt = v steps to
+      mu = x - dt (v + sigma^2 / (2 t) eps_hat),   std = sigma sqrt(dt),   x_next = mu + std z,
+    and logp = sum over the latent elements of log N(x_next; mu, std^2).
+    """
+    t = float(F32(t_i))
+    dt = t - float(F32(t_next))
+    if not dt > 0:
+        raise ValueError("dt must be positive")
+    x = np.asarray(x, np.float64)
+    v = np.asarray(v, np.float64)
+    z = np.asarray(z, np.float64)
+    sigma = t
+    eps_hat = x + (1.0 - t) * v
+    mu = x - dt * (v + sigma * sigma / (2.0 * t) * eps_hat)
+    std = sigma * np.sqrt(dt)
+    x_next = mu + std * z
+    d = x_next - mu
+    logp = -np.sum(d * d) / (2.0 * std * std) - x.size * (np.log(std) + LOG_SQRT_2PI)
+    return {"x_next": x_next, "mu": mu, "std": std, "logp": logp}
+
+
+def e_request_tree_sum(terms):
+    """Sum of the fp32 terms of one request on the fixed tree of the flow kernels: elements in
+    chunks of 8; thread tau of 256 owns the chunks q with q % 256 == tau, summing them in
+    ascending order (the chunk's 8 elements in order) from 0.0; within each warp of 32 threads
+    an xor butterfly with offsets 16, 8, 4, 2, 1; then the 8 warps' sums folded left to right."""
+    terms = np.asarray(terms, F32).reshape(-1)
+    if terms.size % 8:
+        raise ValueError("the tree is defined for a multiple of 8 elements")
+    chunks = terms.reshape(-1, 8)
+    p = np.zeros(256, F32)
+    for q in range(chunks.shape[0]):
+        tau = q % 256
+        for u in range(8):
+            p[tau] = p[tau] + chunks[q, u]
+    lanes = np.arange(32)
+    w = p.reshape(8, 32)
+    for off in (16, 8, 4, 2, 1):
+        w = w + w[:, lanes ^ off]
+    acc = w[0, 0]
+    for k in range(1, 8):
+        acc = acc + w[k, 0]
+    return F32(acc)
+
+
+def e_cfg_combine_renorm(v_c, v_tu, v_iu, t, s_text, s_img, t_lo, t_hi, renorm_min):
+    """fp32 restatement of g_cfg_combine_renorm, each operation rounded on its own:
+    v1 = tu + s_text (c - tu), v2 = iu + s_img (v1 - iu); the sums of squares of c and v2 on
+    e_request_tree_sum; r = sqrt(ss_c) / sqrt(ss_g) (1 if ss_g is 0), then max with renorm_min
+    and min with 1; v = v2 r. Outside the window v = c."""
+    c = np.asarray(v_c, np.float64).astype(F32)
+    if not cfg_guided(t, t_lo, t_hi):
+        return c.copy()
+    tu = np.asarray(v_tu, np.float64).astype(F32)
+    v1 = tu + F32(s_text) * (c - tu)
+    if v_iu is not None:
+        iu = np.asarray(v_iu, np.float64).astype(F32)
+        v2 = iu + F32(s_img) * (v1 - iu)
+    else:
+        v2 = v1
+    ss_c = e_request_tree_sum(c * c)
+    ss_g = e_request_tree_sum(v2 * v2)
+    r = F32(1.0) if ss_g == 0 else np.sqrt(ss_c) / np.sqrt(ss_g)
+    r = min(max(r, F32(renorm_min)), F32(1.0))
+    return v2 * F32(r)
+
+
+def e_flow_sde_step(x, v, z, t_i, t_next):
+    """fp32 restatement of g_flow_sde_step, each operation rounded on its own:
+    dt = t - t_next, k = (sigma sigma) / (2 t), e = x + (1 - t) v, mu = x - dt (v + k e),
+    std = sigma sqrt(dt), x_next = mu + std z; d = x_next - mu, ss = e_request_tree_sum(d d),
+    logp = -(ss / (2 std std)) - N (log(std) + log sqrt(2 pi)) with the host's fp32 log (the
+    GPU's logf may differ in the last bit, so logp is compared within a tolerance)."""
+    t = F32(t_i)
+    dt = t - F32(t_next)
+    sigma = t
+    k = (sigma * sigma) / (F32(2.0) * t)
+    x32 = np.asarray(x, np.float64).astype(F32)
+    v32 = np.asarray(v, np.float64).astype(F32)
+    z32 = np.asarray(z, np.float64).astype(F32)
+    e = x32 + (F32(1.0) - t) * v32
+    mu = x32 - dt * (v32 + k * e)
+    std = sigma * np.sqrt(dt)
+    x_next = mu + std * z32
+    d = x_next - mu
+    ss = e_request_tree_sum(d * d)
+    a = ss / (F32(2.0) * (std * std))
+    logp = -a - F32(x32.size) * (np.log(std) + F32(LOG_SQRT_2PI))
+    return {"x_next": x_next, "mu": mu, "std": std, "logp": F32(logp)}

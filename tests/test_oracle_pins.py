@@ -744,3 +744,104 @@ def test_joint_attention_brute_force_and_sequence_independence():
     qkv2[:6] = O.bf16(rng.standard_normal((6, qkv.shape[1])))
     r2 = O.g_joint_attention(qkv2, seqs, Hq, Hkv, D)
     np.testing.assert_array_equal(r2["out_pre"][6:], r["out_pre"][6:])
+
+
+# ---------------------------------------------------------------------------
+# flow schedule, CFG combine with renorm, SDE step and logp
+# ---------------------------------------------------------------------------
+
+def test_flow_schedule_reproduces_the_printed_guided_step_counts():
+    gd = GOLDEN["flow_schedule_guided_steps"]
+    lo, hi = gd["window"]
+    for shift, want in gd["guided"].items():
+        ts = O.flow_schedule(gd["n"], float(shift))
+        assert sum(O.cfg_guided(ts[i], lo, hi) for i in range(gd["n"] - 1)) == want
+    ts = O.flow_schedule(5, 3.0)
+    assert ts.dtype == np.float32 and ts[0] == 1.0 and ts[-1] == 0.0
+    assert ts[2] == F32(0.75)                                  # u = 1/2: 1.5 / 2
+    np.testing.assert_array_equal(O.flow_schedule(5, 1.0), np.array([1, 0.75, 0.5, 0.25, 0], F32))
+
+
+def test_request_tree_sum_hand_values():
+    gd = GOLDEN["request_tree_sum"]
+    a = np.zeros(16, F32)
+    a[0] = 2.0 ** 24
+    a[1:] = 1.0
+    assert O.e_request_tree_sum(a) == gd["chunks_sum"]
+    b = np.zeros(65 * 8, F32)
+    b[0] = 2.0 ** 24
+    b[32 * 8] = 1.0
+    b[64 * 8] = 1.0
+    assert O.e_request_tree_sum(b) == gd["warps_sum"]
+
+
+def test_cfg_combine_identities_window_and_renorm():
+    rng = np.random.default_rng(61)
+    N = 512
+    c, tu, iu = (rng.standard_normal(N) for _ in range(3))
+    # outside the window: the conditioned velocity itself
+    np.testing.assert_array_equal(O.g_cfg_combine_renorm(c, tu, iu, 0.2, 4.0, 2.0, 0.4, 1.0, 0.0), c)
+    # text scale 1 without an image branch: v1 = c, r = 1
+    np.testing.assert_allclose(O.g_cfg_combine_renorm(c, tu, None, 0.5, 1.0, 1.0, 0.4, 1.0, 0.0), c, atol=1e-15)
+    # equal branches leave c unchanged for any scales
+    np.testing.assert_allclose(O.g_cfg_combine_renorm(c, c, c, 0.5, 4.0, 2.0, 0.0, 1.0, 0.0), c, atol=1e-12)
+    # the two interpolations by hand, and the rescale to ||c|| when the guided norm is larger
+    v = O.g_cfg_combine_renorm(c, tu, iu, 0.5, 4.0, 2.0, 0.4, 1.0, 0.0)
+    v1 = tu + 4.0 * (c - tu)
+    v2 = iu + 2.0 * (v1 - iu)
+    assert np.linalg.norm(v2) > np.linalg.norm(c)
+    np.testing.assert_allclose(v, v2 * np.linalg.norm(c) / np.linalg.norm(v2), rtol=1e-13)
+    np.testing.assert_allclose(np.linalg.norm(v), np.linalg.norm(c), rtol=1e-13)
+    # the clamp from below
+    v_min = O.g_cfg_combine_renorm(c, tu, iu, 0.5, 4.0, 2.0, 0.4, 1.0, 0.9)
+    np.testing.assert_allclose(v_min, float(F32(0.9)) * v2, rtol=1e-13)   # the policy values are fp32
+    # the guided norm below ||c||: r would exceed 1 and is clamped to it (v = v2)
+    np.testing.assert_allclose(O.g_cfg_combine_renorm(c, np.zeros(N), None, 0.5, 0.5, 1.0, 0.4, 1.0, 0.0), 0.5 * c,
+                               rtol=1e-15)
+    # the window includes both ends (compared on fp32 t)
+    assert O.cfg_guided(F32(0.4), 0.4, 1.0) and O.cfg_guided(1.0, 0.4, 1.0)
+    assert not O.cfg_guided(np.nextafter(F32(0.4), F32(0)), 0.4, 1.0)
+    # E follows G
+    e = O.e_cfg_combine_renorm(c, tu, iu, 0.5, 4.0, 2.0, 0.4, 1.0, 0.0)
+    np.testing.assert_allclose(e, v, rtol=2e-5, atol=2e-5)
+
+
+def test_sde_step_closed_forms_and_logp():
+    pytest.importorskip("scipy")
+    from scipy.stats import norm
+    rng = np.random.default_rng(62)
+    N = 256
+    x, v, z = (rng.standard_normal(N) for _ in range(3))
+    # t = 1 (the first step): eps_hat = x, mu = x - dt (v + x / 2), std = sqrt(dt)
+    r = O.g_flow_sde_step(x, v, np.zeros(N), 1.0, 0.75)
+    np.testing.assert_allclose(r["mu"], x - 0.25 * (v + 0.5 * x), rtol=1e-14)
+    assert abs(r["std"] - 0.5) < 1e-15
+    np.testing.assert_array_equal(r["x_next"], r["mu"])
+    assert abs(r["logp"] - N * norm.logpdf(0.0, scale=0.5)) < 1e-9
+    # logp of a noisy step against the library's Gaussian log-density
+    t, tn = float(F32(0.3)), float(F32(0.28))
+    r = O.g_flow_sde_step(x, v, z, t, tn)
+    assert abs(r["logp"] - np.sum(norm.logpdf(r["x_next"], loc=r["mu"], scale=r["std"]))) < 1e-8
+    # E follows G
+    e = O.e_flow_sde_step(x, v, z, t, tn)
+    np.testing.assert_allclose(e["x_next"], r["x_next"], rtol=1e-5, atol=1e-6)
+    assert abs(e["logp"] - r["logp"]) < 1e-4 * abs(r["logp"])
+
+
+def test_sde_step_keeps_the_gaussian_marginals():
+    # data x0 ~ N(0, a^2), eps ~ N(0, 1): x_t ~ N(0, s_t^2), s_t^2 = (1-t)^2 a^2 + t^2, and the exact
+    # velocity is v = beta x with beta = (t - (1-t) a^2) / s_t^2. One step of the reverse SDE must
+    # carry the variance s_t^2 to s_{t-dt}^2 up to O(dt^2); a wrong sign or factor on the score term
+    # leaves an O(dt) error.
+    a2, t = 0.7, 0.6
+    s2 = lambda tt: (1 - tt) ** 2 * a2 + tt * tt
+    errs = []
+    for dt in (1e-2, 5e-3, 2.5e-3):
+        beta = (t - (1 - t) * a2) / s2(t)
+        # the step is linear in x and z: x_next = A x + std z
+        A = O.g_flow_sde_step(np.array([1.0]), np.array([beta]), np.array([0.0]), t, t - dt)["mu"][0]
+        std = O.g_flow_sde_step(np.array([0.0]), np.array([0.0]), np.array([0.0]), t, t - dt)["std"]
+        var = A * A * s2(t) + std * std
+        errs.append(abs(var - s2(t - dt)))
+    assert errs[0] < 1e-3
+    assert errs[1] < errs[0] / 3 and errs[2] < errs[1] / 3     # quadratic convergence
