@@ -690,7 +690,7 @@ def g_cfg_combine_renorm(v_c, v_tu, v_iu, t, s_text, s_img, t_lo, t_hi, renorm_m
     return v2 * r
 
 
-def g_flow_sde_step(x, v, z, t_i, t_next):
+def g_flow_sde_step(x, v, z, t_i, t_next, x_next=None):
     """One SDE step from t_i down to t_next and its log-probability, in float64.
 
     sigma = t_i, dt = t_i - t_next > 0. With eps_hat = x + (1 - t) v (the noise the velocity
@@ -698,6 +698,8 @@ def g_flow_sde_step(x, v, z, t_i, t_next):
     dx/dt = v steps to
       mu = x - dt (v + sigma^2 / (2 t) eps_hat),   std = sigma sqrt(dt),   x_next = mu + std z,
     and logp = sum over the latent elements of log N(x_next; mu, std^2).
+    With z None the step is evaluated, not taken: x_next is given (the latent a rollout stored)
+    and only logp depends on it, so training scores the rollout's transition.
     """
     t = float(F32(t_i))
     dt = t - float(F32(t_next))
@@ -705,12 +707,14 @@ def g_flow_sde_step(x, v, z, t_i, t_next):
         raise ValueError("dt must be positive")
     x = np.asarray(x, np.float64)
     v = np.asarray(v, np.float64)
-    z = np.asarray(z, np.float64)
     sigma = t
     eps_hat = x + (1.0 - t) * v
     mu = x - dt * (v + sigma * sigma / (2.0 * t) * eps_hat)
     std = sigma * np.sqrt(dt)
-    x_next = mu + std * z
+    if z is None:
+        x_next = np.asarray(x_next, np.float64)
+    else:
+        x_next = mu + std * np.asarray(z, np.float64)
     d = x_next - mu
     logp = -np.sum(d * d) / (2.0 * std * std) - x.size * (np.log(std) + LOG_SQRT_2PI)
     return {"x_next": x_next, "mu": mu, "std": std, "logp": logp}
@@ -762,10 +766,11 @@ def e_cfg_combine_renorm(v_c, v_tu, v_iu, t, s_text, s_img, t_lo, t_hi, renorm_m
     return v2 * F32(r)
 
 
-def e_flow_sde_step(x, v, z, t_i, t_next):
+def e_flow_sde_step(x, v, z, t_i, t_next, x_next=None):
     """fp32 restatement of g_flow_sde_step, each operation rounded on its own:
     dt = t - t_next, k = (sigma sigma) / (2 t), e = x + (1 - t) v, mu = x - dt (v + k e),
-    std = sigma sqrt(dt), x_next = mu + std z; d = x_next - mu, ss = e_request_tree_sum(d d),
+    std = sigma sqrt(dt), x_next = mu + std z (or the given x_next when z is None);
+    d = x_next - mu, ss = e_request_tree_sum(d d),
     logp = -(ss / (2 std std)) - N (log(std) + log sqrt(2 pi)) with the host's fp32 log (the
     GPU's logf may differ in the last bit, so logp is compared within a tolerance)."""
     t = F32(t_i)
@@ -774,11 +779,13 @@ def e_flow_sde_step(x, v, z, t_i, t_next):
     k = (sigma * sigma) / (F32(2.0) * t)
     x32 = np.asarray(x, np.float64).astype(F32)
     v32 = np.asarray(v, np.float64).astype(F32)
-    z32 = np.asarray(z, np.float64).astype(F32)
     e = x32 + (F32(1.0) - t) * v32
     mu = x32 - dt * (v32 + k * e)
     std = sigma * np.sqrt(dt)
-    x_next = mu + std * z32
+    if z is None:
+        x_next = np.asarray(x_next, np.float64).astype(F32)
+    else:
+        x_next = mu + std * np.asarray(z, np.float64).astype(F32)
     d = x_next - mu
     ss = e_request_tree_sum(d * d)
     a = ss / (F32(2.0) * (std * std))

@@ -845,3 +845,24 @@ def test_sde_step_keeps_the_gaussian_marginals():
         errs.append(abs(var - s2(t - dt)))
     assert errs[0] < 1e-3
     assert errs[1] < errs[0] / 3 and errs[2] < errs[1] / 3     # quadratic convergence
+
+
+def test_sde_logp_of_a_given_latent():
+    # Training scores the latent a rollout stored: with the same x, v and times, evaluating the
+    # step at the rollout's x_next returns the rollout's logp exactly, and for any other latent
+    # it is the library's Gaussian log-density around mu.
+    pytest.importorskip("scipy")
+    from scipy.stats import norm
+    rng = np.random.default_rng(63)
+    N = 4096
+    x, v, z = (rng.standard_normal(N) for _ in range(3))
+    t, tn = float(F32(0.55)), float(F32(0.5))
+    roll = O.e_flow_sde_step(x, v, z, t, tn)
+    score = O.e_flow_sde_step(x, v, None, t, tn, x_next=roll["x_next"])
+    assert score["logp"] == roll["logp"]
+    np.testing.assert_array_equal(score["x_next"], roll["x_next"])
+    y = rng.standard_normal(N)
+    g = O.g_flow_sde_step(x, v, None, t, tn, x_next=y)
+    assert abs(g["logp"] - np.sum(norm.logpdf(y, loc=g["mu"], scale=g["std"]))) < 1e-7
+    e = O.e_flow_sde_step(x, v, None, t, tn, x_next=y)
+    assert abs(e["logp"] - g["logp"]) < 1e-4 * abs(g["logp"])
