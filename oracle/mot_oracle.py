@@ -720,28 +720,40 @@ def g_flow_sde_step(x, v, z, t_i, t_next, x_next=None):
     return {"x_next": x_next, "mu": mu, "std": std, "logp": logp}
 
 
+FLOW_SEGMENT = 8192  # elements per segment of the request tree
+
+
 def e_request_tree_sum(terms):
-    """Sum of the fp32 terms of one request on the fixed tree of the flow kernels: elements in
-    chunks of 8; thread tau of 256 owns the chunks q with q % 256 == tau, summing them in
-    ascending order (the chunk's 8 elements in order) from 0.0; within each warp of 32 threads
-    an xor butterfly with offsets 16, 8, 4, 2, 1; then the 8 warps' sums folded left to right."""
+    """Sum of the fp32 terms of one request on the fixed tree of the flow kernels. The request's
+    elements are cut into segments of FLOW_SEGMENT (the last may be shorter); each segment is
+    summed on its own: elements in chunks of 8, thread tau of 256 owns the segment's chunks q
+    with q % 256 == tau, summing them in ascending order (the chunk's 8 elements in order) from
+    0.0; within each warp of 32 threads an xor butterfly with offsets 16, 8, 4, 2, 1; then the 8
+    warps' sums folded left to right. The segment sums are then folded left to right. The order
+    depends only on the request's own length, never on the batch around it."""
     terms = np.asarray(terms, F32).reshape(-1)
-    if terms.size % 8:
-        raise ValueError("the tree is defined for a multiple of 8 elements")
-    chunks = terms.reshape(-1, 8)
-    p = np.zeros(256, F32)
-    for q in range(chunks.shape[0]):
-        tau = q % 256
-        for u in range(8):
-            p[tau] = p[tau] + chunks[q, u]
+    if terms.size % 8 or terms.size == 0:
+        raise ValueError("the tree is defined for a positive multiple of 8 elements")
     lanes = np.arange(32)
-    w = p.reshape(8, 32)
-    for off in (16, 8, 4, 2, 1):
-        w = w + w[:, lanes ^ off]
-    acc = w[0, 0]
-    for k in range(1, 8):
-        acc = acc + w[k, 0]
-    return F32(acc)
+    seg_sums = []
+    for s0 in range(0, terms.size, FLOW_SEGMENT):
+        chunks = terms[s0:s0 + FLOW_SEGMENT].reshape(-1, 8)
+        p = np.zeros(256, F32)
+        for q in range(chunks.shape[0]):
+            tau = q % 256
+            for u in range(8):
+                p[tau] = p[tau] + chunks[q, u]
+        w = p.reshape(8, 32)
+        for off in (16, 8, 4, 2, 1):
+            w = w + w[:, lanes ^ off]
+        acc = w[0, 0]
+        for k in range(1, 8):
+            acc = acc + w[k, 0]
+        seg_sums.append(F32(acc))
+    total = seg_sums[0]
+    for v in seg_sums[1:]:
+        total = total + v
+    return F32(total)
 
 
 def e_cfg_combine_renorm(v_c, v_tu, v_iu, t, s_text, s_img, t_lo, t_hi, renorm_min):

@@ -773,6 +773,15 @@ def test_request_tree_sum_hand_values():
     b[32 * 8] = 1.0
     b[64 * 8] = 1.0
     assert O.e_request_tree_sum(b) == gd["warps_sum"]
+    c = np.zeros(2 * O.FLOW_SEGMENT + 8, F32)
+    c[0] = 2.0 ** 24
+    c[O.FLOW_SEGMENT] = 1.0
+    c[2 * O.FLOW_SEGMENT] = 1.0
+    assert O.e_request_tree_sum(c) == gd["segments_sum"]
+    # a small-magnitude sum is the exact sum (every partial sum is representable)
+    rng = np.random.default_rng(64)
+    d = rng.integers(-1000, 1000, 3 * O.FLOW_SEGMENT + 40).astype(F32)
+    assert O.e_request_tree_sum(d) == float(np.sum(d.astype(np.int64)))
 
 
 def test_cfg_combine_identities_window_and_renorm():
