@@ -334,7 +334,8 @@ def run_ours(args, rank, world, local_rank):
         secondary = {"swiglu_mlp_T8192": run_mlp(dev, flush), "cfg_pack_T36864": run_cfg_pack(dev, flush),
                      "fp32_rope_profile_T4096": run_qkv_fp32_rope(dev, flush),
                      "backward_T4096": run_backward(dev, flush),
-                     "joint_attention": run_attention(dev, flush)}
+                     "joint_attention": run_attention(dev, flush),
+                     "flow_step": run_flow(dev, flush)}
     if world > 1:
         dist.barrier()
     if rank != 0:
@@ -647,6 +648,56 @@ def run_attention(dev, flush) -> dict:
     return res
 
 
+def run_flow(dev, flush) -> dict:
+    """One flow-sampler step of 16 requests of a 1024 x 1024 latent (64 x 64 tokens of 64
+    values, N = 262144 each): three-branch renormalised CFG of bf16 velocities into fp32, then
+    the SDE step (x, the guided velocity and the noise in; x_next and logp out), every request at
+    a different step of the 50-step schedule with shift 3."""
+    import numpy as np
+    import torch
+
+    import mixture_transformers_token_gb300 as mot
+    from mixture_transformers_token_gb300 import workloads as W
+
+    stream = torch.cuda.current_stream(dev)
+    n_req, n = W.FLOW_REQUESTS, W.FLOW_N_1024
+    br = {k: W.bf16_normal_device(11, 800 + i, (n_req, n), dev) for i, k in enumerate(("c", "tu", "iu"))}
+    x = W.bf16_normal_device(11, 810, (n_req, n), dev).float()
+    z = W.bf16_normal_device(11, 811, (n_req, n), dev).float()
+    sched = mot.mot_flow_schedule_host(W.FLOW_STEPS, W.FLOW_SHIFT).numpy()
+    p = W.FLOW_POLICY
+    steps = [3 * i for i in range(n_req)]
+    policy = torch.tensor([(float(sched[i]), p["s_text"], p["s_img"], p["t_lo"], p["t_hi"], p["renorm_min"])
+                           for i in steps], dtype=torch.float32, device=dev)
+    times = torch.tensor(np.array([(sched[i], sched[i + 1]) for i in steps], dtype=np.float32), device=dev)
+    ws = torch.zeros(mot.mot_flow_workspace_bytes(n_req, n), dtype=torch.uint8, device=dev)
+    v = torch.empty((n_req, n), dtype=torch.float32, device=dev)
+    x_next = torch.empty_like(v)
+    logp = torch.empty((n_req,), dtype=torch.float32, device=dev)
+    stages = [
+        ("cfg_combine_renorm", lambda: mot.mot_cfg_combine_renorm(br["c"], br["tu"], br["iu"], policy, ws=ws, out=v)),
+        ("flow_sde_step", lambda: mot.mot_flow_sde_step(x, v, z, times, ws=ws, x_next=x_next, logp=logp)),
+    ]
+    r = time_stages(stages, 100, 5, flush, stream)
+    if mot.mot_device_status(ws) != 0:
+        raise RuntimeError("device error flags set in the flow workload")
+    pk = peaks()
+    e = n_req * n
+    b_cfg = 10 * e + 24 * n_req           # three bf16 branches read, fp32 out written, policy
+    b_sde = 16 * e + 12 * n_req           # x, v, z read, x_next written, times, logp
+    return {
+        "workload": f"flow_step_{n_req}x{n}",
+        "cfg_combine_renorm_us": round(r["cfg_combine_renorm"] * 1e6, 2),
+        "cfg_combine_renorm_gbs": round(b_cfg / r["cfg_combine_renorm"] / 1e9, 1),
+        "cfg_combine_renorm_frac_hbm": round(b_cfg / r["cfg_combine_renorm"] / 1e9 / pk["hbm_gbs"], 4),
+        "flow_sde_step_us": round(r["flow_sde_step"] * 1e6, 2),
+        "flow_sde_step_gbs": round(b_sde / r["flow_sde_step"] / 1e9, 1),
+        "flow_sde_step_frac_hbm": round(b_sde / r["flow_sde_step"] / 1e9 / pk["hbm_gbs"], 4),
+        "step_us": round(r["step"] * 1e6, 2), "elements": e, "bytes": {"cfg": b_cfg, "sde": b_sde},
+        "distribution_us": {k: r["dist"][k] for k in ("cfg_combine_renorm", "flow_sde_step")},
+    }
+
+
 def run_cfg_pack(dev, flush) -> dict:
     """CFG pack: 12 sequences of 2048 und + 1024 gen rows (T = 36864), positions restarting per
     sequence: add-RMSNorm (+ plan), routed QKV + QK-norm + RoPE, routed O projection 3584 -> 3584
@@ -787,7 +838,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--secondary", dest="secondary", action="store_true", default=True)
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
-    ap.add_argument("--profile", choices=["mlp", "cfg", "qkv_fp32", "backward", "attention"], default=None,
+    ap.add_argument("--profile", choices=["mlp", "cfg", "qkv_fp32", "backward", "attention", "flow"], default=None,
                     help="run only one secondary workload (mlp, cfg, backward: 5 warm-up + 50 timed steps; "
                          "qkv_fp32: 5 + 200) and print its figures; a short command for profiler captures")
     ap.add_argument("--cpu-baseline-child", type=int, default=None, help=argparse.SUPPRESS)
@@ -806,7 +857,7 @@ def main():
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         fn = {"mlp": run_mlp, "cfg": run_cfg_pack, "qkv_fp32": run_qkv_fp32_rope, "backward": run_backward,
-              "attention": run_attention}[args.profile]
+              "attention": run_attention, "flow": run_flow}[args.profile]
         print(json.dumps({args.profile: fn(dev, L2Flush(dev))}), flush=True)
         return
     if args.warmup < 3:

@@ -63,6 +63,7 @@ extern "C" {
 #define MOT_DEV_PLAN_MISMATCH 0x4u  /* the workspace holds no plan for this T */
 #define MOT_DEV_BAD_POSITION  0x8u  /* a RoPE position outside [0, P) (clamped to 0) */
 #define MOT_DEV_BAD_SEQUENCE  0x10u /* an attention sequence descriptor out of range */
+#define MOT_DEV_BAD_TIME      0x20u /* SDE step times outside 0 <= t_next < t_i <= 1 */
 
 /* epilogues of mot_routed_gemm */
 #define MOT_EPI_CAST   0  /* out = bf16(acc) */
@@ -277,10 +278,13 @@ int mot_rope_table_fill_host_fp32(double theta, int D, int P, float* host_cs);
  *   ws    at least 64 bytes (e.g. a routing plan); its error word receives device errors.
  *   out   [T][Hq D] bf16   out: rows that are some sequence's query; other rows untouched.
  * Query head h reads KV head h / (Hq / Hkv). Arithmetic: S = Q K^T in fp32 on the tensor
- * cores; per row, 128-key blocks in ascending order from the sequence's first key: x = S *
- * (scale * log2 e), running maximum m, p = exp2(x - m), running sum l (fp32, left to right),
- * O = O * exp2(m_old - m) + bf16(p) V in fp32; out = bf16(O / l). D in {64, 128}, Hq a
- * multiple of Hkv.
+ * cores; per row, 64-key blocks in ascending order from the sequence's first key, with
+ * c = scale * log2 e: the reference maximum m starts as the first block's maximum and moves
+ * to a later block's maximum only when that exceeds m by more than 8 / c (so p <= 2^8);
+ * p = 2^(S c - m c) (the hardware exp2 approximation); l = l alpha + the block's sum of p;
+ * O = O alpha + bf16(p) V in fp32 with alpha = 2^((m_old - m) c); out = bf16(O / l). The
+ * result depends only on the row's own sequence, not on the other sequences in the pack.
+ * D in {64, 128}, Hq a multiple of Hkv.
  */
 int mot_joint_attention(const mot_bf16* qkv, int64_t T, int Hq, int Hkv, int D, const int32_t* seqs,
                         int n_seq, float scale, void* ws, size_t ws_bytes, mot_bf16* out, void* stream);
@@ -361,6 +365,74 @@ int mot_add_rmsnorm_backward(const mot_bf16* dy, const mot_bf16* d_res_out, cons
  */
 int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, void* ws, size_t ws_bytes, float* dw,
                         void* stream);
+
+/*
+ * mot_flow_schedule_host -- the sampler's n step times from 1 down to 0 ([RFC-435] §3
+ * BAGEL-specific rules: the schedule is built in FP64 and stored in FP32 with the shift s).
+ *   host_t  host array of n floats: t_i = float(s u / (1 + (s - 1) u)), u = 1 - i / (n - 1),
+ *           evaluated in double; t_0 = 1, t_{n-1} = 0.
+ * Geometry: 2 <= n <= 2^20, else MOT_ERR_GEOMETRY; shift finite and > 0, else MOT_ERR_ARG.
+ */
+int mot_flow_schedule_host(int n, double shift, float* host_t);
+
+/*
+ * mot_flow_workspace_bytes -- workspace bytes that mot_cfg_combine_renorm and
+ * mot_flow_sde_step need for n_req requests of N elements: the 64-byte header (its error word)
+ * and 8 bytes per request and segment of 8192 elements. 0 for a geometry those calls reject.
+ */
+size_t mot_flow_workspace_bytes(int n_req, int64_t N);
+
+/*
+ * mot_cfg_combine_renorm -- three-branch renormalised classifier-free guidance, per request
+ * ([RFC-435] §1 Motivation item 3: up to three branches, two scales, a timestep window and a
+ * norm-ratio rescale; §3 BAGEL-specific rules: the window is compared on FP32 t and the
+ * renorm reduces over each request alone, never over the packed batch).
+ *   v_c, v_tu  [n_req][N] bf16  the conditioned and the text-unconditioned velocities.
+ *   v_iu       [n_req][N] bf16  the image-unconditioned velocity, or NULL for two branches.
+ *   policy     device fp32 [n_req][6] = (t, s_text, s_img, t_lo, t_hi, renorm_min).
+ *   ws         at least mot_flow_workspace_bytes(n_req, N) bytes; everything after its first
+ *              64 bytes is scratch that the call overwrites (so not a routing plan in use).
+ *   out        [n_req][N] fp32  out.
+ * Per request, every operation rounded on its own in fp32: when t_lo <= t <= t_hi,
+ * v1 = tu + s_text (c - tu), v2 = iu + s_img (v1 - iu) (v2 = v1 without iu); the sums of c c
+ * and v2 v2 over the request on a fixed tree (the request cut into segments of 8192
+ * elements; in each, chunks of 8 elements, thread k of 256 summing the chunks q with
+ * q % 256 == k in ascending order, an xor butterfly 16, 8, 4, 2, 1 inside each warp and the 8
+ * warps folded left to right; the segment sums folded left to right); r = sqrt(ss_c) /
+ * sqrt(ss_g) (1 when ss_g is 0), r = min(max(r, renorm_min), 1); out = v2 r. Outside the
+ * window out = c. Nothing depends on the other requests of the batch.
+ * Geometry: 1 <= n_req <= 65535, N a multiple of 8, 8 <= N <= 2^24, else MOT_ERR_GEOMETRY;
+ * all pointers 16-byte aligned device memory of the stream's device.
+ */
+int mot_cfg_combine_renorm(const mot_bf16* v_c, const mot_bf16* v_tu, const mot_bf16* v_iu, int n_req, int64_t N,
+                           const float* policy, void* ws, size_t ws_bytes, float* out, void* stream);
+
+/*
+ * mot_flow_sde_step -- one reverse-SDE step of the flow sampler and the log-probability of
+ * the transition, per request ([RFC-435] §1 Motivation item 2: the policy log-probability is
+ * the ODE-to-SDE transition density; §3 BAGEL-specific rules: FP32, sigma = t,
+ * dt = t_i - t_{i+1} > 0, logp summed over all latent elements in a fixed order; §2: training
+ * and rollout must produce exactly equal logp).
+ *   x, v    [n_req][N] fp32   the latent at t_i and the guided velocity there.
+ *   z       [n_req][N] fp32   the step's standard normal noise (drawn by the caller), or NULL
+ *                             to score a given x_next instead of sampling one.
+ *   x_next  [n_req][N] fp32   out (z given): the latent at t_next; in (z NULL).
+ *   times   device fp32 [n_req][2] = (t_i, t_next).
+ *   ws      at least mot_flow_workspace_bytes(n_req, N) bytes, scratch after the first 64 as
+ *           for mot_cfg_combine_renorm; its error word receives MOT_DEV_BAD_TIME for a request
+ *           whose times are not 0 <= t_next < t_i <= 1 (fp32 dt <= 0 included); that
+ *           request's outputs are then not written.
+ *   logp    device fp32 [n_req]  out.
+ * Per element, every operation rounded on its own in fp32: dt = t - t_next, k = (t t) / (2 t),
+ * e = x + (1 - t) v, mu = x - dt (v + k e), std = t sqrt(dt), x_next = mu + std z; then
+ * d = x_next - mu and ss = the sum of d d on the tree of mot_cfg_combine_renorm;
+ * logp = -(ss / (2 (std std))) - N (logf(std) + log sqrt(2 pi)). Scoring the x_next that a
+ * sampling call wrote returns that call's logp bit for bit.
+ * Geometry: 1 <= n_req <= 65535, N a multiple of 8, 8 <= N <= 2^24, else MOT_ERR_GEOMETRY;
+ * all pointers 16-byte aligned device memory of the stream's device.
+ */
+int mot_flow_sde_step(const float* x, const float* v, const float* z, float* x_next, int n_req, int64_t N,
+                      const float* times, void* ws, size_t ws_bytes, float* logp, void* stream);
 
 /*
  * mot_selftest_wait_timeout -- exercises the bounded wait that every pipeline wait of the

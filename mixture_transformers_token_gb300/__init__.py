@@ -27,6 +27,8 @@ __all__ = [
     "mot_routed_qkv_norm_rope_fp32", "mot_rope_table_fill_host_fp32", "mot_add_rmsnorm_backward",
     "mot_rmsnorm_dweight", "mot_routed_gemm_dx", "mot_routed_gemm_dw", "mot_joint_attention", "DEV_BAD_SEQUENCE",
     "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows", "mot_selftest_wait_timeout",
+    "DEV_BAD_TIME", "mot_flow_workspace_bytes", "mot_flow_schedule_host", "mot_cfg_combine_renorm",
+    "mot_flow_sde_step",
 ]
 
 ABI_VERSION = 1
@@ -39,6 +41,7 @@ DEV_TIMEOUT = 0x2
 DEV_PLAN_MISMATCH = 0x4
 DEV_BAD_POSITION = 0x8
 DEV_BAD_SEQUENCE = 0x10
+DEV_BAD_TIME = 0x20
 NOALLOC_MAX_TOKENS = 65536
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +76,10 @@ _SIGNATURES = {
     "mot_routed_gemm_dx": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_dw": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_joint_attention": (_c_i, [_c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_flow_workspace_bytes": (_c_sz, [_c_i, _c_i64]),
+    "mot_flow_schedule_host": (_c_i, [_c_i, ctypes.c_double, _c_p]),
+    "mot_cfg_combine_renorm": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_i64, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_flow_sde_step": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_i, _c_i64, _c_p, _c_p, _c_sz, _c_p, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
 }
 
@@ -435,6 +442,83 @@ def mot_rope_table_fill_host_fp32(theta: float, D: int, P: int) -> torch.Tensor:
     t = torch.empty((P, D // 2, 2), dtype=torch.float32)
     _check("mot_rope_table_fill_host_fp32", _lib().mot_rope_table_fill_host_fp32(theta, D, P, t.data_ptr()))
     return t
+
+
+def mot_flow_workspace_bytes(n_req: int, N: int) -> int:
+    return int(_lib().mot_flow_workspace_bytes(n_req, N))
+
+
+def mot_flow_schedule_host(n: int, shift: float) -> torch.Tensor:
+    """The sampler's n step times from 1 down to 0 (built in double, stored fp32), a CPU tensor."""
+    t = torch.empty((n,), dtype=torch.float32)
+    _check("mot_flow_schedule_host", _lib().mot_flow_schedule_host(n, shift, t.data_ptr()))
+    return t
+
+
+def _flow_ws(ws, n_req: int, N: int, device) -> torch.Tensor:
+    if ws is None:
+        ws = torch.zeros(max(mot_flow_workspace_bytes(n_req, N), 64), dtype=torch.uint8, device=device)
+    _dev(ws, "ws", torch.uint8, 1)
+    return ws
+
+
+def mot_cfg_combine_renorm(v_c, v_tu, v_iu, policy, ws=None, out=None, stream=None):
+    """Three-branch renormalised CFG per request: v_c, v_tu, v_iu (or None) [n_req][N] bf16,
+    policy a device fp32 [n_req][6] of (t, s_text, s_img, t_lo, t_hi, renorm_min). `ws` (>=
+    mot_flow_workspace_bytes) is scratch after its 64-byte header. Returns out [n_req][N] fp32."""
+    n_req, N = v_c.shape
+    _dev(v_c, "v_c", torch.bfloat16, 2)
+    _dev(v_tu, "v_tu", torch.bfloat16, 2)
+    ip = None
+    if v_iu is not None:
+        _dev(v_iu, "v_iu", torch.bfloat16, 2)
+        ip = v_iu.data_ptr()
+    _dev(policy, "policy", torch.float32, 2)
+    if tuple(v_tu.shape) != (n_req, N) or (v_iu is not None and tuple(v_iu.shape) != (n_req, N)):
+        raise ValueError("the branches must all be [n_req, N]")
+    if tuple(policy.shape) != (n_req, 6):
+        raise ValueError("policy must be [n_req, 6]")
+    ws = _flow_ws(ws, n_req, N, v_c.device)
+    if out is None:
+        out = torch.empty((n_req, N), dtype=torch.float32, device=v_c.device)
+    _dev(out, "out", torch.float32, 2)
+    _check("mot_cfg_combine_renorm", _lib().mot_cfg_combine_renorm(
+        v_c.data_ptr(), v_tu.data_ptr(), ip, n_req, N, policy.data_ptr(), ws.data_ptr(), ws.numel(),
+        out.data_ptr(), _stream(v_c, stream)))
+    return out
+
+
+def mot_flow_sde_step(x, v, z, times, ws=None, x_next=None, logp=None, stream=None):
+    """One reverse-SDE step per request and its log-probability: x, v, z [n_req][N] fp32, times
+    a device fp32 [n_req][2] of (t_i, t_next). With z None, x_next must be given and is scored
+    instead of sampled. `ws`'s error word receives DEV_BAD_TIME. Returns (x_next, logp [n_req])."""
+    n_req, N = x.shape
+    _dev(x, "x", torch.float32, 2)
+    _dev(v, "v", torch.float32, 2)
+    _dev(times, "times", torch.float32, 2)
+    if tuple(v.shape) != (n_req, N) or tuple(times.shape) != (n_req, 2):
+        raise ValueError("v must be [n_req, N] and times [n_req, 2]")
+    zp = None
+    if z is not None:
+        _dev(z, "z", torch.float32, 2)
+        if tuple(z.shape) != (n_req, N):
+            raise ValueError("z must be [n_req, N]")
+        zp = z.data_ptr()
+    elif x_next is None:
+        raise ValueError("either z or x_next must be given")
+    ws = _flow_ws(ws, n_req, N, x.device)
+    if x_next is None:
+        x_next = torch.empty((n_req, N), dtype=torch.float32, device=x.device)
+    _dev(x_next, "x_next", torch.float32, 2)
+    if tuple(x_next.shape) != (n_req, N):
+        raise ValueError("x_next must be [n_req, N]")
+    if logp is None:
+        logp = torch.empty((n_req,), dtype=torch.float32, device=x.device)
+    _dev(logp, "logp", torch.float32, 1)
+    _check("mot_flow_sde_step", _lib().mot_flow_sde_step(
+        x.data_ptr(), v.data_ptr(), zp, x_next.data_ptr(), n_req, N, times.data_ptr(), ws.data_ptr(), ws.numel(),
+        logp.data_ptr(), _stream(x, stream)))
+    return x_next, logp
 
 
 def mot_selftest_wait_timeout(ws, stream=None) -> None:

@@ -23,7 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmot.so")
 
-SOURCES = ["mot_route_norm.cu", "mot_gemm.cu", "mot_misc.cu", "mot_backward.cu", "mot_attention.cu"]
+SOURCES = ["mot_route_norm.cu", "mot_gemm.cu", "mot_misc.cu", "mot_backward.cu", "mot_attention.cu",
+           "mot_flow.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-ffp-contract=off",
          "-I", INCLUDE, "-I", CSRC]

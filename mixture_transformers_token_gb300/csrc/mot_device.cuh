@@ -419,4 +419,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch. A grid launched with programmatic stream serialization may
+// start once every CTA of the grid before it has called pdl_trigger (or exited); pdl_wait then
+// blocks until that grid has completed and its memory is visible. Before pdl_wait a dependent
+// grid may only read what was complete before the preceding grid started. Both are no-ops in
+// a grid launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace mot

@@ -1,0 +1,400 @@
+// Flow-matching sampler pieces: the step schedule, three-branch renormalised CFG and the SDE
+// step with its log-probability, per request.
+//
+// Sources: [RFC][BAGEL-7B-MoT][CUDA/ROCm] WS1/WS2 kernel roadmap and integration plan #435
+// (§1 Motivation items 2 and 3: the policy log-probability is the ODE-to-SDE transition density;
+// three-branch renormalised CFG with two scales, a timestep window and a norm-ratio rescale;
+// §3 BAGEL-specific rules: schedule built in FP64 and stored in FP32 with the shift s; SDE step
+// and logp in FP32 with sigma = t and dt = t_i - t_{i+1} > 0; logp summed over all latent
+// elements in a fixed order; CFG window compared on FP32 t; renorm per request; no fast math).
+//
+// Readings (the pages give no formulas): the rectified-flow path x_t = (1 - t) x_0 + t eps with
+// velocity v = eps - x_0; the SDE step mu = x - dt (v + sigma^2 / (2 t) (x + (1 - t) v)),
+// std = sigma sqrt(dt); CFG v1 = tu + s_text (c - tu), v2 = iu + s_img (v1 - iu), rescaled by
+// clamp(||c|| / ||v2||, min, 1) over the request's elements.
+//
+// A request's elements are cut into segments of 8192; one CTA of 256 threads takes one segment.
+// The segment's elements are taken in chunks of 8; thread tau owns the segment's chunks q with
+// q % 256 == tau (so a warp's loads are consecutive 16- or 32-byte pieces); a segment sum runs
+// sequentially per thread over its chunks in ascending order, then as an xor butterfly (16, 8,
+// 4, 2, 1) inside each warp, then over the 8 warps left to right; the request's sum folds its
+// segment sums left to right. The order depends only on the request's length, never on the
+// batch. Every operation is rounded on its own in fp32 (no fused multiply-add).
+//
+// CFG reads its inputs twice (once for the sums, once to scale), the second time mostly from
+// L2; the SDE step reads them once and a small kernel folds each request's segment sums.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "mot.h"
+#include "mot_device.cuh"
+#include "mot_host.hpp"
+
+namespace mot {
+namespace flow {
+
+constexpr int THREADS = 256;
+constexpr int SEG = 8192;                    // elements per segment
+constexpr int CPT = SEG / 8 / THREADS;       // chunks per thread and segment (4)
+constexpr int64_t kMaxN = int64_t(1) << 24;  // elements per request
+constexpr int kMaxReq = 65535;
+constexpr int kCtasPerSm = 4;                // resident CTAs per SM at the launch bounds below
+constexpr float kLogSqrt2Pi = 0.918938533204672742f;  // log(2 pi) / 2
+
+__host__ __device__ constexpr int segments(int64_t N) { return int((N + SEG - 1) / SEG); }
+
+inline size_t workspace_bytes(int n_req, int64_t N) {
+  return sizeof(PlanHeader) + ((size_t(n_req) * size_t(segments(N)) * 8 + 15) & ~size_t(15));
+}
+
+// The CTA's sum of the per-thread partials p: butterfly inside each warp, then the warps left
+// to right. Returned in thread 0.
+__device__ __forceinline__ float cta_sum(float p, float* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off));
+  __syncthreads();  // every thread has read wsum's previous contents
+  if (lane == 0) wsum[warp] = p;
+  __syncthreads();
+  float acc = wsum[0];
+#pragma unroll
+  for (int k = 1; k < THREADS / 32; ++k) acc = __fadd_rn(acc, wsum[k]);
+  return acc;
+}
+
+__device__ __forceinline__ void unpack8_bf16(const uint4 u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf_lo(w[i]);
+    v[2 * i + 1] = bf_hi(w[i]);
+  }
+}
+
+struct F8 {
+  float4 a, b;
+};
+
+__device__ __forceinline__ F8 load8_f32(const float* p) {
+  return F8{__ldg(reinterpret_cast<const float4*>(p)), __ldg(reinterpret_cast<const float4*>(p) + 1)};
+}
+
+__device__ __forceinline__ void unpack8_f32(const F8& f, float (&v)[8]) {
+  v[0] = f.a.x; v[1] = f.a.y; v[2] = f.a.z; v[3] = f.a.w;
+  v[4] = f.b.x; v[5] = f.b.y; v[6] = f.b.z; v[7] = f.b.w;
+}
+
+__device__ __forceinline__ void store8_f32(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+struct CfgArgs {
+  const uint16_t* c;    // [n_req][N] bf16
+  const uint16_t* tu;
+  const uint16_t* iu;   // or null: two branches
+  const float* policy;  // [n_req][6]: t, s_text, s_img, t_lo, t_hi, renorm_min
+  int64_t N;
+  int S;                // segments per request
+  float2* part;         // [n_req][S]: (sum c c, sum v2 v2) of each segment
+  float* out;           // [n_req][N] fp32
+};
+
+struct CfgPolicy {
+  float t, s_text, s_img, t_lo, t_hi, rmin;
+  __device__ bool guided() const { return t_lo <= t && t <= t_hi; }
+};
+
+__device__ __forceinline__ CfgPolicy load_policy(const float* p) {
+  return CfgPolicy{p[0], p[1], p[2], p[3], p[4], p[5]};
+}
+
+// The segment's chunks of this thread, loaded together (CPT loads of each input in flight).
+struct CfgChunks {
+  uint4 c[CPT], tu[CPT], iu[CPT];
+  int n;  // how many of the CPT chunks exist
+};
+
+__device__ __forceinline__ void cfg_load(const CfgArgs& a, int64_t base, int nch, CfgChunks& k) {
+  k.n = 0;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int q = int(threadIdx.x) + THREADS * j;
+    if (q < nch) {
+      k.n = j + 1;
+      k.c[j] = __ldg(reinterpret_cast<const uint4*>(a.c + base + 8 * q));
+      k.tu[j] = __ldg(reinterpret_cast<const uint4*>(a.tu + base + 8 * q));
+      if (a.iu) k.iu[j] = __ldg(reinterpret_cast<const uint4*>(a.iu + base + 8 * q));
+    }
+  }
+}
+
+// v1 = tu + s_text (c - tu); v2 = iu + s_img (v1 - iu), or v1 without iu.
+__device__ __forceinline__ void cfg_guide(const CfgArgs& a, const CfgPolicy& pol, const CfgChunks& k, int j,
+                                          float (&c)[8], float (&v2)[8]) {
+  float tu[8];
+  unpack8_bf16(k.c[j], c);
+  unpack8_bf16(k.tu[j], tu);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v2[i] = __fadd_rn(tu[i], __fmul_rn(pol.s_text, __fsub_rn(c[i], tu[i])));
+  if (a.iu) {
+    float iu[8];
+    unpack8_bf16(k.iu[j], iu);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v2[i] = __fadd_rn(iu[i], __fmul_rn(pol.s_img, __fsub_rn(v2[i], iu[i])));
+  }
+}
+
+// Pass 1: each segment's sums of c c and v2 v2; outside the window the segment is copied.
+// CTAs stride over the (request, segment) units.
+__global__ void __launch_bounds__(THREADS, 4) cfg_partials_kernel(const CfgArgs a, const int64_t units) {
+  __shared__ float wsum[2][THREADS / 32];
+  pdl_trigger();  // the scale pass may start and load its inputs
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int req = int(u / a.S), seg = int(u % a.S);
+    const CfgPolicy pol = load_policy(a.policy + 6 * req);
+    const int64_t base = int64_t(req) * a.N + int64_t(seg) * SEG;
+    const int nch = int(min(int64_t(SEG), a.N - int64_t(seg) * SEG) / 8);
+    if (!pol.guided()) {
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) {
+        const int q = int(threadIdx.x) + THREADS * j;
+        if (q < nch) {
+          float c[8];
+          unpack8_bf16(__ldg(reinterpret_cast<const uint4*>(a.c + base + 8 * q)), c);
+          store8_f32(a.out + base + 8 * q, c);
+        }
+      }
+      continue;  // uniform across the CTA
+    }
+    CfgChunks k;
+    cfg_load(a, base, nch, k);
+    float pc = 0.0f, pg = 0.0f;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      if (j < k.n) {
+        float c[8], v2[8];
+        cfg_guide(a, pol, k, j, c, v2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          pc = __fadd_rn(pc, __fmul_rn(c[i], c[i]));
+          pg = __fadd_rn(pg, __fmul_rn(v2[i], v2[i]));
+        }
+      }
+    }
+    const float sc = cta_sum(pc, wsum[0]);
+    const float sg = cta_sum(pg, wsum[1]);
+    if (threadIdx.x == 0) a.part[u] = make_float2(sc, sg);
+  }
+}
+
+// Pass 2, launched as a dependent of pass 1: a CTA loads its segment's inputs (written before
+// pass 1 started), waits for pass 1, folds the request's segment sums (the same order in every
+// CTA, so the same r) and writes out = v2 r.
+__global__ void __launch_bounds__(THREADS, 4) cfg_scale_kernel(const CfgArgs a, const int64_t units) {
+  __shared__ float r_s;
+  bool waited = false;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int req = int(u / a.S), seg = int(u % a.S);
+    const CfgPolicy pol = load_policy(a.policy + 6 * req);
+    if (!pol.guided()) continue;  // pass 1 copied c
+    const int64_t base = int64_t(req) * a.N + int64_t(seg) * SEG;
+    const int nch = int(min(int64_t(SEG), a.N - int64_t(seg) * SEG) / 8);
+    CfgChunks k;
+    cfg_load(a, base, nch, k);
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+    if (threadIdx.x == 0) {
+      const float2* p = a.part + int64_t(req) * a.S;
+      float2 acc = p[0];
+#pragma unroll 8
+      for (int s = 1; s < a.S; ++s) {
+        const float2 v = p[s];
+        acc.x = __fadd_rn(acc.x, v.x);
+        acc.y = __fadd_rn(acc.y, v.y);
+      }
+      const float r = acc.y == 0.0f ? 1.0f : __fdiv_rn(__fsqrt_rn(acc.x), __fsqrt_rn(acc.y));
+      r_s = fminf(fmaxf(r, pol.rmin), 1.0f);
+    }
+    __syncthreads();
+    const float r = r_s;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      if (j < k.n) {
+        const int q = int(threadIdx.x) + THREADS * j;
+        float c[8], v2[8];
+        cfg_guide(a, pol, k, j, c, v2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v2[i] = __fmul_rn(v2[i], r);
+        store8_f32(a.out + base + 8 * q, v2);
+      }
+    }
+    __syncthreads();  // r_s is rewritten for the next unit
+  }
+}
+
+struct SdeArgs {
+  const float* x;      // [n_req][N]
+  const float* v;
+  const float* z;      // or null: x_next is an input
+  float* x_next;
+  const float* times;  // [n_req][2]: t_i, t_next
+  int64_t N;
+  int S;
+  int n_req;
+  float* part;         // [n_req][S]: each segment's sum of d d
+  float* logp;         // [n_req]
+  uint32_t* err;
+};
+
+__device__ __forceinline__ bool times_ok(float t, float tn) {
+  return __fsub_rn(t, tn) > 0.0f && tn >= 0.0f && t <= 1.0f;
+}
+
+__global__ void __launch_bounds__(THREADS, 4) sde_step_kernel(const SdeArgs a, const int64_t units) {
+  __shared__ float wsum[THREADS / 32];
+  pdl_trigger();  // the logp fold may start
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int req = int(u / a.S), seg = int(u % a.S);
+    const float t = a.times[2 * req], tn = a.times[2 * req + 1];
+    if (!times_ok(t, tn)) {
+      if (threadIdx.x == 0 && seg == 0) atomicOr(a.err, MOT_DEV_BAD_TIME);
+      continue;  // uniform across the CTA
+    }
+    const float dt = __fsub_rn(t, tn);
+    const float sigma = t;
+    const float kk = __fdiv_rn(__fmul_rn(sigma, sigma), __fmul_rn(2.0f, t));
+    const float omt = __fsub_rn(1.0f, t);
+    const float sd = __fmul_rn(sigma, __fsqrt_rn(dt));
+    const int64_t base = int64_t(req) * a.N + int64_t(seg) * SEG;
+    const int nch = int(min(int64_t(SEG), a.N - int64_t(seg) * SEG) / 8);
+    const float* third = a.z ? a.z : a.x_next;
+    float p = 0.0f;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      const int q = int(threadIdx.x) + THREADS * j;
+      if (q < nch) {
+        float x[8], v[8], w[8], mu[8], xn[8];
+        unpack8_f32(load8_f32(a.x + base + 8 * q), x);
+        unpack8_f32(load8_f32(a.v + base + 8 * q), v);
+        unpack8_f32(load8_f32(third + base + 8 * q), w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float e = __fadd_rn(x[i], __fmul_rn(omt, v[i]));
+          mu[i] = __fsub_rn(x[i], __fmul_rn(dt, __fadd_rn(v[i], __fmul_rn(kk, e))));
+          xn[i] = a.z ? __fadd_rn(mu[i], __fmul_rn(sd, w[i])) : w[i];
+        }
+        if (a.z) store8_f32(a.x_next + base + 8 * q, xn);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float d = __fsub_rn(xn[i], mu[i]);
+          p = __fadd_rn(p, __fmul_rn(d, d));
+        }
+      }
+    }
+    const float ss = cta_sum(p, wsum);
+    if (threadIdx.x == 0) a.part[u] = ss;
+  }
+}
+
+// Launched as a dependent of the step: one thread per request folds the segment sums left to
+// right, then forms logp.
+__global__ void __launch_bounds__(128) sde_logp_kernel(const SdeArgs a) {
+  const int req = int(blockIdx.x) * 128 + int(threadIdx.x);
+  const bool live = req < a.n_req;
+  float t = 0.0f, tn = 0.0f;
+  if (live) {
+    t = a.times[2 * req];
+    tn = a.times[2 * req + 1];
+  }
+  pdl_wait();
+  if (!live || !times_ok(t, tn)) return;
+  const float sd = __fmul_rn(t, __fsqrt_rn(__fsub_rn(t, tn)));
+  const float* p = a.part + int64_t(req) * a.S;
+  float ss = p[0];
+#pragma unroll 8
+  for (int s = 1; s < a.S; ++s) ss = __fadd_rn(ss, p[s]);
+  const float aa = __fdiv_rn(ss, __fmul_rn(2.0f, __fmul_rn(sd, sd)));
+  const float lw = __fmul_rn(float(a.N), __fadd_rn(logf(sd), kLogSqrt2Pi));
+  a.logp[req] = __fsub_rn(-aa, lw);
+}
+
+}  // namespace flow
+}  // namespace mot
+
+using namespace mot;
+
+extern "C" size_t mot_flow_workspace_bytes(int n_req, int64_t N) {
+  if (n_req < 1 || n_req > flow::kMaxReq || N < 8 || N % 8 != 0 || N > flow::kMaxN) return 0;
+  return flow::workspace_bytes(n_req, N);
+}
+
+extern "C" int mot_flow_schedule_host(int n, double shift, float* host_t) {
+  if (host_t == nullptr) return MOT_ERR_NULL;
+  if (n < 2 || n > (1 << 20)) return MOT_ERR_GEOMETRY;
+  if (!(shift > 0.0) || !std::isfinite(shift)) return MOT_ERR_ARG;
+  for (int i = 0; i < n; ++i) {
+    const double u = 1.0 - double(i) / double(n - 1);
+    host_t[i] = float(shift * u / (1.0 + (shift - 1.0) * u));
+  }
+  return MOT_OK;
+}
+
+extern "C" int mot_cfg_combine_renorm(const mot_bf16* v_c, const mot_bf16* v_tu, const mot_bf16* v_iu, int n_req,
+                                      int64_t N, const float* policy, void* ws, size_t ws_bytes, float* out,
+                                      void* stream) {
+  if (!v_c || !v_tu || !policy || !ws || !out) return MOT_ERR_NULL;
+  if (n_req < 1 || n_req > flow::kMaxReq || N < 8 || N % 8 != 0 || N > flow::kMaxN) return MOT_ERR_GEOMETRY;
+  if (!aligned16(v_c) || !aligned16(v_tu) || (v_iu && !aligned16(v_iu)) || !aligned16(policy) || !aligned16(ws) ||
+      !aligned16(out))
+    return MOT_ERR_ALIGN;
+  if (ws_bytes < flow::workspace_bytes(n_req, N)) return MOT_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {v_c, v_tu, v_iu, policy, ws, out};
+  int dev = -1;
+  int st = check_device(s, ptrs, 6, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  const int S = flow::segments(N);
+  flow::CfgArgs a{v_c, v_tu, v_iu, policy, N, S,
+                  reinterpret_cast<float2*>(static_cast<char*>(ws) + sizeof(PlanHeader)), out};
+  const int64_t units = int64_t(n_req) * S;
+  const unsigned grid = unsigned(std::min<int64_t>(units, int64_t(flow::kCtasPerSm) * sm_count(dev)));
+  flow::cfg_partials_kernel<<<grid, flow::THREADS, 0, s>>>(a, units);
+  if (cudaGetLastError() != cudaSuccess) return MOT_ERR_CUDA;
+  if (launch_dependent(flow::cfg_scale_kernel, dim3(grid), dim3(flow::THREADS), 0, s, a, units) != cudaSuccess)
+    return MOT_ERR_CUDA;
+  return MOT_OK;
+}
+
+extern "C" int mot_flow_sde_step(const float* x, const float* v, const float* z, float* x_next, int n_req, int64_t N,
+                                 const float* times, void* ws, size_t ws_bytes, float* logp, void* stream) {
+  if (!x || !v || !x_next || !times || !ws || !logp) return MOT_ERR_NULL;
+  if (n_req < 1 || n_req > flow::kMaxReq || N < 8 || N % 8 != 0 || N > flow::kMaxN) return MOT_ERR_GEOMETRY;
+  if (!aligned16(x) || !aligned16(v) || (z && !aligned16(z)) || !aligned16(x_next) || !aligned16(times) ||
+      !aligned16(ws) || !aligned16(logp))
+    return MOT_ERR_ALIGN;
+  if (ws_bytes < flow::workspace_bytes(n_req, N)) return MOT_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {x, v, z, x_next, times, ws, logp};
+  int dev = -1;
+  int st = check_device(s, ptrs, 7, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  const int S = flow::segments(N);
+  flow::SdeArgs a{x, v, z, x_next, times, N, S, n_req,
+                  reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(PlanHeader)), logp,
+                  &static_cast<PlanHeader*>(ws)->error};
+  const int64_t units = int64_t(n_req) * S;
+  const unsigned grid = unsigned(std::min<int64_t>(units, int64_t(flow::kCtasPerSm) * sm_count(dev)));
+  flow::sde_step_kernel<<<grid, flow::THREADS, 0, s>>>(a, units);
+  if (cudaGetLastError() != cudaSuccess) return MOT_ERR_CUDA;
+  if (launch_dependent(flow::sde_logp_kernel, dim3((n_req + 127) / 128), dim3(128), 0, s, a) != cudaSuccess)
+    return MOT_ERR_CUDA;
+  return MOT_OK;
+}

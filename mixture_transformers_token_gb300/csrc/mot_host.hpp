@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <utility>
 
 #include "mot.h"
 
@@ -63,6 +64,25 @@ inline int check_arch(int dev) {
 }
 
 inline int sm_count(int dev) { return device_info(dev).sms.load(); }
+
+// Launches `kernel` so that it may start while the stream's preceding grid is still running
+// (programmatic dependent launch; the kernel must call pdl_wait before it reads that grid's
+// output).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Makes `dev` current for the lifetime of the guard and restores the previous device.
 struct DeviceGuard {

@@ -201,3 +201,31 @@ def cfg_pack_device_inputs(device, seed: int = 5) -> dict:
         "k_norm": bf16_normal_device(seed, 7, (2, s.D), device, mean=1.0, std=0.1),
         "w_o": bf16_normal_device(seed, 8, (2, h, h), device, std=0.02),
     }
+
+
+# Flow sampler. BAGEL's latents are VAE latents (8x downsampling, 16 channels) patchified 2 x 2,
+# so a 1024 x 1024 image is 64 x 64 latent tokens of 64 values: N = 262144 per request; a
+# 512 x 512 image has N = 65536. 50 steps with shift 3 and the window [0.4, 1] are the settings
+# under which the schedule gives the 41 guided steps of RFC #435 §2; the scales (text 4, image 2)
+# and renorm min 0 are stand-ins, since the pages fix no values for them.
+FLOW_N_1024 = 64 * 64 * 64
+FLOW_N_512 = 32 * 32 * 64
+FLOW_REQUESTS = 16
+FLOW_POLICY = {"s_text": 4.0, "s_img": 2.0, "t_lo": 0.4, "t_hi": 1.0, "renorm_min": 0.0}
+FLOW_STEPS, FLOW_SHIFT = 50, 3.0
+
+
+def flow_branches(rng: np.random.Generator, n_req: int, N: int, spread: float = 0.5) -> dict:
+    """Three CFG branches [n_req][N] bf16: the conditioned velocity c ~ N(0, 1) and the text- and
+    image-unconditioned ones, c plus N(0, spread^2) draws (the branches of one request are the
+    same model's outputs on the same latent, so they are correlated)."""
+    c = rng.standard_normal(size=(n_req, N), dtype=np.float32)
+    tu = c + np.float32(spread) * rng.standard_normal(size=(n_req, N), dtype=np.float32)
+    iu = c + np.float32(spread) * rng.standard_normal(size=(n_req, N), dtype=np.float32)
+    return {k: torch.from_numpy(v).to(torch.bfloat16) for k, v in (("c", c), ("tu", tu), ("iu", iu))}
+
+
+def flow_state(rng: np.random.Generator, n_req: int, N: int) -> dict:
+    """SDE step inputs [n_req][N] fp32: the latent x ~ N(0, 1), a velocity v ~ N(0, 1) and the
+    step's standard normal noise z."""
+    return {k: torch.from_numpy(rng.standard_normal(size=(n_req, N), dtype=np.float32)) for k in ("x", "v", "z")}

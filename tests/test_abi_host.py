@@ -280,3 +280,51 @@ def test_rope_table_rejects(lib):
     assert lib.mot_rope_table_fill_host_fp32(1e6, 3, 2, fbuf) == MOT_ERR_GEOMETRY
     assert lib.mot_rope_table_fill_host_fp32(float("nan"), 4, 2, fbuf) == MOT_ERR_ARG
     assert lib.mot_rope_table_fill_host_fp32(1e6, 4, 2, None) == MOT_ERR_NULL
+
+
+def test_flow_workspace_bytes(lib):
+    f = lib.mot_flow_workspace_bytes
+    assert f(0, 64) == 0 and f(1, 12) == 0 and f(1, 0) == 0 and f(65536, 64) == 0
+    assert f(1, (1 << 24) + 8) == 0
+    # header + 8 bytes per request and 8192-element segment, rounded to 16
+    assert f(1, 8) == 64 + 16
+    assert f(3, 8192) == 64 + 32
+    assert f(3, 8200) == 64 + 48
+    assert f(16, 262144) == 64 + 16 * 32 * 8
+
+
+def test_flow_schedule_matches_oracle():
+    for n, shift in ((50, 1.0), (50, 3.0), (2, 0.5), (1000, 7.25)):
+        got = mot.mot_flow_schedule_host(n, shift).numpy()
+        np.testing.assert_array_equal(got, O.flow_schedule(n, shift))
+
+
+def test_flow_schedule_rejects(lib):
+    buf = (ctypes.c_float * 8)()
+    assert lib.mot_flow_schedule_host(1, 3.0, buf) == MOT_ERR_GEOMETRY
+    assert lib.mot_flow_schedule_host(4, 0.0, buf) == MOT_ERR_ARG
+    assert lib.mot_flow_schedule_host(4, float("inf"), buf) == MOT_ERR_ARG
+    assert lib.mot_flow_schedule_host(4, 3.0, None) == MOT_ERR_NULL
+
+
+def test_cfg_combine_rejects(lib):
+    f = lib.mot_cfg_combine_renorm
+    assert f(None, A, A, 2, 64, A, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert f(A, None, A, 2, 64, A, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert f(A, A, A, 2, 64, None, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert f(A, A, A, 0, 64, A, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, 2, 60, A, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, 2, (1 << 24) + 8, A, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, MIS, 2, 64, A, B, 1 << 20, C, None) == MOT_ERR_ALIGN
+    assert f(A, A, None, 2, 64, A, B, 64, C, None) == MOT_ERR_WORKSPACE
+
+
+def test_flow_sde_step_rejects(lib):
+    f = lib.mot_flow_sde_step
+    assert f(None, A, A, C, 2, 64, A, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert f(A, A, A, None, 2, 64, A, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert f(A, A, A, C, 2, 64, A, B, 1 << 20, None, None) == MOT_ERR_NULL
+    assert f(A, A, A, C, 65536, 64, A, B, 1 << 30, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, A, C, 2, 4, A, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, A, MIS, C, 2, 64, A, B, 1 << 20, C, None) == MOT_ERR_ALIGN
+    assert f(A, A, None, C, 2, 64, A, B, 64, C, None) == MOT_ERR_WORKSPACE
