@@ -385,6 +385,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
+  // Launched as a programmatic dependent: the grid may be resident before the preceding kernel
+  // (typically the norm that writes A and the plan) has finished. Nothing in global memory is
+  // touched before pdl_wait; the tensor maps are kernel parameters.
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_a_rows);
+    tma_prefetch_desc(&tm_w);
+  }
+  pdl_wait();
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(args.ws);
   const int num_m = hdr->num_m_tiles;
   const int nt0 = (hdr->count[0] + kTileRows - 1) / kTileRows;
@@ -412,9 +422,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0u;
     fence_mbar_init();
-    tma_prefetch_desc(&tm_a);
-    tma_prefetch_desc(&tm_a_rows);
-    tma_prefetch_desc(&tm_w);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
@@ -863,8 +870,12 @@ static int launch(const void* a, const void* w, int T, int N, int K, const Args&
   const int64_t work_max = pairs_max * int64_t(N / BN);
   const int64_t cap = max_active_pairs<EPI, B_MN>(dev);
   const int64_t clusters = work_max < cap ? work_max : cap;
-  routed_gemm_kernel<EPI, B_MN><<<unsigned(2 * clusters), THREADS, SMEM_BYTES, s>>>(tm_a, tm_rows, tm_w, args);
-  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+  if (launch_dependent(routed_gemm_kernel<EPI, B_MN>, dim3(unsigned(2 * clusters)), dim3(THREADS), SMEM_BYTES, s,
+                       tm_a, tm_rows, tm_w, args) != cudaSuccess) {
+    cudaGetLastError();
+    return MOT_ERR_CUDA;
+  }
+  return MOT_OK;
 }
 
 }  // namespace gemm

@@ -137,6 +137,7 @@ struct NormArgs {
 
 template <int NJ>
 __global__ void __launch_bounds__(32 * (1 + kNormMaxConsumers), 1) add_rmsnorm_kernel(const NormArgs a) {
+  pdl_trigger();  // a dependent GEMM may be scheduled now; it waits for this grid before any read
   const int plan_ctas = a.plan_ws != nullptr ? 1 : 0;
   if (int(blockIdx.x) < plan_ctas) {
     route_plan_block(a.mod, a.T, a.plan_ws);
