@@ -46,6 +46,8 @@ constexpr float kLogSqrt2Pi = 0.918938533204672742f;  // log(2 pi) / 2
 
 __host__ __device__ constexpr int segments(int64_t N) { return int((N + SEG - 1) / SEG); }
 
+// Workspace: the 64-byte header (error word), then 8 bytes per (request, segment): the CFG's
+// (sum c c, sum v2 v2), or the SDE step's sum d d.
 inline size_t workspace_bytes(int n_req, int64_t N) {
   return sizeof(PlanHeader) + ((size_t(n_req) * size_t(segments(N)) * 8 + 15) & ~size_t(15));
 }
@@ -63,6 +65,49 @@ __device__ __forceinline__ float cta_sum(float p, float* wsum) {
 #pragma unroll
   for (int k = 1; k < THREADS / 32; ++k) acc = __fadd_rn(acc, wsum[k]);
   return acc;
+}
+
+// Left fold of a request's n segment sums p[0..n): ((p0 + p1) + p2) + ... The lanes of the calling
+// warp fetch 32 sums at a time in parallel and the fold takes them in order through shuffles, so
+// the chain waits on one L2 round trip per 32 sums instead of one per sum. Every lane returns it.
+__device__ __forceinline__ float warp_fold(const float* p, int n) {
+  const int lane = threadIdx.x & 31;
+  float acc = 0.0f;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const float v = i0 + lane < n ? __ldcg(p + i0 + lane) : 0.0f;
+    const int m = n - i0 < 32 ? n - i0 : 32;
+    for (int l = 0; l < m; ++l) {
+      const float w = __shfl_sync(0xffffffffu, v, l);
+      acc = (i0 + l == 0) ? w : __fadd_rn(acc, w);
+    }
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float2 warp_fold2(const float2* p, int n) {
+  const int lane = threadIdx.x & 31;
+  float2 acc = make_float2(0.0f, 0.0f);
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const float2 v = i0 + lane < n ? __ldcg(p + i0 + lane) : make_float2(0.0f, 0.0f);
+    const int m = n - i0 < 32 ? n - i0 : 32;
+    for (int l = 0; l < m; ++l) {
+      const float wx = __shfl_sync(0xffffffffu, v.x, l), wy = __shfl_sync(0xffffffffu, v.y, l);
+      if (i0 + l == 0) {
+        acc = make_float2(wx, wy);
+      } else {
+        acc.x = __fadd_rn(acc.x, wx);
+        acc.y = __fadd_rn(acc.y, wy);
+      }
+    }
+  }
+  return acc;
+}
+
+// The CFG's ratio from the request's folded sums: sqrt(ss_c) / sqrt(ss_g) (1 when ss_g is 0),
+// clamped to [renorm_min, 1].
+__device__ __forceinline__ float cfg_ratio(float2 acc, float rmin) {
+  const float r = acc.y == 0.0f ? 1.0f : __fdiv_rn(__fsqrt_rn(acc.x), __fsqrt_rn(acc.y));
+  return fminf(fmaxf(r, rmin), 1.0f);
 }
 
 __device__ __forceinline__ void unpack8_bf16(const uint4 u, float (&v)[8]) {
@@ -209,17 +254,9 @@ __global__ void __launch_bounds__(THREADS, 4) cfg_scale_kernel(const CfgArgs a, 
       pdl_wait();
       waited = true;
     }
-    if (threadIdx.x == 0) {
-      const float2* p = a.part + int64_t(req) * a.S;
-      float2 acc = p[0];
-#pragma unroll 8
-      for (int s = 1; s < a.S; ++s) {
-        const float2 v = p[s];
-        acc.x = __fadd_rn(acc.x, v.x);
-        acc.y = __fadd_rn(acc.y, v.y);
-      }
-      const float r = acc.y == 0.0f ? 1.0f : __fdiv_rn(__fsqrt_rn(acc.x), __fsqrt_rn(acc.y));
-      r_s = fminf(fmaxf(r, pol.rmin), 1.0f);
+    if (threadIdx.x < 32) {
+      const float r = cfg_ratio(warp_fold2(a.part + int64_t(req) * a.S, a.S), pol.rmin);
+      if (threadIdx.x == 0) r_s = r;
     }
     __syncthreads();
     const float r = r_s;
@@ -302,10 +339,18 @@ __global__ void __launch_bounds__(THREADS, 4) sde_step_kernel(const SdeArgs a, c
   }
 }
 
-// Launched as a dependent of the step: one thread per request folds the segment sums left to
+// logp = -(ss / (2 (std std))) - N (log(std) + log sqrt(2 pi)) with std = t sqrt(t - t_next).
+__device__ __forceinline__ float sde_logp(float ss, float t, float tn, int64_t N) {
+  const float sd = __fmul_rn(t, __fsqrt_rn(__fsub_rn(t, tn)));
+  const float aa = __fdiv_rn(ss, __fmul_rn(2.0f, __fmul_rn(sd, sd)));
+  const float lw = __fmul_rn(float(N), __fadd_rn(logf(sd), kLogSqrt2Pi));
+  return __fsub_rn(-aa, lw);
+}
+
+// Launched as a dependent of the step: one warp per request folds the segment sums left to
 // right, then forms logp.
 __global__ void __launch_bounds__(128) sde_logp_kernel(const SdeArgs a) {
-  const int req = int(blockIdx.x) * 128 + int(threadIdx.x);
+  const int req = int(blockIdx.x) * 4 + int(threadIdx.x >> 5);
   const bool live = req < a.n_req;
   float t = 0.0f, tn = 0.0f;
   if (live) {
@@ -313,15 +358,9 @@ __global__ void __launch_bounds__(128) sde_logp_kernel(const SdeArgs a) {
     tn = a.times[2 * req + 1];
   }
   pdl_wait();
-  if (!live || !times_ok(t, tn)) return;
-  const float sd = __fmul_rn(t, __fsqrt_rn(__fsub_rn(t, tn)));
-  const float* p = a.part + int64_t(req) * a.S;
-  float ss = p[0];
-#pragma unroll 8
-  for (int s = 1; s < a.S; ++s) ss = __fadd_rn(ss, p[s]);
-  const float aa = __fdiv_rn(ss, __fmul_rn(2.0f, __fmul_rn(sd, sd)));
-  const float lw = __fmul_rn(float(a.N), __fadd_rn(logf(sd), kLogSqrt2Pi));
-  a.logp[req] = __fsub_rn(-aa, lw);
+  if (!live || !times_ok(t, tn)) return;  // uniform across the warp
+  const float ss = warp_fold(a.part + int64_t(req) * a.S, a.S);
+  if ((threadIdx.x & 31) == 0) a.logp[req] = sde_logp(ss, t, tn, a.N);
 }
 
 }  // namespace flow
@@ -394,7 +433,7 @@ extern "C" int mot_flow_sde_step(const float* x, const float* v, const float* z,
   const unsigned grid = unsigned(std::min<int64_t>(units, int64_t(flow::kCtasPerSm) * sm_count(dev)));
   flow::sde_step_kernel<<<grid, flow::THREADS, 0, s>>>(a, units);
   if (cudaGetLastError() != cudaSuccess) return MOT_ERR_CUDA;
-  if (launch_dependent(flow::sde_logp_kernel, dim3((n_req + 127) / 128), dim3(128), 0, s, a) != cudaSuccess)
+  if (launch_dependent(flow::sde_logp_kernel, dim3((n_req + 3) / 4), dim3(128), 0, s, a) != cudaSuccess)
     return MOT_ERR_CUDA;
   return MOT_OK;
 }
