@@ -22,11 +22,11 @@
 // (the causal tiles near the end carry the most keys). Warp 0 loads both Q tiles once and
 // 64-key K and V blocks into three-stage rings (TMA, 128-byte swizzle); warp 1 issues, per key
 // block, S = Q K^T for both tiles into their double-buffered TMEM S, then O += P V of the
-// previous block for both (V read as an MN-major operand); warps 2-5 and 6-9 are the softmax
-// warpgroups of the two tiles, one query row per thread: they read a block's S from TMEM once
-// (64 columns), form p, rescale O in TMEM when the row maximum moves, and write P (bf16,
-// swizzled K-major) into one of two shared-memory buffers. Each tile's softmax runs while the tensor cores work on
-// the other tile and on its own next block.
+// previous block for both (P read from tensor memory, V as an MN-major operand from shared
+// memory); warps 2-5 and 6-9 are the softmax warpgroups of the two tiles, one query row per
+// thread: they read a block's S from TMEM once (64 columns), form p, rescale O in TMEM when the
+// row maximum moves, and write P as bf16 pairs into one of two TMEM buffers. Each tile's softmax
+// runs while the tensor cores work on the other tile and on its own next block.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -42,7 +42,7 @@ constexpr int BQ = 128, BKV = 64;
 constexpr int TILES = 2;        // query tiles per CTA (ping-pong between two softmax warpgroups)
 constexpr int THREADS = 320;    // producer, MMA, 2 x 4 softmax warps
 constexpr int KV_STAGES = 3;
-constexpr uint32_t SUB = 128 * 64 * 2;   // a [128 rows x 64 columns] bf16 swizzled tile (Q half, P)
+constexpr uint32_t SUB = 128 * 64 * 2;   // a [128 rows x 64 columns] bf16 swizzled tile (Q half)
 constexpr uint32_t KSUB = 64 * 64 * 2;   // a [64 keys x 64 columns] bf16 swizzled tile (K, V half)
 
 template <int D>
@@ -52,11 +52,11 @@ struct Layout {
   static constexpr uint32_t Q = 0;                          // TILES Q tiles
   static constexpr uint32_t K = Q + TILES * QTILE;          // KV_STAGES K blocks
   static constexpr uint32_t V = K + KV_STAGES * KVBLK;      // KV_STAGES V blocks
-  static constexpr uint32_t P = V + KV_STAGES * KVBLK;      // TILES x 2 buffers x [128 rows x 64 keys] bf16
-  static constexpr uint32_t BAR = P + 2 * TILES * SUB;
+  static constexpr uint32_t BAR = V + KV_STAGES * KVBLK;
   static constexpr size_t BYTES = 1024 + size_t(BAR) + 512;  // barriers, tensor-memory slot, work item
-  // tensor memory: S of tile t, buffer b at 128 t + 64 b; O of tile t at 256 + 128 t
-  static constexpr uint32_t TMEM_S = 0, TMEM_O = 256, TMEM_COLS = 512;
+  // tensor memory: S of tile t at 64 t; P of tile t, buffer b (bf16 pairs) at 128 + 64 t + 32 b;
+  // O of tile t at 256 + 128 t
+  static constexpr uint32_t TMEM_S = 0, TMEM_P = 128, TMEM_O = 256, TMEM_COLS = 512;
 };
 
 struct Args {
@@ -172,8 +172,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* k_empty = bars + 4;   // [KV_STAGES]: both tiles' S MMAs have read the block
   uint64_t* v_full = bars + 7;    // [KV_STAGES]
   uint64_t* v_empty = bars + 10;  // [KV_STAGES]: both tiles' P V MMAs have read the block
-  uint64_t* s_full = bars + 13;   // [TILES][2]
-  uint64_t* s_free = bars + 17;   // [TILES][2]: the tile's softmax warps have read the buffer
+  uint64_t* s_full = bars + 13;   // [TILES]
+  uint64_t* s_free = bars + 17;   // [TILES]: the tile's softmax warps have read S
   uint64_t* p_full = bars + 21;   // [TILES]
   uint64_t* o_full = bars + 23;   // [TILES][2]: the tile's P V from P buffer b is done (and every earlier one)
   uint64_t* drain = bars + 27;
@@ -212,10 +212,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&v_empty[i]), 1);
     }
     for (int t = 0; t < TILES; ++t) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(smem_u32(&s_full[2 * t + b]), 1);
-        mbar_init(smem_u32(&s_free[2 * t + b]), 4);
-      }
+      mbar_init(smem_u32(&s_full[t]), 1);
+      mbar_init(smem_u32(&s_free[t]), 4);
       mbar_init(smem_u32(&p_full[t]), 4);
       mbar_init(smem_u32(&o_full[2 * t]), 1);
       mbar_init(smem_u32(&o_full[2 * t + 1]), 1);
@@ -279,21 +277,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(q_full), 0, abort_flag, a.err));
     for (int j = 0; j <= nblk && ok; ++j) {
       if (j < nblk) {
-        const int st = j % KV_STAGES, sb = j & 1;
+        const int st = j % KV_STAGES;
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&k_full[st]), uint32_t(j / KV_STAGES) & 1u, abort_flag,
                                                a.err));
         for (int t = 0; t < TILES && ok; ++t) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_free[2 * t + sb]), (uint32_t(j >> 1) & 1u) ^ 1u,
-                                                 abort_flag, a.err));
-          if (!ok) break;
+          if (j >= 1) {  // the softmax warps have read S of block j - 1
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_free[t]), uint32_t(j - 1) & 1u, abort_flag, a.err));
+            if (!ok) break;
+          }
           tc_fence_after();
           if (lane == 0) {
             const uint32_t qa = smem_u32(smem + L::Q + t * L::QTILE), kb = smem_u32(smem + L::K + st * L::KVBLK);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_bf16(tmem + L::TMEM_S + t * 128 + sb * BKV, smem_desc_sw128(qa + (kk / 4) * SUB + (kk % 4) * 32),
+              mma_bf16(tmem + L::TMEM_S + t * BKV, smem_desc_sw128(qa + (kk / 4) * SUB + (kk % 4) * 32),
                        smem_desc_sw128(kb + (kk / 4) * KSUB + (kk % 4) * 32), idesc_s, kk > 0);
-            mma_commit(smem_u32(&s_full[2 * t + sb]));
+            mma_commit(smem_u32(&s_full[t]));
             if (t == TILES - 1) mma_commit(smem_u32(&k_empty[st]));
           }
           __syncwarp();
@@ -309,12 +308,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t pa = smem_u32(smem + L::P + (2 * t + (jj & 1)) * SUB);
+            const uint32_t pa = tmem + L::TMEM_P + t * 64 + (jj & 1) * 32;  // P in tensor memory
             const uint32_t vb = smem_u32(smem + L::V + st * L::KVBLK);
 #pragma unroll
             for (int kk = 0; kk < BKV / 16; ++kk)
-              mma_bf16(tmem + L::TMEM_O + t * 128, smem_desc_sw128(pa + kk * 32),
-                       smem_desc_mn_sw128(vb + kk * 2048, KSUB), idesc_o, (jj | kk) != 0);
+              mma_bf16_ts(tmem + L::TMEM_O + t * 128, pa + kk * 8, smem_desc_mn_sw128(vb + kk * 2048, KSUB), idesc_o,
+                          (jj | kk) != 0);
             mma_commit(smem_u32(&o_full[2 * t + (jj & 1)]));
             if (t == TILES - 1) mma_commit(smem_u32(&v_empty[st]));
           }
@@ -336,20 +335,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int lim = (valid && i < nc) ? nk - nq + i + 1 : nk;   // keys [0, lim) are visible
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const uint32_t to = tmem + lane_off + L::TMEM_O + t * 128;
-    uint8_t* prow = smem + L::P + 2 * t * SUB + row * 128;  // the row of the tile's P buffer 0
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[2 * t + sb]), uint32_t(j >> 1) & 1u, abort_flag,
-                                             a.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t]), uint32_t(j) & 1u, abort_flag, a.err));
       if (!ok) break;
       tc_fence_after();
       float x[BKV];
-      tmem_ld64(tmem + lane_off + L::TMEM_S + t * 128 + sb * BKV, x);
+      tmem_ld64(tmem + lane_off + L::TMEM_S + t * BKV, x);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_free[2 * t + sb]));  // the S buffer is free again
+      if (lane == 0) mbar_arrive(smem_u32(&s_free[t]));  // S may be overwritten by the next block
       if (__any_sync(0xffffffffu, j * BKV + BKV > lim)) {  // the block reaches past a row's keys
         const int lim_b = lim - j * BKV;
 #pragma unroll
@@ -403,14 +399,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st32(to + c * 32, o);
         }
       }
-      // P as bf16 into the swizzled K-major buffer j & 1: keys 8 cc .. 8 cc + 7 go to the
-      // 16-byte chunk cc ^ (row & 7) of the row
-      uint8_t* pb = prow + (j & 1) * SUB;
+      // P as bf16 pairs into the row's lane of tensor-memory buffer j & 1 (keys 2c, 2c + 1 in
+      // column c), where the P V MMA reads it as its A operand
+      {
+        float pf[BKV / 2];
 #pragma unroll
-      for (int cc = 0; cc < BKV / 8; ++cc)
-        *reinterpret_cast<uint4*>(pb + ((cc ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      fence_proxy_async_smem();
+        for (int c = 0; c < BKV / 2; ++c) pf[c] = __uint_as_float(pk[c]);
+        tmem_st32(tmem + lane_off + L::TMEM_P + t * 64 + (j & 1) * 32, pf);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));

@@ -316,6 +316,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// As mma_bf16 with the A operand read from tensor memory: a_tmem holds the M x K bf16 tile with
+// row m in lane m and K elements packed two per 32-bit column (the lower K index in the low half).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 2-SM MMA issued by the leader CTA: A rows 0..127 from this CTA's shared memory and rows
 // 128..255 from the peer's (same offset), B split by N halves the same way; D lands in both
 // CTAs' tensor memory at d_tmem.
