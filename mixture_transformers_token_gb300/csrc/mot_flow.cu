@@ -13,7 +13,8 @@
 // std = sigma sqrt(dt); CFG v1 = tu + s_text (c - tu), v2 = iu + s_img (v1 - iu), rescaled by
 // clamp(||c|| / ||v2||, min, 1) over the request's elements.
 //
-// A request's elements are cut into segments of 8192; one CTA of 256 threads takes one segment.
+// A request's elements are cut into segments of 8192; a CTA of 256 threads takes one segment at
+// a time (the CTAs stride over all requests' segments).
 // The segment's elements are taken in chunks of 8; thread tau owns the segment's chunks q with
 // q % 256 == tau (so a warp's loads are consecutive 16- or 32-byte pieces); a segment sum runs
 // sequentially per thread over its chunks in ascending order, then as an xor butterfly (16, 8,
@@ -53,7 +54,7 @@ inline size_t workspace_bytes(int n_req, int64_t N) {
 }
 
 // The CTA's sum of the per-thread partials p: butterfly inside each warp, then the warps left
-// to right. Returned in thread 0.
+// to right. Every thread returns it.
 __device__ __forceinline__ float cta_sum(float p, float* wsum) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
