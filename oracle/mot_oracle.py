@@ -803,3 +803,71 @@ def e_flow_sde_step(x, v, z, t_i, t_next, x_next=None):
     a = ss / (F32(2.0) * (std * std))
     logp = -a - F32(x32.size) * (np.log(std) + F32(LOG_SQRT_2PI))
     return {"x_next": x_next, "mu": mu, "std": std, "logp": F32(logp)}
+
+
+# ---------------------------------------------------------------------------
+# Per-sample transition noise: a counter-based generator (Philox4x64-10) and Box-Muller
+# ---------------------------------------------------------------------------
+#
+# [RFC-435] §3 BAGEL-specific rules: initial and transition noise come from an explicit
+# per-sample generator with a fixed device, dtype and consumption order. Reading: the noise of
+# request r at step k is a pure function of (seed_r, k, element index), so it does not depend on
+# the batch, the device count or the order of the calls. The generator is Philox4x64-10 as
+# published by Salmon, Moraes, Dror and Shaw ("Parallel random numbers: as easy as 1, 2, 3",
+# SC 2011): ten rounds of two 64 x 64 -> 128-bit products with the round keys bumped by the
+# Weyl constants; the normal deviates come from the Box-Muller transform.
+
+PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)   # round multipliers
+PHILOX_W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)   # key increments (golden ratio, sqrt(3) - 1)
+NOISE_DOMAIN = 0x4D6F54466C6F77                       # second key word: "MoTFlow" in ASCII
+_M64 = (1 << 64) - 1
+
+
+def philox4x64_10(ctr, key):
+    """One Philox4x64 block with 10 rounds: counter (x0, x1, x2, x3) and key (k0, k1) are
+    64-bit integers. Each round multiplies x0 and x2 by the two multipliers into 128-bit
+    products and forms (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1, lo(M0 x0)); the key
+    words then grow by the two Weyl constants (mod 2^64)."""
+    x0, x1, x2, x3 = (int(v) & _M64 for v in ctr)
+    k0, k1 = (int(v) & _M64 for v in key)
+    for _ in range(10):
+        p0 = PHILOX_M[0] * x0
+        p1 = PHILOX_M[1] * x2
+        x0, x1, x2, x3 = (p1 >> 64) ^ x1 ^ k0, p1 & _M64, (p0 >> 64) ^ x3 ^ k1, p0 & _M64
+        k0 = (k0 + PHILOX_W[0]) & _M64
+        k1 = (k1 + PHILOX_W[1]) & _M64
+    return (x0, x1, x2, x3)
+
+
+def noise_uniform(x):
+    """The top 23 bits of a 64-bit word as a uniform in (0, 1): ((x >> 41) + 0.5) 2^-23, exact
+    in fp32 (at most 24 significant bits) and never 0 or 1."""
+    return F32(((int(x) >> 41) + 0.5) * 2.0 ** -23)
+
+
+def flow_noise_uniforms(seed, step, N):
+    """The N uniforms of one request at one step, fp32: element 4b + m takes word m of
+    philox4x64_10(counter = (b, step, 0, 0), key = (seed, NOISE_DOMAIN))."""
+    if N % 4:
+        raise ValueError("N must be a multiple of 4")
+    u = np.empty(N, F32)
+    for b in range(N // 4):
+        words = philox4x64_10((b, step, 0, 0), (seed, NOISE_DOMAIN))
+        for m in range(4):
+            u[4 * b + m] = noise_uniform(words[m])
+    return u
+
+
+def g_flow_noise(seeds, step, N):
+    """Standard normal transition noise z [n_req][N], fp64: Box-Muller on the uniforms of each
+    request, pairs (u_{2p}, u_{2p+1}) giving z_{2p} = sqrt(-2 ln u_{2p}) cos(2 pi u_{2p+1}) and
+    z_{2p+1} = sqrt(-2 ln u_{2p}) sin(2 pi u_{2p+1})."""
+    out = np.empty((len(seeds), N), np.float64)
+    for r, seed in enumerate(seeds):
+        u = flow_noise_uniforms(int(seed), int(step), N).astype(np.float64)
+        rad = np.sqrt(-2.0 * np.log(u[0::2]))
+        ang = 2.0 * np.pi * u[1::2]
+        out[r, 0::2] = rad * np.cos(ang)
+        out[r, 1::2] = rad * np.sin(ang)
+    return out
+

@@ -875,3 +875,47 @@ def test_sde_logp_of_a_given_latent():
     assert abs(g["logp"] - np.sum(norm.logpdf(y, loc=g["mu"], scale=g["std"]))) < 1e-7
     e = O.e_flow_sde_step(x, v, None, t, tn, x_next=y)
     assert abs(e["logp"] - g["logp"]) < 1e-4 * abs(g["logp"])
+
+
+def test_philox_matches_numpy_bit_generator():
+    # numpy's Philox bit generator is Philox4x64-10; it advances the counter before each block
+    for ctr, key in (((0, 0, 0, 0), (0, 0)), ((5, 7, 0, 3), (11, 13)),
+                     ((2 ** 64 - 1, 2 ** 64 - 1, 2 ** 64 - 1, 2 ** 64 - 2), (2 ** 64 - 1, 2 ** 63)),
+                     ((123456789, 42, 0, 0), (987654321, O.NOISE_DOMAIN))):
+        bg = np.random.Philox(counter=list(ctr), key=list(key))
+        got = [int(v) for v in bg.random_raw(4)]
+        c = list(ctr)
+        c[0] = (c[0] + 1) % 2 ** 64
+        if c[0] == 0:
+            c[1] = (c[1] + 1) % 2 ** 64
+            if c[1] == 0:
+                c[2] = (c[2] + 1) % 2 ** 64
+                if c[2] == 0:
+                    c[3] = (c[3] + 1) % 2 ** 64
+        assert list(O.philox4x64_10(c, key)) == got
+
+
+def test_noise_uniform_mapping_and_box_muller():
+    # the mapping's ends and exactness
+    assert O.noise_uniform(0) == F32(0.5 * 2.0 ** -23)
+    assert O.noise_uniform(2 ** 64 - 1) == F32(1.0 - 2.0 ** -24)
+    assert O.noise_uniform(1 << 41) == F32(1.5 * 2.0 ** -23)
+    # Box-Muller identities: the pair's squared radius is -2 ln u_even and its angle 2 pi u_odd
+    N = 64
+    u = O.flow_noise_uniforms(7, 3, N).astype(np.float64)
+    z = O.g_flow_noise([7], 3, N)[0]
+    np.testing.assert_allclose(z[0::2] ** 2 + z[1::2] ** 2, -2.0 * np.log(u[0::2]), rtol=1e-12)
+    ang = np.mod(np.arctan2(z[1::2], z[0::2]), 2 * np.pi)
+    np.testing.assert_allclose(ang, 2 * np.pi * u[1::2], rtol=1e-9, atol=1e-12)
+    # a different seed, step or element block gives different deviates
+    assert not np.array_equal(O.g_flow_noise([8], 3, N)[0], z)
+    assert not np.array_equal(O.g_flow_noise([7], 4, N)[0], z)
+
+
+def test_noise_is_standard_normal():
+    pytest.importorskip("scipy")
+    from scipy import stats
+    z = O.g_flow_noise([2024, 7], 11, 8192).reshape(-1)
+    assert abs(z.mean()) < 0.03 and abs(z.var() - 1.0) < 0.04
+    assert stats.kstest(z, "norm").pvalue > 1e-3
+
