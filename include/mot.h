@@ -435,6 +435,23 @@ int mot_flow_sde_step(const float* x, const float* v, const float* z, float* x_n
                       const float* times, void* ws, size_t ws_bytes, float* logp, void* stream);
 
 /*
+ * mot_flow_noise -- the per-sample standard normal noise of one sampler step ([RFC-435] §3
+ * BAGEL-specific rules: initial and transition noise from an explicit per-sample generator with
+ * a fixed device, dtype and consumption order).
+ *   seeds   device uint64 [n_req]   one seed per request (sample).
+ *   step    the step index k (any value; each step draws its own stream).
+ *   z       [n_req][N] fp32         out: element 4b + m of request r is word m of the
+ *           Philox4x64-10 block (Salmon et al., SC 2011) with counter (b, k, 0, 0) and key
+ *           (seeds[r], 0x4D6F54466C6F77), mapped to u = ((x >> 41) + 0.5) 2^-23 (exact fp32 in
+ *           (0, 1)); pairs (u_2p, u_2p+1) give z_2p = sqrt(-2 logf(u_2p)) cos(2 pi u_2p+1) and
+ *           z_2p+1 = the same radius times sin(2 pi u_2p+1) (sincospif), fp32.
+ * A request's noise depends only on its seed, the step and the element index, never on the
+ * batch. Geometry: 1 <= n_req <= 65535, N a multiple of 8, 8 <= N <= 2^24; seeds and z 16-byte
+ * aligned device memory of the stream's device.
+ */
+int mot_flow_noise(const uint64_t* seeds, uint64_t step, int n_req, int64_t N, float* z, void* stream);
+
+/*
  * mot_selftest_wait_timeout -- exercises the bounded wait that every pipeline wait of the
  * library uses ([RFC-435] §3: fail closed instead of hanging). One thread waits on an mbarrier
  * that nothing signals; after about one second the wait gives up, MOT_DEV_TIMEOUT is OR-ed into

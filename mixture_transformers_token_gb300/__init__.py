@@ -28,7 +28,7 @@ __all__ = [
     "mot_rmsnorm_dweight", "mot_routed_gemm_dx", "mot_routed_gemm_dw", "mot_joint_attention", "DEV_BAD_SEQUENCE",
     "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows", "mot_selftest_wait_timeout",
     "DEV_BAD_TIME", "mot_flow_workspace_bytes", "mot_flow_schedule_host", "mot_cfg_combine_renorm",
-    "mot_flow_sde_step",
+    "mot_flow_sde_step", "mot_flow_noise",
 ]
 
 ABI_VERSION = 1
@@ -80,6 +80,7 @@ _SIGNATURES = {
     "mot_flow_schedule_host": (_c_i, [_c_i, ctypes.c_double, _c_p]),
     "mot_cfg_combine_renorm": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_i64, _c_p, _c_p, _c_sz, _c_p, _c_p]),
     "mot_flow_sde_step": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_i, _c_i64, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_flow_noise": (_c_i, [_c_p, ctypes.c_uint64, _c_i, _c_i64, _c_p, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
 }
 
@@ -519,6 +520,21 @@ def mot_flow_sde_step(x, v, z, times, ws=None, x_next=None, logp=None, stream=No
         x.data_ptr(), v.data_ptr(), zp, x_next.data_ptr(), n_req, N, times.data_ptr(), ws.data_ptr(), ws.numel(),
         logp.data_ptr(), _stream(x, stream)))
     return x_next, logp
+
+
+def mot_flow_noise(seeds, step: int, N: int, z=None, stream=None):
+    """Per-sample standard normal noise [n_req][N] fp32 of sampler step `step`: `seeds` is a
+    device int64 tensor [n_req] (reinterpreted as uint64), one seed per request."""
+    _dev(seeds, "seeds", torch.int64, 1)
+    n_req = seeds.shape[0]
+    if z is None:
+        z = torch.empty((n_req, N), dtype=torch.float32, device=seeds.device)
+    _dev(z, "z", torch.float32, 2)
+    if tuple(z.shape) != (n_req, N):
+        raise ValueError(f"z must be [{n_req}, {N}]")
+    _check("mot_flow_noise", _lib().mot_flow_noise(seeds.data_ptr(), int(step) & (2 ** 64 - 1), n_req, N,
+                                                   z.data_ptr(), _stream(seeds, stream)))
+    return z
 
 
 def mot_selftest_wait_timeout(ws, stream=None) -> None:

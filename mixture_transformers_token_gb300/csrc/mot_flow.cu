@@ -364,6 +364,60 @@ __global__ void __launch_bounds__(128) sde_logp_kernel(const SdeArgs a) {
   if ((threadIdx.x & 31) == 0) a.logp[req] = sde_logp(ss, t, tn, a.N);
 }
 
+// ---------------------------------------------------------------------------
+// Per-sample transition noise: Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011) and the Box-Muller transform
+// ---------------------------------------------------------------------------
+// Element 4b + m of request r at step k takes word m of the block with counter (b, k, 0, 0) and
+// key (seed_r, kNoiseDomain); the top 23 bits give u = ((x >> 41) + 0.5) 2^-23, exact in fp32
+// and inside (0, 1); pairs (u_even, u_odd) give sqrt(-2 ln u_even) (cos, sin)(2 pi u_odd).
+
+constexpr uint64_t kPhiloxM0 = 0xD2E7470EE14C6C93ull, kPhiloxM1 = 0xCA5A826395121157ull;
+constexpr uint64_t kPhiloxW0 = 0x9E3779B97F4A7C15ull, kPhiloxW1 = 0xBB67AE8584CAA73Bull;
+constexpr uint64_t kNoiseDomain = 0x4D6F54466C6F77ull;  // "MoTFlow"
+
+__device__ __forceinline__ void philox4x64_10(uint64_t (&x)[4], uint64_t k0, uint64_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t hi0 = __umul64hi(kPhiloxM0, x[0]), lo0 = kPhiloxM0 * x[0];
+    const uint64_t hi1 = __umul64hi(kPhiloxM1, x[2]), lo1 = kPhiloxM1 * x[2];
+    x[0] = hi1 ^ x[1] ^ k0;
+    x[1] = lo1;
+    x[2] = hi0 ^ x[3] ^ k1;
+    x[3] = lo0;
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
+  }
+}
+
+__device__ __forceinline__ float noise_uniform(uint64_t x) {
+  return __fmul_rn(__fadd_rn(float(uint32_t(x >> 41)), 0.5f), 1.1920928955078125e-7f);  // 2^-23
+}
+
+__device__ __forceinline__ void box_muller(float u0, float u1, float& z0, float& z1) {
+  const float rad = __fsqrt_rn(__fmul_rn(-2.0f, logf(u0)));
+  float sn, cs;
+  sincospif(__fmul_rn(2.0f, u1), &sn, &cs);
+  z0 = __fmul_rn(rad, cs);
+  z1 = __fmul_rn(rad, sn);
+}
+
+__global__ void __launch_bounds__(256) flow_noise_kernel(const uint64_t* seeds, uint64_t step, int n_req, int64_t N,
+                                                         float* z) {
+  const int64_t nb = N / 4;  // four deviates per block
+  const int64_t total = int64_t(n_req) * nb;
+  for (int64_t u = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; u < total; u += int64_t(gridDim.x) * blockDim.x) {
+    const int r = int(u / nb);
+    const int64_t b = u % nb;
+    uint64_t x[4] = {uint64_t(b), step, 0ull, 0ull};
+    philox4x64_10(x, seeds[r], kNoiseDomain);
+    float4 o;
+    box_muller(noise_uniform(x[0]), noise_uniform(x[1]), o.x, o.y);
+    box_muller(noise_uniform(x[2]), noise_uniform(x[3]), o.z, o.w);
+    reinterpret_cast<float4*>(z + int64_t(r) * N)[b] = o;
+  }
+}
+
 }  // namespace flow
 }  // namespace mot
 
@@ -437,4 +491,20 @@ extern "C" int mot_flow_sde_step(const float* x, const float* v, const float* z,
   if (launch_dependent(flow::sde_logp_kernel, dim3((n_req + 3) / 4), dim3(128), 0, s, a) != cudaSuccess)
     return MOT_ERR_CUDA;
   return MOT_OK;
+}
+
+extern "C" int mot_flow_noise(const uint64_t* seeds, uint64_t step, int n_req, int64_t N, float* z, void* stream) {
+  if (!seeds || !z) return MOT_ERR_NULL;
+  if (n_req < 1 || n_req > flow::kMaxReq || N < 8 || N % 8 != 0 || N > flow::kMaxN) return MOT_ERR_GEOMETRY;
+  if (!aligned16(seeds) || !aligned16(z)) return MOT_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {seeds, z};
+  int dev = -1;
+  int st = check_device(s, ptrs, 2, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  const int64_t total = int64_t(n_req) * (N / 4);
+  const int64_t grid = std::min<int64_t>((total + 255) / 256, int64_t(8) * sm_count(dev));
+  flow::flow_noise_kernel<<<unsigned(grid), 256, 0, s>>>(seeds, step, n_req, N, z);
+  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }

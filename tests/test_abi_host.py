@@ -328,3 +328,14 @@ def test_flow_sde_step_rejects(lib):
     assert f(A, A, A, C, 2, 4, A, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
     assert f(A, A, MIS, C, 2, 64, A, B, 1 << 20, C, None) == MOT_ERR_ALIGN
     assert f(A, A, None, C, 2, 64, A, B, 64, C, None) == MOT_ERR_WORKSPACE
+
+
+def test_flow_noise_rejects(lib):
+    f = lib.mot_flow_noise
+    assert f(None, 0, 2, 64, C, None) == MOT_ERR_NULL
+    assert f(A, 0, 2, 64, None, None) == MOT_ERR_NULL
+    assert f(A, 0, 0, 64, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, 0, 2, 12, C, None) == MOT_ERR_GEOMETRY
+    assert f(A, 0, 2, (1 << 24) + 8, C, None) == MOT_ERR_GEOMETRY
+    assert f(MIS, 0, 2, 64, C, None) == MOT_ERR_ALIGN
+

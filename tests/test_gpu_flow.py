@@ -259,3 +259,38 @@ def test_sde_batch_invariance_and_full_size_sampled():
     xa, la, _ = _sde_gpu({k: v[5:6].clone() for k, v in st.items()}, times[5:6])
     assert_f32_bitwise(xa[0], xn[5], "x_next alone vs in the batch")
     assert_f32_bitwise(la, lp[5:6], "logp alone vs in the batch")
+
+
+# ---------------------------------------------------------------------------
+# Per-sample transition noise
+# ---------------------------------------------------------------------------
+
+SEEDS = [0, 1, 2 ** 63 + 5, 2 ** 64 - 1, 123456789]
+
+
+def _seeds_dev(seeds):
+    return torch.tensor(np.array(seeds, dtype=np.uint64).view(np.int64), device="cuda")
+
+
+@pytest.mark.parametrize("N,step", [(8, 0), (2056, 3), (8192 + 40, 2 ** 40 + 7)])
+def test_flow_noise_vs_oracle(N, step):
+    # Philox4x64-10 counters and keys must match exactly (a slip gives unrelated deviates); the
+    # fp32 Box-Muller (logf, sqrt, sincospif) is within a few ulps of the fp64 transform of the
+    # same uniforms
+    z = mot.mot_flow_noise(_seeds_dev(SEEDS), step, N).cpu().numpy().astype(np.float64)
+    g = O.g_flow_noise(SEEDS, step, N)
+    d = np.abs(z - g)
+    assert np.all(d <= 1e-6 + 4e-6 * np.abs(g)), f"max |diff| {d.max():.3e}"
+
+
+def test_flow_noise_per_sample_and_per_step():
+    N = 4096
+    full = mot.mot_flow_noise(_seeds_dev(SEEDS), 9, N)
+    alone = mot.mot_flow_noise(_seeds_dev(SEEDS[2:3]), 9, N)
+    assert torch.equal(alone[0], full[2])                        # independent of the batch
+    other = mot.mot_flow_noise(_seeds_dev(SEEDS), 10, N)
+    assert not torch.equal(other, full)                          # each step has its own stream
+    again = mot.mot_flow_noise(_seeds_dev(SEEDS), 9, N)
+    assert torch.equal(again, full)                              # deterministic
+    zz = full.double()
+    assert abs(float(zz.mean())) < 0.05 and abs(float(zz.var()) - 1.0) < 0.05
