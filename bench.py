@@ -650,9 +650,9 @@ def run_attention(dev, flush) -> dict:
 
 def run_flow(dev, flush) -> dict:
     """One flow-sampler step of 16 requests of a 1024 x 1024 latent (64 x 64 tokens of 64
-    values, N = 262144 each): three-branch renormalised CFG of bf16 velocities into fp32, then
-    the SDE step (x, the guided velocity and the noise in; x_next and logp out), every request at
-    a different step of the 50-step schedule with shift 3."""
+    values, N = 262144 each): the per-sample transition noise, three-branch renormalised CFG of
+    bf16 velocities into fp32, then the SDE step (x, the guided velocity and the noise in; x_next
+    and logp out), every request at a different step of the 50-step schedule with shift 3."""
     import numpy as np
     import torch
 
@@ -663,7 +663,8 @@ def run_flow(dev, flush) -> dict:
     n_req, n = W.FLOW_REQUESTS, W.FLOW_N_1024
     br = {k: W.bf16_normal_device(11, 800 + i, (n_req, n), dev) for i, k in enumerate(("c", "tu", "iu"))}
     x = W.bf16_normal_device(11, 810, (n_req, n), dev).float()
-    z = W.bf16_normal_device(11, 811, (n_req, n), dev).float()
+    z = torch.empty((n_req, n), dtype=torch.float32, device=dev)
+    seeds = torch.arange(1000, 1000 + n_req, dtype=torch.int64, device=dev)
     sched = mot.mot_flow_schedule_host(W.FLOW_STEPS, W.FLOW_SHIFT).numpy()
     p = W.FLOW_POLICY
     steps = [3 * i for i in range(n_req)]
@@ -675,6 +676,7 @@ def run_flow(dev, flush) -> dict:
     x_next = torch.empty_like(v)
     logp = torch.empty((n_req,), dtype=torch.float32, device=dev)
     stages = [
+        ("flow_noise", lambda: mot.mot_flow_noise(seeds, 7, n, z=z)),
         ("cfg_combine_renorm", lambda: mot.mot_cfg_combine_renorm(br["c"], br["tu"], br["iu"], policy, ws=ws, out=v)),
         ("flow_sde_step", lambda: mot.mot_flow_sde_step(x, v, z, times, ws=ws, x_next=x_next, logp=logp)),
     ]
@@ -687,6 +689,8 @@ def run_flow(dev, flush) -> dict:
     b_sde = 16 * e + 12 * n_req           # x, v, z read, x_next written, times, logp
     return {
         "workload": f"flow_step_{n_req}x{n}",
+        "flow_noise_us": round(r["flow_noise"] * 1e6, 2),
+        "flow_noise_gdev_per_s": round(e / r["flow_noise"] / 1e9, 1),
         "cfg_combine_renorm_us": round(r["cfg_combine_renorm"] * 1e6, 2),
         "cfg_combine_renorm_gbs": round(b_cfg / r["cfg_combine_renorm"] / 1e9, 1),
         "cfg_combine_renorm_frac_hbm": round(b_cfg / r["cfg_combine_renorm"] / 1e9 / pk["hbm_gbs"], 4),
@@ -694,7 +698,7 @@ def run_flow(dev, flush) -> dict:
         "flow_sde_step_gbs": round(b_sde / r["flow_sde_step"] / 1e9, 1),
         "flow_sde_step_frac_hbm": round(b_sde / r["flow_sde_step"] / 1e9 / pk["hbm_gbs"], 4),
         "step_us": round(r["step"] * 1e6, 2), "elements": e, "bytes": {"cfg": b_cfg, "sde": b_sde},
-        "distribution_us": {k: r["dist"][k] for k in ("cfg_combine_renorm", "flow_sde_step")},
+        "distribution_us": {k: r["dist"][k] for k in ("flow_noise", "cfg_combine_renorm", "flow_sde_step")},
     }
 
 
