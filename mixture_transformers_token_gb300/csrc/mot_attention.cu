@@ -38,25 +38,26 @@
 namespace mot {
 namespace attn {
 
-constexpr int BQ = 128, BKV = 64;
+constexpr int BQ = 128, BKV = 128;
 constexpr int TILES = 2;        // query tiles per CTA (ping-pong between two softmax warpgroups)
 constexpr int THREADS = 320;    // producer, MMA, 2 x 4 softmax warps
-constexpr int KV_STAGES = 3;
-constexpr uint32_t SUB = 128 * 64 * 2;   // a [128 rows x 64 columns] bf16 swizzled tile (Q half)
-constexpr uint32_t KSUB = 64 * 64 * 2;   // a [64 keys x 64 columns] bf16 swizzled tile (K, V half)
+constexpr int K_STAGES = 1, V_STAGES = 2;
+constexpr uint32_t SUB = 128 * 64 * 2;   // a [128 rows x 64 columns] bf16 swizzled tile (Q, P half)
+constexpr uint32_t KSUB = BKV * 64 * 2;  // a [128 keys x 64 columns] bf16 swizzled tile (K, V half)
 
 template <int D>
 struct Layout {
   static constexpr uint32_t QTILE = BQ * D * 2;    // a Q tile
   static constexpr uint32_t KVBLK = BKV * D * 2;   // one K or V block
+  static constexpr uint32_t PTILE = BQ * BKV * 2;  // a tile's P: [128 rows x 128 keys] bf16, two halves
   static constexpr uint32_t Q = 0;                          // TILES Q tiles
-  static constexpr uint32_t K = Q + TILES * QTILE;          // KV_STAGES K blocks
-  static constexpr uint32_t V = K + KV_STAGES * KVBLK;      // KV_STAGES V blocks
-  static constexpr uint32_t BAR = V + KV_STAGES * KVBLK;
+  static constexpr uint32_t K = Q + TILES * QTILE;          // K_STAGES K blocks
+  static constexpr uint32_t V = K + K_STAGES * KVBLK;       // V_STAGES V blocks
+  static constexpr uint32_t P = V + V_STAGES * KVBLK;       // TILES P tiles
+  static constexpr uint32_t BAR = P + TILES * PTILE;
   static constexpr size_t BYTES = 1024 + size_t(BAR) + 512;  // barriers, tensor-memory slot, work item
-  // tensor memory: S of tile t at 64 t; P of tile t, buffer b (bf16 pairs) at 128 + 64 t + 32 b;
-  // O of tile t at 256 + 128 t
-  static constexpr uint32_t TMEM_S = 0, TMEM_P = 128, TMEM_O = 256, TMEM_COLS = 512;
+  // tensor memory: S of tile t at 128 t (128 keys), O of tile t at 256 + 128 t
+  static constexpr uint32_t TMEM_S = 0, TMEM_O = 256, TMEM_COLS = 512;
 };
 
 struct Args {
@@ -168,14 +169,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR);
   uint64_t* q_full = bars;        // both Q tiles
-  uint64_t* k_full = bars + 1;    // [KV_STAGES]
-  uint64_t* k_empty = bars + 4;   // [KV_STAGES]: both tiles' S MMAs have read the block
-  uint64_t* v_full = bars + 7;    // [KV_STAGES]
-  uint64_t* v_empty = bars + 10;  // [KV_STAGES]: both tiles' P V MMAs have read the block
+  uint64_t* k_full = bars + 1;    // [K_STAGES]
+  uint64_t* k_empty = bars + 4;   // [K_STAGES]: both tiles' S MMAs have read the block
+  uint64_t* v_full = bars + 7;    // [V_STAGES]
+  uint64_t* v_empty = bars + 10;  // [V_STAGES]: both tiles' P V MMAs have read the block
   uint64_t* s_full = bars + 13;   // [TILES]
   uint64_t* s_free = bars + 17;   // [TILES]: the tile's softmax warps have read S
   uint64_t* p_full = bars + 21;   // [TILES]
-  uint64_t* o_full = bars + 23;   // [TILES][2]: the tile's P V from P buffer b is done (and every earlier one)
+  uint64_t* o_full = bars + 23;   // [TILES]: the tile's P V of the block is done (and every earlier one)
   uint64_t* drain = bars + 27;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 28);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -205,9 +206,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
-    for (int i = 0; i < KV_STAGES; ++i) {
+    for (int i = 0; i < K_STAGES; ++i) {
       mbar_init(smem_u32(&k_full[i]), 1);
       mbar_init(smem_u32(&k_empty[i]), 1);
+    }
+    for (int i = 0; i < V_STAGES; ++i) {
       mbar_init(smem_u32(&v_full[i]), 1);
       mbar_init(smem_u32(&v_empty[i]), 1);
     }
@@ -215,8 +218,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&s_full[t]), 1);
       mbar_init(smem_u32(&s_free[t]), 4);
       mbar_init(smem_u32(&p_full[t]), 4);
-      mbar_init(smem_u32(&o_full[2 * t]), 1);
-      mbar_init(smem_u32(&o_full[2 * t + 1]), 1);
+      mbar_init(smem_u32(&o_full[t]), 1);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0u;
@@ -244,41 +246,41 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_2d(smem_u32(smem + L::Q + t * L::QTILE + b * SUB), &tm_q, h * D + 64 * b, q0 + i0 + t * BQ,
                       smem_u32(q_full));
       for (int j = 0; j < nblk && ok; ++j) {
-        const int st = j % KV_STAGES;
-        const uint32_t ph = uint32_t(j / KV_STAGES) & 1u;
+        const int ks = j % K_STAGES, vs = j % V_STAGES;
         const int y = k0 + j * BKV;
-        ok = mbar_wait(smem_u32(&k_empty[st]), ph ^ 1u, abort_flag, a.err);
+        ok = mbar_wait(smem_u32(&k_empty[ks]), (uint32_t(j / K_STAGES) & 1u) ^ 1u, abort_flag, a.err);
         if (!ok) break;
-        mbar_arrive_expect_tx(smem_u32(&k_full[st]), L::KVBLK);
+        mbar_arrive_expect_tx(smem_u32(&k_full[ks]), L::KVBLK);
         for (int b = 0; b < D / 64; ++b)
-          tma_load_2d(smem_u32(smem + L::K + st * L::KVBLK + b * KSUB), &tm_kv, (a.Hq + g) * D + 64 * b, y,
-                      smem_u32(&k_full[st]));
+          tma_load_2d(smem_u32(smem + L::K + ks * L::KVBLK + b * KSUB), &tm_kv, (a.Hq + g) * D + 64 * b, y,
+                      smem_u32(&k_full[ks]));
         kdone = j + 1;
-        ok = mbar_wait(smem_u32(&v_empty[st]), ph ^ 1u, abort_flag, a.err);
+        ok = mbar_wait(smem_u32(&v_empty[vs]), (uint32_t(j / V_STAGES) & 1u) ^ 1u, abort_flag, a.err);
         if (!ok) break;
-        mbar_arrive_expect_tx(smem_u32(&v_full[st]), L::KVBLK);
+        mbar_arrive_expect_tx(smem_u32(&v_full[vs]), L::KVBLK);
         for (int b = 0; b < D / 64; ++b)
-          tma_load_2d(smem_u32(smem + L::V + st * L::KVBLK + b * KSUB), &tm_kv, (a.Hq + a.Hkv + g) * D + 64 * b, y,
-                      smem_u32(&v_full[st]));
+          tma_load_2d(smem_u32(smem + L::V + vs * L::KVBLK + b * KSUB), &tm_kv, (a.Hq + a.Hkv + g) * D + 64 * b, y,
+                      smem_u32(&v_full[vs]));
         vdone = j + 1;
       }
       // every issued copy has landed before the CTA can exit
       mbar_drain(smem_u32(q_full), 0);
-      for (int j = kdone - KV_STAGES > 0 ? kdone - KV_STAGES : 0; j < kdone; ++j)
-        mbar_drain(smem_u32(&k_full[j % KV_STAGES]), uint32_t(j / KV_STAGES) & 1u);
-      for (int j = vdone - KV_STAGES > 0 ? vdone - KV_STAGES : 0; j < vdone; ++j)
-        mbar_drain(smem_u32(&v_full[j % KV_STAGES]), uint32_t(j / KV_STAGES) & 1u);
+      for (int j = kdone - K_STAGES > 0 ? kdone - K_STAGES : 0; j < kdone; ++j)
+        mbar_drain(smem_u32(&k_full[j % K_STAGES]), uint32_t(j / K_STAGES) & 1u);
+      for (int j = vdone - V_STAGES > 0 ? vdone - V_STAGES : 0; j < vdone; ++j)
+        mbar_drain(smem_u32(&v_full[j % V_STAGES]), uint32_t(j / V_STAGES) & 1u);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    // per block j: S of both tiles into their buffer j & 1, then P V of block j - 1 for both
+    // per block j: S of both tiles (M128 N128: 128 keys per instruction), then P V of block
+    // j - 1 for both (P from shared memory, V MN-major)
     constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV);
     constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, D) | kIdescBMnMajor;
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(q_full), 0, abort_flag, a.err));
     for (int j = 0; j <= nblk && ok; ++j) {
       if (j < nblk) {
-        const int st = j % KV_STAGES;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&k_full[st]), uint32_t(j / KV_STAGES) & 1u, abort_flag,
+        const int ks = j % K_STAGES;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&k_full[ks]), uint32_t(j / K_STAGES) & 1u, abort_flag,
                                                a.err));
         for (int t = 0; t < TILES && ok; ++t) {
           if (j >= 1) {  // the softmax warps have read S of block j - 1
@@ -287,35 +289,35 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t qa = smem_u32(smem + L::Q + t * L::QTILE), kb = smem_u32(smem + L::K + st * L::KVBLK);
+            const uint32_t qa = smem_u32(smem + L::Q + t * L::QTILE), kb = smem_u32(smem + L::K + ks * L::KVBLK);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
               mma_bf16(tmem + L::TMEM_S + t * BKV, smem_desc_sw128(qa + (kk / 4) * SUB + (kk % 4) * 32),
                        smem_desc_sw128(kb + (kk / 4) * KSUB + (kk % 4) * 32), idesc_s, kk > 0);
             mma_commit(smem_u32(&s_full[t]));
-            if (t == TILES - 1) mma_commit(smem_u32(&k_empty[st]));
+            if (t == TILES - 1) mma_commit(smem_u32(&k_empty[ks]));
           }
           __syncwarp();
         }
         if (!ok) break;
       }
       if (j >= 1) {
-        const int jj = j - 1, st = jj % KV_STAGES;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&v_full[st]), uint32_t(jj / KV_STAGES) & 1u, abort_flag,
+        const int jj = j - 1, vs = jj % V_STAGES;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&v_full[vs]), uint32_t(jj / V_STAGES) & 1u, abort_flag,
                                                a.err));
         for (int t = 0; t < TILES && ok; ++t) {
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_full[t]), uint32_t(jj) & 1u, abort_flag, a.err));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t pa = tmem + L::TMEM_P + t * 64 + (jj & 1) * 32;  // P in tensor memory
-            const uint32_t vb = smem_u32(smem + L::V + st * L::KVBLK);
+            const uint32_t pa = smem_u32(smem + L::P + t * L::PTILE);
+            const uint32_t vb = smem_u32(smem + L::V + vs * L::KVBLK);
 #pragma unroll
             for (int kk = 0; kk < BKV / 16; ++kk)
-              mma_bf16_ts(tmem + L::TMEM_O + t * 128, pa + kk * 8, smem_desc_mn_sw128(vb + kk * 2048, KSUB), idesc_o,
-                          (jj | kk) != 0);
-            mma_commit(smem_u32(&o_full[2 * t + (jj & 1)]));
-            if (t == TILES - 1) mma_commit(smem_u32(&v_empty[st]));
+              mma_bf16(tmem + L::TMEM_O + t * 128, smem_desc_sw128(pa + (kk / 4) * SUB + (kk % 4) * 32),
+                       smem_desc_mn_sw128(vb + kk * 2048, KSUB), idesc_o, (jj | kk) != 0);
+            mma_commit(smem_u32(&o_full[t]));
+            if (t == TILES - 1) mma_commit(smem_u32(&v_empty[vs]));
           }
           __syncwarp();
         }
@@ -335,6 +337,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int lim = (valid && i < nc) ? nk - nq + i + 1 : nk;   // keys [0, lim) are visible
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const uint32_t to = tmem + lane_off + L::TMEM_O + t * 128;
+    uint8_t* prow = smem + L::P + t * L::PTILE + row * 128;  // the row in the tile's P (half 0)
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
@@ -342,7 +345,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       float x[BKV];
-      tmem_ld64(tmem + lane_off + L::TMEM_S + t * BKV, x);
+      {
+        float (&x0)[64] = *reinterpret_cast<float (*)[64]>(&x[0]);
+        float (&x1)[64] = *reinterpret_cast<float (*)[64]>(&x[64]);
+        tmem_ld64(tmem + lane_off + L::TMEM_S + t * BKV, x0);
+        tmem_ld64(tmem + lane_off + L::TMEM_S + t * BKV + 64, x1);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s_free[t]));  // S may be overwritten by the next block
@@ -364,32 +372,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         m = bmax;
       }
       const float mc = m == -INFINITY ? 0.0f : __fmul_rn(m, a.c);
-      // p = 2^(S c - m c), four interleaved partial sums, packed to bf16 pairs
-      float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      uint32_t pk[BKV / 2];
-#pragma unroll
-      for (int c = 0; c < BKV; c += 2) {
-        const float p0 = ex2(fmaf(x[c], a.c, -mc)), p1 = ex2(fmaf(x[c + 1], a.c, -mc));
-        ps[c & 3] = __fadd_rn(ps[c & 3], p0);
-        ps[(c + 1) & 3] = __fadd_rn(ps[(c + 1) & 3], p1);
-        pk[c / 2] = pack_bf2(p0, p1);
-      }
-      const float psum = __fadd_rn(__fadd_rn(ps[0], ps[1]), __fadd_rn(ps[2], ps[3]));
-      l = __fadd_rn(__fmul_rn(l, alpha), psum);
-      // P buffer j & 1 was last read by the P V of block j - 2. The waits are per buffer, so a
-      // barrier never runs two phases ahead of its waiter (the next P V on a buffer needs this
-      // warpgroup's next P).
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[2 * t + (j & 1)]), uint32_t((j - 2) >> 1) & 1u,
-                                               abort_flag, a.err));
-        if (!ok) break;
-      }
-      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        // rescale O: every earlier P V (the last is block j - 1's) must be done
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[2 * t + ((j - 1) & 1)]),
-                                               uint32_t((j - 1) >> 1) & 1u, abort_flag, a.err));
+      // the tile's single P buffer and O are free once the P V of block j - 1 is done
+      if (j >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(j - 1) & 1u, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -399,22 +388,33 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st32(to + c * 32, o);
         }
       }
-      // P as bf16 pairs into the row's lane of tensor-memory buffer j & 1 (keys 2c, 2c + 1 in
-      // column c), where the P V MMA reads it as its A operand
-      {
-        float pf[BKV / 2];
+      // p = 2^(S c - m c), four interleaved partial sums; every 8 keys go as bf16 to the
+      // 16-byte chunk (cc ^ (row & 7)) of the row in half cc / 8 of the swizzled P tile
+      float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int c = 0; c < BKV / 2; ++c) pf[c] = __uint_as_float(pk[c]);
-        tmem_st32(tmem + lane_off + L::TMEM_P + t * 64 + (j & 1) * 32, pf);
+      for (int cc = 0; cc < BKV / 8; ++cc) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = 8 * cc + 2 * u;
+          const float p0 = ex2(fmaf(x[c], a.c, -mc)), p1 = ex2(fmaf(x[c + 1], a.c, -mc));
+          ps[c & 3] = __fadd_rn(ps[c & 3], p0);
+          ps[(c + 1) & 3] = __fadd_rn(ps[(c + 1) & 3], p1);
+          pk[u] = pack_bf2(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(prow + (cc >> 3) * SUB + (((cc & 7) ^ (row & 7)) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      const float psum = __fadd_rn(__fadd_rn(ps[0], ps[1]), __fadd_rn(ps[2], ps[3]));
+      l = __fadd_rn(__fmul_rn(l, alpha), psum);
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
     }
     if (ok && nblk > 0) {
       // the last P V (and with it every earlier one) is done
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[2 * t + ((nblk - 1) & 1)]),
-                                             uint32_t((nblk - 1) >> 1) & 1u, abort_flag, a.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(nblk - 1) & 1u, abort_flag, a.err));
       if (ok) {
         tc_fence_after();
         uint16_t* orow = a.out + int64_t(q0 + i) * (int64_t(a.Hq) * D) + int64_t(h) * D;
