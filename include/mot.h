@@ -278,7 +278,7 @@ int mot_rope_table_fill_host_fp32(double theta, int D, int P, float* host_cs);
  *   ws    at least 64 bytes (e.g. a routing plan); its error word receives device errors.
  *   out   [T][Hq D] bf16   out: rows that are some sequence's query; other rows untouched.
  * Query head h reads KV head h / (Hq / Hkv). Arithmetic: S = Q K^T in fp32 on the tensor
- * cores; per row, 64-key blocks in ascending order from the sequence's first key, with
+ * cores; per row, 128-key blocks in ascending order from the sequence's first key, with
  * c = scale * log2 e: the reference maximum m starts as the first block's maximum and moves
  * to a later block's maximum only when that exceeds m by more than 8 / c (so p <= 2^8);
  * p = 2^(S c - m c) (the hardware exp2 approximation); l = l alpha + the block's sum of p;

@@ -11,7 +11,7 @@
 // in place from the fused QKV output (row stride (Hq + 2 Hkv) D).
 //
 // Arithmetic, the same for every tile of every pack: S = Q K^T in fp32 on the tensor cores;
-// per row, in 64-key blocks in ascending key order, with c = scale * log2 e: the running
+// per row, in 128-key blocks in ascending key order, with c = scale * log2 e: the running
 // maximum m of S (masked keys excluded) moves to the block maximum only when that exceeds it
 // by more than 8 / c (then O and l are scaled by 2^((m_old - m) c)); p = 2^(S c - m c) (one
 // fused multiply-add and the SFU's exp2); l += the block's p (four interleaved partial sums);
@@ -19,14 +19,16 @@
 // key, so a row's bits do not depend on the other sequences of the pack.
 //
 // One CTA per (pair of 128-row query tiles, head); pairs of a sequence are visited last first
-// (the causal tiles near the end carry the most keys). Warp 0 loads both Q tiles once and
-// 64-key K and V blocks into three-stage rings (TMA, 128-byte swizzle); warp 1 issues, per key
-// block, S = Q K^T for both tiles into their double-buffered TMEM S, then O += P V of the
-// previous block for both (P read from tensor memory, V as an MN-major operand from shared
-// memory); warps 2-5 and 6-9 are the softmax warpgroups of the two tiles, one query row per
-// thread: they read a block's S from TMEM once (64 columns), form p, rescale O in TMEM when the
-// row maximum moves, and write P as bf16 pairs into one of two TMEM buffers. Each tile's softmax
-// runs while the tensor cores work on the other tile and on its own next block.
+// (the causal tiles near the end carry the most keys). Warp 0 loads both Q tiles once, each
+// 128-key K block into one buffer and each V block into a two-stage ring (TMA, 128-byte
+// swizzle); warp 1 issues, per key block, S = Q K^T for both tiles (M128 N128: every tcgen05
+// instruction costs at least about 107 cycles, so 128 keys per instruction keep it at 60 % of
+// the tensor rate where 64 keys reached 30 %), then O += P V of the previous block for both
+// (P and V from shared memory, V as an MN-major operand); warps 2-5 and 6-9 are the softmax
+// warpgroups of the two tiles, one query row per thread: they read a block's 128 scores from
+// TMEM, form p, rescale O in TMEM when the row maximum moves, and write P (bf16, swizzled
+// K-major) into the tile's shared-memory P tile once the previous P V has read it. Each tile's
+// softmax runs while the tensor cores work on the other tile.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
