@@ -78,6 +78,28 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (Blackwell f32x2 arithmetic: two IEEE operations per instruction, each
+// rounded as the scalar one would be).
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // The running maximum moves only when a block's maximum exceeds it by more than this many
 // powers of two: until then p = 2^(S c - m c) stays below 2^8, and O and l, which share m,
 // need no rescaling.
@@ -390,23 +412,31 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st32(to + c * 32, o);
         }
       }
-      // p = 2^(S c - m c), four interleaved partial sums; every 8 keys go as bf16 to the
-      // 16-byte chunk (cc ^ (row & 7)) of the row in half cc / 8 of the swizzled P tile
-      float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // p = 2^(S c - m c), four interleaved partial sums (key c adds to sum c mod 4), as f32x2
+      // pairs; every 8 keys go as bf16 to the 16-byte chunk (cc ^ (row & 7)) of the row in half
+      // cc / 8 of the swizzled P tile
+      const unsigned long long c2 = f2_pack(a.c, a.c), nmc2 = f2_pack(-mc, -mc);
+      unsigned long long ps01 = 0ull, ps23 = 0ull;  // (sum 0, sum 1), (sum 2, sum 3), from +0
 #pragma unroll
       for (int cc = 0; cc < BKV / 8; ++cc) {
         uint32_t pk[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int c = 8 * cc + 2 * u;
-          const float p0 = ex2(fmaf(x[c], a.c, -mc)), p1 = ex2(fmaf(x[c + 1], a.c, -mc));
-          ps[c & 3] = __fadd_rn(ps[c & 3], p0);
-          ps[(c + 1) & 3] = __fadd_rn(ps[(c + 1) & 3], p1);
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), c2, nmc2), t0, t1);
+          const float p0 = ex2(t0), p1 = ex2(t1);
+          const unsigned long long p01 = f2_pack(p0, p1);
+          if (u & 1) ps23 = f2_add(ps23, p01);
+          else ps01 = f2_add(ps01, p01);
           pk[u] = pack_bf2(p0, p1);
         }
         *reinterpret_cast<uint4*>(prow + (cc >> 3) * SUB + (((cc & 7) ^ (row & 7)) << 4)) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      float ps[4];
+      f2_unpack(ps01, ps[0], ps[1]);
+      f2_unpack(ps23, ps[2], ps[3]);
       const float psum = __fadd_rn(__fadd_rn(ps[0], ps[1]), __fadd_rn(ps[2], ps[3]));
       l = __fadd_rn(__fmul_rn(l, alpha), psum);
       fence_proxy_async_smem();
