@@ -402,16 +402,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tmem_ld32(to + c * 32, o);
-#pragma unroll
-          for (int u = 0; u < 32; ++u) o[u] = __fmul_rn(o[u], alpha);
-          tmem_st32(to + c * 32, o);
-        }
-      }
       // p = 2^(S c - m c), four interleaved partial sums (key c adds to sum c mod 4), as f32x2
       // pairs; every 8 keys go as bf16 to the 16-byte chunk (cc ^ (row & 7)) of the row in half
       // cc / 8 of the swizzled P tile
@@ -439,6 +429,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       f2_unpack(ps23, ps[2], ps[3]);
       const float psum = __fadd_rn(__fadd_rn(ps[0], ps[1]), __fadd_rn(ps[2], ps[3]));
       l = __fadd_rn(__fmul_rn(l, alpha), psum);
+      // O takes the new maximum before the P V of block j adds to it
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(to + c * 32, o);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[u] = __fmul_rn(o[u], alpha);
+          tmem_st32(to + c * 32, o);
+        }
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
