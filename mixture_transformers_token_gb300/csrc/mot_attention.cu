@@ -15,7 +15,8 @@
 // maximum m of S (masked keys excluded) moves to the block maximum only when that exceeds it
 // by more than 8 / c (then O and l are scaled by 2^((m_old - m) c)); p = 2^(S c - m c) (one
 // fused multiply-add and the SFU's exp2); l += the block's p (four interleaved partial sums);
-// O += bf16(p) V (fp32, tensor cores); out = bf16(O / l). Blocks start at the sequence's first
+// O += bf16(p) V (fp32, tensor cores); out = bf16(O * (1 / l)), 1 / l rounded to fp32 once
+// per row. Blocks start at the sequence's first
 // key, so a row's bits do not depend on the other sequences of the pack.
 //
 // One CTA per (pair of 128-row query tiles, head); pairs of a sequence are visited last first
@@ -450,6 +451,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(nblk - 1) & 1u, abort_flag, a.err));
       if (ok) {
         tc_fence_after();
+        const float rl = __frcp_rn(l);  // one rounded reciprocal per row, then products
         uint16_t* orow = a.out + int64_t(q0 + i) * (int64_t(a.Hq) * D) + int64_t(h) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (valid) {
             uint32_t ok16[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) ok16[u] = pack_bf2(__fdiv_rn(o[2 * u], l), __fdiv_rn(o[2 * u + 1], l));
+            for (int u = 0; u < 16; ++u) ok16[u] = pack_bf2(__fmul_rn(o[2 * u], rl), __fmul_rn(o[2 * u + 1], rl));
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
