@@ -188,7 +188,7 @@ __device__ void check_sequences(const Args& a) {
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     joint_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                           const Args a) {
+                           const __grid_constant__ CUtensorMap tm_out, const Args a) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -250,6 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
@@ -446,12 +447,43 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
     }
-    if (ok && nblk > 0) {
+    if (nblk > 0) {
       // the last P V (and with it every earlier one) is done
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(nblk - 1) & 1u, abort_flag, a.err));
-      if (ok) {
+      if (ok)
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(nblk - 1) & 1u, abort_flag, a.err));
+      const float rl = __frcp_rn(l);  // one rounded reciprocal per row, then products
+      if (i0 + t * BQ + BQ <= nq) {
+        // every row of the tile is a query: the bf16 tile goes to the tile's Q buffer (no MMA
+        // reads it any more) in the 128-byte swizzled box layout, then out by tensor stores.
+        // Every warp of the tile reaches the barrier, the stores go only if no wait gave up.
+        if (ok) {
+          tc_fence_after();
+          uint8_t* qrow = smem + L::Q + t * L::QTILE + row * 128;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(to + c * 32, o);
+            uint32_t ok16[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) ok16[u] = pack_bf2(__fmul_rn(o[2 * u], rl), __fmul_rn(o[2 * u + 1], rl));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int k = 4 * c + u;  // 16-byte piece of the row: box k / 8, chunk k % 8
+              *reinterpret_cast<uint4*>(qrow + (k >> 3) * SUB + (((k & 7) ^ (row & 7)) << 4)) =
+                  make_uint4(ok16[4 * u], ok16[4 * u + 1], ok16[4 * u + 2], ok16[4 * u + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        named_bar_sync(1 + t, 4 * 32);
+        if (warp == 2 + 4 * t && lane == 0 && *abort_flag == 0u) {
+          for (int b = 0; b < D / 64; ++b)
+            tma_store_2d(&tm_out, smem_u32(smem + L::Q + t * L::QTILE + b * SUB), h * D + 64 * b, q0 + i0 + t * BQ);
+          bulk_store_commit_and_wait_read();
+        }
+      } else if (ok) {
+        // a ragged tile (rows past the sequence's queries belong to others): row by row
         tc_fence_after();
-        const float rl = __frcp_rn(l);  // one rounded reciprocal per row, then products
         uint16_t* orow = a.out + int64_t(q0 + i) * (int64_t(a.Hq) * D) + int64_t(h) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -484,15 +516,16 @@ constexpr size_t kSmemBytes = Layout<128>::BYTES;
 
 template <int D>
 static int launch(const mot_bf16* qkv, const Args& a, int n_tiles_max, cudaStream_t s) {
-  CUtensorMap tm_q, tm_kv;
+  CUtensorMap tm_q, tm_kv, tm_out;
   const uint64_t ncol = uint64_t(a.Hq + 2 * a.Hkv) * D;
   if (!make_tmap_bf16(&tm_q, qkv, ncol, uint64_t(a.T), 64, BQ) ||
-      !make_tmap_bf16(&tm_kv, qkv, ncol, uint64_t(a.T), 64, BKV))
+      !make_tmap_bf16(&tm_kv, qkv, ncol, uint64_t(a.T), 64, BKV) ||
+      !make_tmap_bf16(&tm_out, a.out, uint64_t(a.Hq) * D, uint64_t(a.T), 64, BQ))
     return MOT_ERR_CUDA;
   if (cudaFuncSetAttribute(joint_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmemBytes)) != cudaSuccess)
     return MOT_ERR_CUDA;
-  joint_attention_kernel<D><<<unsigned(int64_t(n_tiles_max) * a.Hq), THREADS, kSmemBytes, s>>>(tm_q, tm_kv, a);
+  joint_attention_kernel<D><<<unsigned(int64_t(n_tiles_max) * a.Hq), THREADS, kSmemBytes, s>>>(tm_q, tm_kv, tm_out, a);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 

@@ -160,6 +160,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// 2D tiled store of one box from shared memory (in the tensor map's swizzled layout) to
+// global memory, tracked by the issuing thread's bulk-async group.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(x),
+               "r"(y), "r"(src)
+               : "memory");
+}
+
+// Closes the issuing thread's bulk-async group, then waits until every bulk store it issued
+// has finished reading shared memory (the source may then be reused or released).
+__device__ __forceinline__ void bulk_store_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Barrier over `threads` threads (a multiple of 32) of the CTA under hardware barrier `id`.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Contiguous bytes from global to shared memory (1D bulk copy); both addresses 16-byte
 // aligned and `bytes` a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

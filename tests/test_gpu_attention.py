@@ -30,10 +30,10 @@ def _qkv(T, Hq, Hkv, D, seed):
     return W.bf16_normal(W.rng_for(seed, 500), (T, (Hq + 2 * Hkv) * D))
 
 
-def _run(qkv, seqs, Hq, Hkv, D):
+def _run(qkv, seqs, Hq, Hkv, D, out=None):
     ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
     s = torch.tensor(seqs, dtype=torch.int32, device="cuda")
-    out = mot.mot_joint_attention(qkv.cuda(), s, Hq, Hkv, D, ws)
+    out = mot.mot_joint_attention(qkv.cuda(), s, Hq, Hkv, D, ws, out=out)
     flags = mot.mot_device_status(ws)
     return out, flags
 
@@ -63,11 +63,31 @@ def test_attention_cached_prefix_bottom_right_and_latents_only():
     T = 1000
     seqs = [(250, 0, 70, 320, 70), (520, 320, 64, 264, 0), (900, 771, 1, 129, 1)]
     qkv = _qkv(T, Hq, Hkv, D, seed=7)
-    out, flags = _run(qkv, seqs, Hq, Hkv, D)
+    # rows that are no sequence's query keep what the caller left there
+    sentinel = torch.full((T, Hq * D), -7.0, dtype=torch.bfloat16, device="cuda")
+    out, flags = _run(qkv, seqs, Hq, Hkv, D, out=sentinel.clone())
     assert flags == 0
     g = O.g_joint_attention(f64(qkv), seqs, Hq, Hkv, D)
     rows = _query_rows(seqs)
     assert_tolerance(f64(out)[rows], g["out_pre"][rows], "cached prefix / latents only")
+    others = np.setdiff1d(np.arange(T), rows)
+    assert torch.equal(out[torch.from_numpy(others).cuda()], sentinel[: len(others)])
+
+
+def test_attention_full_tiles_leave_neighbouring_rows_untouched():
+    # sequences of whole 128-row tiles (written by tensor stores) between untouched rows
+    D, Hq, Hkv = 128, 4, 2
+    T = 1280
+    seqs = [(128, 0, 256, 384, 128), (640, 512, 512, 640, 0)]
+    qkv = _qkv(T, Hq, Hkv, D, seed=8)
+    sentinel = torch.full((T, Hq * D), 3.0, dtype=torch.bfloat16, device="cuda")
+    out, flags = _run(qkv, seqs, Hq, Hkv, D, out=sentinel.clone())
+    assert flags == 0
+    g = O.g_joint_attention(f64(qkv), seqs, Hq, Hkv, D)
+    rows = _query_rows(seqs)
+    assert_tolerance(f64(out)[rows], g["out_pre"][rows], "whole tiles")
+    others = np.setdiff1d(np.arange(T), rows)
+    assert torch.equal(out[torch.from_numpy(others).cuda()], sentinel[: len(others)])
 
 
 def test_attention_rows_do_not_depend_on_the_pack():
