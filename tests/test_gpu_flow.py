@@ -102,7 +102,8 @@ def _cfg_oracle(b, pol, i, three=True, level="e"):
     return f(c, tu, iu if three else None, t, s_text, s_img, t_lo, t_hi, rmin)
 
 
-@pytest.mark.parametrize("N", [8, 2056, 8192, 3 * 8192 + 40])
+# 32 and 33 segments: the request's fold fetches its segment sums 32 at a time
+@pytest.mark.parametrize("N", [8, 2056, 8192, 3 * 8192 + 40, 32 * 8192, 32 * 8192 + 8])
 @pytest.mark.parametrize("three", [True, False])
 def test_cfg_combine_bitwise_vs_oracle(N, three):
     b, pol = _cfg_case(len(POLICIES), N, seed=N + three)
@@ -198,7 +199,7 @@ def _sde_check(st, times, xn, lp, i, what):
     assert abs(float(lp[i]) - g["logp"]) <= 1e-4 * (a_g + abs(g["logp"] + a_g)), f"{what}: logp vs fp64"
 
 
-@pytest.mark.parametrize("N", [8, 2056, 8192, 3 * 8192 + 40])
+@pytest.mark.parametrize("N", [8, 2056, 8192, 3 * 8192 + 40, 32 * 8192 + 8])
 def test_sde_step_first_middle_last_steps(N):
     st = W.flow_state(W.rng_for(N, 710), len(STEPS), N)
     xn, lp, flags = _sde_gpu(st, STEPS)
