@@ -82,12 +82,24 @@ struct Args {
   float eps;
   int a_plan_order;      // rows of A are in plan order
   int out_plan_order;    // rows of out are written in plan order
+  int st32;              // out and its row pitch are 32-byte aligned: 32-byte stores (set at launch)
 };
 
-__device__ __forceinline__ void store_row_u4(uint16_t* dst, const uint32_t* pk, int n_u4) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+// n_u4 (even) 16-byte pieces of a row: one lane writes whole 32-byte sectors when the output
+// allows 32-byte stores, else 16-byte ones.
+__device__ __forceinline__ void store_row_u4(const Args& a, uint16_t* dst, const uint32_t* pk, int n_u4) {
+  if (a.st32) {
 #pragma unroll
-  for (int i = 0; i < n_u4; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    for (int i = 0; i < n_u4; i += 2)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * i), "r"(pk[4 * i]),
+                   "r"(pk[4 * i + 1]), "r"(pk[4 * i + 2]), "r"(pk[4 * i + 3]), "r"(pk[4 * i + 4]), "r"(pk[4 * i + 5]),
+                   "r"(pk[4 * i + 6]), "r"(pk[4 * i + 7])
+                   : "memory");
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < n_u4; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  }
 }
 
 // Epilogue warps: two per TMEM lane quarter; warp "half" h handles the tile's columns
@@ -103,7 +115,7 @@ __device__ __forceinline__ void epi_cast(const Args& a, uint32_t taddr, bool val
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
-    if (valid) store_row_u4(orow + c * 32, pk, 4);
+    if (valid) store_row_u4(a, orow + c * 32, pk, 4);
   }
 }
 
@@ -129,7 +141,7 @@ __device__ __forceinline__ void epi_swiglu(const Args& a, uint32_t taddr, bool v
       }
       pk[i / 2] = pack_bf2(h[0], h[1]);
     }
-    if (valid) store_row_u4(orow + c * 32, pk, 4);
+    if (valid) store_row_u4(a, orow + c * 32, pk, 4);
   }
 }
 
@@ -225,7 +237,7 @@ __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool vali
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
-        if (valid) store_row_u4(ohead + c * 32, pk, 4);
+        if (valid) store_row_u4(a, ohead + c * 32, pk, 4);
       }
       continue;
     }
@@ -280,8 +292,8 @@ __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool vali
                            __fadd_rn(__fmul_rn(u2b, t[j].z), __fmul_rn(u1b, t[j].w)));
         }
         if (valid) {
-          store_row_u4(ohead + c * 16, o1, 2);
-          store_row_u4(ohead + NP + c * 16, o2, 2);
+          store_row_u4(a, ohead + c * 16, o1, 2);
+          store_row_u4(a, ohead + NP + c * 16, o2, 2);
         }
       }
       continue;
@@ -312,8 +324,8 @@ __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool vali
         o2[j] = bf2_add(bf2_mul(u2, c2), bf2_mul(u1, s2));
       }
       if (valid) {
-        store_row_u4(ohead + c * 16, o1, 2);
-        store_row_u4(ohead + NP + c * 16, o2, 2);
+        store_row_u4(a, ohead + c * 16, o1, 2);
+        store_row_u4(a, ohead + NP + c * 16, o2, 2);
       }
     }
   }
@@ -870,8 +882,10 @@ static int launch(const void* a, const void* w, int T, int N, int K, const Args&
   const int64_t work_max = pairs_max * int64_t(N / BN);
   const int64_t cap = max_active_pairs<EPI, B_MN>(dev);
   const int64_t clusters = work_max < cap ? work_max : cap;
+  Args la = args;
+  la.st32 = (reinterpret_cast<uintptr_t>(args.out) % 32 == 0 && (int64_t(args.ldo) * 2) % 32 == 0) ? 1 : 0;
   if (launch_dependent(routed_gemm_kernel<EPI, B_MN>, dim3(unsigned(2 * clusters)), dim3(THREADS), SMEM_BYTES, s,
-                       tm_a, tm_rows, tm_w, args) != cudaSuccess) {
+                       tm_a, tm_rows, tm_w, la) != cudaSuccess) {
     cudaGetLastError();
     return MOT_ERR_CUDA;
   }

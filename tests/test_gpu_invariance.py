@@ -149,3 +149,30 @@ def test_repeat_is_deterministic(setup):
     again = run_pack(ref, wt)
     for k in base:
         assert np.array_equal(again[k], base[k]), k
+
+
+def _out_at_16_bytes(T, n):
+    """A [T][n] bf16 output whose data starts 16 bytes past a 32-byte boundary."""
+    buf = torch.empty(T * n + 16, dtype=torch.bfloat16, device="cuda")
+    v = buf[8:8 + T * n].view(T, n)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+def test_outputs_only_16_byte_aligned_give_the_same_bits(setup):
+    # the epilogues write whole 32-byte sectors when the output allows it, 16-byte pieces
+    # otherwise; both must produce the same bytes
+    ref, wt, base = setup
+    dev = "cuda"
+    x, res, mod, pos = (ref[k].to(dev) for k in ("x", "res", "mod", "pos"))
+    ws = mot.mot_route_plan(mod)
+    y, _ = mot.mot_fused_add_rmsnorm(x, res, wt["w_norm"], mod, EPS, ws=ws)
+    qkv = mot.mot_routed_qkv_norm_rope(y, wt["w_qkv"], wt["q_norm"], wt["k_norm"], pos, wt["cs"], HQ, HKV, D, EPS, ws,
+                                       out=_out_at_16_bytes(N_REF, N))
+    qkv32 = mot.mot_routed_qkv_norm_rope_fp32(y, wt["w_qkv"], wt["q_norm"], wt["k_norm"], pos, wt["cs32"], HQ, HKV, D,
+                                              EPS, ws, out=_out_at_16_bytes(N_REF, N))
+    o = mot.mot_routed_gemm(y, wt["w_o"], ws, mot.EPI_CAST, out=_out_at_16_bytes(N_REF, 512))
+    h = mot.mot_routed_gemm(y, wt["w_gu"], ws, mot.EPI_SWIGLU, out=_out_at_16_bytes(N_REF, 256))
+    assert mot.mot_device_status(ws) == 0
+    for k, v in (("qkv", qkv), ("qkv_fp32_rope", qkv32), ("o", o), ("h", h)):
+        assert np.array_equal(bits(v), base[k]), k
