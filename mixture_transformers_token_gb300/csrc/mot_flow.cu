@@ -124,7 +124,16 @@ struct F8 {
   float4 a, b;
 };
 
-__device__ __forceinline__ F8 load8_f32(const float* p) {
+// Eight consecutive floats: one 32-byte load when the array allows it (w32), else two 16-byte ones.
+__device__ __forceinline__ F8 load8_f32(const float* p, bool w32) {
+  if (w32) {
+    F8 f;
+    asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(f.a.x), "=f"(f.a.y), "=f"(f.a.z), "=f"(f.a.w), "=f"(f.b.x), "=f"(f.b.y), "=f"(f.b.z),
+                   "=f"(f.b.w)
+                 : "l"(p));
+    return f;
+  }
   return F8{__ldg(reinterpret_cast<const float4*>(p)), __ldg(reinterpret_cast<const float4*>(p) + 1)};
 }
 
@@ -133,7 +142,14 @@ __device__ __forceinline__ void unpack8_f32(const F8& f, float (&v)[8]) {
   v[4] = f.b.x; v[5] = f.b.y; v[6] = f.b.z; v[7] = f.b.w;
 }
 
-__device__ __forceinline__ void store8_f32(float* p, const float (&v)[8]) {
+// Eight consecutive floats: one 32-byte store when the array allows it (w32), else two 16-byte ones.
+__device__ __forceinline__ void store8_f32(float* p, const float (&v)[8], bool w32) {
+  if (w32) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+                 "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+    return;
+  }
   reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
   reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
@@ -147,6 +163,7 @@ struct CfgArgs {
   int S;                // segments per request
   float2* part;         // [n_req][S]: (sum c c, sum v2 v2) of each segment
   float* out;           // [n_req][N] fp32
+  int w32;              // out is 32-byte aligned
 };
 
 struct CfgPolicy {
@@ -211,7 +228,7 @@ __global__ void __launch_bounds__(THREADS, 4) cfg_partials_kernel(const CfgArgs 
         if (q < nch) {
           float c[8];
           unpack8_bf16(__ldg(reinterpret_cast<const uint4*>(a.c + base + 8 * q)), c);
-          store8_f32(a.out + base + 8 * q, c);
+          store8_f32(a.out + base + 8 * q, c, a.w32);
         }
       }
       continue;  // uniform across the CTA
@@ -269,7 +286,7 @@ __global__ void __launch_bounds__(THREADS, 4) cfg_scale_kernel(const CfgArgs a, 
         cfg_guide(a, pol, k, j, c, v2);
 #pragma unroll
         for (int i = 0; i < 8; ++i) v2[i] = __fmul_rn(v2[i], r);
-        store8_f32(a.out + base + 8 * q, v2);
+        store8_f32(a.out + base + 8 * q, v2, a.w32);
       }
     }
     __syncthreads();  // r_s is rewritten for the next unit
@@ -288,6 +305,7 @@ struct SdeArgs {
   float* part;         // [n_req][S]: each segment's sum of d d
   float* logp;         // [n_req]
   uint32_t* err;
+  int w32;             // x, v, z and x_next are 32-byte aligned
 };
 
 __device__ __forceinline__ bool times_ok(float t, float tn) {
@@ -318,16 +336,16 @@ __global__ void __launch_bounds__(THREADS, 4) sde_step_kernel(const SdeArgs a, c
       const int q = int(threadIdx.x) + THREADS * j;
       if (q < nch) {
         float x[8], v[8], w[8], mu[8], xn[8];
-        unpack8_f32(load8_f32(a.x + base + 8 * q), x);
-        unpack8_f32(load8_f32(a.v + base + 8 * q), v);
-        unpack8_f32(load8_f32(third + base + 8 * q), w);
+        unpack8_f32(load8_f32(a.x + base + 8 * q, a.w32), x);
+        unpack8_f32(load8_f32(a.v + base + 8 * q, a.w32), v);
+        unpack8_f32(load8_f32(third + base + 8 * q, a.w32), w);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float e = __fadd_rn(x[i], __fmul_rn(omt, v[i]));
           mu[i] = __fsub_rn(x[i], __fmul_rn(dt, __fadd_rn(v[i], __fmul_rn(kk, e))));
           xn[i] = a.z ? __fadd_rn(mu[i], __fmul_rn(sd, w[i])) : w[i];
         }
-        if (a.z) store8_f32(a.x_next + base + 8 * q, xn);
+        if (a.z) store8_f32(a.x_next + base + 8 * q, xn, a.w32);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float d = __fsub_rn(xn[i], mu[i]);
@@ -456,7 +474,8 @@ extern "C" int mot_cfg_combine_renorm(const mot_bf16* v_c, const mot_bf16* v_tu,
   DeviceGuard guard(dev);
   const int S = flow::segments(N);
   flow::CfgArgs a{v_c, v_tu, v_iu, policy, N, S,
-                  reinterpret_cast<float2*>(static_cast<char*>(ws) + sizeof(PlanHeader)), out};
+                  reinterpret_cast<float2*>(static_cast<char*>(ws) + sizeof(PlanHeader)), out,
+                  reinterpret_cast<uintptr_t>(out) % 32 == 0 ? 1 : 0};
   const int64_t units = int64_t(n_req) * S;
   const unsigned grid = unsigned(std::min<int64_t>(units, int64_t(flow::kCtasPerSm) * sm_count(dev)));
   flow::cfg_partials_kernel<<<grid, flow::THREADS, 0, s>>>(a, units);
@@ -481,9 +500,11 @@ extern "C" int mot_flow_sde_step(const float* x, const float* v, const float* z,
   if (st != MOT_OK) return st;
   DeviceGuard guard(dev);
   const int S = flow::segments(N);
+  const bool w32 = reinterpret_cast<uintptr_t>(x) % 32 == 0 && reinterpret_cast<uintptr_t>(v) % 32 == 0 &&
+                   reinterpret_cast<uintptr_t>(z) % 32 == 0 && reinterpret_cast<uintptr_t>(x_next) % 32 == 0;
   flow::SdeArgs a{x, v, z, x_next, times, N, S, n_req,
                   reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(PlanHeader)), logp,
-                  &static_cast<PlanHeader*>(ws)->error};
+                  &static_cast<PlanHeader*>(ws)->error, w32 ? 1 : 0};
   const int64_t units = int64_t(n_req) * S;
   const unsigned grid = unsigned(std::min<int64_t>(units, int64_t(flow::kCtasPerSm) * sm_count(dev)));
   flow::sde_step_kernel<<<grid, flow::THREADS, 0, s>>>(a, units);

@@ -295,3 +295,36 @@ def test_flow_noise_per_sample_and_per_step():
     assert torch.equal(again, full)                              # deterministic
     zz = full.double()
     assert abs(float(zz.mean())) < 0.05 and abs(float(zz.var()) - 1.0) < 0.05
+
+
+def _at_16_bytes(t):
+    """A copy of the fp32 tensor t on the GPU whose data starts 16 bytes past a 32-byte boundary."""
+    buf = torch.empty(t.numel() + 4, dtype=torch.float32, device="cuda")
+    v = buf[4:4 + t.numel()].view(t.shape)
+    assert v.data_ptr() % 32 == 16
+    v.copy_(t.cuda())
+    return v
+
+
+def test_cfg_and_sde_with_16_byte_aligned_tensors_give_the_same_bits():
+    # 32-byte loads and stores are used when every tensor allows them, 16-byte ones otherwise
+    N = 3 * 8192 + 40
+    b, pol = _cfg_case(len(POLICIES), N, seed=77)
+    aligned = _cfg_gpu(b, pol)
+    d = {k: v.cuda() for k, v in b.items()}
+    ws = torch.zeros(mot.mot_flow_workspace_bytes(len(POLICIES), N), dtype=torch.uint8, device="cuda")
+    out16 = _at_16_bytes(torch.zeros((len(POLICIES), N)))
+    mot.mot_cfg_combine_renorm(d["c"], d["tu"], d["iu"], torch.from_numpy(pol).cuda(), ws=ws, out=out16)
+    assert mot.mot_device_status(ws) == 0
+    np.testing.assert_array_equal(out16.cpu().numpy().view(np.uint32), aligned.view(np.uint32))
+    st = W.flow_state(W.rng_for(N, 711), len(STEPS), N)
+    xn, lp, flags = _sde_gpu(st, STEPS)
+    assert flags == 0
+    ws2 = torch.zeros(mot.mot_flow_workspace_bytes(len(STEPS), N), dtype=torch.uint8, device="cuda")
+    tt = torch.from_numpy(np.asarray(STEPS, dtype=F32)).cuda()
+    xn16 = _at_16_bytes(torch.zeros((len(STEPS), N)))
+    _, lp16 = mot.mot_flow_sde_step(_at_16_bytes(st["x"]), _at_16_bytes(st["v"]), _at_16_bytes(st["z"]), tt, ws=ws2,
+                                    x_next=xn16)
+    assert mot.mot_device_status(ws2) == 0
+    np.testing.assert_array_equal(xn16.cpu().numpy().view(np.uint32), xn.view(np.uint32))
+    np.testing.assert_array_equal(lp16.cpu().numpy().view(np.uint32), lp.view(np.uint32))
