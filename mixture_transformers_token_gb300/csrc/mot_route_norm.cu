@@ -283,7 +283,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   for (int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < T; i += warps) {
     const uint4* s = src + int64_t(perm[i]) * K8;
     uint4* d = dst + i * K8;
-    for (int k = lane; k < K8; k += 32) __stcs(d + k, __ldcs(s + k));
+    int k = lane;
+    for (; k + 96 < K8; k += 128) {  // four loads in flight per lane
+      const uint4 v0 = __ldcs(s + k), v1 = __ldcs(s + k + 32), v2 = __ldcs(s + k + 64), v3 = __ldcs(s + k + 96);
+      __stcs(d + k, v0);
+      __stcs(d + k + 32, v1);
+      __stcs(d + k + 64, v2);
+      __stcs(d + k + 96, v3);
+    }
+    for (; k < K8; k += 32) __stcs(d + k, __ldcs(s + k));
   }
 }
 
