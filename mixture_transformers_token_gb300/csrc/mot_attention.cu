@@ -125,39 +125,54 @@ __device__ __forceinline__ int seq_items(const Args& a, int s) {
   return bad_seq(d, a.T) ? 0 : (d[2] + TILES * BQ - 1) / (TILES * BQ);
 }
 
-__device__ bool find_tile(const Args& a, int k, int4& sq, int& nc, int& i0) {
+// Finds the item of CTA index k; called by a whole warp, every lane returns the same answer.
+// The lanes fetch the descriptors in parallel (one sequence per lane and round of 32), so the
+// lookup costs a few memory round trips, not one per sequence.
+__device__ bool find_tile(const Args& a, int k, int lane, int4& sq, int& nc, int& i0) {
   int found_s = -1, r = -1;
   if (a.n_seq <= kSortedSeqs) {
-    int items[kSortedSeqs];
-    int most = 0;
-    for (int s = 0; s < a.n_seq; ++s) {
-      items[s] = seq_items(a, s);
-      most = items[s] > most ? items[s] : most;
+    // items of sequences lane and lane + 32; round rr takes every sequence with more than rr
+    // items, in sequence order
+    const int it0 = lane < a.n_seq ? seq_items(a, lane) : 0;
+    const int it1 = lane + 32 < a.n_seq ? seq_items(a, lane + 32) : 0;
+    int most = it0 > it1 ? it0 : it1;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const int o = __shfl_xor_sync(0xffffffffu, most, off);
+      most = o > most ? o : most;
     }
     int acc = 0;
-    for (int rr = 0; rr < most && found_s < 0; ++rr) {
-      for (int s = 0; s < a.n_seq; ++s) {
-        if (items[s] > rr) {
-          if (acc == k) {
-            found_s = s;
-            r = rr;
-            break;
-          }
-          ++acc;
-        }
+    for (int rr = 0; rr < most; ++rr) {
+      const uint32_t m0 = __ballot_sync(0xffffffffu, it0 > rr), m1 = __ballot_sync(0xffffffffu, it1 > rr);
+      const int c0 = __popc(m0), c1 = __popc(m1);
+      if (k < acc + c0 + c1) {
+        const int t = k - acc;  // the t-th sequence (from 0) taking part in this round
+        found_s = t < c0 ? int(__fns(m0, 0, t + 1)) : 32 + int(__fns(m1, 0, t - c0 + 1));
+        r = rr;
+        break;
       }
+      acc += c0 + c1;
     }
     if (found_s < 0) return false;
   } else {
+    // sequence by sequence: a warp-wide running count over rounds of 32 sequences
     int acc = 0;
-    for (int s = 0; s < a.n_seq; ++s) {
-      const int nt = seq_items(a, s);
-      if (k < acc + nt) {
-        found_s = s;
-        r = k - acc;
-        break;
+    for (int s0 = 0; s0 < a.n_seq && found_s < 0; s0 += 32) {
+      const int s = s0 + lane;
+      const int nt = s < a.n_seq ? seq_items(a, s) : 0;
+      int incl = nt;  // inclusive prefix sum over the lanes
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
       }
-      acc += nt;
+      const uint32_t hit = __ballot_sync(0xffffffffu, k < acc + incl && k >= acc + incl - nt);
+      if (hit != 0u) {
+        const int l = __ffs(hit) - 1;
+        found_s = s0 + l;
+        r = k - acc - (__shfl_sync(0xffffffffu, incl, l) - __shfl_sync(0xffffffffu, nt, l));
+      }
+      acc += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (found_s < 0) return false;
   }
@@ -169,11 +184,12 @@ __device__ bool find_tile(const Args& a, int k, int4& sq, int& nc, int& i0) {
 }
 
 // CTA 0 checks every descriptor, that the query ranges do not overlap (their rows sum to
-// at most T) and that the grid covers every tile; a failure sets MOT_DEV_BAD_SEQUENCE.
-__device__ void check_sequences(const Args& a) {
+// at most T) and that the grid covers every tile; a failure sets MOT_DEV_BAD_SEQUENCE. Called
+// by a whole warp, one sequence per lane and round.
+__device__ void check_sequences(const Args& a, int lane) {
   int64_t tiles = 0, rows = 0;
   bool bad = false;
-  for (int s = 0; s < a.n_seq; ++s) {
+  for (int s = lane; s < a.n_seq; s += 32) {
     const int32_t* d = a.seqs + 5 * s;
     if (bad_seq(d, a.T)) {
       bad = true;
@@ -182,7 +198,13 @@ __device__ void check_sequences(const Args& a) {
     tiles += (d[2] + TILES * BQ - 1) / (TILES * BQ);
     rows += d[2];
   }
-  if (bad || rows > a.T || tiles * a.Hq > int64_t(gridDim.x)) atomicOr(a.err, MOT_DEV_BAD_SEQUENCE);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    tiles += __shfl_xor_sync(0xffffffffu, tiles, off);
+    rows += __shfl_xor_sync(0xffffffffu, rows, off);
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0 && (bad || rows > a.T || tiles * a.Hq > int64_t(gridDim.x))) atomicOr(a.err, MOT_DEV_BAD_SEQUENCE);
 }
 
 template <int D>
@@ -206,19 +228,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 28);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
-  // thread 0 finds the CTA's work item; the others read it from shared memory
+  // warp 0 finds the CTA's work item; the others read it from shared memory
   int* item = reinterpret_cast<int*>(tmem_slot + 2);  // found, q0, k0, nq, nk, n_causal, i0
-  if (threadIdx.x == 0) {
-    if (blockIdx.x == 0) check_sequences(a);
-    int4 sq4;
+  if (threadIdx.x < 32) {
+    if (blockIdx.x == 0) check_sequences(a, int(threadIdx.x));
+    int4 sq4 = make_int4(0, 0, 0, 0);
     int c4 = 0, i04 = 0;
-    item[0] = find_tile(a, int(blockIdx.x) / a.Hq, sq4, c4, i04) ? 1 : 0;
-    item[1] = sq4.x;
-    item[2] = sq4.y;
-    item[3] = sq4.z;
-    item[4] = sq4.w;
-    item[5] = c4;
-    item[6] = i04;
+    const bool found = find_tile(a, int(blockIdx.x) / a.Hq, int(threadIdx.x), sq4, c4, i04);
+    if (threadIdx.x == 0) {
+      item[0] = found ? 1 : 0;
+      item[1] = sq4.x;
+      item[2] = sq4.y;
+      item[3] = sq4.z;
+      item[4] = sq4.w;
+      item[5] = c4;
+      item[6] = i04;
+    }
   }
   __syncthreads();
   if (!item[0]) return;  // uniform across the CTA

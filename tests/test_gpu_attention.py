@@ -104,6 +104,25 @@ def test_attention_rows_do_not_depend_on_the_pack():
     assert_bitwise(again, out, "repeat")
 
 
+def test_attention_more_than_64_sequences():
+    # past 64 sequences the grid takes the items sequence by sequence instead of heaviest first
+    D, Hq, Hkv = 64, 2, 1
+    rng = W.rng_for(9, 501)
+    lens = rng.integers(1, 40, 70)
+    seqs, q0 = [], 0
+    for i, n in enumerate(lens):
+        n = int(n)
+        seqs.append((q0, q0, n, n, n if i % 3 else n // 2))   # causal, half causal, ...
+        q0 += n
+    T = q0 + 5
+    qkv = _qkv(T, Hq, Hkv, D, seed=16)
+    out, flags = _run(qkv, seqs, Hq, Hkv, D)
+    assert flags == 0
+    g = O.g_joint_attention(f64(qkv), seqs, Hq, Hkv, D)
+    rows = _query_rows(seqs)
+    assert_tolerance(f64(out)[rows], g["out_pre"][rows], "70 sequences")
+
+
 def test_attention_bad_descriptor_flags():
     D, Hq, Hkv = 64, 2, 1
     qkv = _qkv(100, Hq, Hkv, D, seed=14)
