@@ -29,7 +29,10 @@
 // warpgroups of the two tiles, one query row per thread: they read a block's 128 scores from
 // TMEM, form p, rescale O in TMEM when the row maximum moves, and write P (bf16, swizzled
 // K-major) into the tile's shared-memory P tile once the previous P V has read it. Each tile's
-// softmax runs while the tensor cores work on the other tile.
+// softmax runs while the tensor cores work on the other tile. Warp 0 first finds the CTA's work
+// item, reading the sequence descriptors one per lane. A whole output tile goes, as bf16, to the
+// tile's Q buffer (idle after its last S MMA) and out by TMA tensor stores; a ragged tile is
+// written row by row so that rows of other sequences are never touched.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
