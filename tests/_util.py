@@ -29,23 +29,35 @@ def half_bf16_step(v: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, ex - 9)
 
 
-def allowed_abs(ref: np.ndarray) -> np.ndarray:
+def allowed_abs(ref: np.ndarray, acc_err=None) -> np.ndarray:
     """max |diff| bound per element: 2e-2, or -- where |ref| >= 8, since no bf16 number lies
-    within 2e-2 of an exact value there -- half a bf16 step plus 1e-5 |ref| for the fp32
-    accumulation rounding that can put a value just past a rounding tie."""
-    return np.maximum(MAX_ABS, half_bf16_step(ref) + 1e-5 * np.abs(ref))
+    within 2e-2 of an exact value there -- half a bf16 step (a correctly rounded result) plus
+    the accumulation error that can carry an fp32 sum across the rounding tie, capped at half a
+    step so that only the other neighbour of the exact value is admitted. acc_err is that error
+    bound per element when the caller has it (2 K 2^-24 sum|a||w| for a K-long fp32 dot
+    product); otherwise 1e-5 |ref|."""
+    h = half_bf16_step(ref)
+    slack = 1e-5 * np.abs(ref) if acc_err is None else np.minimum(acc_err, h)
+    return np.maximum(MAX_ABS, h + slack)
 
 
-def tol_report(gpu: np.ndarray, ref: np.ndarray) -> tuple[float, float, int]:
+def gemm_acc_err(K: int, acc_abs: np.ndarray) -> np.ndarray:
+    """Bound on the fp32 accumulation error of K-long dot products whose absolute terms sum to
+    acc_abs (the products of bf16 numbers are exact; each of at most K additions rounds by at
+    most one fp32 unit, counted twice for a non-nearest rounding of the accumulator)."""
+    return 2.0 * K * 2.0 ** -24 * acc_abs
+
+
+def tol_report(gpu: np.ndarray, ref: np.ndarray, acc_err=None) -> tuple[float, float, int]:
     d = np.abs(gpu - ref)
     rel = float(np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300))
-    return float(d.max()) if d.size else 0.0, rel, int(np.sum(d > allowed_abs(ref)))
+    return float(d.max()) if d.size else 0.0, rel, int(np.sum(d > allowed_abs(ref, acc_err)))
 
 
-def assert_tolerance(gpu: np.ndarray, ref: np.ndarray, what: str) -> None:
-    maxd, rel, nbad = tol_report(gpu, ref)
+def assert_tolerance(gpu: np.ndarray, ref: np.ndarray, what: str, acc_err=None) -> None:
+    maxd, rel, nbad = tol_report(gpu, ref, acc_err)
     if nbad:
-        idx = np.argwhere(np.abs(gpu - ref) > allowed_abs(ref))[:10]
+        idx = np.argwhere(np.abs(gpu - ref) > allowed_abs(ref, acc_err))[:10]
         detail = [(tuple(int(v) for v in i), float(gpu[tuple(i)]), float(ref[tuple(i)])) for i in idx]
     else:
         detail = []
@@ -85,64 +97,108 @@ def bf16_step(v):
     return np.ldexp(1.0, ex - 8)
 
 
-def check_end_to_end(out, g, q_gpu, u_e, acc_abs, shape, what, profile="bf16"):
-    """End to end against the fp64 golden chain.
+def _rope_pre_of_u(u, c, s, profile):
+    """The value of the emulator's output before its final bf16 cast, from its own normalized
+    heads u [T][heads][D]: in the BF16 profile bf16(u_i c) + bf16(partner_i s), exact in fp64
+    (products of two bf16 numbers and the sum of two are exact there); in the FP32 profile the
+    fp32 products and sum, each rounded to fp32."""
+    if profile == "bf16":
+        from oracle import mot_oracle as O
 
-    The relative-L2 bound holds for the whole output. An element may exceed 2e-2 only when a
-    legitimate one-step difference at a declared bf16 cast explains it: the GEMM's fp32
-    accumulation rounding q to the other bf16 neighbour of the exact value (anywhere in the
-    element's head, which moves rstd), the fp32 statistics rounding u the other way at the
-    element or its rotation partner (BF16 profile; the FP32 profile does not round u), or the
-    final cast alone -- within half a step, plus in the FP32 profile the fp32 rounding of u,
-    both products and the sum, which can carry a value across the cast's rounding tie. Every q
-    itself must lie within half a bf16 step plus the fp32 accumulation error bound
-    2 K 2^-24 sum|a||w| (acc_abs) of the exact accumulation.
+        return O.g_rope_bf16(u, c[:, None, :], s[:, None, :])[1]
+    u32 = u.astype(np.float32)
+    c32 = c.astype(np.float32)[:, None, :]
+    s32 = s.astype(np.float32)[:, None, :]
+    h = u.shape[-1] // 2
+    u1, u2 = u32[..., :h], u32[..., h:]
+    return np.concatenate([(u1 * c32) + (-u2 * s32), (u2 * c32) + (u1 * s32)], axis=-1).astype(np.float64)
+
+
+def check_end_to_end(out, g, q_gpu, u_e, acc_abs, shape, what, profile, epi):
+    """End to end against the fp64 golden chain G, with a cause proven for every element
+    beyond the tolerance.
+
+    The pages declare bf16 casts after the GEMM (q = bf16(acc), u in the BF16 profile, each
+    RoPE product and the sum), so a legitimate one-step difference at one of them can grow
+    past 2e-2 downstream. The check:
+      0. rel-L2 <= 4e-3 over the whole output; every GEMM output q_gpu lies within half a bf16
+         step plus the fp32 accumulation bound 2 K 2^-24 sum|a||w| (acc_abs) of the exact
+         accumulation (a legitimate fixed-order fp32 sum, rounded once).
+      1. G_tf = G's fp64 epilogue applied to the GPU's own q_gpu (teacher forcing). An element
+         beyond the bound of G but within it of G_tf is caused by the GEMM's rounding of q
+         (G and G_tf differ only in q), which step 0 bounds.
+      2. An element beyond the bound of G_tf too is accepted only if the emulator's u (fp32
+         statistics, which the GPU matches bit for bit) and G_tf's u differ at the element or
+         at its rotation partner (BF16 profile), and the output is the final cast of the
+         emulator's rotation of its u: |out - pre_E| <= half a bf16 step. In the FP32 profile
+         u is not rounded; the emulator's pre-cast value must lie within the fp32 rounding of
+         u, both products and the sum of G_tf's, and the output within half a step of it.
+    Anything else fails. `epi` holds the epilogue's inputs: q_norm, k_norm, pos, mod, eps,
+    theta (float64 / integer arrays). Returns the counts of each cause.
     """
+    from oracle import mot_oracle as O
+
     D, nqk = shape.D, shape.Hq + shape.Hkv
     ref = g["out_pre"]
     d = np.abs(out - ref)
     rel = float(np.linalg.norm(out - ref) / np.linalg.norm(ref))
-    assert rel <= 4e-3, f"{what}: rel-L2 {rel:.3e}"
+    assert rel <= MAX_REL_L2, f"{what}: rel-L2 {rel:.3e}"
     K = shape.H
     gemm_err = np.abs(q_gpu - g["acc"])
-    allowed = 0.5 * bf16_step(q_gpu) + 2.0 * K * 2.0 ** -24 * acc_abs
+    allowed = 0.5 * bf16_step(q_gpu) + gemm_acc_err(K, acc_abs)
     assert np.all(gemm_err <= allowed), f"{what}: GEMM output outside half a step plus the accumulation bound"
-    flips = q_gpu != g["q"]
-    bad = np.argwhere(d > allowed_abs(ref))
-    unexplained = []
-    for r, c in bad:
-        h, i = divmod(int(c), D)
-        j = (i + D // 2) % D
-        slack = 0.0
-        if profile == "fp32" and h < nqk:
-            slack = 16 * 2.0 ** -24 * (abs(g["u"][r, h, i]) + abs(g["u"][r, h, j]))
-        final_cast = d[r, c] <= 0.5 * bf16_step(out[r, c]) * (1 + 1e-9) + slack
-        q_flip = bool(np.any(flips[r, h * D:(h + 1) * D]))
-        u_flip = profile == "bf16" and h < nqk and (u_e[r, h, i] != g["u"][r, h, i] or u_e[r, h, j] != g["u"][r, h, j])
-        if not (final_cast or q_flip or u_flip):
-            unexplained.append((int(r), int(c), float(out[r, c]), float(ref[r, c])))
-    assert not unexplained, f"{what}: unexplained |diff| > 2e-2 at {unexplained[:10]}"
-    # scale-aware sanity bound on Q/K columns: a few bf16 steps of the rotated pair (u_i, u_j)
-    cols = np.arange(nqk * D)
-    hh, ii = cols // D, cols % D
-    jj = (ii + D // 2) % D
-    scale = np.maximum(np.abs(g["u"][:, hh, ii]), np.abs(g["u"][:, hh, jj]))
-    # plus what the GEMM's own cast output carries in: q_gpu may sit several bf16 steps from the
-    # golden q where the accumulation cancels (the fp32 bound above is absolute), and the head's
-    # norm scales that difference by rstd * g, bounded here by twice the head's |u| / |q| ratio
-    dq = np.abs(q_gpu[:, : nqk * D] - g["q"][:, : nqk * D]).reshape(-1, nqk, D)
-    qh = np.sqrt(np.sum(g["q"][:, : nqk * D].reshape(-1, nqk, D) ** 2, axis=2))
-    uh = np.sqrt(np.sum(g["u"] ** 2, axis=2))
-    factor = 2.0 * uh / np.maximum(qh, 1e-300)
-    prop = (factor[:, hh] * (dq[:, hh, ii] + dq[:, hh, jj]))
-    lim = 3 * bf16_step(scale) + bf16_step(ref[:, : nqk * D]) + prop
-    over = np.argwhere(d[:, : nqk * D] > lim)
-    detail = [(int(r), int(c), float(out[r, c]), float(ref[r, c]), float(g["u"][r, c // D, c % D]),
-               float(g["u"][r, c // D, (c % D + D // 2) % D]), float(q_gpu[r, c]), float(g["q"][r, c]))
-              for r, c in over[:8]]
-    assert over.size == 0, f"{what}: {len(over)} errors beyond 3 bf16 steps of the rotated pair " \
-                           f"(row, col, out, ref, u_i, u_partner, q_gpu, q_golden): {detail}"
-    print(f"{what}: max|diff| {d.max():.3e}, rel-L2 {rel:.2e}, {len(bad)} of {d.size} elements beyond 2e-2, "
-          f"each explained by a one-step flip at a bf16 cast; q flips at the GEMM cast: {int(flips.sum())}; "
-          f"elements beyond 2e-2 at (row, column): {[tuple(int(v) for v in x) for x in bad[:20]]}")
-    return {"max_abs": float(d.max()), "rel_l2": rel, "beyond": int(len(bad)), "q_flips": int(flips.sum())}
+    q_flips = int(np.sum(q_gpu != g["q"]))
+    bad = d > allowed_abs(ref)
+    n_bad = int(bad.sum())
+    n_gemm = n_stats = 0
+    if n_bad:
+        rows = np.unique(np.nonzero(bad)[0])
+        g_tf = O.g_qk_norm_rope(q_gpu[rows], epi["q_norm"], epi["k_norm"], epi["pos"][rows], epi["mod"][rows],
+                                shape.Hq, shape.Hkv, D, shape.eps, shape.theta, rope_profile=profile)
+        o, b = out[rows], bad[rows]
+        tf_ok = np.abs(o - g_tf["out_pre"]) <= allowed_abs(g_tf["out_pre"])
+        n_gemm = int(np.sum(b & tf_ok))
+        rest = b & ~tf_ok
+        unexplained = []
+        if rest.any():
+            table = O.rope_cos_sin if profile == "bf16" else O.rope_cos_sin_f32
+            c, s = table(shape.theta, D, epi["pos"][rows])
+            ue = u_e[rows]
+            pre_e = _rope_pre_of_u(ue, c, s, profile).reshape(len(rows), nqk * D)
+            utf = g_tf["u"]
+            for rr, col in np.argwhere(rest):
+                h, i = divmod(int(col), D)
+                r = int(rows[rr])
+                if h >= nqk:
+                    unexplained.append((r, int(col), float(o[rr, col]), float(ref[r, col]), "V column"))
+                    continue
+                j = (i + D // 2) % D
+                cast_only = abs(o[rr, col] - pre_e[rr, col]) <= 0.5 * bf16_step(o[rr, col]) * (1 + 1e-9)
+                if profile == "bf16":
+                    # u differs by at most one bf16 step at i or its partner j, and the rotations
+                    # of the two u differ by no more than that flip times (cos, sin) plus the
+                    # rounding of each side's two products
+                    f = i % (D // 2)
+                    du_i, du_j = abs(ue[rr, h, i] - utf[rr, h, i]), abs(ue[rr, h, j] - utf[rr, h, j])
+                    one_step = (du_i <= bf16_step(max(abs(ue[rr, h, i]), abs(utf[rr, h, i]))) and
+                                du_j <= bf16_step(max(abs(ue[rr, h, j]), abs(utf[rr, h, j]))))
+                    cf, sf = abs(c[rr, f]), abs(s[rr, f])
+                    prop = (du_i * cf + du_j * sf + bf16_step(abs(utf[rr, h, i]) * cf) +
+                            bf16_step(abs(utf[rr, h, j]) * sf))
+                    ok = (du_i > 0 or du_j > 0) and one_step and cast_only and \
+                        abs(pre_e[rr, col] - g_tf["out_pre"][rr, col]) <= prop * (1 + 1e-9)
+                else:
+                    slack = 16 * 2.0 ** -24 * (abs(utf[rr, h, i]) + abs(utf[rr, h, j]))
+                    ok = cast_only and abs(pre_e[rr, col] - g_tf["out_pre"][rr, col]) <= slack
+                if ok:
+                    n_stats += 1
+                else:
+                    unexplained.append((r, int(col), float(o[rr, col]), float(ref[r, col]),
+                                        float(g_tf["out_pre"][rr, col])))
+        assert not unexplained, f"{what}: |diff| beyond the bound with no proven cause (row, col, out, G, G_tf): " \
+                                f"{unexplained[:10]}"
+    print(f"{what}: max|diff| {d.max():.3e}, rel-L2 {rel:.2e}; q flips at the GEMM cast: {q_flips}; "
+          f"{n_bad} of {d.size} elements beyond the bound of G: {n_gemm} within it of the teacher-forced "
+          f"golden (GEMM rounding of q), {n_stats} from an fp32-statistics flip of u and the final cast")
+    return {"max_abs": float(d.max()), "rel_l2": rel, "beyond": n_bad, "q_flips": q_flips, "gemm_cause": n_gemm,
+            "stats_cause": n_stats}

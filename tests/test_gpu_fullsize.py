@@ -1,9 +1,10 @@
 """Parity at the benchmark's full sizes, in the launch configuration bench.py times.
 
 Same inputs (workloads.mlp_device_inputs / cfg_pack_device_inputs) and the same sequence of
-entry points as the secondary workloads of bench.py. The CFG pack is also checked on its whole
-output (the fp64 golden over all 36864 rows). Elsewhere each stage is checked on outputs the
-oracle can compute one by one, with the previous stage's GPU output as its input:
+entry points as the secondary workloads of bench.py. The CFG pack and the SwiGLU MLP are also
+checked on their whole outputs (the fp64 golden over every row and column), with a cause proven
+for each element beyond the tolerance. Elsewhere each stage is checked on outputs the oracle can
+compute one by one, with the previous stage's GPU output as its input:
   - add-RMSNorm on sampled rows, bit for bit against the fp32 emulator;
   - routed GEMMs on sampled rows x sampled columns, against the fp64 golden within the
     tolerance (max |diff| <= 2e-2, or half a bf16 step where |value| >= 8; rel-L2 <= 4e-3);
@@ -19,7 +20,8 @@ import mixture_transformers_token_gb300 as mot
 from mixture_transformers_token_gb300 import workloads as W
 from oracle import mot_oracle as O
 
-from _util import assert_bitwise, assert_tolerance, check_end_to_end, f64, need_gpu, np_bits
+from _util import (allowed_abs, assert_bitwise, assert_tolerance, bf16_step, check_end_to_end, f64, gemm_acc_err,
+                   need_gpu, np_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +67,97 @@ def test_swiglu_mlp_T8192_sampled():
     ocols = torch.from_numpy(np.sort(rng.choice(h, 128, replace=False))).to(dev)
     ref = O.g_routed_gemm_cast(f64(hid[p_t]), f64(m["w_down"][:, ocols, :]), mod[rows])
     assert_tolerance(f64(out[r_t][:, ocols]), ref["out_pre"], "down projection (sampled rows x columns)")
+
+
+def test_swiglu_mlp_T8192_full_output():
+    # Every element of the routed SwiGLU MLP that bench.py times (T = 8192, hidden 3584,
+    # intermediate 18944, 2048 gen rows scattered), in its launch configuration:
+    #  - add-RMSNorm: y and res_out of all rows bit for bit against the fp32 emulator;
+    #  - gate/up GEMM: its bf16 outputs g and u (the cast epilogue on the same weights and plan
+    #    order, the same mainloop) within the tolerance of the exact accumulation;
+    #  - SwiGLU epilogue: h within one bf16 step of the emulator on the GPU's own g and u (the
+    #    host's expf may differ from CUDA's in the last bit);
+    #  - h end to end against the fp64 golden: an element beyond the bound must have g or u
+    #    rounded to the other bf16 neighbour at that element (h depends on nothing else) and lie
+    #    within the bound of the golden SwiGLU of the GPU's g and u;
+    #  - down projection: every element within the tolerance of the exact accumulation of the
+    #    GPU's own h; end to end against the golden chain, rel-L2 within 4e-3.
+    need_gpu()
+    dev = torch.device("cuda")
+    m = W.mlp_device_inputs(dev)
+    t, hd, i = W.MLP_T, W.MLP_H, W.MLP_I
+    w_gu = mot.mot_swiglu_interleave(m["w_gate"], m["w_up"])
+    ws = torch.empty(mot.mot_workspace_bytes(t), dtype=torch.uint8, device=dev)
+    y, ro = mot.mot_fused_add_rmsnorm(m["x"], m["res"], m["w_norm"], m["mod"], 1e-6, ws=ws)
+    y_plan = mot.mot_gather_rows(y, ws)
+    hid = mot.mot_routed_gemm(y_plan, w_gu, ws, mot.EPI_SWIGLU | mot.A_PLAN_ORDER | mot.OUT_PLAN_ORDER)
+    out = mot.mot_routed_gemm(hid, m["w_down"], ws, mot.EPI_CAST | mot.A_PLAN_ORDER)
+    gu = mot.mot_routed_gemm(y_plan, w_gu, ws, mot.EPI_CAST | mot.A_PLAN_ORDER | mot.OUT_PLAN_ORDER)
+    assert mot.mot_device_status(ws) == 0
+    del w_gu
+    mod = m["mod"].cpu().numpy()
+
+    e = O.e_fused_add_rmsnorm(f64(m["x"]), f64(m["res"]), f64(m["w_norm"]), mod, 1e-6)
+    assert_bitwise(y, np_bits(e["y"]), "add-RMSNorm y (all rows)")
+    assert_bitwise(ro, np_bits(e["res_out"]), "add-RMSNorm res_out (all rows)")
+    del e, ro
+
+    perm = np.concatenate([np.nonzero(mod == 0)[0], np.nonzero(mod == 1)[0]])
+    mp = mod[perm]                                  # modality of each plan-order row
+    yp = f64(y)[perm]
+    assert_bitwise(y_plan, np_bits(yp), "rows in plan order")
+    # gate and up columns alternate in blocks of 128 in the interleaved weights
+    guv = f64(gu).reshape(t, i // 128, 2, 128)
+    g_gpu, u_gpu = guv[:, :, 0, :].reshape(t, i), guv[:, :, 1, :].reshape(t, i)
+    del guv, gu
+    acc_g = O.g_routed_matmul(yp, f64(m["w_gate"]), mp)
+    assert_tolerance(g_gpu, acc_g, "gate GEMM (bf16 cast, all rows)")
+    acc_u = O.g_routed_matmul(yp, f64(m["w_up"]), mp)
+    assert_tolerance(u_gpu, acc_u, "up GEMM (bf16 cast, all rows)")
+    del yp
+
+    hv = f64(hid)
+    e_h = O.e_swiglu(g_gpu, u_gpu).astype(np.float64)
+    assert np.all(np.abs(hv - e_h) <= bf16_step(np.maximum(np.abs(hv), np.abs(e_h)))), \
+        "SwiGLU epilogue beyond one bf16 step of the emulator on the GPU's own g and u"
+    del e_h
+    g = O.g_swiglu(acc_g, acc_u)
+    del acc_g, acc_u
+    d = np.abs(hv - g["h_pre"])
+    rel = float(np.linalg.norm(hv - g["h_pre"]) / np.linalg.norm(g["h_pre"]))
+    assert rel <= 4e-3, f"h rel-L2 {rel:.3e}"
+    beyond = d > allowed_abs(g["h_pre"])
+    n_beyond = int(beyond.sum())
+    if n_beyond:
+        rr, cc = np.nonzero(beyond)
+        flip = (g_gpu[rr, cc] != g["g"][rr, cc]) | (u_gpu[rr, cc] != g["u"][rr, cc])
+        tf = O.g_swiglu(g_gpu[rr, cc], u_gpu[rr, cc])["h_pre"]
+        within_tf = np.abs(hv[rr, cc] - tf) <= allowed_abs(tf)
+        bad = ~(flip & within_tf)
+        assert not bad.any(), f"h beyond the bound with no proven cause at (plan row, col) " \
+                              f"{list(zip(rr[bad][:10].tolist(), cc[bad][:10].tolist()))}"
+    flips = int(np.sum((g_gpu != g["g"]) | (u_gpu != g["u"])))
+    print(f"SwiGLU T=8192 vs G (all rows): max|diff| {d.max():.3e}, rel-L2 {rel:.2e}; elements whose g or u "
+          f"rounded the other way at the GEMM cast: {flips}; {n_beyond} of {d.size} beyond the bound, each at "
+          f"such an element and within the bound of the golden SwiGLU of the GPU's g and u")
+    del g_gpu, u_gpu, d, beyond
+
+    wd = f64(m["w_down"])
+    ov = f64(out)[perm]                              # plan order, as h
+    tf_down = O.g_routed_matmul(hv, wd, mp)
+    # K = 18944: where |value| >= 8 a result one step from the nearest bf16 is admitted only when
+    # the exact value lies within the fp32 accumulation bound of the rounding tie
+    acc_err = gemm_acc_err(i, O.g_routed_matmul(np.abs(hv), np.abs(wd), mp))
+    assert_tolerance(ov, tf_down, "down projection vs the exact accumulation of the GPU's h (all rows)", acc_err)
+    del acc_err
+    chain = O.g_routed_matmul(g["h"], wd, mp)
+    rel_c = float(np.linalg.norm(ov - chain) / np.linalg.norm(chain))
+    dc = np.abs(ov - chain)
+    n_bc = int(np.sum(dc > allowed_abs(chain)))     # each caused by the h flips proven above
+    assert rel_c <= 4e-3, f"down end to end rel-L2 {rel_c:.3e}"
+    print(f"down T=8192 vs the golden chain (all rows): max|diff| {dc.max():.3e}, rel-L2 {rel_c:.2e}; "
+          f"{n_bc} elements beyond the bound of the chain, every element within it of the exact "
+          f"accumulation of the GPU's own h")
 
 
 def test_cfg_pack_T36864_sampled():
@@ -140,7 +233,9 @@ def test_cfg_pack_T36864_full_output():
     assert_bitwise(qkv, np_bits(e_out), "QK-norm + RoPE epilogue (all rows)")
     del e_out
     acc_abs = O.g_routed_matmul(np.abs(yv), np.abs(wq), mod)
-    check_end_to_end(f64(qkv), g, qv, u_e.astype(np.float64), acc_abs, s, "CFG pack T=36864 QKV vs G (all rows)")
+    epi = {"q_norm": f64(c["q_norm"]), "k_norm": f64(c["k_norm"]), "pos": pos, "mod": mod}
+    check_end_to_end(f64(qkv), g, qv, u_e.astype(np.float64), acc_abs, s, "CFG pack T=36864 QKV vs G (all rows)",
+                     "bf16", epi)
     del g, acc_abs, u_e, qv, yv, wq
 
     ref = O.g_routed_gemm_cast(f64(c["attn"]), f64(c["w_o"]), mod)

@@ -328,8 +328,9 @@ def _check_qkv(shape, inp, out, ws, dev, rows=None, with_bias=False, profile="bf
     assert_bitwise(out, np_bits(e_out), f"fused QKV ({profile} RoPE) vs E on the cast GEMM output")
     # end to end against the golden chain
     acc_abs = O.g_routed_matmul(np.abs(f64(inp["x"])[r]), np.abs(f64(inp["w_qkv"])), mod[r])
+    epi = {"q_norm": f64(inp["q_norm"]), "k_norm": f64(inp["k_norm"]), "pos": pos[r], "mod": mod[r]}
     check_end_to_end(outv, g, qv[r], u_e[r].astype(np.float64), acc_abs, shape, f"QKV ({profile} RoPE) vs G",
-                      profile)
+                     profile, epi)
 
 
 @pytest.mark.parametrize("profile", PROFILES)
@@ -366,6 +367,33 @@ def test_qkv_with_bias(profile):
     inp = W.qkv_layer_inputs(shape, inp["mod"], inp["pos"], seed=4, with_bias=True)
     out, ws, dev = _qkv_run(shape, inp, with_bias=True, profile=profile)
     _check_qkv(shape, inp, out, ws, dev, with_bias=True, profile=profile)
+
+
+@pytest.mark.parametrize("profile", PROFILES)
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 4, 2), (128, 4, 2)])
+def test_qkv_bias_epilogue_bitwise_on_integer_inputs(D, Hq, Hkv, profile):
+    # Small-integer x and W make every partial sum of the routed GEMM an integer below 2^24, so
+    # the tensor cores' fp32 accumulation is exact in any order and acc + b (b a bf16 number) is
+    # exact too: q = bf16(acc + b) is known on the host. The fused epilogue must then equal the
+    # fp32 emulator on that q bit for bit -- the stage check of the bias path.
+    T, H = 200, 256
+    shape = W.QKVShape(T=T, H=H, Hq=Hq, Hkv=Hkv, D=D)
+    mod = W.modality_bernoulli(W.rng_for(8, 70), T, 0.5)
+    pos = torch.from_numpy(W.rng_for(8, 71).integers(0, 64, T).astype(np.int32))
+    inp = W.qkv_layer_inputs(shape, mod, pos, seed=8, with_bias=True)
+    inp["x"] = W.bf16_integers(W.rng_for(8, 72), (T, H), -2, 2)
+    inp["w_qkv"] = W.bf16_integers(W.rng_for(8, 73), (2, shape.n_qkv, H), -2, 2)
+    out, ws, dev = _qkv_run(shape, inp, with_bias=True, profile=profile)
+    assert mot.mot_device_status(ws) == 0
+    m, p = mod.numpy(), pos.numpy()
+    acc = O.g_routed_matmul(f64(inp["x"]), f64(inp["w_qkv"]), m) + f64(inp["b_qkv"])[m.astype(np.int64)]
+    assert np.all(acc == acc.astype(np.float32)), "acc + b must be exact in fp32"
+    q = O.bf16(acc)
+    table = O.rope_cos_sin if profile == "bf16" else O.rope_cos_sin_f32
+    c, s = table(shape.theta, D, p)
+    e_out = O.e_qk_norm_rope(q, f64(inp["q_norm"]), f64(inp["k_norm"]), c, s, m, Hq, Hkv, D, shape.eps,
+                             rope_profile=profile)
+    assert_bitwise(out, np_bits(e_out), f"fused QKV with bias ({profile} RoPE) vs E on bf16(acc + b)")
 
 
 @pytest.mark.parametrize("profile", PROFILES)
