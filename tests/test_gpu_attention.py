@@ -148,3 +148,18 @@ def test_attention_bagel_layer_full_size_sampled():
         want.append(g["out_pre"][r])
         got.append(f64(out)[r])
     assert_tolerance(np.array(got), np.array(want), "BAGEL layer attention, sampled rows")
+
+
+def test_attention_cfg_pack_whole_sequences():
+    # The CFG pack bench.py times: 12 sequences of 2048 causal prompt rows and 1024 latent rows
+    # (T = 36864), 28 query / 4 KV heads of 128, the same device-drawn Q/K/V; every output
+    # element of the first and the last sequence against the fp64 golden.
+    T, Hq, Hkv, D = 36864, 28, 4, 128
+    seqs = [(3072 * i, 3072 * i, 3072, 3072, 2048) for i in range(12)]
+    qkv = W.bf16_normal_device(9, 600, (T, (Hq + 2 * Hkv) * D), "cuda")
+    out, flags = _run(qkv, seqs, Hq, Hkv, D)
+    assert flags == 0
+    for i in (0, 11):
+        rows = slice(3072 * i, 3072 * (i + 1))
+        g = O.g_joint_attention(f64(qkv[rows]), [(0, 0, 3072, 3072, 2048)], Hq, Hkv, D)
+        assert_tolerance(f64(out[rows]), g["out_pre"], f"CFG pack attention, sequence {i} (all rows and heads)")
