@@ -13,8 +13,10 @@
 // Arithmetic, the same for every tile of every pack: S = Q K^T in fp32 on the tensor cores;
 // per row, in 128-key blocks in ascending key order, with c = scale * log2 e: the running
 // maximum m of S (masked keys excluded) moves to the block maximum only when that exceeds it
-// by more than 8 / c (then O and l are scaled by 2^((m_old - m) c)); p = 2^(S c - m c) (one
-// fused multiply-add and the SFU's exp2); l += the block's p (four interleaved partial sums);
+// by more than 8 / c (then O and l are scaled by 2^((m_old - m) c)); p = 2^(S c - m c) (the
+// product and the difference each rounded to fp32, then CUDA's accurate exp2f -- no fused
+// multiply-add, no approximate or flush-to-zero instruction, as the numerical contract
+// requires); l += the block's p (four interleaved partial sums);
 // O += bf16(p) V (fp32, tensor cores); out = bf16(O * (1 / l)), 1 / l rounded to fp32 once
 // per row. Blocks start at the sequence's first
 // key, so a row's bits do not depend on the other sequences of the pack.
@@ -75,12 +77,9 @@ struct Args {
   uint32_t* err;
 };
 
-// 2^x by the SFU instruction (relative error about 2^-22, subnormal results flushed to zero).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+// 2^x: CUDA's exp2f (the library's accurate function, with subnormal results; this code is
+// built without fast-math options).
+__device__ __forceinline__ float ex2(float x) { return exp2f(x); }
 
 // Packed pairs of fp32 (Blackwell f32x2 arithmetic: two IEEE operations per instruction, each
 // rounded as the scalar one would be).
@@ -92,10 +91,9 @@ __device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
 __device__ __forceinline__ void f2_unpack(unsigned long long v, float& a, float& b) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
 }
-__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
-                                                     unsigned long long c) {
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
   unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
@@ -432,7 +430,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      // p = 2^(S c - m c), four interleaved partial sums (key c adds to sum c mod 4), as f32x2
+      // p = 2^(fp32(S c) - m c), four interleaved partial sums (key c adds to sum c mod 4), as f32x2
       // pairs; every 8 keys go as bf16 to the 16-byte chunk (cc ^ (row & 7)) of the row in half
       // cc / 8 of the swizzled P tile
       const unsigned long long c2 = f2_pack(a.c, a.c), nmc2 = f2_pack(-mc, -mc);
@@ -444,7 +442,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int u = 0; u < 4; ++u) {
           const int c = 8 * cc + 2 * u;
           float t0, t1;
-          f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), c2, nmc2), t0, t1);
+          f2_unpack(f2_add(f2_mul(f2_pack(x[c], x[c + 1]), c2), nmc2), t0, t1);
           const float p0 = ex2(t0), p1 = ex2(t1);
           const unsigned long long p01 = f2_pack(p0, p1);
           if (u & 1) ps23 = f2_add(ps23, p01);
