@@ -35,10 +35,10 @@ struct Tile {
   int32_t row0;        // first row if the tile's rows are consecutive, else -1
 };
 
-__host__ __device__ inline int64_t max_m_tiles(int64_t T) { return (T + kTileRows - 1) / kTileRows + 1; }
-__host__ __device__ inline int64_t perm_offset() { return 64; }
-__host__ __device__ inline int64_t tiles_offset(int64_t T) { return 64 + ((4 * T + 15) / 16) * 16; }
-__host__ __device__ inline int64_t plan_bytes(int64_t T) { return tiles_offset(T) + 16 * max_m_tiles(T); }
+__host__ __device__ constexpr int64_t max_m_tiles(int64_t T) { return (T + kTileRows - 1) / kTileRows + 1; }
+__host__ __device__ constexpr int64_t perm_offset() { return 64; }
+__host__ __device__ constexpr int64_t tiles_offset(int64_t T) { return 64 + ((4 * T + 15) / 16) * 16; }
+__host__ __device__ constexpr int64_t plan_bytes(int64_t T) { return tiles_offset(T) + 16 * max_m_tiles(T); }
 
 // ---------------------------------------------------------------------------
 // bf16 with explicit round-to-nearest-even

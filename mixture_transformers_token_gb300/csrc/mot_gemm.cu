@@ -1092,7 +1092,10 @@ namespace mot {
 namespace noalloc {
 
 constexpr int64_t kMaxTokens = MOT_NOALLOC_MAX_TOKENS;
-constexpr size_t kScratchBytes = 64 + 4 * kMaxTokens + 16 * (kMaxTokens / kTileRows + 1);
+// the routing plan of kMaxTokens rows, laid out exactly as in a caller's workspace
+constexpr size_t kScratchBytes = size_t(plan_bytes(kMaxTokens));
+static_assert(kScratchBytes >= size_t(plan_bytes(kMaxTokens)), "the array must hold the largest plan");
+static_assert(kScratchBytes <= (size_t(1) << 20), "the array stays a modest fixed size");
 
 static __device__ __align__(256) uint8_t g_plan_scratch[kScratchBytes];
 

@@ -6,8 +6,10 @@ memory without lending them an allocator. They cannot pass the routing-plan work
 mot_routed_gemm needs, so mot_routed_gemm_noalloc keeps the plan in a fixed array inside the
 library. This test calls it through the C ABI twice in a row (different row counts, modality
 mixes and epilogues, so a stale plan left in the shared array by the first call would show in
-the second) and compares each result with mot_routed_gemm on a caller-owned workspace, within
-the tolerance the other GPU tests use.
+the second) and compares each result with mot_routed_gemm on a caller-owned workspace bit for
+bit: both build the same routing plan with the same kernel and run the same GEMM, so the only
+difference is where the plan lives. One more call fills the array to its limit of
+MOT_NOALLOC_MAX_TOKENS rows.
 
 The file name makes pytest collect it last, so a run that stops at the first failure has
 already run every other test; it needs nothing from them and also passes on its own.
@@ -20,7 +22,7 @@ import torch
 import mixture_transformers_token_gb300 as mot
 from mixture_transformers_token_gb300 import workloads as W
 
-from _util import assert_tolerance, f64, need_gpu
+from _util import assert_bitwise, f64, need_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -59,9 +61,25 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
     ref1 = mot.mot_routed_gemm(a1, w1, mot.mot_route_plan(m1), mot.EPI_CAST)
     ref2 = mot.mot_routed_gemm(a2, w2, mot.mot_route_plan(m2), mot.EPI_SWIGLU)
     torch.cuda.synchronize()
-    assert_tolerance(f64(got1), f64(ref1), "allocation-free call 1 vs mot_routed_gemm")
-    assert_tolerance(f64(got2), f64(ref2), "allocation-free call 2 vs mot_routed_gemm")
+    assert_bitwise(got1, ref1, "allocation-free call 1 vs mot_routed_gemm")
+    assert_bitwise(got2, ref2, "allocation-free call 2 vs mot_routed_gemm")
     assert np.isfinite(f64(got1)).all() and np.isfinite(f64(got2)).all()
+
+
+def test_noalloc_at_its_row_limit():
+    # the largest plan the array holds: MOT_NOALLOC_MAX_TOKENS rows, gen rows scattered so every
+    # tile record and the whole row list are written
+    need_gpu()
+    lib = mot.load_library()
+    dev = torch.device("cuda")
+    T = mot.NOALLOC_MAX_TOKENS
+    a = W.bf16_normal_device(33, 1, (T, 128), dev)
+    w = W.bf16_normal_device(33, 2, (2, 256, 128), dev, std=0.02)
+    m = W.modality_bernoulli(W.rng_for(33, 3), T, 0.25).to(dev)
+    got = _noalloc_through_c_abi(lib, a, w, m, mot.EPI_CAST, 256)
+    ref = mot.mot_routed_gemm(a, w, mot.mot_route_plan(m), mot.EPI_CAST)
+    torch.cuda.synchronize()
+    assert_bitwise(got, ref, "allocation-free call at MOT_NOALLOC_MAX_TOKENS rows vs mot_routed_gemm")
 
 
 def test_noalloc_rejects_rows_beyond_its_limit():
