@@ -48,7 +48,7 @@ def norm_bytes(t: int, h: int) -> int:
 
 # DRAM traffic of one QKV kernel launch from an ncu capture of this workload, keyed by the
 # hash of the kernel source it was taken on (null once the kernel has changed).
-NCU_TRAFFIC = {"7963e379ca9e9cbc": 127652864}   # profiles/routed_gemm_qkv128_bagel_layer_T4096.md
+NCU_TRAFFIC = {"7963e379ca9e9cbc": 127652864}
 
 
 def src_hash(name: str) -> str:
@@ -63,6 +63,15 @@ def peaks() -> dict:
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "of measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "of fallback"}
+
+
+def bench_config(world: int) -> dict:
+    """The workload both arms measure (the same dict on the reference arm's line)."""
+    return {"workload": WORKLOAD, "T": T, "hidden": H, "q_heads": HQ, "kv_heads": HKV, "head_dim": D,
+            "und_rows": 3072, "gen_rows": 1024,
+            "step": "fused add-RMSNorm (its launch also builds the routing plan) + routed QKV/QK-norm/RoPE",
+            "l2": "flushed before every timed step (write then read of 2x L2, outside the timed events)",
+            "parallelism": f"replicas x{world} (one pack per GPU, no collective)"}
 
 
 # ---------------------------------------------------------------------------
@@ -336,6 +345,9 @@ def run_ours(args, rank, world, local_rank):
                      "backward_T4096": run_backward(dev, flush),
                      "joint_attention": run_attention(dev, flush),
                      "flow_step": run_flow(dev, flush)}
+    if rank == 0 and secondary is not None and args.cpu_baseline and world == 1:
+        secondary["swiglu_mlp_T8192"]["cpu_baseline"] = cpu_baseline_secondary("mlp")
+        secondary["cfg_pack_T36864"]["cpu_baseline"] = cpu_baseline_secondary("cfg")
     if world > 1:
         dist.barrier()
     if rank != 0:
@@ -358,11 +370,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights of the BAGEL layer shape)",
-        "config": {"workload": WORKLOAD, "T": T, "hidden": H, "q_heads": HQ, "kv_heads": HKV, "head_dim": D,
-                   "und_rows": 3072, "gen_rows": 1024,
-                   "step": "fused add-RMSNorm (its launch also builds the routing plan) + routed QKV/QK-norm/RoPE",
-                   "l2": "flushed before every timed step (write then read of 2x L2, outside the timed events)",
-                   "parallelism": f"replicas x{world} (one pack per GPU, no collective)"},
+        "config": bench_config(world),
         "roofline": {"kernel": "routed_gemm_kernel<QKV128>", "bound": "tensor", "achieved": round(qkv_tflops, 2),
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(qkv_tflops / pk["bf16_tflops"], 4),
                      "peak_source": pk["source"] + " (bf16 dense, burst)", "traffic": NCU_TRAFFIC.get(h),
@@ -650,9 +658,10 @@ def run_attention(dev, flush) -> dict:
 
 def run_flow(dev, flush) -> dict:
     """One flow-sampler step of 16 requests of a 1024 x 1024 latent (64 x 64 tokens of 64
-    values, N = 262144 each): the per-sample transition noise, three-branch renormalised CFG of
-    bf16 velocities into fp32, then the SDE step (x, the guided velocity and the noise in; x_next
-    and logp out), every request at a different step of the 50-step schedule with shift 3."""
+    values, N = 262144 each): the per-sample transition noise, then three-branch renormalised
+    CFG of bf16 velocities and the SDE step (x and the noise in; x_next and logp out) in one
+    call, every request at a different step of the 50-step schedule with shift 3. The same
+    step as two calls (CFG into an fp32 velocity, then the SDE step) is timed beside it."""
     import numpy as np
     import torch
 
@@ -677,28 +686,38 @@ def run_flow(dev, flush) -> dict:
     logp = torch.empty((n_req,), dtype=torch.float32, device=dev)
     stages = [
         ("flow_noise", lambda: mot.mot_flow_noise(seeds, 7, n, z=z)),
+        ("cfg_sde_step", lambda: mot.mot_flow_cfg_sde_step(br["c"], br["tu"], br["iu"], policy, x, z, times, ws=ws,
+                                                           x_next=x_next, logp=logp)),
+    ]
+    r = time_stages(stages, 100, 5, flush, stream)
+    chain = [
         ("cfg_combine_renorm", lambda: mot.mot_cfg_combine_renorm(br["c"], br["tu"], br["iu"], policy, ws=ws, out=v)),
         ("flow_sde_step", lambda: mot.mot_flow_sde_step(x, v, z, times, ws=ws, x_next=x_next, logp=logp)),
     ]
-    r = time_stages(stages, 100, 5, flush, stream)
+    rc = time_stages(chain, 100, 5, flush, stream)
     if mot.mot_device_status(ws) != 0:
         raise RuntimeError("device error flags set in the flow workload")
     pk = peaks()
     e = n_req * n
+    b_fused = 18 * e + 36 * n_req         # three bf16 branches, x and z read, x_next written; policy, times, logp
     b_cfg = 10 * e + 24 * n_req           # three bf16 branches read, fp32 out written, policy
     b_sde = 16 * e + 12 * n_req           # x, v, z read, x_next written, times, logp
     return {
         "workload": f"flow_step_{n_req}x{n}",
         "flow_noise_us": round(r["flow_noise"] * 1e6, 2),
         "flow_noise_gdev_per_s": round(e / r["flow_noise"] / 1e9, 1),
-        "cfg_combine_renorm_us": round(r["cfg_combine_renorm"] * 1e6, 2),
-        "cfg_combine_renorm_gbs": round(b_cfg / r["cfg_combine_renorm"] / 1e9, 1),
-        "cfg_combine_renorm_frac_hbm": round(b_cfg / r["cfg_combine_renorm"] / 1e9 / pk["hbm_gbs"], 4),
-        "flow_sde_step_us": round(r["flow_sde_step"] * 1e6, 2),
-        "flow_sde_step_gbs": round(b_sde / r["flow_sde_step"] / 1e9, 1),
-        "flow_sde_step_frac_hbm": round(b_sde / r["flow_sde_step"] / 1e9 / pk["hbm_gbs"], 4),
-        "step_us": round(r["step"] * 1e6, 2), "elements": e, "bytes": {"cfg": b_cfg, "sde": b_sde},
-        "distribution_us": {k: r["dist"][k] for k in ("flow_noise", "cfg_combine_renorm", "flow_sde_step")},
+        "cfg_sde_step_us": round(r["cfg_sde_step"] * 1e6, 2),
+        "cfg_sde_step_gbs": round(b_fused / r["cfg_sde_step"] / 1e9, 1),
+        "cfg_sde_step_frac_hbm": round(b_fused / r["cfg_sde_step"] / 1e9 / pk["hbm_gbs"], 4),
+        "two_calls": {
+            "cfg_combine_renorm_us": round(rc["cfg_combine_renorm"] * 1e6, 2),
+            "cfg_combine_renorm_frac_hbm": round(b_cfg / rc["cfg_combine_renorm"] / 1e9 / pk["hbm_gbs"], 4),
+            "flow_sde_step_us": round(rc["flow_sde_step"] * 1e6, 2),
+            "flow_sde_step_frac_hbm": round(b_sde / rc["flow_sde_step"] / 1e9 / pk["hbm_gbs"], 4),
+            "sum_us": round((rc["cfg_combine_renorm"] + rc["flow_sde_step"]) * 1e6, 2)},
+        "step_us": round(r["step"] * 1e6, 2), "elements": e,
+        "bytes": {"cfg_sde_step": b_fused, "cfg": b_cfg, "sde": b_sde},
+        "distribution_us": {k: r["dist"][k] for k in ("flow_noise", "cfg_sde_step")},
     }
 
 
@@ -753,6 +772,10 @@ def run_cfg_pack(dev, flush) -> dict:
 # CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
 
+SINGLE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                     "BLIS_NUM_THREADS": "1", "VECLIB_MAXIMUM_THREADS": "1"}
+
+
 def oracle_layer_rows(rows, seed=1):
     """Inputs of the bench workload restricted to `rows`, as the oracle's float64 arrays."""
     import numpy as np
@@ -776,58 +799,144 @@ def oracle_step(shape, a):
                      HQ, HKV, D, shape.eps, shape.theta)
 
 
-def cpu_baseline_child(rows_n: int) -> None:
+def _host_sample_inputs(kind: str, rows_n: int):
+    """Host-drawn inputs of a secondary workload restricted to a uniform sample of rows (the
+    same shapes and distributions as the device-drawn ones; the rows are independent, so a
+    sample's cost scales to the whole pack). Returns (arrays, flops of the sample)."""
+    import numpy as np
+    import torch
+
+    from mixture_transformers_token_gb300 import workloads as W
+
+    def f(t):
+        return t.float().numpy().astype(np.float64)
+
+    if kind == "mlp":
+        t, h, i = W.MLP_T, W.MLP_H, W.MLP_I
+        rows = np.sort(np.random.default_rng(5).choice(t, rows_n, replace=False))
+        m = W.mlp_inputs(t, h, i, 2048, seed=3)
+        a = {"x": f(m["x"])[rows], "res": f(m["res"])[rows], "w_norm": f(m["w_norm"]), "w_gate": f(m["w_gate"]),
+             "w_up": f(m["w_up"]), "w_down": f(m["w_down"]), "mod": m["mod"].numpy()[rows]}
+        return a, rows_n * (2 * h * 2 * i + 2 * i * h)
+    s = W.CFG_PACK
+    mod, pos = W.cfg_pack_layout()
+    rows = np.sort(np.random.default_rng(5).choice(s.T, rows_n, replace=False))
+    inp = W.qkv_layer_inputs(W.QKVShape(T=rows_n, H=s.H, Hq=s.Hq, Hkv=s.Hkv, D=s.D), mod[rows], pos[rows], seed=5)
+    a = {k: f(v) for k, v in inp.items() if isinstance(v, torch.Tensor) and k not in ("mod", "pos")}
+    a["mod"], a["pos"] = mod.numpy()[rows], pos.numpy()[rows]
+    a["attn"] = f(W.bf16_normal(W.rng_for(5, 99), (rows_n, s.H)))
+    a["w_o"] = f(W.bf16_normal(W.rng_for(5, 98), (2, s.H, s.H), std=0.02))
+    return a, rows_n * (2 * s.H * s.n_qkv + 2 * s.H * s.H)
+
+
+def _oracle_secondary(kind: str, a) -> None:
+    from oracle import mot_oracle as O
+
+    from mixture_transformers_token_gb300 import workloads as W
+
+    if kind == "mlp":
+        n = O.g_fused_add_rmsnorm(a["x"], a["res"], a["w_norm"], a["mod"], 1e-6)
+        g = O.g_routed_swiglu(n["y"], a["w_gate"], a["w_up"], a["mod"])
+        O.g_routed_gemm_cast(g["h"], a["w_down"], a["mod"])
+        return
+    s = W.CFG_PACK
+    O.g_layer(a["x"], a["res"], a["w_norm"], a["w_qkv"], None, a["q_norm"], a["k_norm"], a["pos"], a["mod"], s.Hq,
+              s.Hkv, s.D, s.eps, s.theta)
+    O.g_routed_gemm_cast(a["attn"], a["w_o"], a["mod"])
+
+
+def cpu_baseline_child(kind: str, rows_n: int) -> None:
     import numpy as np
 
-    rows = np.sort(np.random.default_rng(5).choice(T, rows_n, replace=False))
-    shape, a = oracle_layer_rows(rows)
-    t0 = time.perf_counter()
-    oracle_step(shape, a)
-    dt = time.perf_counter() - t0
-    print(json.dumps({"seconds": dt, "rows": rows_n}))
+    if kind == "layer":
+        rows = np.sort(np.random.default_rng(5).choice(T, rows_n, replace=False))
+        shape, a = oracle_layer_rows(rows)
+        t0 = time.perf_counter()
+        oracle_step(shape, a)
+        dt = time.perf_counter() - t0
+        flops = QKV_FLOPS * rows_n / T
+    else:
+        a, flops = _host_sample_inputs(kind, rows_n)
+        t0 = time.perf_counter()
+        _oracle_secondary(kind, a)
+        dt = time.perf_counter() - t0
+    print(json.dumps({"seconds": dt, "rows": rows_n, "flops": flops}))
+
+
+def _run_child(argv: list, timeout: int = 900) -> dict:
+    env = dict(os.environ, **SINGLE_THREAD_ENV)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), *argv], env=env, capture_output=True, text=True,
+                       timeout=timeout)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-400:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def cpu_baseline(rows: int) -> dict:
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", str(rows)], env=env,
-                       capture_output=True, text=True, timeout=900)
-    if r.returncode != 0:
-        return {"value": None, "error": r.stderr[-400:]}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    flops = QKV_FLOPS * d["rows"] / T
-    return {"value": round(flops / d["seconds"] / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+    try:
+        d = _run_child(["--cpu-baseline-child", "layer", str(rows)])
+    except (RuntimeError, subprocess.SubprocessError) as e:
+        return {"value": None, "error": str(e)[-400:]}
+    return {"value": round(d["flops"] / d["seconds"] / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
             "host": host_cpu(),
             "sample": f"{d['rows']} of {T} rows of the same pack (fp64 golden: add-RMSNorm + routed QKV + QK-norm "
                       f"+ RoPE), {d['seconds']:.1f} s single-threaded; rows are independent, so the rate scales"}
 
 
-def run_reference(args, rank, world) -> dict | None:
-    if rank != 0:
-        return None
+def cpu_baseline_secondary(kind: str, rows: int = 256) -> dict:
+    """The fp64 golden of a secondary workload, single-threaded, on a uniform sample of `rows`
+    rows, as a rate (TFLOP/s of the workload's GEMMs): the rate of the whole pack extrapolated
+    from the sample."""
+    try:
+        d = _run_child(["--cpu-baseline-child", kind, str(rows)])
+    except (RuntimeError, subprocess.SubprocessError) as e:
+        return {"value": None, "error": str(e)[-400:]}
+    what = {"mlp": "add-RMSNorm + routed gate/up + SwiGLU + routed down, T=8192",
+            "cfg": "add-RMSNorm + routed QKV + QK-norm + RoPE + routed O, T=36864"}[kind]
+    return {"value": round(d["flops"] / d["seconds"] / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "extrapolated": True,
+            "sample": f"{d['rows']} uniformly sampled rows of the pack (fp64 golden: {what}; host-drawn inputs of the "
+                      f"same shapes), {d['seconds']:.1f} s single-threaded; scaled to the pack by rows"}
+
+
+def reference_child(steps: int, warmup: int, rows_per_step: int) -> None:
+    """The reference arm's timed loop, run in a child process with the thread count fixed by
+    its environment: every step evaluates the fp64 golden on its own random sample of rows."""
     import numpy as np
 
-    rows_per_step = int(max(1, min(64, 4096 // max(1, args.steps + args.warmup))))
     rng = np.random.default_rng(7)
     shape, full = oracle_layer_rows(np.arange(T))
     times = []
-    for i in range(args.warmup + args.steps):
+    for i in range(warmup + steps):
         rows = np.sort(rng.choice(T, rows_per_step, replace=False))
         a = dict(full, x=full["x"][rows], res=full["res"][rows], pos=full["pos"][rows], mod=full["mod"][rows])
         t0 = time.perf_counter()
         oracle_step(shape, a)
-        if i >= args.warmup:
+        if i >= warmup:
             times.append(time.perf_counter() - t0)
-    sec_per_row = sum(times) / (len(times) * rows_per_step)
-    value = QKV_FLOPS / (sec_per_row * T) / 1e12
-    threads = os.environ.get("OMP_NUM_THREADS") or os.environ.get("OPENBLAS_NUM_THREADS") or str(os.cpu_count())
+    print(json.dumps({"seconds": times}))
+
+
+def run_reference(args, rank, world) -> dict | None:
+    if rank != 0:
+        return None
+    rows_per_step = 64
+    d = _run_child(["--reference-child", str(args.steps), str(args.warmup), str(rows_per_step)],
+                   timeout=max(900, 20 * (args.steps + args.warmup)))
+    sec = statistics.fmean(d["seconds"])
+    flops = QKV_FLOPS * rows_per_step / T
+    value = flops / sec / 1e12
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec_per_row * T * 1e3, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "step": "oracle fp64 golden on a row sample, scaled to the full pack"},
-            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": int(threads) if threads.isdigit()
-                             else threads, "kind": "oracle", "host": host_cpu(),
-                             "sample": f"{rows_per_step} random rows of {T} per step, scaled to the pack"},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; random-init weights of the BAGEL layer shape)",
+            "config": bench_config(world),
+            "arm": "the CPU oracle (fp64 golden: add-RMSNorm + routed QKV + QK-norm + RoPE) on the host cores, "
+                   f"{rows_per_step} random rows of the pack per step; a step's time is the oracle's own time on "
+                   "those rows and the rate is their flops over it",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "host": host_cpu(), "threads_env": SINGLE_THREAD_ENV,
+                             "sample": f"{rows_per_step} random rows of {T} per step, single-threaded"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -845,10 +954,14 @@ def main():
     ap.add_argument("--profile", choices=["mlp", "cfg", "qkv_fp32", "backward", "attention", "flow"], default=None,
                     help="run only one secondary workload (mlp, cfg, backward: 5 warm-up + 50 timed steps; "
                          "qkv_fp32: 5 + 200) and print its figures; a short command for profiler captures")
-    ap.add_argument("--cpu-baseline-child", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-baseline-child", nargs=2, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--reference-child", nargs=3, type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_baseline_child is not None:
-        cpu_baseline_child(args.cpu_baseline_child)
+        cpu_baseline_child(args.cpu_baseline_child[0], int(args.cpu_baseline_child[1]))
+        return
+    if args.reference_child is not None:
+        reference_child(*args.reference_child)
         return
     if args.profile is not None:
         import torch

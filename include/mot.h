@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define MOT_ABI_VERSION 1
+#define MOT_ABI_VERSION 2
 
 /* host-detected status codes (return values) */
 #define MOT_OK            0
@@ -377,9 +377,10 @@ int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, void* ws, si
 int mot_flow_schedule_host(int n, double shift, float* host_t);
 
 /*
- * mot_flow_workspace_bytes -- workspace bytes that mot_cfg_combine_renorm and
- * mot_flow_sde_step need for n_req requests of N elements: the 64-byte header (its error word)
- * and 8 bytes per request and segment of 8192 elements. 0 for a geometry those calls reject.
+ * mot_flow_workspace_bytes -- workspace bytes that mot_cfg_combine_renorm, mot_flow_sde_step
+ * and mot_flow_cfg_sde_step need for n_req requests of N elements: the 64-byte header (its error
+ * word), 8 bytes per request and segment of 8192 elements (rounded up to 16 bytes), and 4 more
+ * per request and segment (rounded up to 16 bytes). 0 for a geometry those calls reject.
  */
 size_t mot_flow_workspace_bytes(int n_req, int64_t N);
 
@@ -434,6 +435,25 @@ int mot_cfg_combine_renorm(const mot_bf16* v_c, const mot_bf16* v_tu, const mot_
  */
 int mot_flow_sde_step(const float* x, const float* v, const float* z, float* x_next, int n_req, int64_t N,
                       const float* times, void* ws, size_t ws_bytes, float* logp, void* stream);
+
+/*
+ * mot_flow_cfg_sde_step -- mot_cfg_combine_renorm followed by mot_flow_sde_step on its output,
+ * in one call that does not write the guided velocity to memory and read it back ([RFC-435] §1
+ * Motivation items 2 and 3; §3 BAGEL-specific rules as for the two calls: window on FP32 t,
+ * renorm per request, SDE and logp in FP32 in a fixed order).
+ *   v_c, v_tu, v_iu, policy   as for mot_cfg_combine_renorm (v_iu may be NULL).
+ *   x, z, x_next, times       as for mot_flow_sde_step (z NULL: x_next is scored, not sampled).
+ *   ws       at least mot_flow_workspace_bytes(n_req, N) bytes, scratch after the first 64; its
+ *            error word receives MOT_DEV_BAD_TIME as for mot_flow_sde_step.
+ *   v_out    [n_req][N] fp32  out: the guided velocity, or NULL not to write it.
+ *   logp     device fp32 [n_req]  out.
+ * x_next, logp and v_out are bit for bit those of the two calls in sequence on the same inputs
+ * (the same trees, the same order of every fp32 operation). Geometry and alignment as for the
+ * two calls; every pointer 16-byte aligned device memory of the stream's device.
+ */
+int mot_flow_cfg_sde_step(const mot_bf16* v_c, const mot_bf16* v_tu, const mot_bf16* v_iu, const float* policy,
+                          const float* x, const float* z, float* x_next, int n_req, int64_t N, const float* times,
+                          void* ws, size_t ws_bytes, float* v_out, float* logp, void* stream);
 
 /*
  * mot_flow_noise -- the per-sample standard normal noise of one sampler step ([RFC-435] §3

@@ -28,10 +28,10 @@ __all__ = [
     "mot_rmsnorm_dweight", "mot_routed_gemm_dx", "mot_routed_gemm_dw", "mot_joint_attention", "DEV_BAD_SEQUENCE",
     "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows", "mot_selftest_wait_timeout",
     "DEV_BAD_TIME", "mot_flow_workspace_bytes", "mot_flow_schedule_host", "mot_cfg_combine_renorm",
-    "mot_flow_sde_step", "mot_flow_noise",
+    "mot_flow_sde_step", "mot_flow_cfg_sde_step", "mot_flow_noise",
 ]
 
-ABI_VERSION = 1
+ABI_VERSION = 2
 EPI_CAST = 0
 EPI_SWIGLU = 1
 A_PLAN_ORDER = 0x100
@@ -80,6 +80,8 @@ _SIGNATURES = {
     "mot_flow_schedule_host": (_c_i, [_c_i, ctypes.c_double, _c_p]),
     "mot_cfg_combine_renorm": (_c_i, [_c_p, _c_p, _c_p, _c_i, _c_i64, _c_p, _c_p, _c_sz, _c_p, _c_p]),
     "mot_flow_sde_step": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_i, _c_i64, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_flow_cfg_sde_step": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i, _c_i64, _c_p, _c_p, _c_sz,
+                                     _c_p, _c_p, _c_p]),
     "mot_flow_noise": (_c_i, [_c_p, ctypes.c_uint64, _c_i, _c_i64, _c_p, _c_p]),
     "mot_device_status": (_c_i, [_c_p, ctypes.POINTER(ctypes.c_uint32), _c_p]),
 }
@@ -519,6 +521,56 @@ def mot_flow_sde_step(x, v, z, times, ws=None, x_next=None, logp=None, stream=No
     _check("mot_flow_sde_step", _lib().mot_flow_sde_step(
         x.data_ptr(), v.data_ptr(), zp, x_next.data_ptr(), n_req, N, times.data_ptr(), ws.data_ptr(), ws.numel(),
         logp.data_ptr(), _stream(x, stream)))
+    return x_next, logp
+
+
+def mot_flow_cfg_sde_step(v_c, v_tu, v_iu, policy, x, z, times, ws=None, x_next=None, v_out=None, logp=None,
+                          stream=None):
+    """CFG combine + renorm and the SDE step in one call, without writing the guided velocity:
+    the branches and policy as for mot_cfg_combine_renorm, x, z, times as for mot_flow_sde_step
+    (z None: x_next is given and scored). v_out, if given ([n_req][N] fp32), receives the guided
+    velocity. Returns (x_next, logp), bit for bit those of the two calls in sequence."""
+    n_req, N = v_c.shape
+    _dev(v_c, "v_c", torch.bfloat16, 2)
+    _dev(v_tu, "v_tu", torch.bfloat16, 2)
+    ip = None
+    if v_iu is not None:
+        _dev(v_iu, "v_iu", torch.bfloat16, 2)
+        ip = v_iu.data_ptr()
+    _dev(policy, "policy", torch.float32, 2)
+    _dev(x, "x", torch.float32, 2)
+    _dev(times, "times", torch.float32, 2)
+    if tuple(v_tu.shape) != (n_req, N) or (v_iu is not None and tuple(v_iu.shape) != (n_req, N)) \
+            or tuple(x.shape) != (n_req, N):
+        raise ValueError("the branches and x must all be [n_req, N]")
+    if tuple(policy.shape) != (n_req, 6) or tuple(times.shape) != (n_req, 2):
+        raise ValueError("policy must be [n_req, 6] and times [n_req, 2]")
+    zp = None
+    if z is not None:
+        _dev(z, "z", torch.float32, 2)
+        if tuple(z.shape) != (n_req, N):
+            raise ValueError("z must be [n_req, N]")
+        zp = z.data_ptr()
+    elif x_next is None:
+        raise ValueError("either z or x_next must be given")
+    ws = _flow_ws(ws, n_req, N, x.device)
+    if x_next is None:
+        x_next = torch.empty((n_req, N), dtype=torch.float32, device=x.device)
+    _dev(x_next, "x_next", torch.float32, 2)
+    if tuple(x_next.shape) != (n_req, N):
+        raise ValueError("x_next must be [n_req, N]")
+    vp = None
+    if v_out is not None:
+        _dev(v_out, "v_out", torch.float32, 2)
+        if tuple(v_out.shape) != (n_req, N):
+            raise ValueError("v_out must be [n_req, N]")
+        vp = v_out.data_ptr()
+    if logp is None:
+        logp = torch.empty((n_req,), dtype=torch.float32, device=x.device)
+    _dev(logp, "logp", torch.float32, 1)
+    _check("mot_flow_cfg_sde_step", _lib().mot_flow_cfg_sde_step(
+        v_c.data_ptr(), v_tu.data_ptr(), ip, policy.data_ptr(), x.data_ptr(), zp, x_next.data_ptr(), n_req, N,
+        times.data_ptr(), ws.data_ptr(), ws.numel(), vp, logp.data_ptr(), _stream(x, stream)))
     return x_next, logp
 
 

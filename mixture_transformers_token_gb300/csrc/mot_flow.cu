@@ -23,7 +23,9 @@
 // batch. Every operation is rounded on its own in fp32 (no fused multiply-add).
 //
 // CFG reads its inputs twice (once for the sums, once to scale), the second time mostly from
-// L2; the SDE step reads them once and a small kernel folds each request's segment sums.
+// L2; the SDE step reads them once and a small kernel folds each request's segment sums. The
+// fused CFG + SDE step applies the CFG's rescale inside the SDE step's element pass, so the
+// guided velocity never goes to memory and back.
 
 #include <cuda_runtime.h>
 
@@ -48,9 +50,13 @@ constexpr float kLogSqrt2Pi = 0.918938533204672742f;  // log(2 pi) / 2
 __host__ __device__ constexpr int segments(int64_t N) { return int((N + SEG - 1) / SEG); }
 
 // Workspace: the 64-byte header (error word), then 8 bytes per (request, segment): the CFG's
-// (sum c c, sum v2 v2), or the SDE step's sum d d.
+// (sum c c, sum v2 v2), or the SDE step's sum d d; then 4 bytes per (request, segment), where
+// the fused CFG + SDE step keeps its sums of d d while the CFG's are still being read.
+inline size_t cfg_region_bytes(int n_req, int64_t N) {
+  return (size_t(n_req) * size_t(segments(N)) * 8 + 15) & ~size_t(15);
+}
 inline size_t workspace_bytes(int n_req, int64_t N) {
-  return sizeof(PlanHeader) + ((size_t(n_req) * size_t(segments(N)) * 8 + 15) & ~size_t(15));
+  return sizeof(PlanHeader) + cfg_region_bytes(n_req, N) + ((size_t(n_req) * size_t(segments(N)) * 4 + 15) & ~size_t(15));
 }
 
 // The CTA's sum of the per-thread partials p: butterfly inside each warp, then the warps left
@@ -222,6 +228,7 @@ __global__ void __launch_bounds__(THREADS, 4) cfg_partials_kernel(const CfgArgs 
     const int64_t base = int64_t(req) * a.N + int64_t(seg) * SEG;
     const int nch = int(min(int64_t(SEG), a.N - int64_t(seg) * SEG) / 8);
     if (!pol.guided()) {
+      if (a.out == nullptr) continue;  // the fused step reads c itself
 #pragma unroll
       for (int j = 0; j < CPT; ++j) {
         const int q = int(threadIdx.x) + THREADS * j;
@@ -291,6 +298,7 @@ __global__ void __launch_bounds__(THREADS, 4) cfg_scale_kernel(const CfgArgs a, 
     }
     __syncthreads();  // r_s is rewritten for the next unit
   }
+  if (!waited) pdl_wait();  // this grid completes only after pass 1 has
 }
 
 struct SdeArgs {
@@ -356,6 +364,108 @@ __global__ void __launch_bounds__(THREADS, 4) sde_step_kernel(const SdeArgs a, c
     const float ss = cta_sum(p, wsum);
     if (threadIdx.x == 0) a.part[u] = ss;
   }
+}
+
+// The fused CFG + SDE step, launched as a dependent of the CFG's pass 1 (cfg_partials_kernel
+// without a copy): per (request, segment) unit it loads the branches, x and z (inputs complete
+// before pass 1 started), waits for pass 1 once, folds the request's CFG sums (the same order
+// as cfg_scale_kernel, so the same r), forms v = v2 r (c outside the window) in registers and
+// runs the SDE step's arithmetic on it, exactly as sde_step_kernel would on the v that the
+// two-call chain writes. Its sums of d d go to their own region (sp).
+__global__ void __launch_bounds__(THREADS, 2) cfg_sde_kernel(const CfgArgs c, const SdeArgs a, float* v_out,
+                                                             const int64_t units) {
+  __shared__ float wsum[THREADS / 32];
+  __shared__ float r_s;
+  bool waited = false;
+  pdl_trigger();  // the logp fold may start
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int req = int(u / a.S), seg = int(u % a.S);
+    const float t = a.times[2 * req], tn = a.times[2 * req + 1];
+    if (!times_ok(t, tn)) {
+      if (threadIdx.x == 0 && seg == 0) atomicOr(a.err, MOT_DEV_BAD_TIME);
+      continue;  // uniform across the CTA
+    }
+    const CfgPolicy pol = load_policy(c.policy + 6 * req);
+    const bool guided = pol.guided();
+    const int64_t base = int64_t(req) * a.N + int64_t(seg) * SEG;
+    const int nch = int(min(int64_t(SEG), a.N - int64_t(seg) * SEG) / 8);
+    const float* third = a.z ? a.z : a.x_next;
+    CfgChunks k;
+    if (guided) {
+      cfg_load(c, base, nch, k);
+    } else {
+      k.n = 0;
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) {
+        const int q = int(threadIdx.x) + THREADS * j;
+        if (q < nch) {
+          k.n = j + 1;
+          k.c[j] = __ldg(reinterpret_cast<const uint4*>(c.c + base + 8 * q));
+        }
+      }
+    }
+    F8 xs[CPT], ws3[CPT];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      if (j < k.n) {
+        const int q = int(threadIdx.x) + THREADS * j;
+        xs[j] = load8_f32(a.x + base + 8 * q, a.w32);
+        ws3[j] = load8_f32(third + base + 8 * q, a.w32);
+      }
+    }
+    float r = 1.0f;
+    if (guided) {
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
+      if (threadIdx.x < 32) {
+        const float rr = cfg_ratio(warp_fold2(c.part + int64_t(req) * a.S, a.S), pol.rmin);
+        if (threadIdx.x == 0) r_s = rr;
+      }
+      __syncthreads();
+      r = r_s;
+    }
+    const float dt = __fsub_rn(t, tn);
+    const float sigma = t;
+    const float kk = __fdiv_rn(__fmul_rn(sigma, sigma), __fmul_rn(2.0f, t));
+    const float omt = __fsub_rn(1.0f, t);
+    const float sd = __fmul_rn(sigma, __fsqrt_rn(dt));
+    float p = 0.0f;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      if (j < k.n) {
+        const int q = int(threadIdx.x) + THREADS * j;
+        float v[8], x[8], w[8], mu[8], xn[8];
+        if (guided) {
+          float cc[8];
+          cfg_guide(c, pol, k, j, cc, v);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], r);
+        } else {
+          unpack8_bf16(k.c[j], v);
+        }
+        if (v_out) store8_f32(v_out + base + 8 * q, v, c.w32);
+        unpack8_f32(xs[j], x);
+        unpack8_f32(ws3[j], w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float e = __fadd_rn(x[i], __fmul_rn(omt, v[i]));
+          mu[i] = __fsub_rn(x[i], __fmul_rn(dt, __fadd_rn(v[i], __fmul_rn(kk, e))));
+          xn[i] = a.z ? __fadd_rn(mu[i], __fmul_rn(sd, w[i])) : w[i];
+        }
+        if (a.z) store8_f32(a.x_next + base + 8 * q, xn, a.w32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float d = __fsub_rn(xn[i], mu[i]);
+          p = __fadd_rn(p, __fmul_rn(d, d));
+        }
+      }
+    }
+    const float ss = cta_sum(p, wsum);  // its barriers also order r_s's reads before the next write
+    if (threadIdx.x == 0) a.part[u] = ss;
+  }
+  if (!waited) pdl_wait();  // this grid completes only after pass 1 has
 }
 
 // logp = -(ss / (2 (std std))) - N (log(std) + log sqrt(2 pi)) with std = t sqrt(t - t_next).
@@ -510,6 +620,45 @@ extern "C" int mot_flow_sde_step(const float* x, const float* v, const float* z,
   flow::sde_step_kernel<<<grid, flow::THREADS, 0, s>>>(a, units);
   if (cudaGetLastError() != cudaSuccess) return MOT_ERR_CUDA;
   if (launch_dependent(flow::sde_logp_kernel, dim3((n_req + 3) / 4), dim3(128), 0, s, a) != cudaSuccess)
+    return MOT_ERR_CUDA;
+  return MOT_OK;
+}
+
+extern "C" int mot_flow_cfg_sde_step(const mot_bf16* v_c, const mot_bf16* v_tu, const mot_bf16* v_iu,
+                                     const float* policy, const float* x, const float* z, float* x_next, int n_req,
+                                     int64_t N, const float* times, void* ws, size_t ws_bytes, float* v_out,
+                                     float* logp, void* stream) {
+  if (!v_c || !v_tu || !policy || !x || !x_next || !times || !ws || !logp) return MOT_ERR_NULL;
+  if (n_req < 1 || n_req > flow::kMaxReq || N < 8 || N % 8 != 0 || N > flow::kMaxN) return MOT_ERR_GEOMETRY;
+  if (!aligned16(v_c) || !aligned16(v_tu) || (v_iu && !aligned16(v_iu)) || !aligned16(policy) || !aligned16(x) ||
+      (z && !aligned16(z)) || !aligned16(x_next) || !aligned16(times) || !aligned16(ws) || (v_out && !aligned16(v_out)) ||
+      !aligned16(logp))
+    return MOT_ERR_ALIGN;
+  if (ws_bytes < flow::workspace_bytes(n_req, N)) return MOT_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[] = {v_c, v_tu, v_iu, policy, x, z, x_next, times, ws, v_out, logp};
+  int dev = -1;
+  int st = check_device(s, ptrs, 11, &dev);
+  if (st != MOT_OK) return st;
+  DeviceGuard guard(dev);
+  const int S = flow::segments(N);
+  char* scratch = static_cast<char*>(ws) + sizeof(PlanHeader);
+  flow::CfgArgs ca{v_c, v_tu, v_iu, policy, N, S, reinterpret_cast<float2*>(scratch), nullptr,
+                   v_out != nullptr && reinterpret_cast<uintptr_t>(v_out) % 32 == 0 ? 1 : 0};
+  const bool w32 = reinterpret_cast<uintptr_t>(x) % 32 == 0 && reinterpret_cast<uintptr_t>(z) % 32 == 0 &&
+                   reinterpret_cast<uintptr_t>(x_next) % 32 == 0;
+  flow::SdeArgs sa{x, nullptr, z, x_next, times, N, S, n_req,
+                   reinterpret_cast<float*>(scratch + flow::cfg_region_bytes(n_req, N)), logp,
+                   &static_cast<PlanHeader*>(ws)->error, w32 ? 1 : 0};
+  const int64_t units = int64_t(n_req) * S;
+  const unsigned grid1 = unsigned(std::min<int64_t>(units, int64_t(flow::kCtasPerSm) * sm_count(dev)));
+  const unsigned grid2 = unsigned(std::min<int64_t>(units, int64_t(2) * sm_count(dev)));
+  flow::cfg_partials_kernel<<<grid1, flow::THREADS, 0, s>>>(ca, units);
+  if (cudaGetLastError() != cudaSuccess) return MOT_ERR_CUDA;
+  if (launch_dependent(flow::cfg_sde_kernel, dim3(grid2), dim3(flow::THREADS), 0, s, ca, sa, v_out, units) !=
+      cudaSuccess)
+    return MOT_ERR_CUDA;
+  if (launch_dependent(flow::sde_logp_kernel, dim3((n_req + 3) / 4), dim3(128), 0, s, sa) != cudaSuccess)
     return MOT_ERR_CUDA;
   return MOT_OK;
 }

@@ -286,11 +286,12 @@ def test_flow_workspace_bytes(lib):
     f = lib.mot_flow_workspace_bytes
     assert f(0, 64) == 0 and f(1, 12) == 0 and f(1, 0) == 0 and f(65536, 64) == 0
     assert f(1, (1 << 24) + 8) == 0
-    # header + 8 bytes per request and 8192-element segment, rounded to 16
-    assert f(1, 8) == 64 + 16
-    assert f(3, 8192) == 64 + 32
-    assert f(3, 8200) == 64 + 48
-    assert f(16, 262144) == 64 + 16 * 32 * 8
+    # header + 8 bytes per request and 8192-element segment, rounded to 16, + 4 bytes per
+    # request and segment, rounded to 16
+    assert f(1, 8) == 64 + 16 + 16
+    assert f(3, 8192) == 64 + 32 + 16
+    assert f(3, 8200) == 64 + 48 + 32
+    assert f(16, 262144) == 64 + 16 * 32 * 8 + 16 * 32 * 4
 
 
 def test_flow_schedule_matches_oracle():
@@ -328,6 +329,29 @@ def test_flow_sde_step_rejects(lib):
     assert f(A, A, A, C, 2, 4, A, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
     assert f(A, A, MIS, C, 2, 64, A, B, 1 << 20, C, None) == MOT_ERR_ALIGN
     assert f(A, A, None, C, 2, 64, A, B, 64, C, None) == MOT_ERR_WORKSPACE
+
+
+def test_flow_cfg_sde_step_rejects(lib):
+    f = lib.mot_flow_cfg_sde_step
+    ok = (A, A, A, A, A, A, C, 2, 64, A, B, 1 << 20, C, C, None)
+
+    def with_(i, v):
+        a = list(ok)
+        a[i] = v
+        return f(*a)
+
+    for i in (0, 1, 3, 4, 6, 9, 10, 13):       # v_c, v_tu, policy, x, x_next, times, ws, logp
+        assert with_(i, None) == MOT_ERR_NULL, i
+    assert with_(7, 0) == MOT_ERR_GEOMETRY
+    assert with_(8, 60) == MOT_ERR_GEOMETRY
+    assert with_(8, (1 << 24) + 8) == MOT_ERR_GEOMETRY
+    assert with_(2, MIS) == MOT_ERR_ALIGN       # v_iu
+    assert with_(5, MIS) == MOT_ERR_ALIGN       # z
+    assert with_(12, MIS) == MOT_ERR_ALIGN      # v_out
+    assert with_(11, 64) == MOT_ERR_WORKSPACE
+    a = list(ok)
+    a[2] = a[5] = a[12] = None                  # two branches, scoring, no v_out: still only a device error
+    assert f(*a) not in (MOT_ERR_NULL, MOT_ERR_GEOMETRY, MOT_ERR_ALIGN, MOT_ERR_WORKSPACE, 0)
 
 
 def test_flow_noise_rejects(lib):

@@ -328,3 +328,99 @@ def test_cfg_and_sde_with_16_byte_aligned_tensors_give_the_same_bits():
     assert mot.mot_device_status(ws2) == 0
     np.testing.assert_array_equal(xn16.cpu().numpy().view(np.uint32), xn.view(np.uint32))
     np.testing.assert_array_equal(lp16.cpu().numpy().view(np.uint32), lp.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# CFG combine + renorm and the SDE step in one call
+# ---------------------------------------------------------------------------
+
+def _fused_inputs(N, seed, three=True):
+    b, pol = _cfg_case(len(POLICIES), N, seed=seed)
+    st = W.flow_state(W.rng_for(seed, 720), len(POLICIES), N)
+    times = np.array([(p[0], p[0] - F32(0.05)) for p in pol], dtype=F32)   # t_i is the policy's t
+    d = {k: v.cuda() for k, v in b.items()}
+    d.update({k: v.cuda() for k, v in st.items() if k != "v"})
+    return d, torch.from_numpy(pol).cuda(), torch.from_numpy(times).cuda()
+
+
+def _chain(d, pol, times, three=True):
+    n_req, N = d["c"].shape
+    ws = torch.zeros(mot.mot_flow_workspace_bytes(n_req, N), dtype=torch.uint8, device="cuda")
+    v = mot.mot_cfg_combine_renorm(d["c"], d["tu"], d["iu"] if three else None, pol, ws=ws)
+    xn, lp = mot.mot_flow_sde_step(d["x"], v, d["z"], times, ws=ws)
+    assert mot.mot_device_status(ws) == 0
+    return v, xn, lp
+
+
+@pytest.mark.parametrize("N", [8, 2056, 3 * 8192 + 40, 32 * 8192 + 8])
+@pytest.mark.parametrize("three", [True, False])
+def test_fused_cfg_sde_equals_the_two_calls(N, three):
+    # the guided velocity, x_next and logp bit for bit those of mot_cfg_combine_renorm followed by
+    # mot_flow_sde_step: guided and unguided requests, the window edge, the clamp, zero branches
+    d, pol, times = _fused_inputs(N, N + 3 * three, three)
+    v, xn, lp = _chain(d, pol, times, three)
+    n_req = d["c"].shape[0]
+    ws = torch.zeros(mot.mot_flow_workspace_bytes(n_req, N), dtype=torch.uint8, device="cuda")
+    v2 = torch.empty_like(v)
+    xn2, lp2 = mot.mot_flow_cfg_sde_step(d["c"], d["tu"], d["iu"] if three else None, pol, d["x"], d["z"], times,
+                                         ws=ws, v_out=v2)
+    assert mot.mot_device_status(ws) == 0
+    assert_f32_bitwise(v2, v, "fused guided velocity vs the CFG call")
+    assert_f32_bitwise(xn2, xn, "fused x_next vs the two calls")
+    assert_f32_bitwise(lp2, lp, "fused logp vs the two calls")
+    # without v_out, and scoring the sampled latent: the same logp
+    xn3, lp3 = mot.mot_flow_cfg_sde_step(d["c"], d["tu"], d["iu"] if three else None, pol, d["x"], None, times,
+                                         ws=ws, x_next=xn2.clone())
+    assert mot.mot_device_status(ws) == 0
+    assert_f32_bitwise(lp3, lp, "fused scoring of the sampled latent")
+    # and against the oracle's fp32 restatement for one guided request
+    e_v = _cfg_oracle({k: t.cpu() for k, t in d.items() if k in ("c", "tu", "iu")}, pol.cpu().numpy(), 0, three)
+    assert_f32_bitwise(v2[0].cpu().numpy(), e_v, "fused guided velocity vs E")
+
+
+def test_fused_cfg_sde_bad_times_fail_closed():
+    N = 64
+    d, pol, _ = _fused_inputs(N, 5)
+    times = torch.tensor([(0.5, 0.6), (0.3, 0.3), (0.4, -0.1), (1.5, 0.9), (0.7, 0.6), (1.0, 0.95)],
+                         dtype=torch.float32, device="cuda")
+    ws = torch.zeros(mot.mot_flow_workspace_bytes(6, N), dtype=torch.uint8, device="cuda")
+    xn = torch.full((6, N), 7.0, device="cuda")
+    lp = torch.full((6,), 7.0, device="cuda")
+    vo = torch.full((6, N), 7.0, device="cuda")
+    mot.mot_flow_cfg_sde_step(d["c"], d["tu"], d["iu"], pol, d["x"], d["z"], times, ws=ws, x_next=xn, v_out=vo,
+                              logp=lp)
+    assert mot.mot_device_status(ws) == mot.DEV_BAD_TIME
+    assert torch.all(xn[:4] == 7.0) and torch.all(lp[:4] == 7.0) and torch.all(vo[:4] == 7.0)
+    v, xc, lc = _chain({k: t[4:] for k, t in d.items()}, pol[4:], times[4:])
+    assert_f32_bitwise(xn[4:], xc, "valid requests beside bad ones: x_next")
+    assert_f32_bitwise(lp[4:], lc, "valid requests beside bad ones: logp")
+    assert_f32_bitwise(vo[4:], v, "valid requests beside bad ones: v")
+
+
+def test_fused_cfg_sde_full_size_and_16_byte_alignment():
+    # the bench leg: 16 requests of a 1024 x 1024 latent, each at its own step of the 50-step,
+    # shift-3 schedule; the same bits as the two calls, and with 16-byte-aligned fp32 tensors
+    n_req, N = W.FLOW_REQUESTS, W.FLOW_N_1024
+    b = W.flow_branches(W.rng_for(30, 730), n_req, N)
+    st = W.flow_state(W.rng_for(30, 731), n_req, N)
+    p = W.FLOW_POLICY
+    steps = [3 * i for i in range(n_req)]
+    pol = torch.tensor([(float(SCHED[i]), p["s_text"], p["s_img"], p["t_lo"], p["t_hi"], p["renorm_min"])
+                        for i in steps], dtype=torch.float32, device="cuda")
+    times = torch.tensor(np.array([(SCHED[i], SCHED[i + 1]) for i in steps], dtype=F32), device="cuda")
+    d = {k: v.cuda() for k, v in b.items()}
+    d.update({k: v.cuda() for k, v in st.items() if k != "v"})
+    v, xn, lp = _chain(d, pol, times)
+    ws = torch.zeros(mot.mot_flow_workspace_bytes(n_req, N), dtype=torch.uint8, device="cuda")
+    xn2, lp2 = mot.mot_flow_cfg_sde_step(d["c"], d["tu"], d["iu"], pol, d["x"], d["z"], times, ws=ws)
+    assert mot.mot_device_status(ws) == 0
+    assert_f32_bitwise(xn2, xn, "full-size fused x_next")
+    assert_f32_bitwise(lp2, lp, "full-size fused logp")
+    xn16 = _at_16_bytes(torch.zeros((n_req, N)))
+    v16 = _at_16_bytes(torch.zeros((n_req, N)))
+    _, lp16 = mot.mot_flow_cfg_sde_step(d["c"], d["tu"], d["iu"], pol, _at_16_bytes(d["x"]), _at_16_bytes(d["z"]),
+                                        times, ws=ws, x_next=xn16, v_out=v16)
+    assert mot.mot_device_status(ws) == 0
+    assert_f32_bitwise(xn16, xn, "16-byte-aligned fused x_next")
+    assert_f32_bitwise(lp16, lp, "16-byte-aligned fused logp")
+    assert_f32_bitwise(v16, v, "16-byte-aligned fused v")
