@@ -399,30 +399,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t rank = cluster_rank();
   // Launched as a programmatic dependent: the grid may be resident before the preceding kernel
   // (typically the norm that writes A and the plan) has finished. Nothing in global memory is
-  // touched before pdl_wait; the tensor maps are kernel parameters.
+  // touched before pdl_wait; the tensor maps are kernel parameters. The barriers and tensor
+  // memory are set up while the preceding kernel drains.
   pdl_trigger();
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_a_rows);
     tma_prefetch_desc(&tm_w);
-  }
-  pdl_wait();
-  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(args.ws);
-  const int num_m = hdr->num_m_tiles;
-  const int nt0 = (hdr->count[0] + kTileRows - 1) / kTileRows;
-  const int nt1 = (hdr->count[1] + kTileRows - 1) / kTileRows;
-  if (hdr->magic != kPlanMagic || hdr->T != args.T || num_m < 0 || num_m > max_m_tiles(args.T) ||
-      num_m != nt0 + nt1) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.err, MOT_DEV_PLAN_MISMATCH);
-    return;  // uniform across the grid
-  }
-  const int P0 = (nt0 + 1) / 2, P = P0 + (nt1 + 1) / 2;
-  const int total = P * args.n_tiles;
-  const int band = P > 0 ? band_pairs(P, args.K) : 1;
-  const int cluster = int(blockIdx.x >> 1), nclusters = int(gridDim.x >> 1);
-  if (cluster >= total) return;  // uniform across the pair
-
-  if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
@@ -443,6 +426,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();  // both CTAs' barriers are initialized before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(args.ws);
+  const int num_m = hdr->num_m_tiles;
+  const int nt0 = (hdr->count[0] + kTileRows - 1) / kTileRows;
+  const int nt1 = (hdr->count[1] + kTileRows - 1) / kTileRows;
+  const bool plan_ok = hdr->magic == kPlanMagic && hdr->T == args.T && num_m >= 0 && num_m <= max_m_tiles(args.T) &&
+                       num_m == nt0 + nt1;
+  if (!plan_ok && threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.err, MOT_DEV_PLAN_MISMATCH);
+  const int P0 = (nt0 + 1) / 2, P = P0 + (nt1 + 1) / 2;
+  // a bad plan (uniform across the grid) leaves no work; the pair still frees its tensor memory
+  const int total = plan_ok ? P * args.n_tiles : 0;
+  const int band = P > 0 ? band_pairs(P, args.K) : 1;
+  const int cluster = int(blockIdx.x >> 1), nclusters = int(gridDim.x >> 1);
 
   const Tile* tiles = reinterpret_cast<const Tile*>(args.ws + tiles_offset(args.T));
   const int32_t* perm = reinterpret_cast<const int32_t*>(args.ws + perm_offset());
