@@ -61,12 +61,33 @@ __device__ __forceinline__ float warp_tree(float p) {
   return p;
 }
 
+// Elements 2t and 2t + 1 of eight bf16 values, as fp32.
+__device__ __forceinline__ float2 f2_of(const uint4& v, int t) {
+  const uint32_t wd = t == 0 ? v.x : (t == 1 ? v.y : (t == 2 ? v.z : v.w));
+  return make_float2(bf_lo(wd), bf_hi(wd));
+}
+
+// Two IEEE fp32 multiplies per instruction, each rounded as the scalar one would be; used only
+// where the products feed further multiplies or scalar additions. The pairs move between
+// float2 and the 64-bit register pair by mov.b64.
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  unsigned long long pa, pb, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pa), "l"(pb));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+  return r;
+}
+
 // One CTA per SM, persistent over the plan positions b + k G (b = blockIdx.x), so the
 // weight-gradient partials of each weight set come out as one contiguous run. Warp 0 streams
 // the whole rows of s, dy (and d_res_out) of those positions into C shared-memory slots with
-// 1D bulk copies; consumer warp c owns slot c and takes every C-th position of the CTA. A consumer keeps the row's s in registers
-// after the first pass, reads dy, the weights and d_res_out from shared memory, writes dx
-// and rstd, and hands the slot back after the last pass.
+// 1D bulk copies; consumer warp c owns slot c and takes every C-th position of the CTA. A
+// consumer reads s, dy, the weights and d_res_out from shared memory in its three passes
+// (independent products two at a time with packed fp32 multiplies, each rounded on its own;
+// the sums in the tree's order), writes dx and rstd, and hands the slot back after the last
+// pass.
 constexpr int kBwdMaxConsumers = 8;
 constexpr size_t kBwdSlotBudget = 180 * 1024;
 
@@ -168,70 +189,74 @@ __global__ void __launch_bounds__(32 * (1 + kBwdMaxConsumers), 1) add_rmsnorm_bw
     const uint32_t round = uint32_t(k / C);
     if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[c]), round & 1u, abort_flag, a.err))) break;
     {
-      // pass 1: sum of s^2 on the forward's tree; s stays in registers (rows up to 4096 wide;
-      // wider rows read it from the slot again)
-      constexpr bool kHoldS = NJ <= 16;
-      uint4 sv[kHoldS ? NJ : 1];
-      auto s_at = [&](int j) { if constexpr (kHoldS) return sv[j]; else return ss4[32 * j + lane]; };
+      // pass 1: sum of s^2 on the forward's tree (lane l: columns 256 j + 8 l + t, j outer)
       float ss = 0.0f;
+#pragma unroll 2
+      for (int j = 0; j < nj; ++j) {
+        const uint4 s1 = ss4[32 * j + lane];
+        float2 sq[4];
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        if (j < nj) {
-          const uint4 s1 = ss4[32 * j + lane];
-          if constexpr (kHoldS) sv[j] = s1;
+        for (int t = 0; t < 4; ++t) sq[t] = f2_mul(f2_of(s1, t), f2_of(s1, t));
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const float v = elem(s1, t);
-            ss = __fadd_rn(ss, __fmul_rn(v, v));
-          }
+        for (int t = 0; t < 4; ++t) {
+          ss = __fadd_rn(ss, sq[t].x);
+          ss = __fadd_rn(ss, sq[t].y);
         }
       }
       ss = warp_tree(ss);
       const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, fH), a.eps)));
+      const float2 rstd2 = make_float2(rstd, rstd);
       // pass 2: dot = sum of (dy * w) * (s * rstd) on the same tree
       const uint4* wrow = reinterpret_cast<const uint4*>(wbuf + size_t(e) * row_bytes);
       float dot = 0.0f;
+#pragma unroll 2
+      for (int j = 0; j < nj; ++j) {
+        const uint4 wv = wrow[32 * j + lane], d = sd4[32 * j + lane], sj = ss4[32 * j + lane];
+        float2 pr[4];
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        if (j < nj) {
-          const uint4 wv = wrow[32 * j + lane], d = sd4[32 * j + lane], sj = s_at(j);
+        for (int t = 0; t < 4; ++t)
+          pr[t] = f2_mul(f2_mul(f2_of(d, t), f2_of(wv, t)), f2_mul(f2_of(sj, t), rstd2));
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const float xh = __fmul_rn(elem(sj, t), rstd);
-            const float g = __fmul_rn(elem(d, t), elem(wv, t));
-            dot = __fadd_rn(dot, __fmul_rn(g, xh));
-          }
+        for (int t = 0; t < 4; ++t) {
+          dot = __fadd_rn(dot, pr[t].x);
+          dot = __fadd_rn(dot, pr[t].y);
         }
       }
       dot = warp_tree(dot);
       const float cc = __fdiv_rn(dot, fH);
-      // pass 3: ds = rstd * (g - xh * c) (+ d_res_out), one cast
+      // pass 3: ds = rstd * (g - xh * c) (+ d_res_out), one cast; partials dy * xh
       uint4* orow = a.dx + row * h8 + lane;
+#pragma unroll 2
+      for (int j = 0; j < nj; ++j) {
+        const uint4 wv = wrow[32 * j + lane], d = sd4[32 * j + lane], sj = ss4[32 * j + lane];
+        const uint4 rv = a.dro ? sr4[32 * j + lane] : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t ow[4];
+        float2 pp[4];
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        if (j < nj) {
-          const uint4 wv = wrow[32 * j + lane], d = sd4[32 * j + lane], sj = s_at(j);
-          const uint4 rv = a.dro ? sr4[32 * j + lane] : make_uint4(0u, 0u, 0u, 0u);
-          float o[8], pp[8];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const float xh = __fmul_rn(elem(sj, t), rstd);
-            const float g = __fmul_rn(elem(d, t), elem(wv, t));
-            float ds = __fmul_rn(rstd, __fsub_rn(g, __fmul_rn(xh, cc)));
-            if (a.dro) ds = __fadd_rn(ds, elem(rv, t));
-            o[t] = ds;
-            pp[t] = __fmul_rn(elem(d, t), xh);
+        for (int t = 0; t < 4; ++t) {
+          const float2 dd = f2_of(d, t);
+          const float2 xh = f2_mul(f2_of(sj, t), rstd2);
+          const float2 g = f2_mul(dd, f2_of(wv, t));
+          const float2 r = f2_of(rv, t);
+          // a product that feeds an addition stays a scalar multiply, so no multiply-add can
+          // take its place
+          float ds0 = __fmul_rn(rstd, __fsub_rn(g.x, __fmul_rn(xh.x, cc)));
+          float ds1 = __fmul_rn(rstd, __fsub_rn(g.y, __fmul_rn(xh.y, cc)));
+          if (a.dro) {
+            ds0 = __fadd_rn(ds0, r.x);
+            ds1 = __fadd_rn(ds1, r.y);
           }
-          if (a.part) {
-            // columns 256 j + 8 lane + t: block 4 j + lane / 8, offset 8 (lane % 8) + t
-            float4* pd = reinterpret_cast<float4*>(a.part + ((int64_t(4 * j + (lane >> 3)) * a.T + pos) << 6) +
-                                                   8 * (lane & 7));
-            __stcs(pd, make_float4(pp[0], pp[1], pp[2], pp[3]));
-            __stcs(pd + 1, make_float4(pp[4], pp[5], pp[6], pp[7]));
-          }
-          __stcs(orow + 32 * j, make_uint4(pack_bf2(o[0], o[1]), pack_bf2(o[2], o[3]), pack_bf2(o[4], o[5]),
-                                           pack_bf2(o[6], o[7])));
+          ow[t] = pack_bf2(ds0, ds1);
+          pp[t] = f2_mul(dd, xh);
         }
+        if (a.part) {
+          // columns 256 j + 8 lane + t: block 4 j + lane / 8, offset 8 (lane % 8) + t
+          float4* pd = reinterpret_cast<float4*>(a.part + ((int64_t(4 * j + (lane >> 3)) * a.T + pos) << 6) +
+                                                 8 * (lane & 7));
+          __stcs(pd, make_float4(pp[0].x, pp[0].y, pp[1].x, pp[1].y));
+          __stcs(pd + 1, make_float4(pp[2].x, pp[2].y, pp[3].x, pp[3].y));
+        }
+        __stcs(orow + 32 * j, make_uint4(ow[0], ow[1], ow[2], ow[3]));
       }
       if (lane == 0) a.rstd[row] = rstd;
     }
