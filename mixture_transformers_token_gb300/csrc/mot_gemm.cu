@@ -607,12 +607,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // loads, the last partial block is gathered four rows at a time with rows past the run
 // pointed outside the tensor, which the copy fills with zeros. Pair tiles cover 256 n x 256 k;
 // each accumulates its 64-row blocks in ascending order into one fp32 accumulator (no split
-// of the reduction), and the epilogue stores fp32 rows of dW through a per-warp transpose in
-// shared memory (five pipeline stages leave room for it).
-constexpr int kDwStages = 5;  // one stage fewer than the routed kernel: room for the store staging
+// of the reduction), and the epilogue writes each accumulator row of dW from the lane that reads
+// it, in 32-byte sectors.
+constexpr int kDwStages = 5;
 constexpr int kDwBars = 2 * kDwStages + 5;
-constexpr int kDwStageFloats = 32 * 36;  // a warp's 32 x 32 fp32 block, rows padded to 36
-constexpr size_t kDwSmem = 1024 + size_t(kDwStages) * STAGE_BYTES + 256 + size_t(EPI_WARPS) * kDwStageFloats * 4;
+constexpr size_t kDwSmem = 1024 + size_t(kDwStages) * STAGE_BYTES + 256;
 
 struct DwArgs {
   const uint8_t* ws;
@@ -620,6 +619,7 @@ struct DwArgs {
   int T, N, K;  // dout [T][N], a [T][K], dw [N][K]
   int expert;
   float* dw;
+  int st32;     // dw is 32-byte aligned (its rows, K * 4 bytes apart, then are too)
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
@@ -639,7 +639,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* drain = bars + 2 * STAGES + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kDwBars);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  float* stagebuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -789,37 +788,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else {
     // ---------------- epilogue (both CTAs): fp32 rows of dW ----------------
-    // Each warp turns its 32 rows x 32 columns blocks around in shared memory, so one store
-    // instruction writes four whole 128-byte row segments instead of 32 scattered pieces.
+    // Each lane writes its accumulator row's 32 columns per TMEM load as whole 32-byte sectors
+    // (16-byte pieces when dw is only 16-byte aligned).
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
-    float* buf = stagebuf + (warp - 2) * kDwStageFloats;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cluster; u < total; u += nclusters) {
       const int mt = u % m_tiles, nt = u / m_tiles;
-      const int n_base = mt * BN + int(rank) * BN_HALF + quarter * 32;  // this warp's first dW row
+      const int n_row = mt * BN + int(rank) * BN_HALF + quarter * 32 + lane;  // this lane's dW row
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16) + half * 128;
+      float* drow = args.dw + int64_t(n_row) * args.K + nt * BN + half * 128;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float v[32];
-        tmem_ld32(taddr + c * 32, v);  // row n_base + lane, columns 32 c .. 32 c + 31 of this half
+        tmem_ld32(taddr + c * 32, v);
+        if (args.st32) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float4*>(buf + lane * 36 + 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2],
+          for (int i = 0; i < 4; ++i)
+            asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(drow + c * 32 + 8 * i),
+                         "f"(v[8 * i]), "f"(v[8 * i + 1]), "f"(v[8 * i + 2]), "f"(v[8 * i + 3]), "f"(v[8 * i + 4]),
+                         "f"(v[8 * i + 5]), "f"(v[8 * i + 6]), "f"(v[8 * i + 7])
+                         : "memory");
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(drow + c * 32 + 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2],
                                                                             v[4 * i + 3]);
-        __syncwarp();
-        const int col4 = lane & 7;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int r = q * 4 + (lane >> 3);
-          const float4 val = *reinterpret_cast<const float4*>(buf + r * 36 + 4 * col4);
-          *reinterpret_cast<float4*>(args.dw + int64_t(n_base + r) * args.K + nt * BN + half * 128 + c * 32 +
-                                     4 * col4) = val;
         }
-        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
@@ -1027,6 +1025,7 @@ extern "C" int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_p
   a.K = K;
   a.expert = expert;
   a.dw = dw;
+  a.st32 = reinterpret_cast<uintptr_t>(dw) % 32 == 0 ? 1 : 0;
   const int64_t total = int64_t(N / gemm::BN) * (K / gemm::BN);
   // same threads and cluster shape as the routed kernel and more shared memory than half an
   // SM: one pair per two SMs, the same residency

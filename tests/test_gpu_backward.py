@@ -245,3 +245,21 @@ def test_routed_gemm_dw_is_deterministic():
     d1 = _dw_run(dout, a, mod, 1)
     d2 = _dw_run(dout, a, mod, 1)
     assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))
+
+
+def test_routed_gemm_dw_into_16_byte_aligned_output_gives_the_same_bits():
+    # the epilogue writes 32-byte sectors when dw is 32-byte aligned, 16-byte pieces otherwise
+    T, N, K = 700, 512, 768
+    mod = W.modality_bernoulli(W.rng_for(16, 360), T, 0.5)
+    dout = W.bf16_normal(W.rng_for(16, 361), (T, N))
+    a = W.bf16_normal(W.rng_for(16, 362), (T, K))
+    ref = _dw_run(dout, a, mod, 1)
+    ws = mot.mot_route_plan(mod.cuda())
+    dp = mot.mot_gather_rows(dout.cuda(), ws)
+    ap = mot.mot_gather_rows(a.cuda(), ws)
+    buf = torch.empty(N * K + 4, dtype=torch.float32, device="cuda")
+    out = buf[4:4 + N * K].view(N, K)
+    assert out.data_ptr() % 32 == 16
+    mot.mot_routed_gemm_dw(dp, ap, ws, expert=1, out=out)
+    assert mot.mot_device_status(ws) == 0
+    assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
