@@ -268,11 +268,12 @@ __global__ void __launch_bounds__(32 * (1 + kBwdMaxConsumers), 1) add_rmsnorm_bw
 // Weight-gradient fold. The backward kernel leaves the per-row partials p = dy * (s * rstd)
 // in fp32 blocks of 64 columns by plan position, part[cb][i][64], so the rows of a weight set
 // in a column block are one contiguous run in ascending row order. One CTA per (set, block):
-// warp 0 streams 64-row tiles of the run (16 KB) with TMA into a ring of kFoldStages slots;
-// warps 1 and 2 fold 32 columns each, one column per thread.
-constexpr int kFoldCols = 64, kFoldRows = 64, kFoldStages = 8;
+// warp 0 streams 128-row tiles of the run (32 KB) with TMA into a ring of kFoldStages slots
+// (larger tiles halve the per-tile barrier handshakes on the fold's critical path); warps 1
+// and 2 fold 32 columns each, one column per thread.
+constexpr int kFoldCols = 64, kFoldRows = 128, kFoldStages = 4;
 constexpr int kFoldThreads = 32 * 3;
-constexpr uint32_t kFoldPartBytes = kFoldRows * kFoldCols * 4;  // 16 KB
+constexpr uint32_t kFoldPartBytes = kFoldRows * kFoldCols * 4;  // 32 KB
 constexpr size_t kFoldSmem = 128 + kFoldStages * size_t(kFoldPartBytes) + 2 * kFoldStages * 8 + 16;
 
 struct FoldArgs {

@@ -367,12 +367,13 @@ __global__ void __launch_bounds__(THREADS, 4) sde_step_kernel(const SdeArgs a, c
 }
 
 // The fused CFG + SDE step, launched as a dependent of the CFG's pass 1 (cfg_partials_kernel
-// without a copy): per (request, segment) unit it loads the branches, x and z (inputs complete
-// before pass 1 started), waits for pass 1 once, folds the request's CFG sums (the same order
-// as cfg_scale_kernel, so the same r), forms v = v2 r (c outside the window) in registers and
-// runs the SDE step's arithmetic on it, exactly as sde_step_kernel would on the v that the
-// two-call chain writes. Its sums of d d go to their own region (sp).
-__global__ void __launch_bounds__(THREADS, 2) cfg_sde_kernel(const CfgArgs c, const SdeArgs a, float* v_out,
+// without a copy): per (request, segment) unit it waits for pass 1 once, folds the request's
+// CFG sums (the same order as cfg_scale_kernel, so the same r), then chunk by chunk loads the
+// branches, x and z, forms v = v2 r (c outside the window) in registers and runs the SDE
+// step's arithmetic on it, exactly as sde_step_kernel would on the v that the two-call chain
+// writes. Its sums of d d go to their own region. Nothing is loaded ahead of its chunk: at 63
+// registers four CTAs fit on an SM, and their warps keep the loads in flight.
+__global__ void __launch_bounds__(THREADS, 4) cfg_sde_kernel(const CfgArgs c, const SdeArgs a, float* v_out,
                                                              const int64_t units) {
   __shared__ float wsum[THREADS / 32];
   __shared__ float r_s;
@@ -390,29 +391,7 @@ __global__ void __launch_bounds__(THREADS, 2) cfg_sde_kernel(const CfgArgs c, co
     const int64_t base = int64_t(req) * a.N + int64_t(seg) * SEG;
     const int nch = int(min(int64_t(SEG), a.N - int64_t(seg) * SEG) / 8);
     const float* third = a.z ? a.z : a.x_next;
-    CfgChunks k;
-    if (guided) {
-      cfg_load(c, base, nch, k);
-    } else {
-      k.n = 0;
-#pragma unroll
-      for (int j = 0; j < CPT; ++j) {
-        const int q = int(threadIdx.x) + THREADS * j;
-        if (q < nch) {
-          k.n = j + 1;
-          k.c[j] = __ldg(reinterpret_cast<const uint4*>(c.c + base + 8 * q));
-        }
-      }
-    }
-    F8 xs[CPT], ws3[CPT];
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-      if (j < k.n) {
-        const int q = int(threadIdx.x) + THREADS * j;
-        xs[j] = load8_f32(a.x + base + 8 * q, a.w32);
-        ws3[j] = load8_f32(third + base + 8 * q, a.w32);
-      }
-    }
+    const int kn = nch / THREADS + (int(threadIdx.x) < nch % THREADS ? 1 : 0);  // this thread's chunks
     float r = 1.0f;
     if (guided) {
       if (!waited) {
@@ -434,20 +413,24 @@ __global__ void __launch_bounds__(THREADS, 2) cfg_sde_kernel(const CfgArgs c, co
     float p = 0.0f;
 #pragma unroll
     for (int j = 0; j < CPT; ++j) {
-      if (j < k.n) {
+      if (j < kn) {
         const int q = int(threadIdx.x) + THREADS * j;
         float v[8], x[8], w[8], mu[8], xn[8];
         if (guided) {
+          CfgChunks k;
+          k.c[j] = __ldg(reinterpret_cast<const uint4*>(c.c + base + 8 * q));
+          k.tu[j] = __ldg(reinterpret_cast<const uint4*>(c.tu + base + 8 * q));
+          if (c.iu) k.iu[j] = __ldg(reinterpret_cast<const uint4*>(c.iu + base + 8 * q));
           float cc[8];
           cfg_guide(c, pol, k, j, cc, v);
 #pragma unroll
           for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], r);
         } else {
-          unpack8_bf16(k.c[j], v);
+          unpack8_bf16(__ldg(reinterpret_cast<const uint4*>(c.c + base + 8 * q)), v);
         }
         if (v_out) store8_f32(v_out + base + 8 * q, v, c.w32);
-        unpack8_f32(xs[j], x);
-        unpack8_f32(ws3[j], w);
+        unpack8_f32(load8_f32(a.x + base + 8 * q, a.w32), x);
+        unpack8_f32(load8_f32(third + base + 8 * q, a.w32), w);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float e = __fadd_rn(x[i], __fmul_rn(omt, v[i]));
@@ -652,7 +635,7 @@ extern "C" int mot_flow_cfg_sde_step(const mot_bf16* v_c, const mot_bf16* v_tu, 
                    &static_cast<PlanHeader*>(ws)->error, w32 ? 1 : 0};
   const int64_t units = int64_t(n_req) * S;
   const unsigned grid1 = unsigned(std::min<int64_t>(units, int64_t(flow::kCtasPerSm) * sm_count(dev)));
-  const unsigned grid2 = unsigned(std::min<int64_t>(units, int64_t(2) * sm_count(dev)));
+  const unsigned grid2 = unsigned(std::min<int64_t>(units, int64_t(4) * sm_count(dev)));
   flow::cfg_partials_kernel<<<grid1, flow::THREADS, 0, s>>>(ca, units);
   if (cudaGetLastError() != cudaSuccess) return MOT_ERR_CUDA;
   if (launch_dependent(flow::cfg_sde_kernel, dim3(grid2), dim3(flow::THREADS), 0, s, ca, sa, v_out, units) !=
