@@ -609,7 +609,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // each accumulates its 64-row blocks in ascending order into one fp32 accumulator (no split
 // of the reduction), and the epilogue writes each accumulator row of dW from the lane that reads
 // it, in 32-byte sectors.
-constexpr int kDwStages = 5;
+constexpr int kDwStages = 6;
 constexpr int kDwBars = 2 * kDwStages + 5;
 constexpr size_t kDwSmem = 1024 + size_t(kDwStages) * STAGE_BYTES + 256;
 
