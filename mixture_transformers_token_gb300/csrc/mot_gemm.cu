@@ -56,7 +56,7 @@ constexpr int EPI_WARPS = 8;
 constexpr uint32_t ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256 + 1024;  // + QK-norm weights
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 256 + 2048;  // + QK-norm weights (fp32)
 
 enum Epi { EPI_CAST = 0, EPI_SWIGLU = 1, EPI_QKV64 = 2, EPI_QKV128 = 3, EPI_QKV64_F32 = 4, EPI_QKV128_F32 = 5 };
 
@@ -160,6 +160,19 @@ __device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
 }
 __device__ __forceinline__ uint32_t bf2_neg(uint32_t a) { return a ^ 0x80008000u; }
 
+// Two fp32 multiplies in one instruction, each rounded as the scalar one would be; the pair
+// moves between float2 and the 64-bit register pair by mov.b64.
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  unsigned long long pa, pb, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pa), "l"(pb));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+  return r;
+}
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) { return make_float2(bf_lo(w), bf_hi(w)); }
+
 // The RoPE (cos, sin) words of the row's position for the head dimension D, loaded before the
 // accumulator is ready. Word i holds (cos_i, sin_i).
 template <int D>
@@ -217,7 +230,7 @@ __device__ __forceinline__ void add_bias(const Args& a, int e, int64_t col, floa
 // and writes the outputs.
 template <int D, bool F32>
 __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool valid, int grow, int e, int nt, int half,
-                                        const uint32_t* gs, const uint32_t (&cw)[D / 2], const float4* crow) {
+                                        const float2* gs, const uint32_t (&cw)[D / 2], const float4* crow) {
   constexpr int HEADS = 128 / D;  // heads in this half
   constexpr int NP = D / 2;       // packed words per head
   uint16_t* orow = a.out + int64_t(grow) * a.ldo + int64_t(nt) * BN + half * 128;
@@ -251,16 +264,17 @@ __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool vali
       float part = 0.0f;
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
-        const uint32_t pk = pack_bf2(v[i], v[i + 1]);
-        const float q0 = bf_lo(pk), q1 = bf_hi(pk);
-        part = __fadd_rn(part, __fmul_rn(q0, q0));
-        part = __fadd_rn(part, __fmul_rn(q1, q1));
+        const float2 q = bf2_to_f2(pack_bf2(v[i], v[i + 1]));
+        const float2 sq = f2_mul(q, q);
+        part = __fadd_rn(part, sq.x);
+        part = __fadd_rn(part, sq.y);
       }
       ss = c == 0 ? part : __fadd_rn(ss, part);
     }
     const float ms = __fdiv_rn(ss, float(D));
     const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
-    const uint32_t* g = gs + (kind * 2 + e) * NP;
+    const float2* g = gs + (kind * 2 + e) * NP;  // (g_2w, g_2w+1) in g[w]
+    const float2 rstd2 = make_float2(rstd, rstd);
     if constexpr (F32) {
       // pass 2, FP32 profile: u = (q * rstd) * g in fp32, not rounded;
       // out_i = bf16(u_i c + (-u_{i+D/2}) s), out_{i+D/2} = bf16(u_{i+D/2} c + u_i s), each
@@ -281,11 +295,9 @@ __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool vali
           const int w = c * 8 + j;
           const uint32_t q1 = pack_bf2(v1[2 * j], v1[2 * j + 1]);
           const uint32_t q2 = pack_bf2(v2[2 * j], v2[2 * j + 1]);
-          const uint32_t g1 = g[w], g2 = g[NP / 2 + w];
-          const float u1a = __fmul_rn(__fmul_rn(bf_lo(q1), rstd), bf_lo(g1));
-          const float u1b = __fmul_rn(__fmul_rn(bf_hi(q1), rstd), bf_hi(g1));
-          const float u2a = __fmul_rn(__fmul_rn(bf_lo(q2), rstd), bf_lo(g2));
-          const float u2b = __fmul_rn(__fmul_rn(bf_hi(q2), rstd), bf_hi(g2));
+          const float2 u1 = f2_mul(f2_mul(bf2_to_f2(q1), rstd2), g[w]);
+          const float2 u2 = f2_mul(f2_mul(bf2_to_f2(q2), rstd2), g[NP / 2 + w]);
+          const float u1a = u1.x, u1b = u1.y, u2a = u2.x, u2b = u2.y;
           o1[j] = pack_bf2(__fadd_rn(__fmul_rn(u1a, t[j].x), __fmul_rn(-u2a, t[j].y)),
                            __fadd_rn(__fmul_rn(u1b, t[j].z), __fmul_rn(-u2b, t[j].w)));
           o2[j] = pack_bf2(__fadd_rn(__fmul_rn(u2a, t[j].x), __fmul_rn(u1a, t[j].y)),
@@ -313,11 +325,10 @@ __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool vali
         const int w = c * 8 + j;  // word index within the head's first half
         const uint32_t q1 = pack_bf2(v1[2 * j], v1[2 * j + 1]);
         const uint32_t q2 = pack_bf2(v2[2 * j], v2[2 * j + 1]);
-        const uint32_t g1 = g[w], g2 = g[NP / 2 + w];
-        const uint32_t u1 = pack_bf2(__fmul_rn(__fmul_rn(bf_lo(q1), rstd), bf_lo(g1)),
-                                     __fmul_rn(__fmul_rn(bf_hi(q1), rstd), bf_hi(g1)));
-        const uint32_t u2 = pack_bf2(__fmul_rn(__fmul_rn(bf_lo(q2), rstd), bf_lo(g2)),
-                                     __fmul_rn(__fmul_rn(bf_hi(q2), rstd), bf_hi(g2)));
+        const float2 uf1 = f2_mul(f2_mul(bf2_to_f2(q1), rstd2), g[w]);
+        const float2 uf2 = f2_mul(f2_mul(bf2_to_f2(q2), rstd2), g[NP / 2 + w]);
+        const uint32_t u1 = pack_bf2(uf1.x, uf1.y);
+        const uint32_t u2 = pack_bf2(uf2.x, uf2.y);
         const uint32_t c2 = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x5410);  // (cos_2w, cos_2w+1)
         const uint32_t s2 = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x7632);  // (sin_2w, sin_2w+1)
         o1[j] = bf2_add(bf2_mul(u1, c2), bf2_mul(bf2_neg(u2), s2));
@@ -393,7 +404,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* drain = bars + 2 * STAGES + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  uint32_t* gnorm = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES + 256);  // [2][2][D/2] words
+  float2* gnorm = reinterpret_cast<float2*>(smem + STAGES * STAGE_BYTES + 256);  // [2][2][D/2] fp32 pairs
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -552,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // both experts' q and k norm weights, once per CTA
       for (int i = et; i < 2 * D; i += 32 * EPI_WARPS) {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(i < D ? args.qn : args.kn);
-        gnorm[i] = __ldg(src + (i % D));
+        gnorm[i] = bf2_to_f2(__ldg(src + (i % D)));
       }
       asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
     }
