@@ -107,6 +107,171 @@ __global__ void __launch_bounds__(kRouteThreads) route_plan_kernel(const uint8_t
 }
 
 // ---------------------------------------------------------------------------
+// routing pre-pass over many CTAs, for packs above kPlanOneCta rows: the same plan, built by
+// four small kernels. Block b owns rows [b C, b C + C) with C = kPlanChunk; within a block,
+// round i covers rows b C + 256 i + t (thread t), so every load of the modality bytes is
+// coalesced and a block-wide prefix over each round keeps the lists stable.
+//   plan_count_kernel    und rows per block (-1 for a block with a bad modality byte), into
+//                        the tile table's space, which is rewritten last
+//   plan_scan_kernel     one CTA: the exclusive prefix of the und counts, the header
+//   plan_scatter_kernel  every row to its slot: und rows ascending, then gen rows ascending
+//   plan_tiles_kernel    the 128-row tile records, as route_plan_block writes them
+// ---------------------------------------------------------------------------
+constexpr int kPlanOneCta = 65536;
+constexpr int kPlanThreads = 256;
+constexpr int kPlanRounds = 32;
+constexpr int kPlanChunk = kPlanThreads * kPlanRounds;  // 8192 rows per block
+
+__device__ __forceinline__ int32_t* plan_block_scratch(uint8_t* ws, int T) {
+  return reinterpret_cast<int32_t*>(ws + tiles_offset(T));
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const uint8_t* __restrict__ mod, int T,
+                                                                   uint8_t* __restrict__ ws) {
+  __shared__ int wsum[kPlanThreads / 32];
+  const int b = int(blockIdx.x), t = int(threadIdx.x);
+  const int64_t base = int64_t(b) * kPlanChunk;
+  int n_und = 0, bad = 0;
+#pragma unroll 4
+  for (int i = 0; i < kPlanRounds; ++i) {
+    const int64_t r = base + int64_t(i) * kPlanThreads + t;
+    if (r < T) {
+      const int m = mod[r];
+      bad |= (m > 1);
+      n_und += (m == 0);
+    }
+  }
+  bad = __syncthreads_or(bad);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) n_und += __shfl_xor_sync(0xffffffffu, n_und, off);
+  if ((t & 31) == 0) wsum[t >> 5] = n_und;
+  __syncthreads();
+  if (t == 0) {
+    int tot = 0;
+    for (int w = 0; w < kPlanThreads / 32; ++w) tot += wsum[w];
+    plan_block_scratch(ws, T)[b] = bad ? -1 : tot;
+  }
+}
+
+__global__ void __launch_bounds__(1024) plan_scan_kernel(int T, int nblocks, uint8_t* __restrict__ ws) {
+  __shared__ int warp_incl[32];
+  int32_t* cnt = plan_block_scratch(ws, T);
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
+  const int tid = int(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+  // thread tid owns blocks [tid k, tid k + k), k = ceil(nblocks / 1024)
+  const int k = (nblocks + 1023) / 1024;
+  const int begin = min(tid * k, nblocks), end = min(begin + k, nblocks);
+  int sum = 0, bad = 0;
+  for (int i = begin; i < end; ++i) {
+    const int c = cnt[i];
+    bad |= (c < 0);
+    sum += c < 0 ? 0 : c;
+  }
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    if (tid == 0) {
+      hdr->T = T;
+      hdr->count[0] = hdr->count[1] = 0;
+      hdr->num_m_tiles = 0;
+      hdr->error = MOT_DEV_BAD_MODALITY;
+      hdr->magic = kPlanMagic;
+    }
+    return;
+  }
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_incl[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = warp_incl[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += u;
+    }
+    warp_incl[lane] = v;
+  }
+  __syncthreads();
+  const int total_und = warp_incl[31];
+  int run = (warp > 0 ? warp_incl[warp - 1] : 0) + incl - sum;  // und rows before block `begin`
+  for (int i = begin; i < end; ++i) {
+    const int c = cnt[i];
+    cnt[i] = run;  // und rows before block i
+    run += c;
+  }
+  if (tid == 0) {
+    const int total_gen = T - total_und;
+    hdr->T = T;
+    hdr->count[0] = total_und;
+    hdr->count[1] = total_gen;
+    hdr->num_m_tiles = (total_und + kTileRows - 1) / kTileRows + (total_gen + kTileRows - 1) / kTileRows;
+    hdr->error = 0;
+    hdr->magic = kPlanMagic;
+  }
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_scatter_kernel(const uint8_t* __restrict__ mod, int T,
+                                                                     uint8_t* __restrict__ ws) {
+  __shared__ int wcnt[kPlanThreads / 32];
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(ws);
+  if (hdr->error != 0) return;  // bad modality: no lists (uniform across the grid)
+  int32_t* perm = reinterpret_cast<int32_t*>(ws + perm_offset());
+  const int b = int(blockIdx.x), t = int(threadIdx.x), lane = t & 31, warp = t >> 5;
+  const int64_t base = int64_t(b) * kPlanChunk;
+  const int total_und = hdr->count[0];
+  int und = plan_block_scratch(ws, T)[b];     // und rows before this block's next round
+  int gen = int(base) - und;                  // gen rows before it
+  for (int i = 0; i < kPlanRounds; ++i) {
+    const int64_t r = base + int64_t(i) * kPlanThreads + t;
+    if (base + int64_t(i) * kPlanThreads >= T) break;  // uniform across the block
+    const bool live = r < T;
+    const bool is_und = live && mod[r] == 0;
+    const uint32_t bu = __ballot_sync(0xffffffffu, is_und), bl = __ballot_sync(0xffffffffu, live);
+    if (lane == 0) wcnt[warp] = __popc(bu);
+    __syncthreads();
+    int und_before = und, live_before = 0;
+    for (int w = 0; w < warp; ++w) und_before += wcnt[w];
+    live_before = min(max(int(T - (base + int64_t(i) * kPlanThreads)), 0), warp * 32);  // live rows of earlier warps
+    const uint32_t lt = (1u << lane) - 1u;
+    und_before += __popc(bu & lt);
+    const int gen_before = gen + live_before + __popc(bl & lt) - (und_before - und);
+    if (live) perm[is_und ? und_before : total_und + gen_before] = int32_t(r);
+    int round_und = 0;
+    for (int w = 0; w < kPlanThreads / 32; ++w) round_und += wcnt[w];
+    const int round_live = int(min(int64_t(kPlanThreads), T - (base + int64_t(i) * kPlanThreads)));
+    __syncthreads();  // wcnt is rewritten by the next round
+    und += round_und;
+    gen += round_live - round_und;
+  }
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_tiles_kernel(int T, uint8_t* __restrict__ ws) {
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(ws);
+  if (hdr->error != 0) return;
+  const int32_t* perm = reinterpret_cast<const int32_t*>(ws + perm_offset());
+  Tile* tiles = reinterpret_cast<Tile*>(ws + tiles_offset(T));
+  const int total_und = hdr->count[0], total_gen = hdr->count[1];
+  const int nt0 = (total_und + kTileRows - 1) / kTileRows;
+  const int nt1 = (total_gen + kTileRows - 1) / kTileRows;
+  for (int t = int(blockIdx.x) * kPlanThreads + int(threadIdx.x); t < nt0 + nt1; t += int(gridDim.x) * kPlanThreads) {
+    const int e = t < nt0 ? 0 : 1;
+    const int i = e == 0 ? t : t - nt0;
+    const int cnt = e == 0 ? total_und : total_gen;
+    Tile tl;
+    tl.list_begin = (e == 0 ? 0 : total_und) + kTileRows * i;
+    tl.n_rows = min(kTileRows, cnt - kTileRows * i);
+    tl.expert = e;
+    const int first = perm[tl.list_begin], last = perm[tl.list_begin + tl.n_rows - 1];
+    tl.row0 = (last - first == tl.n_rows - 1) ? first : -1;
+    tiles[t] = tl;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // fused residual add + routed RMSNorm, fed by bulk copies through shared memory
 // ---------------------------------------------------------------------------
 // One CTA per SM, persistent over rows (blockIdx.x - 1) + k G. Warp 0 streams whole rows of x
@@ -296,7 +461,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }
 
 int enqueue_route_plan(const uint8_t* mod, int T, uint8_t* ws, cudaStream_t s) {
-  route_plan_kernel<<<1, kRouteThreads, 0, s>>>(mod, T, ws);
+  if (T <= kPlanOneCta) {
+    route_plan_kernel<<<1, kRouteThreads, 0, s>>>(mod, T, ws);
+    return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+  }
+  const int nblocks = (T + kPlanChunk - 1) / kPlanChunk;  // <= 2048 for T <= MOT_MAX_TOKENS
+  plan_count_kernel<<<nblocks, kPlanThreads, 0, s>>>(mod, T, ws);
+  plan_scan_kernel<<<1, 1024, 0, s>>>(T, nblocks, ws);
+  plan_scatter_kernel<<<nblocks, kPlanThreads, 0, s>>>(mod, T, ws);
+  const int ntiles = int(max_m_tiles(T));
+  plan_tiles_kernel<<<(ntiles + kPlanThreads - 1) / kPlanThreads, kPlanThreads, 0, s>>>(T, ws);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
@@ -347,14 +521,21 @@ extern "C" int mot_fused_add_rmsnorm(const mot_bf16* x, const mot_bf16* res, con
   a.eps = eps;
   a.y = y;
   a.res_out = res_out;
+  // up to kPlanOneCta rows one extra CTA of this launch builds the plan; a larger pack's plan
+  // is built first by the many-CTA kernels (one CTA would then outlast a narrow norm)
+  const bool embed_plan = ws != nullptr && T <= kPlanOneCta;
+  if (ws != nullptr && !embed_plan) {
+    st = enqueue_route_plan(mod, int(T), static_cast<uint8_t*>(ws), s);
+    if (st != MOT_OK) return st;
+  }
   a.err = ws ? &static_cast<PlanHeader*>(ws)->error : nullptr;
-  a.plan_ws = static_cast<uint8_t*>(ws);
+  a.plan_ws = embed_plan ? static_cast<uint8_t*>(ws) : nullptr;
   const int sms = sm_count(dev);
-  const int avail = ws ? (sms > 1 ? sms - 1 : 1) : sms;  // the plan CTA gets an SM of its own
+  const int avail = embed_plan ? (sms > 1 ? sms - 1 : 1) : sms;  // the plan CTA gets an SM of its own
   a.norm_blocks = int(T < avail ? T : avail);
   a.consumers = C;
   const size_t smem = 2 * row_bytes + size_t(C) * 2 * row_bytes + (2 * kNormMaxConsumers + 2) * sizeof(uint64_t);
-  const int grid = a.norm_blocks + (ws ? 1 : 0);
+  const int grid = a.norm_blocks + (embed_plan ? 1 : 0);
   const int nj = H / 256;
   cudaError_t e;
   if (nj <= 4)

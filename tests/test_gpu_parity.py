@@ -51,6 +51,11 @@ def _mods():
         "blocks4096": W.bagel_layer(1, T=4096)[1]["mod"],
         "scatter8192": W.modality_scattered(W.rng_for(4, 60), 8192, 2048),
         "cfg36864": W.cfg_pack_layout()[0],
+        # above 65536 rows the plan is built by the many-CTA kernels (blocks of 8192 rows)
+        "bern100003": W.modality_bernoulli(W.rng_for(5, 60), 100003),
+        "scatter1M": W.modality_scattered(W.rng_for(6, 60), 1 << 20, 1 << 18),
+        "blocks200k": W.modality_blocks([(0, 8191), (1, 3), (0, 70000), (1, 50000), (0, 1), (1, 71805)]),
+        "all_gen65537": torch.ones(65537, dtype=torch.uint8),
     }
 
 
@@ -74,7 +79,7 @@ def test_route_plan_bitwise(name):
     np.testing.assert_array_equal(p["tiles"], np.array(want, dtype=np.int32).reshape(-1, 4))
 
 
-@pytest.mark.parametrize("name", ["bern1", "bern1000", "blocks4096", "scatter8192"])
+@pytest.mark.parametrize("name", ["bern1", "bern1000", "blocks4096", "scatter8192", "bern100003"])
 def test_fused_norm_writes_the_same_plan(name):
     # the extra CTA of mot_fused_add_rmsnorm builds exactly the plan of mot_route_plan
     mod = _mods()[name].cuda()
@@ -90,12 +95,23 @@ def test_fused_norm_writes_the_same_plan(name):
     np.testing.assert_array_equal(a["tiles"], b["tiles"])
 
 
-def test_route_plan_rejects_bad_modality():
-    mod = torch.zeros(500, dtype=torch.uint8)
-    mod[321] = 2
+@pytest.mark.parametrize("T,bad_row", [(500, 321), (300000, 299999), (300000, 8192)])
+def test_route_plan_rejects_bad_modality(T, bad_row):
+    mod = torch.zeros(T, dtype=torch.uint8)
+    mod[bad_row] = 2
     ws = mot.mot_route_plan(mod.cuda())
     assert mot.mot_device_status(ws) == mot.DEV_BAD_MODALITY
-    assert decode_plan(ws, 500)["num_m_tiles"] == 0
+    assert decode_plan(ws, T)["num_m_tiles"] == 0
+
+
+def test_fused_norm_with_a_many_cta_plan_flags_bad_modality():
+    T = 70000
+    x, res, w, mod = _norm_inputs(T, 256, 12)
+    mod = mod.clone()
+    mod[69999] = 3
+    ws = torch.empty(mot.mot_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    mot.mot_fused_add_rmsnorm(x.cuda(), res.cuda(), w.cuda(), mod.cuda(), EPS, ws=ws)
+    assert mot.mot_device_status(ws) & mot.DEV_BAD_MODALITY
 
 
 # ---------------------------------------------------------------------------
