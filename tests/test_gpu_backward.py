@@ -124,6 +124,35 @@ def test_add_rmsnorm_backward_flags_and_partials_layout():
     assert np.array_equal(part.cpu().numpy().view(np.uint32), np.ascontiguousarray(want).view(np.uint32))
 
 
+@pytest.mark.parametrize("T,H,case", [(4096, 3584, "bernoulli_0.25"), (4096, 3584, "contiguous_3_1"),
+                                       (1, 256, "bernoulli_0.5"), (300, 8192, "bernoulli_0.3"),
+                                       (5000, 256, "one_gen_row"), (5000, 768, "one_und_row"),
+                                       (2500, 1024, "all_und"), (2500, 1024, "all_gen"),
+                                       (20000, 512, "bernoulli_0.02")])
+def test_rmsnorm_dweight_fold_bitwise_vs_emulator(T, H, case):
+    # the fold alone, on random partials: the grid splits its CTAs between the sets by their row
+    # counts, so one-row sets, empty sets and many units per CTA all take other assignments
+    rng = W.rng_for(T * 7 + H, 320)
+    if case.startswith("bernoulli"):
+        mod = W.modality_bernoulli(rng, T, float(case.split("_")[1]))
+    elif case == "contiguous_3_1":
+        mod = torch.cat([torch.zeros(3 * T // 4, dtype=torch.uint8), torch.ones(T - 3 * T // 4, dtype=torch.uint8)])
+    elif case in ("one_gen_row", "one_und_row"):
+        mod = torch.full((T,), 0 if case == "one_gen_row" else 1, dtype=torch.uint8)
+        mod[int(rng.integers(0, T))] = 1 if case == "one_gen_row" else 0
+    else:
+        mod = torch.full((T,), 0 if case == "all_und" else 1, dtype=torch.uint8)
+    p = rng.standard_normal((T, H)).astype(np.float32) * np.float32(0.01)
+    m = mod.numpy()
+    perm = np.concatenate([np.nonzero(m == 0)[0], np.nonzero(m == 1)[0]])
+    blocks = np.ascontiguousarray(p[perm].reshape(T, H // 64, 64).transpose(1, 0, 2))
+    ws = mot.mot_route_plan(mod.cuda())
+    dw = mot.mot_rmsnorm_dweight(torch.from_numpy(blocks).cuda(), ws)
+    assert mot.mot_device_status(ws) == 0
+    want = np.stack([O.e_left_fold_rows(p, m, 0), O.e_left_fold_rows(p, m, 1)]).astype(np.float32)
+    assert np.array_equal(dw.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
 # ---------------------------------------------------------------------------
 # routed GEMM input gradient (both weight sets, MN-major weight operand)
 # ---------------------------------------------------------------------------
