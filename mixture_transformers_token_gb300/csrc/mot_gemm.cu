@@ -619,7 +619,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // pointed outside the tensor, which the copy fills with zeros. Pair tiles cover 256 n x 256 k;
 // each accumulates its 64-row blocks in ascending order into one fp32 accumulator (no split
 // of the reduction), and the epilogue writes each accumulator row of dW from the lane that reads
-// it, in 32-byte sectors.
+// it, in 32-byte sectors. The tiles from split_from on are each done as two 256 n x 128 k
+// halves (N = 128 MMAs, one B box per CTA): the host splits the tiles of a last round that
+// would leave at least half the clusters idle, so that round takes half as long and its
+// exposed epilogue halves too. A half covers its columns with the same ascending row blocks,
+// so the bits do not depend on the split.
 constexpr int kDwStages = 6;
 constexpr int kDwBars = 2 * kDwStages + 5;
 constexpr size_t kDwSmem = 1024 + size_t(kDwStages) * STAGE_BYTES + 256;
@@ -631,7 +635,30 @@ struct DwArgs {
   int expert;
   float* dw;
   int st32;     // dw is 32-byte aligned (its rows, K * 4 bytes apart, then are too)
+  int split_from;  // tiles from this index on are done as two halves of 128 k
 };
+
+// A work item of the dW grid: full tile u, or half h of tile u.
+struct DwItem {
+  int mt, nt, h, split;
+};
+
+__device__ __forceinline__ DwItem dw_item(int it, int split_from, int m_tiles) {
+  DwItem r;
+  int u;
+  if (it < split_from) {
+    u = it;
+    r.h = 0;
+    r.split = 0;
+  } else {
+    u = split_from + ((it - split_from) >> 1);
+    r.h = (it - split_from) & 1;
+    r.split = 1;
+  }
+  r.mt = u % m_tiles;
+  r.nt = u / m_tiles;
+  return r;
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     routed_gemm_dw_kernel(const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_d_rows,
@@ -664,6 +691,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int kblocks = (count + BK - 1) / BK;
   const int m_tiles = args.N / BN, n_tiles = args.K / BN;
   const int total = m_tiles * n_tiles;
+  const int items = args.split_from + 2 * (total - args.split_from);
   if (kblocks == 0) {
     // a set without rows: its gradient is zero
     const int64_t n4 = int64_t(args.N) * args.K / 4;
@@ -673,7 +701,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     return;
   }
   const int cluster = int(blockIdx.x >> 1), nclusters = int(gridDim.x >> 1);
-  if (cluster >= total) return;  // uniform across the pair
+  if (cluster >= items) return;  // uniform across the pair
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -706,10 +734,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = cluster; u < total && ok; u += nclusters) {
-      const int mt = u % m_tiles, nt = u / m_tiles;
-      const int n0 = mt * BN + int(rank) * BN_HALF;  // this CTA's 128 rows of dW
-      const int k0 = nt * BN + int(rank) * BN_HALF;  // this CTA's 128 columns of the B' operand
+    for (int it = cluster; it < items && ok; it += nclusters) {
+      const DwItem w = dw_item(it, args.split_from, m_tiles);
+      const int n0 = w.mt * BN + int(rank) * BN_HALF;  // this CTA's 128 rows of dW
+      // this CTA's 128 (a half: 64) columns of the B' operand
+      const int k0 = w.nt * BN + (w.split ? w.h * BN_HALF + int(rank) * 64 : int(rank) * BN_HALF);
+      const uint32_t stage_tx = w.split ? 2 * (A_BYTES + B_BYTES / 2) : 2 * STAGE_BYTES;
       for (int kb = 0; kb < kblocks; ++kb) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err));
         if (!ok) break;
@@ -718,21 +748,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int valid = count - kb * BK;
         const uint32_t da = smem_u32(sa + stage * A_BYTES), db = smem_u32(sb + stage * B_BYTES);
         if (lane == 0) {
-          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), stage_tx);
           if (valid >= BK) {
             tma_load_2d_pair(da, &tm_d, n0, row0, fb);
             tma_load_2d_pair(da + A_BYTES / 2, &tm_d, n0 + 64, row0, fb);
             tma_load_2d_pair(db, &tm_a, k0, row0, fb);
-            tma_load_2d_pair(db + B_BYTES / 2, &tm_a, k0 + 64, row0, fb);
+            if (!w.split) tma_load_2d_pair(db + B_BYTES / 2, &tm_a, k0 + 64, row0, fb);
           }
         }
         __syncwarp();
         if (valid < BK) {
-          // 4 boxes x 16 four-row groups, two per lane; rows past the run read as zeros
+          // 4 boxes x 16 four-row groups, two per lane (a half has no second B box); rows past
+          // the run read as zeros
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int idx = lane + 32 * q;
             const int box = idx >> 4, quad = idx & 15;
+            if (w.split && box == 3) continue;
             int r[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) r[i] = quad * 4 + i < valid ? row0 + quad * 4 + i : args.T;
@@ -760,11 +792,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer (leader CTA only) ----------------
     if (rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN) | kIdescAMnMajor | kIdescBMnMajor;
+      constexpr uint32_t idesc_full = idesc_bf16_f32(2 * BM, BN) | kIdescAMnMajor | kIdescBMnMajor;
+      constexpr uint32_t idesc_half = idesc_bf16_f32(2 * BM, BN_HALF) | kIdescAMnMajor | kIdescBMnMajor;
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = cluster; u < total && ok; u += nclusters) {
+      for (int it = cluster; it < items && ok; it += nclusters) {
+        const uint32_t idesc = it < args.split_from ? idesc_full : idesc_half;
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err));
         if (!ok) break;
         tc_fence_after();
@@ -805,15 +839,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int half = (warp - 2) >> 2;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = cluster; u < total; u += nclusters) {
-      const int mt = u % m_tiles, nt = u / m_tiles;
-      const int n_row = mt * BN + int(rank) * BN_HALF + quarter * 32 + lane;  // this lane's dW row
+    for (int it = cluster; it < items; it += nclusters) {
+      const DwItem w = dw_item(it, args.split_from, m_tiles);
+      const int n_row = w.mt * BN + int(rank) * BN_HALF + quarter * 32 + lane;  // this lane's dW row
+      const int wcols = w.split ? 64 : 128;  // this warp's columns of the item
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err))) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16) + half * 128;
-      float* drow = args.dw + int64_t(n_row) * args.K + nt * BN + half * 128;
+      const uint32_t taddr = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16) + half * wcols;
+      float* drow = args.dw + int64_t(n_row) * args.K + w.nt * BN + w.h * BN_HALF + half * wcols;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < wcols / 32; ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
         if (args.st32) {
@@ -1041,7 +1076,14 @@ extern "C" int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_p
   // same threads and cluster shape as the routed kernel and more shared memory than half an
   // SM: one pair per two SMs, the same residency
   const int64_t cap = gemm::max_active_pairs<gemm::EPI_CAST, true>(dev);
-  const int64_t clusters = total < cap ? total : cap;
+  // the tiles of a last round that would leave at least half the clusters idle are split in
+  // halves (all of them when the whole problem is such a round)
+  const int64_t rem = total > cap ? total % cap : total;
+  const int64_t split_from = rem > 0 && 2 * rem <= cap ? total - rem : total;
+  const int64_t items = split_from + 2 * (total - split_from);
+  if (items > INT32_MAX) return MOT_ERR_GEOMETRY;
+  a.split_from = int(split_from);
+  const int64_t clusters = items < cap ? items : cap;
   gemm::routed_gemm_dw_kernel<<<unsigned(2 * clusters), gemm::THREADS, gemm::kDwSmem, s>>>(tm_d, tm_d_rows, tm_a,
                                                                                             tm_a_rows, a);
   return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
