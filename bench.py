@@ -199,6 +199,42 @@ def time_stages(stages, steps: int, warmup: int, flush, stream) -> dict:
     return out
 
 
+def time_compared(candidates: dict, steps: int, warmup: int, flush, stream) -> dict:
+    """Times several candidate stage lists against each other: every iteration runs each
+    candidate once, after its own L2 flush, in an order that is reversed on every other
+    iteration, so drift and order effects fall on all candidates alike. Returns, per candidate,
+    what time_stages returns."""
+    import torch
+
+    names = list(candidates)
+    for _ in range(warmup):
+        for name in names:
+            flush()
+            for _, fn in candidates[name]:
+                fn()
+    torch.cuda.synchronize()
+    ev = {name: [[torch.cuda.Event(enable_timing=True) for _ in range(len(candidates[name]) + 1)]
+                 for _ in range(steps)] for name in names}
+    for i in range(steps):
+        for name in (names if i % 2 == 0 else names[::-1]):
+            flush()
+            e = ev[name][i]
+            e[0].record(stream)
+            for j, (_, fn) in enumerate(candidates[name]):
+                fn()
+                e[j + 1].record(stream)
+    torch.cuda.synchronize()
+    out = {}
+    for name in names:
+        stages = candidates[name]
+        samples = {sn: [e[j].elapsed_time(e[j + 1]) / 1e3 for e in ev[name]] for j, (sn, _) in enumerate(stages)}
+        samples["step"] = [e[0].elapsed_time(e[-1]) / 1e3 for e in ev[name]]
+        r = {sn: statistics.fmean(v) for sn, v in samples.items()}
+        r["dist"] = {sn: percentiles_us(v) for sn, v in samples.items()}
+        out[name] = r
+    return out
+
+
 def percentiles_us(seconds: list) -> dict:
     v = sorted(seconds)
 
@@ -661,7 +697,8 @@ def run_flow(dev, flush) -> dict:
     values, N = 262144 each): the per-sample transition noise, then three-branch renormalised
     CFG of bf16 velocities and the SDE step (x and the noise in; x_next and logp out) in one
     call, every request at a different step of the 50-step schedule with shift 3. The same
-    step as two calls (CFG into an fp32 velocity, then the SDE step) is timed beside it."""
+    step as two calls (CFG into an fp32 velocity, then the SDE step) is timed in the same loop,
+    the two orders alternating."""
     import numpy as np
     import torch
 
@@ -689,12 +726,13 @@ def run_flow(dev, flush) -> dict:
         ("cfg_sde_step", lambda: mot.mot_flow_cfg_sde_step(br["c"], br["tu"], br["iu"], policy, x, z, times, ws=ws,
                                                            x_next=x_next, logp=logp)),
     ]
-    r = time_stages(stages, 100, 5, flush, stream)
     chain = [
         ("cfg_combine_renorm", lambda: mot.mot_cfg_combine_renorm(br["c"], br["tu"], br["iu"], policy, ws=ws, out=v)),
         ("flow_sde_step", lambda: mot.mot_flow_sde_step(x, v, z, times, ws=ws, x_next=x_next, logp=logp)),
     ]
-    rc = time_stages(chain, 100, 5, flush, stream)
+    # the one-call step and the two calls, in the same loop with the order reversed every step
+    both = time_compared({"one_call": stages, "two_calls": chain}, 100, 5, flush, stream)
+    r, rc = both["one_call"], both["two_calls"]
     if mot.mot_device_status(ws) != 0:
         raise RuntimeError("device error flags set in the flow workload")
     pk = peaks()
