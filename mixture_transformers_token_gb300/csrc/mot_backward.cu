@@ -105,6 +105,10 @@ __global__ void __launch_bounds__(32 * (1 + kBwdMaxConsumers), 1) add_rmsnorm_bw
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(wbar + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = int(blockIdx.x), G = int(gridDim.x);
+  // a programmatic dependent: launched while the preceding grid (the input gradient's GEMM)
+  // runs, it reads nothing before that grid has completed
+  pdl_trigger();
+  pdl_wait();
   if (threadIdx.x == 0) {
     for (int c = 0; c < C; ++c) {
       mbar_init(smem_u32(&full[c]), 1);
@@ -298,6 +302,8 @@ __global__ void __launch_bounds__(kFoldThreads) rmsnorm_dw_fold_kernel(const __g
   uint64_t* full = reinterpret_cast<uint64_t*>(fsm + kFoldStages * size_t(kFoldPartBytes));
   uint64_t* empty = full + kFoldStages;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + kFoldStages);
+  pdl_trigger();  // a programmatic dependent: nothing is read before the preceding grid completes
+  pdl_wait();
   const int ncb = a.H / kFoldCols;
   const int e = int(blockIdx.x) / ncb, cb = int(blockIdx.x) % ncb;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -366,8 +372,7 @@ static cudaError_t launch_bwd(const NormBwdArgs& a, int grid, size_t smem, cudaS
   cudaError_t st = cudaFuncSetAttribute(add_rmsnorm_bwd_kernel<NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         int(smem));
   if (st != cudaSuccess) return st;
-  add_rmsnorm_bwd_kernel<NJ><<<grid, 32 * (1 + a.consumers), smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(add_rmsnorm_bwd_kernel<NJ>, dim3(grid), dim3(32 * (1 + a.consumers)), smem, s, a);
 }
 
 }  // namespace bwd
@@ -459,6 +464,7 @@ extern "C" int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, v
   a.H = H;
   a.dw = dw;
   a.err = &static_cast<PlanHeader*>(ws)->error;
-  bwd::rmsnorm_dw_fold_kernel<<<2 * (H / bwd::kFoldCols), bwd::kFoldThreads, bwd::kFoldSmem, st>>>(tm_part, a);
-  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+  const cudaError_t e = launch_dependent(bwd::rmsnorm_dw_fold_kernel, dim3(2 * (H / bwd::kFoldCols)),
+                                         dim3(bwd::kFoldThreads), bwd::kFoldSmem, st, tm_part, a);
+  return e == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }

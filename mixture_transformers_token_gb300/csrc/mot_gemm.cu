@@ -682,6 +682,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
+  pdl_trigger();  // a programmatic dependent: nothing is read before the preceding grid completes
+  pdl_wait();
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(args.ws);
   if (hdr->magic != kPlanMagic || hdr->T != args.T) {
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.err, MOT_DEV_PLAN_MISMATCH);
@@ -1086,9 +1088,9 @@ extern "C" int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_p
   if (items > INT32_MAX) return MOT_ERR_GEOMETRY;
   a.split_from = int(split_from);
   const int64_t clusters = items < cap ? items : cap;
-  gemm::routed_gemm_dw_kernel<<<unsigned(2 * clusters), gemm::THREADS, gemm::kDwSmem, s>>>(tm_d, tm_d_rows, tm_a,
-                                                                                            tm_a_rows, a);
-  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+  const cudaError_t e = launch_dependent(gemm::routed_gemm_dw_kernel, dim3(unsigned(2 * clusters)),
+                                         dim3(gemm::THREADS), gemm::kDwSmem, s, tm_d, tm_d_rows, tm_a, tm_a_rows, a);
+  return e == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
 extern "C" int mot_routed_gemm(const mot_bf16* a_in, const mot_bf16* w, int64_t T, int N, int K, int epilogue,

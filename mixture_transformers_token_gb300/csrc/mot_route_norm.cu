@@ -436,6 +436,10 @@ static cudaError_t launch_norm(const NormArgs& a, int grid, size_t smem, cudaStr
 // dst[i] = src[perm[i]]: one warp per row, 16-byte vectors, persistent grid
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src, int T, int K8,
                                                           const uint8_t* __restrict__ ws, uint4* __restrict__ dst) {
+  // a programmatic dependent: launched while the preceding grid runs, it reads nothing before
+  // that grid has completed
+  pdl_trigger();
+  pdl_wait();
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(ws);
   if (hdr->magic != kPlanMagic || hdr->T != T) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(const_cast<uint32_t*>(&hdr->error), MOT_DEV_PLAN_MISMATCH);
@@ -563,7 +567,8 @@ extern "C" int mot_gather_rows(const mot_bf16* src, int64_t T, int K, void* ws, 
   if (st != MOT_OK) return st;
   DeviceGuard guard(dev);
   const int grid = 4 * sm_count(dev);
-  gather_rows_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), int(T), K / 8,
-                                          static_cast<const uint8_t*>(ws), reinterpret_cast<uint4*>(dst));
-  return cudaGetLastError() == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
+  const cudaError_t e = launch_dependent(gather_rows_kernel, dim3(grid), dim3(256), 0, s,
+                                         reinterpret_cast<const uint4*>(src), int(T), K / 8,
+                                         static_cast<const uint8_t*>(ws), reinterpret_cast<uint4*>(dst));
+  return e == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
