@@ -281,7 +281,8 @@ int mot_rope_table_fill_host_fp32(double theta, int D, int P, float* host_cs);
  * cores; per row, 128-key blocks in ascending order from the sequence's first key, with
  * c = scale * log2 e: the reference maximum m starts as the first block's maximum and moves
  * to a later block's maximum only when that exceeds m by more than 8 / c (so p <= 2^8);
- * p = 2^(S c - m c) (the hardware exp2 approximation); l = l alpha + the block's sum of p;
+ * p = 2^((S - m) c), the difference and the product each rounded to fp32, then CUDA's accurate
+ * exp2f (no fused multiply-add, no approximate instruction); l = l alpha + the block's sum of p;
  * O = O alpha + bf16(p) V in fp32 with alpha = 2^((m_old - m) c); out = bf16(O r), r = 1 / l
  * rounded to fp32 once per row. The
  * result depends only on the row's own sequence, not on the other sequences in the pack.

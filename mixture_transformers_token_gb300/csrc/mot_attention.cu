@@ -13,10 +13,12 @@
 // Arithmetic, the same for every tile of every pack: S = Q K^T in fp32 on the tensor cores;
 // per row, in 128-key blocks in ascending key order, with c = scale * log2 e: the running
 // maximum m of S (masked keys excluded) moves to the block maximum only when that exceeds it
-// by more than 8 / c (then O and l are scaled by 2^((m_old - m) c)); p = 2^(S c - m c) (the
-// product and the difference each rounded to fp32, then CUDA's accurate exp2f -- no fused
+// by more than 8 / c (then O and l are scaled by 2^((m_old - m) c)); p = 2^((S - m) c) (the
+// difference and then the product each rounded to fp32, then CUDA's accurate exp2f -- no fused
 // multiply-add, no approximate or flush-to-zero instruction, as the numerical contract
-// requires); l += the block's p (four interleaved partial sums);
+// requires; a subtraction that feeds a product cannot be fused into one, so the pair runs as
+// packed f32x2 instructions, which a product feeding a packed addition did not survive);
+// l += the block's p (four interleaved partial sums);
 // O += bf16(p) V (fp32, tensor cores); out = bf16(O * (1 / l)), 1 / l rounded to fp32 once
 // per row. Blocks start at the sequence's first
 // key, so a row's bits do not depend on the other sequences of the pack.
@@ -423,17 +425,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         alpha = ex2(__fmul_rn(__fsub_rn(m, bmax), a.c));
         m = bmax;
       }
-      const float mc = m == -INFINITY ? 0.0f : __fmul_rn(m, a.c);
+      const float nm = m == -INFINITY ? 0.0f : -m;  // no visible key yet: every score is -inf
       // the tile's single P buffer and O are free once the P V of block j - 1 is done
       if (j >= 1) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[t]), uint32_t(j - 1) & 1u, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
       }
-      // p = 2^(fp32(S c) - m c), four interleaved partial sums (key c adds to sum c mod 4), as f32x2
+      // p = 2^(fp32(fp32(S - m) c)), four interleaved partial sums (key c adds to sum c mod 4), as f32x2
       // pairs; every 8 keys go as bf16 to the 16-byte chunk (cc ^ (row & 7)) of the row in half
       // cc / 8 of the swizzled P tile
-      const unsigned long long c2 = f2_pack(a.c, a.c), nmc2 = f2_pack(-mc, -mc);
+      const unsigned long long c2 = f2_pack(a.c, a.c), nm2 = f2_pack(nm, nm);
       unsigned long long ps01 = 0ull, ps23 = 0ull;  // (sum 0, sum 1), (sum 2, sum 3), from +0
 #pragma unroll
       for (int cc = 0; cc < BKV / 8; ++cc) {
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int u = 0; u < 4; ++u) {
           const int c = 8 * cc + 2 * u;
           float t0, t1;
-          f2_unpack(f2_add(f2_mul(f2_pack(x[c], x[c + 1]), c2), nmc2), t0, t1);
+          f2_unpack(f2_mul(f2_add(f2_pack(x[c], x[c + 1]), nm2), c2), t0, t1);
           const float p0 = ex2(t0), p1 = ex2(t1);
           const unsigned long long p01 = f2_pack(p0, p1);
           if (u & 1) ps23 = f2_add(ps23, p01);
