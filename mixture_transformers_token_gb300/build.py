@@ -26,7 +26,10 @@ LIB = os.path.join(PKG, "libmot.so")
 SOURCES = ["mot_route_norm.cu", "mot_gemm.cu", "mot_misc.cu", "mot_backward.cu", "mot_attention.cu",
            "mot_flow.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-ffp-contract=off",
+# --fmad=false: no multiply and add are ever contracted into a fused multiply-add, which the
+# numerical contract forbids (the kernels' arithmetic is written with explicitly rounded operations;
+# the flag makes that hold for any expression, packed pairs included)
+FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC,-ffp-contract=off",
          "-I", INCLUDE, "-I", CSRC]
 
 
