@@ -105,7 +105,7 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
 }
 
 // The running maximum moves only when a block's maximum exceeds it by more than this many
-// powers of two: until then p = 2^(S c - m c) stays below 2^8, and O and l, which share m,
+// powers of two: until then p = 2^((S - m) c) stays below 2^8, and O and l, which share m,
 // need no rescaling.
 constexpr float kLazyLog2 = 8.0f;
 
