@@ -26,9 +26,10 @@ LIB = os.path.join(PKG, "libmot.so")
 SOURCES = ["mot_route_norm.cu", "mot_gemm.cu", "mot_misc.cu", "mot_backward.cu", "mot_attention.cu",
            "mot_flow.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-# --fmad=false: no multiply and add are ever contracted into a fused multiply-add, which the
-# numerical contract forbids (the kernels' arithmetic is written with explicitly rounded operations;
-# the flag makes that hold for any expression, packed pairs included)
+# --fmad=false: no scalar multiply and add are contracted into a fused multiply-add, which the
+# numerical contract forbids (the kernels write their arithmetic with explicitly rounded operations;
+# the flag makes that hold for any scalar expression). It does not stop a packed f32x2 product that
+# feeds a packed f32x2 addition from being fused, so the kernels never write that pair.
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC,-ffp-contract=off",
          "-I", INCLUDE, "-I", CSRC]
 
