@@ -308,35 +308,35 @@ __device__ __forceinline__ void epi_qkv(const Args& a, uint32_t taddr, bool vali
           store_row_u4(a, ohead + NP + c * 16, o2, 2);
         }
       }
-      continue;
-    }
-    // pass 2: u = bf16((q * rstd) * g); out_i = bf16(bf16(u_i c) + bf16(-u_{i+D/2} s)),
-    // out_{i+D/2} = bf16(bf16(u_{i+D/2} c) + bf16(u_i s)); two neighbouring i per word
+    } else {
+      // pass 2: u = bf16((q * rstd) * g); out_i = bf16(bf16(u_i c) + bf16(-u_{i+D/2} s)),
+      // out_{i+D/2} = bf16(bf16(u_{i+D/2} c) + bf16(u_i s)); two neighbouring i per word
 #pragma unroll
-    for (int c = 0; c < NP / 16; ++c) {
-      float v1[16], v2[16];
-      tmem_ld16(taddr + col0 + c * 16, v1);
-      tmem_ld16(taddr + col0 + NP + c * 16, v2);
-      add_bias<16>(a, e, gcol0 + c * 16, v1);
-      add_bias<16>(a, e, gcol0 + NP + c * 16, v2);
-      uint32_t o1[8], o2[8];
+      for (int c = 0; c < NP / 16; ++c) {
+        float v1[16], v2[16];
+        tmem_ld16(taddr + col0 + c * 16, v1);
+        tmem_ld16(taddr + col0 + NP + c * 16, v2);
+        add_bias<16>(a, e, gcol0 + c * 16, v1);
+        add_bias<16>(a, e, gcol0 + NP + c * 16, v2);
+        uint32_t o1[8], o2[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int w = c * 8 + j;  // word index within the head's first half
-        const uint32_t q1 = pack_bf2(v1[2 * j], v1[2 * j + 1]);
-        const uint32_t q2 = pack_bf2(v2[2 * j], v2[2 * j + 1]);
-        const float2 uf1 = f2_mul(f2_mul(bf2_to_f2(q1), rstd2), g[w]);
-        const float2 uf2 = f2_mul(f2_mul(bf2_to_f2(q2), rstd2), g[NP / 2 + w]);
-        const uint32_t u1 = pack_bf2(uf1.x, uf1.y);
-        const uint32_t u2 = pack_bf2(uf2.x, uf2.y);
-        const uint32_t c2 = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x5410);  // (cos_2w, cos_2w+1)
-        const uint32_t s2 = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x7632);  // (sin_2w, sin_2w+1)
-        o1[j] = bf2_add(bf2_mul(u1, c2), bf2_mul(bf2_neg(u2), s2));
-        o2[j] = bf2_add(bf2_mul(u2, c2), bf2_mul(u1, s2));
-      }
-      if (valid) {
-        store_row_u4(a, ohead + c * 16, o1, 2);
-        store_row_u4(a, ohead + NP + c * 16, o2, 2);
+        for (int j = 0; j < 8; ++j) {
+          const int w = c * 8 + j;  // word index within the head's first half
+          const uint32_t q1 = pack_bf2(v1[2 * j], v1[2 * j + 1]);
+          const uint32_t q2 = pack_bf2(v2[2 * j], v2[2 * j + 1]);
+          const float2 uf1 = f2_mul(f2_mul(bf2_to_f2(q1), rstd2), g[w]);
+          const float2 uf2 = f2_mul(f2_mul(bf2_to_f2(q2), rstd2), g[NP / 2 + w]);
+          const uint32_t u1 = pack_bf2(uf1.x, uf1.y);
+          const uint32_t u2 = pack_bf2(uf2.x, uf2.y);
+          const uint32_t c2 = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x5410);  // (cos_2w, cos_2w+1)
+          const uint32_t s2 = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x7632);  // (sin_2w, sin_2w+1)
+          o1[j] = bf2_add(bf2_mul(u1, c2), bf2_mul(bf2_neg(u2), s2));
+          o2[j] = bf2_add(bf2_mul(u2, c2), bf2_mul(u1, s2));
+        }
+        if (valid) {
+          store_row_u4(a, ohead + c * 16, o1, 2);
+          store_row_u4(a, ohead + NP + c * 16, o2, 2);
+        }
       }
     }
   }
