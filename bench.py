@@ -605,11 +605,10 @@ def run_qkv_fp32_rope(dev, flush) -> dict:
 
 
 def run_backward(dev, flush) -> dict:
-    """Backward of the bench layer's projection step (T = 4096, hidden 3584, QKV out 4608):
-    add-RMSNorm backward (dx, rstd and the per-row weight partials), the norm-weight fold, the
-    QKV GEMM's input gradient
-    through both weight sets, the rows of dqkv and y into plan order, and the gen set's weight
-    gradient (1024 rows)."""
+    """Backward of the bench layer's projection step (T = 4096, hidden 3584, QKV out 4608): the
+    QKV GEMM's input gradient through both weight sets, add-RMSNorm backward (dx, rstd and the
+    per-row weight partials), the norm-weight fold, and the gen set's weight gradient (1024 rows)
+    from token-order dqkv and y."""
     import torch
 
     import mixture_transformers_token_gb300 as mot
@@ -627,8 +626,6 @@ def run_backward(dev, flush) -> dict:
     rstd = torch.empty((T,), dtype=torch.float32, device=dev)
     dwn = torch.empty((2, H), dtype=torch.float32, device=dev)
     part = torch.empty((H // 64, T, 64), dtype=torch.float32, device=dev)
-    dq_plan = torch.empty_like(dqkv)
-    y_plan = torch.empty_like(y)
     dw_gen = torch.empty((N_QKV, H), dtype=torch.float32, device=dev)
     stages = [
         ("qkv_dx", lambda: mot.mot_routed_gemm_dx(dqkv, d["w_qkv"], ws, out=dy)),
@@ -636,8 +633,7 @@ def run_backward(dev, flush) -> dict:
                                                                 d_res_out=dres, dx=dxn, rstd=rstd,
                                                                 dw_partials=part)),
         ("rmsnorm_dweight", lambda: mot.mot_rmsnorm_dweight(part, ws, dw=dwn)),
-        ("gather_dqkv_y", lambda: (mot.mot_gather_rows(dqkv, ws, out=dq_plan), mot.mot_gather_rows(y, ws, out=y_plan))),
-        ("qkv_dw_gen", lambda: mot.mot_routed_gemm_dw(dq_plan, y_plan, ws, expert=1, out=dw_gen)),
+        ("qkv_dw_gen", lambda: mot.mot_routed_gemm_dw(dqkv, y, ws, expert=1, out=dw_gen)),
     ]
     r = time_stages(stages, 50, 5, flush, stream)
 
@@ -669,7 +665,6 @@ def run_backward(dev, flush) -> dict:
         "rmsnorm_dweight_us": round(r["rmsnorm_dweight"] * 1e6, 2),
         "rmsnorm_dweight_gbs": gbs(b_dw, "rmsnorm_dweight"),
         "rmsnorm_dweight_frac_hbm": round(b_dw / r["rmsnorm_dweight"] / 1e9 / pk["hbm_gbs"], 4),
-        "gather_dqkv_y_us": round(r["gather_dqkv_y"] * 1e6, 2),
         "qkv_dw_gen_us": round(r["qkv_dw_gen"] * 1e6, 2), "qkv_dw_gen_tflops": _tflops(f_dw, r["qkv_dw_gen"]),
         "qkv_dw_gen_frac": round(f_dw / r["qkv_dw_gen"] / 1e12 / pk["bf16_tflops"], 4),
         "gen_rows": n_gen, "step_us": round(rw["step"] * 1e6, 2),

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define MOT_ABI_VERSION 2
+#define MOT_ABI_VERSION 3
 
 /* host-detected status codes (return values) */
 #define MOT_OK            0
@@ -313,10 +313,15 @@ int mot_routed_gemm_dx(const mot_bf16* dout, const mot_bf16* w, int64_t T, int N
  * mot_routed_gemm_dw -- gradient of one weight set of the routed GEMM out = a W[mod]^T
  * ([RFC-435] §3 BAGEL-specific rules: phase A trains the gen set; §3 Numerical contract:
  * fixed accumulation order, no split-K or atomics).
- *   dout_plan [T][N] bf16    gradient of the forward output, rows in the plan's order
- *                            (mot_gather_rows, or a GEMM run with MOT_OUT_PLAN_ORDER).
- *   a_plan    [T][K] bf16    the forward GEMM's input, rows in the plan's order.
+ *   dout      [T][N] bf16    gradient of the forward output: rows in token order, or in the
+ *                            plan's order with MOT_A_PLAN_ORDER (mot_gather_rows, or a GEMM run
+ *                            with MOT_OUT_PLAN_ORDER).
+ *   a         [T][K] bf16    the forward GEMM's input, rows in the same order as dout.
  *   expert    0 (und) or 1 (gen): the weight set whose gradient is formed.
+ *   flags     MOT_A_PLAN_ORDER or 0. In token order, each 64-row block of the set whose rows
+ *             are consecutive token rows is read with one tiled copy, any other block by
+ *             four-row gathers through the plan; the same bytes reach the tensor cores either
+ *             way, so the result is the same bit for bit in both orders.
  *   ws        the routing plan of mod for this T.
  *   dw        [N][K] fp32    out: dw[n][k] = sum over the set's rows r of dout[r][n] a[r][k],
  *                            accumulated in fp32 on the tensor cores over the rows in
@@ -325,8 +330,8 @@ int mot_routed_gemm_dx(const mot_bf16* dout, const mot_bf16* w, int64_t T, int N
  * Geometry: N and K multiples of 256. A plan for another T sets MOT_DEV_PLAN_MISMATCH; a plan
  * that failed (bad modality) leaves dw undefined. Other errors as mot_routed_gemm.
  */
-int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_plan, int64_t T, int N, int K,
-                       int expert, void* ws, size_t ws_bytes, float* dw, void* stream);
+int mot_routed_gemm_dw(const mot_bf16* dout, const mot_bf16* a, int64_t T, int N, int K,
+                       int expert, int flags, void* ws, size_t ws_bytes, float* dw, void* stream);
 
 /*
  * mot_add_rmsnorm_backward -- input gradient of mot_fused_add_rmsnorm ([RFC-435] §3

@@ -31,7 +31,7 @@ __all__ = [
     "mot_flow_sde_step", "mot_flow_cfg_sde_step", "mot_flow_noise",
 ]
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 EPI_CAST = 0
 EPI_SWIGLU = 1
 A_PLAN_ORDER = 0x100
@@ -74,7 +74,7 @@ _SIGNATURES = {
                                         _c_p]),
     "mot_rmsnorm_dweight": (_c_i, [_c_p, _c_i64, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_dx": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
-    "mot_routed_gemm_dw": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
+    "mot_routed_gemm_dw": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_joint_attention": (_c_i, [_c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p]),
     "mot_flow_workspace_bytes": (_c_sz, [_c_i, _c_i64]),
     "mot_flow_schedule_host": (_c_i, [_c_i, ctypes.c_double, _c_p]),
@@ -336,23 +336,24 @@ def mot_routed_gemm_dx(dout, w, ws, flags: int = 0, out=None, stream=None):
     return out
 
 
-def mot_routed_gemm_dw(dout_plan, a_plan, ws, expert: int = 1, out=None, stream=None):
-    """Gradient [N][K] fp32 of weight set `expert` from plan-order rows of dout [T][N] and a [T][K]."""
-    T, N = dout_plan.shape
-    _dev(dout_plan, "dout_plan", torch.bfloat16, 2)
-    _dev(a_plan, "a_plan", torch.bfloat16, 2)
+def mot_routed_gemm_dw(dout, a, ws, expert: int = 1, flags: int = 0, out=None, stream=None):
+    """Gradient [N][K] fp32 of weight set `expert` from dout [T][N] and a [T][K]: rows in token
+    order, or in the plan's order with flags = A_PLAN_ORDER (the same bits either way)."""
+    T, N = dout.shape
+    _dev(dout, "dout", torch.bfloat16, 2)
+    _dev(a, "a", torch.bfloat16, 2)
     _dev(ws, "ws", torch.uint8, 1)
-    if a_plan.shape[0] != T:
-        raise ValueError("dout_plan and a_plan must have the same rows")
-    K = a_plan.shape[1]
+    if a.shape[0] != T:
+        raise ValueError("dout and a must have the same rows")
+    K = a.shape[1]
     if out is None:
-        out = torch.empty((N, K), dtype=torch.float32, device=dout_plan.device)
+        out = torch.empty((N, K), dtype=torch.float32, device=dout.device)
     _dev(out, "out", torch.float32, 2)
     if tuple(out.shape) != (N, K):
         raise ValueError(f"out must be [{N}, {K}]")
     _check("mot_routed_gemm_dw", _lib().mot_routed_gemm_dw(
-        dout_plan.data_ptr(), a_plan.data_ptr(), T, N, K, expert, ws.data_ptr(), ws.numel(), out.data_ptr(),
-        _stream(dout_plan, stream)))
+        dout.data_ptr(), a.data_ptr(), T, N, K, expert, flags, ws.data_ptr(), ws.numel(), out.data_ptr(),
+        _stream(dout, stream)))
     return out
 
 

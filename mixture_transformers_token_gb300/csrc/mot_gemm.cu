@@ -615,10 +615,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // dout[r][n] * a[r][k], fp32, no cast.
 // ---------------------------------------------------------------------------
 // Both operands are MN-major (the reduction runs over rows): A' = dout^T, 128 n per CTA, and
-// B' = a^T, 128 k per CTA, each staged as two 64-column boxes of 64 rows. The inputs are in
-// the plan's order, so the set's rows are one contiguous run; full 64-row blocks are tiled
-// loads, the last partial block is gathered four rows at a time with rows past the run
-// pointed outside the tensor, which the copy fills with zeros. Pair tiles cover 256 n x 256 k;
+// B' = a^T, 128 k per CTA, each staged as two 64-column boxes of 64 rows. The set's rows are
+// read in the plan's order, 64 at a time: from inputs in the plan's order a full block is one
+// tiled load; from inputs in token order it is one tiled load when its rows are consecutive
+// token rows, else it is gathered four rows at a time through the plan's permutation. The last
+// partial block is always gathered, with rows past the set pointed outside the tensor, which
+// the copy fills with zeros. Pair tiles cover 256 n x 256 k;
 // each accumulates its 64-row blocks in ascending order into one fp32 accumulator (no split
 // of the reduction), and the epilogue writes each accumulator row of dW from the lane that reads
 // it, in 32-byte sectors. The tiles from split_from on are each done as two 256 n x 128 k
@@ -627,6 +629,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // exposed epilogue halves too. A half covers its columns with the same ascending row blocks,
 // so the bits do not depend on the split.
 constexpr int kDwStages = 6;
+constexpr int kGathered = -0x7fffffff - 1;  // a run of tiles read by gathers
+constexpr int kNoTile = 0x7fffffff;
 constexpr int kDwBars = 2 * kDwStages + 5;
 constexpr size_t kDwSmem = 1024 + size_t(kDwStages) * STAGE_BYTES + 256;
 
@@ -638,6 +642,7 @@ struct DwArgs {
   float* dw;
   int st32;     // dw is 32-byte aligned (its rows, K * 4 bytes apart, then are too)
   int split_from;  // tiles from this index on are done as two halves of 128 k
+  int token_order;  // dout and a in token order (else in the plan's order)
 };
 
 // A work item of the dW grid: full tile u, or half h of tile u.
@@ -693,6 +698,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int row_start = args.expert == 0 ? 0 : hdr->count[0];
   const int count = hdr->count[args.expert];
   const int kblocks = (count + BK - 1) / BK;
+  // token-order inputs: a 64-row block of the set lies inside one 128-row tile of the plan, whose
+  // record says whether its rows are consecutive token rows (then one tiled load) or not (then
+  // four-row gathers through the plan's permutation)
+  const Tile* plan_tiles = reinterpret_cast<const Tile*>(args.ws + tiles_offset(args.T));
+  const int32_t* perm = reinterpret_cast<const int32_t*>(args.ws + perm_offset());
+  const int tile_first = args.expert == 0 ? 0 : (hdr->count[0] + kTileRows - 1) / kTileRows;
   const int m_tiles = args.N / BN, n_tiles = args.K / BN;
   const int total = m_tiles * n_tiles;
   const int items = args.split_from + 2 * (total - args.split_from);
@@ -735,6 +746,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
+    // In token order the set's tiles form runs: consecutive tiles whose rows are consecutive token
+    // rows at one offset from their plan positions (a full block is one tiled copy at plan
+    // position + offset), or consecutive tiles that are not (four-row gathers through the plan's
+    // permutation). The producer keeps the run of the block it reaches next in warp-uniform values
+    // (reductions across the warp), so no block's copies wait on per-block data: a tile-record
+    // load, or even a selection on one, per block costs the producer more than the MMA's time
+    // for the block. A run is looked up when the loop leaves the last one, in the tile records
+    // read 32 at a time, one per lane. In the plan's order the whole set is one run at offset 0.
+    const int set_tiles = (count + kTileRows - 1) / kTileRows;
+    int rec_chunk = -1, rec_cls = kGathered;  // the class of the set's tile 32 * rec_chunk + lane
+    int run_lo = 0, run_hi = kblocks, run_off = 0;  // blocks [run_lo, run_hi) and their offset
+    auto load_chunk = [&](int c) {
+      if (c != rec_chunk) {
+        rec_chunk = c;
+        const int t = 32 * c + lane;
+        const int r0 = t < set_tiles ? plan_tiles[tile_first + t].row0 : -1;
+        rec_cls = r0 >= 0 ? r0 - (row_start + t * kTileRows) : kGathered;
+      }
+    };
+    auto find_run = [&](int kb) {  // warp-collective: the run holding block kb, from kb on
+      const int t0 = (kb * BK) / kTileRows;
+      load_chunk(t0 >> 5);
+      const int cls = __reduce_max_sync(0xffffffffu, lane == (t0 & 31) ? rec_cls : kGathered);
+      int end = set_tiles;
+      for (int c = t0 >> 5; 32 * c < set_tiles; ++c) {
+        load_chunk(c);
+        const int t = 32 * c + lane;
+        const int first = __reduce_min_sync(0xffffffffu, t > t0 && t < set_tiles && rec_cls != cls ? t : kNoTile);
+        if (first != kNoTile) {
+          end = first;
+          break;
+        }
+      }
+      run_lo = kb;
+      run_hi = min(kblocks, end * (kTileRows / BK));
+      run_off = cls;
+    };
+    if (args.token_order) find_run(0);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -748,36 +797,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err));
         if (!ok) break;
         const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
-        const int row0 = row_start + kb * BK;
+        const int row0 = row_start + kb * BK;  // the block's first plan position
         const int valid = count - kb * BK;
+        const bool tiled = valid >= BK && run_off != kGathered;
+        const int y0 = tiled ? row0 + run_off : 0;  // its first input row
         const uint32_t da = smem_u32(sa + stage * A_BYTES), db = smem_u32(sb + stage * B_BYTES);
         if (lane == 0) {
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), stage_tx);
-          if (valid >= BK) {
-            tma_load_2d_pair(da, &tm_d, n0, row0, fb);
-            tma_load_2d_pair(da + A_BYTES / 2, &tm_d, n0 + 64, row0, fb);
-            tma_load_2d_pair(db, &tm_a, k0, row0, fb);
-            if (!w.split) tma_load_2d_pair(db + B_BYTES / 2, &tm_a, k0 + 64, row0, fb);
+          if (tiled) {
+            tma_load_2d_pair(da, &tm_d, n0, y0, fb);
+            tma_load_2d_pair(da + A_BYTES / 2, &tm_d, n0 + 64, y0, fb);
+            tma_load_2d_pair(db, &tm_a, k0, y0, fb);
+            if (!w.split) tma_load_2d_pair(db + B_BYTES / 2, &tm_a, k0 + 64, y0, fb);
           }
         }
         __syncwarp();
-        if (valid < BK) {
-          // 4 boxes x 16 four-row groups, two per lane (a half has no second B box); rows past
-          // the run read as zeros
+        if (!tiled) {
+          // 4 boxes x 16 four-row groups, two per lane (a half has no second B box), the lane's
+          // quad the same in both; rows past the set read as zeros
+          int r[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int p = (lane & 15) * 4 + i;
+            r[i] = p < valid ? (args.token_order ? perm[row0 + p] : row0 + p) : args.T;
+          }
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int idx = lane + 32 * q;
             const int box = idx >> 4, quad = idx & 15;
             if (w.split && box == 3) continue;
-            int r[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) r[i] = quad * 4 + i < valid ? row0 + quad * 4 + i : args.T;
             const uint32_t dst = (box < 2 ? da : db) + (box & 1) * (A_BYTES / 2) + quad * 512;
             const int x = (box < 2 ? n0 : k0) + 64 * (box & 1);
             tma_gather4_pair(dst, box < 2 ? static_cast<const void*>(&tm_d_rows) : static_cast<const void*>(&tm_a_rows),
                              x, r[0], r[1], r[2], r[3], fb);
           }
         }
+        const int next_kb = kb + 1 < kblocks ? kb + 1 : 0;  // the next item starts at block 0
+        if (args.token_order && (next_kb < run_lo || next_kb >= run_hi)) find_run(next_kb);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -1043,26 +1099,27 @@ extern "C" int mot_routed_gemm_dx(const mot_bf16* dout, const mot_bf16* w, int64
   return gemm::launch<gemm::EPI_CAST, true>(dout, w, int(T), K, N, a, dev, s);
 }
 
-extern "C" int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_plan, int64_t T, int N, int K,
-                                  int expert, void* ws, size_t ws_bytes, float* dw, void* stream) {
-  if (!dout_plan || !a_plan || !ws || !dw) return MOT_ERR_NULL;
+extern "C" int mot_routed_gemm_dw(const mot_bf16* dout, const mot_bf16* a_in, int64_t T, int N, int K,
+                                  int expert, int flags, void* ws, size_t ws_bytes, float* dw, void* stream) {
+  if (!dout || !a_in || !ws || !dw) return MOT_ERR_NULL;
   if (expert != 0 && expert != 1) return MOT_ERR_ARG;
+  if ((flags & ~MOT_A_PLAN_ORDER) != 0) return MOT_ERR_ARG;
   if (T < 1 || T > MOT_MAX_TOKENS) return MOT_ERR_GEOMETRY;
   if (N < gemm::BN || N % gemm::BN != 0 || N > (1 << 20)) return MOT_ERR_GEOMETRY;
   if (K < gemm::BN || K % gemm::BN != 0 || K > (1 << 20)) return MOT_ERR_GEOMETRY;
-  if (!aligned16(dout_plan) || !aligned16(a_plan) || !aligned16(ws) || !aligned16(dw)) return MOT_ERR_ALIGN;
+  if (!aligned16(dout) || !aligned16(a_in) || !aligned16(ws) || !aligned16(dw)) return MOT_ERR_ALIGN;
   if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const void* ptrs[] = {dout_plan, a_plan, ws, dw};
+  const void* ptrs[] = {dout, a_in, ws, dw};
   int dev = -1;
   int st = check_device(s, ptrs, 4, &dev);
   if (st != MOT_OK) return st;
   DeviceGuard guard(dev);
   CUtensorMap tm_d, tm_d_rows, tm_a, tm_a_rows;
-  if (!make_tmap_bf16(&tm_d, dout_plan, uint64_t(N), uint64_t(T), 64, gemm::BK) ||
-      !make_tmap_bf16(&tm_d_rows, dout_plan, uint64_t(N), uint64_t(T), 64, 1) ||
-      !make_tmap_bf16(&tm_a, a_plan, uint64_t(K), uint64_t(T), 64, gemm::BK) ||
-      !make_tmap_bf16(&tm_a_rows, a_plan, uint64_t(K), uint64_t(T), 64, 1))
+  if (!make_tmap_bf16(&tm_d, dout, uint64_t(N), uint64_t(T), 64, gemm::BK) ||
+      !make_tmap_bf16(&tm_d_rows, dout, uint64_t(N), uint64_t(T), 64, 1) ||
+      !make_tmap_bf16(&tm_a, a_in, uint64_t(K), uint64_t(T), 64, gemm::BK) ||
+      !make_tmap_bf16(&tm_a_rows, a_in, uint64_t(K), uint64_t(T), 64, 1))
     return MOT_ERR_CUDA;
   if (cudaFuncSetAttribute(gemm::routed_gemm_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(gemm::kDwSmem)) != cudaSuccess)
@@ -1076,6 +1133,7 @@ extern "C" int mot_routed_gemm_dw(const mot_bf16* dout_plan, const mot_bf16* a_p
   a.expert = expert;
   a.dw = dw;
   a.st32 = reinterpret_cast<uintptr_t>(dw) % 32 == 0 ? 1 : 0;
+  a.token_order = (flags & MOT_A_PLAN_ORDER) ? 0 : 1;
   const int64_t total = int64_t(N / gemm::BN) * (K / gemm::BN);
   // same threads and cluster shape as the routed kernel and more shared memory than half an
   // SM: one pair per two SMs, the same residency

@@ -172,12 +172,13 @@ def test_gemm_backward_rejects(lib):
     assert dx(A, MIS, 8, 64, 256, 0, B, 1 << 20, C, None) == MOT_ERR_ALIGN
     assert dx(A, A, 1000, 64, 256, 0, B, 100, C, None) == MOT_ERR_WORKSPACE
     dw = lib.mot_routed_gemm_dw
-    assert dw(None, A, 8, 256, 256, 1, B, 1 << 20, C, None) == MOT_ERR_NULL
-    assert dw(A, A, 8, 256, 256, 2, B, 1 << 20, C, None) == MOT_ERR_ARG
-    assert dw(A, A, 8, 128, 256, 1, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
-    assert dw(A, A, 8, 256, 320, 1, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
-    assert dw(A, A, 8, 256, 256, 1, B, 1 << 20, MIS, None) == MOT_ERR_ALIGN
-    assert dw(A, A, 1000, 256, 256, 1, B, 100, C, None) == MOT_ERR_WORKSPACE
+    assert dw(None, A, 8, 256, 256, 1, 0, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert dw(A, A, 8, 256, 256, 2, 0, B, 1 << 20, C, None) == MOT_ERR_ARG
+    assert dw(A, A, 8, 256, 256, 1, 0x200, B, 1 << 20, C, None) == MOT_ERR_ARG     # only MOT_A_PLAN_ORDER
+    assert dw(A, A, 8, 128, 256, 1, 0, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert dw(A, A, 8, 256, 320, 1, 0x100, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert dw(A, A, 8, 256, 256, 1, 0, B, 1 << 20, MIS, None) == MOT_ERR_ALIGN
+    assert dw(A, A, 1000, 256, 256, 1, 0, B, 100, C, None) == MOT_ERR_WORKSPACE
 
 
 def test_joint_attention_rejects(lib):

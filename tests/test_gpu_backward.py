@@ -218,7 +218,7 @@ def _dw_run(dout, a, mod, expert):
     ws = mot.mot_route_plan(mod.cuda())
     dp = mot.mot_gather_rows(dout.cuda(), ws)
     ap = mot.mot_gather_rows(a.cuda(), ws)
-    dw = mot.mot_routed_gemm_dw(dp, ap, ws, expert=expert)
+    dw = mot.mot_routed_gemm_dw(dp, ap, ws, expert=expert, flags=mot.A_PLAN_ORDER)
     assert mot.mot_device_status(ws) == 0
     return dw
 
@@ -291,6 +291,48 @@ def test_routed_gemm_dw_into_16_byte_aligned_output_gives_the_same_bits():
     buf = torch.empty(N * K + 4, dtype=torch.float32, device="cuda")
     out = buf[4:4 + N * K].view(N, K)
     assert out.data_ptr() % 32 == 16
-    mot.mot_routed_gemm_dw(dp, ap, ws, expert=1, out=out)
+    mot.mot_routed_gemm_dw(dp, ap, ws, expert=1, flags=mot.A_PLAN_ORDER, out=out)
     assert mot.mot_device_status(ws) == 0
     assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+
+
+@pytest.mark.parametrize("T,N,K,layout,expert", [(300, 256, 512, "scatter", 1), (300, 256, 512, "scatter", 0),
+                                                 (1000, 768, 1024, "blocks", 0), (1000, 768, 1024, "blocks", 1),
+                                                 (4096, 4608, 3584, "bagel", 1), (777, 2560, 2816, "mixed", 1),
+                                                 (129, 512, 256, "gen", 1), (64, 256, 256, "und", 1),
+                                                 (36864, 256, 256, "cfg", 1), (36000, 256, 256, "cfg_ragged", 1),
+                                                 (36000, 256, 256, "cfg_ragged", 0), (9000, 256, 512, "runs", 1)])
+def test_routed_gemm_dw_token_order_gives_the_plan_order_bits(T, N, K, layout, expert):
+    # token-order inputs: consecutive 64-row blocks by tiled loads, the others (and the ragged
+    # last block) by four-row gathers through the plan; the same bytes as from gathered inputs.
+    # cfg: 12 runs of 8 consecutive gen tiles at different offsets (96 tiles, three chunks of 32
+    # tile records); cfg_ragged: runs of 1000 rows, so a gathered tile sits between runs; runs:
+    # runs of 1500 gen rows, one crossing the 32-tile boundary of the records
+    rng = W.rng_for(17, T + N)
+    if layout == "cfg":
+        mod = W.cfg_pack_layout(12, 2048, 1024)[0]
+    elif layout == "cfg_ragged":
+        mod = W.modality_blocks([b for _ in range(12) for b in ((0, 2000), (1, 1000))])
+    elif layout == "runs":
+        mod = W.modality_blocks([b for _ in range(4) for b in ((1, 1500), (0, 700))] + [(1, 200)])
+    elif layout == "scatter":
+        mod = W.modality_bernoulli(rng, T, 0.4)
+    elif layout == "blocks":
+        mod = W.modality_blocks([(0, 300), (1, 200), (0, 100), (1, T - 600)])
+    elif layout == "bagel":
+        mod = W.modality_blocks([(0, 3 * T // 4), (1, T - 3 * T // 4)])
+    elif layout == "mixed":  # a long consecutive gen run, then scattered rows
+        m = np.zeros(T, np.uint8)
+        m[100:400] = 1
+        m[400:] = (rng.random(T - 400) < 0.3).astype(np.uint8)
+        mod = torch.from_numpy(m)
+    else:
+        mod = torch.full((T,), 1 if layout == "gen" else 0, dtype=torch.uint8)
+    dout = W.bf16_normal(W.rng_for(17, 1), (T, N)).cuda()
+    a = W.bf16_normal(W.rng_for(17, 2), (T, K)).cuda()
+    ws = mot.mot_route_plan(mod.cuda())
+    ref = mot.mot_routed_gemm_dw(mot.mot_gather_rows(dout, ws), mot.mot_gather_rows(a, ws), ws, expert=expert,
+                                 flags=mot.A_PLAN_ORDER)
+    got = mot.mot_routed_gemm_dw(dout, a, ws, expert=expert)
+    assert mot.mot_device_status(ws) == 0
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
