@@ -615,24 +615,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // dout[r][n] * a[r][k], fp32, no cast.
 // ---------------------------------------------------------------------------
 // Both operands are MN-major (the reduction runs over rows): A' = dout^T, 128 n per CTA, and
-// B' = a^T, 128 k per CTA, each staged as two 64-column boxes of 64 rows. The set's rows are
-// read in the plan's order, 64 at a time: from inputs in the plan's order a full block is one
-// tiled load; from inputs in token order it is one tiled load when its rows are consecutive
-// token rows, else it is gathered four rows at a time through the plan's permutation. The last
-// partial block is always gathered, with rows past the set pointed outside the tensor, which
-// the copy fills with zeros. Pair tiles cover 256 n x 256 k;
-// each accumulates its 64-row blocks in ascending order into one fp32 accumulator (no split
-// of the reduction), and the epilogue writes each accumulator row of dW from the lane that reads
-// it, in 32-byte sectors. The tiles from split_from on are each done as two 256 n x 128 k
+// B' = a^T, 128 k per CTA, each staged as two 64-column boxes of 128 rows. The set's rows are
+// read in the plan's order, 128 at a time (one tile of the plan): from inputs in the plan's
+// order a full block is one tiled load per box; from inputs in token order it is one tiled
+// load per box when its rows are consecutive token rows, else it is gathered four rows at a
+// time through the plan's permutation. The last partial block is always gathered, with rows
+// past the set pointed outside the tensor, which the copy fills with zeros, and its MMAs stop
+// at the last 16-row group that holds a row of the set. Pair tiles cover 256 n x 256 k; each
+// accumulates its row blocks in ascending order, 16 rows per MMA, into one fp32 accumulator (no
+// split of the reduction), and the epilogue writes each accumulator row of dW from the lane
+// that reads it, in 32-byte sectors. The tiles from split_from on are each done as two 256 n x 128 k
 // halves (N = 128 MMAs, one B box per CTA): the host splits the tiles of a last round that
 // would leave at least half the clusters idle, so that round takes half as long and its
 // exposed epilogue halves too. A half covers its columns with the same ascending row blocks,
 // so the bits do not depend on the split.
-constexpr int kDwStages = 6;
+constexpr int kDwStages = 3;
+constexpr int DW_BK = 128;  // rows of the set per stage (one tile of the plan)
+constexpr uint32_t DW_A_BYTES = BM * DW_BK * 2, DW_B_BYTES = BN_HALF * DW_BK * 2;
+constexpr uint32_t DW_STAGE_BYTES = DW_A_BYTES + DW_B_BYTES;  // 64 KB
 constexpr int kGathered = -0x7fffffff - 1;  // a run of tiles read by gathers
 constexpr int kNoTile = 0x7fffffff;
 constexpr int kDwBars = 2 * kDwStages + 5;
-constexpr size_t kDwSmem = 1024 + size_t(kDwStages) * STAGE_BYTES + 256;
+constexpr size_t kDwSmem = 1024 + size_t(kDwStages) * DW_STAGE_BYTES + 256;
 
 struct DwArgs {
   const uint8_t* ws;
@@ -675,8 +679,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int STAGES = kDwStages;
   uint8_t* sa = smem;
-  uint8_t* sb = smem + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* sb = smem + STAGES * DW_A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * DW_STAGE_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -697,10 +701,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (hdr->count[0] + hdr->count[1] != args.T) return;  // no plan (bad modality): nothing is defined
   const int row_start = args.expert == 0 ? 0 : hdr->count[0];
   const int count = hdr->count[args.expert];
-  const int kblocks = (count + BK - 1) / BK;
-  // token-order inputs: a 64-row block of the set lies inside one 128-row tile of the plan, whose
-  // record says whether its rows are consecutive token rows (then one tiled load) or not (then
-  // four-row gathers through the plan's permutation)
+  const int kblocks = (count + DW_BK - 1) / DW_BK;
+  // token-order inputs: a row block of the set is one 128-row tile of the plan, whose record says
+  // whether its rows are consecutive token rows (then tiled loads) or not (then four-row gathers
+  // through the plan's permutation)
   const Tile* plan_tiles = reinterpret_cast<const Tile*>(args.ws + tiles_offset(args.T));
   const int32_t* perm = reinterpret_cast<const int32_t*>(args.ws + perm_offset());
   const int tile_first = args.expert == 0 ? 0 : (hdr->count[0] + kTileRows - 1) / kTileRows;
@@ -766,7 +770,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
     };
     auto find_run = [&](int kb) {  // warp-collective: the run holding block kb, from kb on
-      const int t0 = (kb * BK) / kTileRows;
+      const int t0 = (kb * DW_BK) / kTileRows;
       load_chunk(t0 >> 5);
       const int cls = __reduce_max_sync(0xffffffffu, lane == (t0 & 31) ? rec_cls : kGathered);
       int end = set_tiles;
@@ -780,7 +784,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
       run_lo = kb;
-      run_hi = min(kblocks, end * (kTileRows / BK));
+      run_hi = min(kblocks, end * (kTileRows / DW_BK));
       run_off = cls;
     };
     if (args.token_order) find_run(0);
@@ -792,41 +796,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int n0 = w.mt * BN + int(rank) * BN_HALF;  // this CTA's 128 rows of dW
       // this CTA's 128 (a half: 64) columns of the B' operand
       const int k0 = w.nt * BN + (w.split ? w.h * BN_HALF + int(rank) * 64 : int(rank) * BN_HALF);
-      const uint32_t stage_tx = w.split ? 2 * (A_BYTES + B_BYTES / 2) : 2 * STAGE_BYTES;
+      const uint32_t stage_tx = w.split ? 2 * (DW_A_BYTES + DW_B_BYTES / 2) : 2 * DW_STAGE_BYTES;
       for (int kb = 0; kb < kblocks; ++kb) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err));
         if (!ok) break;
         const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
-        const int row0 = row_start + kb * BK;  // the block's first plan position
-        const int valid = count - kb * BK;
-        const bool tiled = valid >= BK && run_off != kGathered;
+        const int row0 = row_start + kb * DW_BK;  // the block's first plan position
+        const int valid = count - kb * DW_BK;
+        const bool tiled = valid >= DW_BK && run_off != kGathered;
         const int y0 = tiled ? row0 + run_off : 0;  // its first input row
-        const uint32_t da = smem_u32(sa + stage * A_BYTES), db = smem_u32(sb + stage * B_BYTES);
+        const uint32_t da = smem_u32(sa + stage * DW_A_BYTES), db = smem_u32(sb + stage * DW_B_BYTES);
         if (lane == 0) {
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), stage_tx);
           if (tiled) {
             tma_load_2d_pair(da, &tm_d, n0, y0, fb);
-            tma_load_2d_pair(da + A_BYTES / 2, &tm_d, n0 + 64, y0, fb);
+            tma_load_2d_pair(da + DW_A_BYTES / 2, &tm_d, n0 + 64, y0, fb);
             tma_load_2d_pair(db, &tm_a, k0, y0, fb);
-            if (!w.split) tma_load_2d_pair(db + B_BYTES / 2, &tm_a, k0 + 64, y0, fb);
+            if (!w.split) tma_load_2d_pair(db + DW_B_BYTES / 2, &tm_a, k0 + 64, y0, fb);
           }
         }
         __syncwarp();
         if (!tiled) {
-          // 4 boxes x 16 four-row groups, two per lane (a half has no second B box), the lane's
-          // quad the same in both; rows past the set read as zeros
+          // 4 boxes x 32 four-row groups, lane l the group l of each box (a half has no second B
+          // box); rows past the set read as zeros
           int r[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int p = (lane & 15) * 4 + i;
+            const int p = lane * 4 + i;
             r[i] = p < valid ? (args.token_order ? perm[row0 + p] : row0 + p) : args.T;
           }
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int idx = lane + 32 * q;
-            const int box = idx >> 4, quad = idx & 15;
+          for (int box = 0; box < 4; ++box) {
             if (w.split && box == 3) continue;
-            const uint32_t dst = (box < 2 ? da : db) + (box & 1) * (A_BYTES / 2) + quad * 512;
+            const uint32_t dst = (box < 2 ? da : db) + (box & 1) * (box < 2 ? DW_A_BYTES / 2 : DW_B_BYTES / 2) + lane * 512;
             const int x = (box < 2 ? n0 : k0) + 64 * (box & 1);
             tma_gather4_pair(dst, box < 2 ? static_cast<const void*>(&tm_d_rows) : static_cast<const void*>(&tm_a_rows),
                              x, r[0], r[1], r[2], r[3], fb);
@@ -868,11 +870,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t a0 = smem_u32(sa + stage * A_BYTES), b0 = smem_u32(sb + stage * B_BYTES);
+            const uint32_t a0 = smem_u32(sa + stage * DW_A_BYTES), b0 = smem_u32(sb + stage * DW_B_BYTES);
+            // K16 steps up to the last 16-row group that holds a row of the set
+            const int valid = count - kb * DW_BK;
+            const int nk = valid >= DW_BK ? DW_BK / 16 : (valid + 15) / 16;
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              mma_bf16_pair(d, smem_desc_mn_sw128(a0 + k * 2048, A_BYTES / 2),
-                            smem_desc_mn_sw128(b0 + k * 2048, B_BYTES / 2), idesc, (kb | k) != 0);
+            for (int k = 0; k < DW_BK / 16; ++k)
+              if (k < nk)
+                mma_bf16_pair(d, smem_desc_mn_sw128(a0 + k * 2048, DW_A_BYTES / 2), smem_desc_mn_sw128(b0 + k * 2048, DW_B_BYTES / 2),
+                              idesc, (kb | k) != 0);
             mma_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
           }
           __syncwarp();
@@ -1116,9 +1122,9 @@ extern "C" int mot_routed_gemm_dw(const mot_bf16* dout, const mot_bf16* a_in, in
   if (st != MOT_OK) return st;
   DeviceGuard guard(dev);
   CUtensorMap tm_d, tm_d_rows, tm_a, tm_a_rows;
-  if (!make_tmap_bf16(&tm_d, dout, uint64_t(N), uint64_t(T), 64, gemm::BK) ||
+  if (!make_tmap_bf16(&tm_d, dout, uint64_t(N), uint64_t(T), 64, gemm::DW_BK) ||
       !make_tmap_bf16(&tm_d_rows, dout, uint64_t(N), uint64_t(T), 64, 1) ||
-      !make_tmap_bf16(&tm_a, a_in, uint64_t(K), uint64_t(T), 64, gemm::BK) ||
+      !make_tmap_bf16(&tm_a, a_in, uint64_t(K), uint64_t(T), 64, gemm::DW_BK) ||
       !make_tmap_bf16(&tm_a_rows, a_in, uint64_t(K), uint64_t(T), 64, 1))
     return MOT_ERR_CUDA;
   if (cudaFuncSetAttribute(gemm::routed_gemm_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -224,11 +224,13 @@ def _dw_run(dout, a, mod, expert):
 
 
 @pytest.mark.parametrize("T,N,K,mode,expert", [(300, 256, 512, "scatter", 1), (300, 256, 512, "scatter", 0),
-                                               (129, 512, 256, "gen", 1), (64, 256, 256, "scatter", 0),
+                                               (129, 512, 256, "gen", 1), (250, 256, 256, "gen", 1),
+                                               (64, 256, 256, "scatter", 0),
                                                (1000, 768, 1024, "blocks", 0), (300, 2560, 2816, "scatter", 1)])
 def test_routed_gemm_dw_integer_inputs_exact(T, N, K, mode, expert):
     # small problems run every tile as two 128-column halves; 10 x 11 tiles on 76 clusters run
-    # 76 whole tiles and the last 34 as halves
+    # 76 whole tiles and the last 34 as halves; the sets' last 128-row blocks hold 1 (T = 129),
+    # 122 (T = 250) and about 60 rows
     rng = W.rng_for(13, T + N + expert)
     if mode == "scatter":
         mod = W.modality_bernoulli(rng, T, 0.4)
