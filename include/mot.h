@@ -318,8 +318,8 @@ int mot_routed_gemm_dx(const mot_bf16* dout, const mot_bf16* w, int64_t T, int N
  *                            with MOT_OUT_PLAN_ORDER).
  *   a         [T][K] bf16    the forward GEMM's input, rows in the same order as dout.
  *   expert    0 (und) or 1 (gen): the weight set whose gradient is formed.
- *   flags     MOT_A_PLAN_ORDER or 0. In token order, each 64-row block of the set whose rows
- *             are consecutive token rows is read with one tiled copy, any other block by
+ *   flags     MOT_A_PLAN_ORDER or 0. In token order, each 128-row block of the set whose rows
+ *             are consecutive token rows is read with tiled copies, any other block by
  *             four-row gathers through the plan; the same bytes reach the tensor cores either
  *             way, so the result is the same bit for bit in both orders.
  *   ws        the routing plan of mod for this T.

@@ -305,7 +305,7 @@ def test_routed_gemm_dw_into_16_byte_aligned_output_gives_the_same_bits():
                                                  (36864, 256, 256, "cfg", 1), (36000, 256, 256, "cfg_ragged", 1),
                                                  (36000, 256, 256, "cfg_ragged", 0), (9000, 256, 512, "runs", 1)])
 def test_routed_gemm_dw_token_order_gives_the_plan_order_bits(T, N, K, layout, expert):
-    # token-order inputs: consecutive 64-row blocks by tiled loads, the others (and the ragged
+    # token-order inputs: consecutive 128-row blocks by tiled loads, the others (and the ragged
     # last block) by four-row gathers through the plan; the same bytes as from gathered inputs.
     # cfg: 12 runs of 8 consecutive gen tiles at different offsets (96 tiles, three chunks of 32
     # tile records); cfg_ragged: runs of 1000 rows, so a gathered tile sits between runs; runs:
