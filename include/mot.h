@@ -319,9 +319,10 @@ int mot_routed_gemm_dx(const mot_bf16* dout, const mot_bf16* w, int64_t T, int N
  *   a         [T][K] bf16    the forward GEMM's input, rows in the same order as dout.
  *   expert    0 (und) or 1 (gen): the weight set whose gradient is formed.
  *   flags     MOT_A_PLAN_ORDER or 0. In token order, each 128-row block of the set whose rows
- *             are consecutive token rows is read with tiled copies, any other block by
- *             four-row gathers through the plan; the same bytes reach the tensor cores either
- *             way, so the result is the same bit for bit in both orders.
+ *             are consecutive token rows is read with tiled copies; any other block is read in
+ *             16-row groups, tiled where the group's rows are consecutive, else by four-row
+ *             gathers through the plan. The same bytes reach the tensor cores either way, so
+ *             the result is the same bit for bit in both orders.
  *   ws        the routing plan of mod for this T.
  *   dw        [N][K] fp32    out: dw[n][k] = sum over the set's rows r of dout[r][n] a[r][k],
  *                            accumulated in fp32 on the tensor cores over the rows in

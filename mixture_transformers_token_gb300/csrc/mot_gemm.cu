@@ -618,14 +618,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // B' = a^T, 128 k per CTA, each staged as two 64-column boxes of 128 rows. The set's rows are
 // read in the plan's order, 128 at a time (one tile of the plan): from inputs in the plan's
 // order a full block is one tiled load per box; from inputs in token order it is one tiled
-// load per box when its rows are consecutive token rows, else it is gathered four rows at a
-// time through the plan's permutation. The last partial block is always gathered, with rows
-// past the set pointed outside the tensor, which the copy fills with zeros, and its MMAs stop
-// at the last 16-row group that holds a row of the set. Pair tiles cover 256 n x 256 k; each
-// accumulates its row blocks in ascending order, 16 rows per MMA, into one fp32 accumulator (no
-// split of the reduction), and the epilogue writes each accumulator row of dW from the lane
-// that reads it, in 32-byte sectors. The tiles from split_from on are each done as two 256 n x 128 k
-// halves (N = 128 MMAs, one B box per CTA): the host splits the tiles of a last round that
+// load per box when its rows are consecutive token rows. Any other block (and the last partial
+// one) is read in 16-row groups: a group of 16 consecutive token rows of the set by one tiled
+// load per box, any other group four rows at a time through the plan's permutation, with rows
+// past the set pointed outside the tensor, which the copy fills with zeros. The last block's
+// MMAs stop at the last 16-row group that holds a row of the set. Pair tiles cover 256 n x
+// 256 k; each accumulates its row blocks in ascending order, 16 rows per MMA, into one fp32
+// accumulator (no split of the reduction), and the epilogue writes each accumulator row of dW
+// from the lane that reads it, in 32-byte sectors. The tiles from split_from on are each done as
+// two 256 n x 128 k halves (N = 128 MMAs, one B box per CTA): the host splits the tiles of a last round that
 // would leave at least half the clusters idle, so that round takes half as long and its
 // exposed epilogue halves too. A half covers its columns with the same ascending row blocks,
 // so the bits do not depend on the split.
@@ -673,7 +674,8 @@ __device__ __forceinline__ DwItem dw_item(int it, int split_from, int m_tiles) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     routed_gemm_dw_kernel(const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_d_rows,
-                          const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_rows,
+                          const __grid_constant__ CUtensorMap tm_d16, const __grid_constant__ CUtensorMap tm_a,
+                          const __grid_constant__ CUtensorMap tm_a_rows, const __grid_constant__ CUtensorMap tm_a16,
                           const DwArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -736,8 +738,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tm_d);
     tma_prefetch_desc(&tm_d_rows);
+    tma_prefetch_desc(&tm_d16);
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_a_rows);
+    tma_prefetch_desc(&tm_a16);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
@@ -817,21 +821,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
         if (!tiled) {
-          // 4 boxes x 32 four-row groups, lane l the group l of each box (a half has no second B
-          // box); rows past the set read as zeros
+          // Lane l holds the block's rows 4 l .. 4 l + 3 (rows past the set point outside the
+          // tensor and read as zeros). The set's rows ascend in token order, so a 16-row group
+          // (lanes 4 g .. 4 g + 3) whose last row is its first + 15 is 16 consecutive token rows:
+          // one tiled copy per box from its group leader; any other group is four-row gathers
+          // from each of its lanes (a half has no second B box). Same bytes either way.
           int r[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int p = lane * 4 + i;
             r[i] = p < valid ? (args.token_order ? perm[row0 + p] : row0 + p) : args.T;
           }
+          const int g = lane >> 2;
+          const int first = __shfl_sync(0xffffffffu, r[0], lane & ~3);
+          const int last = __shfl_sync(0xffffffffu, r[3], lane | 3);
+          const bool whole = 16 * g + 15 < valid && last - first == 15;
 #pragma unroll
           for (int box = 0; box < 4; ++box) {
             if (w.split && box == 3) continue;
-            const uint32_t dst = (box < 2 ? da : db) + (box & 1) * (box < 2 ? DW_A_BYTES / 2 : DW_B_BYTES / 2) + lane * 512;
+            const uint32_t base = (box < 2 ? da : db) + (box & 1) * (box < 2 ? DW_A_BYTES / 2 : DW_B_BYTES / 2);
             const int x = (box < 2 ? n0 : k0) + 64 * (box & 1);
-            tma_gather4_pair(dst, box < 2 ? static_cast<const void*>(&tm_d_rows) : static_cast<const void*>(&tm_a_rows),
-                             x, r[0], r[1], r[2], r[3], fb);
+            if (whole) {
+              if ((lane & 3) == 0)
+                tma_load_2d_pair(base + g * 2048, box < 2 ? &tm_d16 : &tm_a16, x, first, fb);
+            } else {
+              tma_gather4_pair(base + lane * 512,
+                               box < 2 ? static_cast<const void*>(&tm_d_rows) : static_cast<const void*>(&tm_a_rows), x,
+                               r[0], r[1], r[2], r[3], fb);
+            }
           }
         }
         const int next_kb = kb + 1 < kblocks ? kb + 1 : 0;  // the next item starts at block 0
@@ -1121,9 +1138,11 @@ extern "C" int mot_routed_gemm_dw(const mot_bf16* dout, const mot_bf16* a_in, in
   int st = check_device(s, ptrs, 4, &dev);
   if (st != MOT_OK) return st;
   DeviceGuard guard(dev);
-  CUtensorMap tm_d, tm_d_rows, tm_a, tm_a_rows;
+  CUtensorMap tm_d, tm_d_rows, tm_d16, tm_a, tm_a_rows, tm_a16;
   if (!make_tmap_bf16(&tm_d, dout, uint64_t(N), uint64_t(T), 64, gemm::DW_BK) ||
       !make_tmap_bf16(&tm_d_rows, dout, uint64_t(N), uint64_t(T), 64, 1) ||
+      !make_tmap_bf16(&tm_d16, dout, uint64_t(N), uint64_t(T), 64, 16) ||
+      !make_tmap_bf16(&tm_a16, a_in, uint64_t(K), uint64_t(T), 64, 16) ||
       !make_tmap_bf16(&tm_a, a_in, uint64_t(K), uint64_t(T), 64, gemm::DW_BK) ||
       !make_tmap_bf16(&tm_a_rows, a_in, uint64_t(K), uint64_t(T), 64, 1))
     return MOT_ERR_CUDA;
@@ -1153,7 +1172,7 @@ extern "C" int mot_routed_gemm_dw(const mot_bf16* dout, const mot_bf16* a_in, in
   a.split_from = int(split_from);
   const int64_t clusters = items < cap ? items : cap;
   const cudaError_t e = launch_dependent(gemm::routed_gemm_dw_kernel, dim3(unsigned(2 * clusters)),
-                                         dim3(gemm::THREADS), gemm::kDwSmem, s, tm_d, tm_d_rows, tm_a, tm_a_rows, a);
+                                         dim3(gemm::THREADS), gemm::kDwSmem, s, tm_d, tm_d_rows, tm_d16, tm_a, tm_a_rows, tm_a16, a);
   return e == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
