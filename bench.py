@@ -48,7 +48,7 @@ def norm_bytes(t: int, h: int) -> int:
 
 # DRAM traffic of one QKV kernel launch from an ncu capture of this workload, keyed by the
 # hash of the kernel source it was taken on (null once the kernel has changed).
-NCU_TRAFFIC = {"5e9fcf999d413087": 127865344}
+NCU_TRAFFIC = {"c684d9c7f878127e": 127496448}
 
 
 def src_hash(name: str) -> str:
