@@ -755,13 +755,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
     // In token order the set's tiles form runs: consecutive tiles whose rows are consecutive token
-    // rows at one offset from their plan positions (a full block is one tiled copy at plan
-    // position + offset), or consecutive tiles that are not (four-row gathers through the plan's
-    // permutation). The producer keeps the run of the block it reaches next in warp-uniform values
-    // (reductions across the warp), so no block's copies wait on per-block data: a tile-record
-    // load, or even a selection on one, per block costs the producer more than the MMA's time
-    // for the block. A run is looked up when the loop leaves the last one, in the tile records
-    // read 32 at a time, one per lane. In the plan's order the whole set is one run at offset 0.
+    // rows at one offset from their plan positions (a full block is one tiled copy per box at plan
+    // position + offset), or consecutive tiles that are not (read in 16-row groups, below). The
+    // producer keeps the run of the block it reaches next in warp-uniform values (reductions
+    // across the warp), so no block's copies wait on per-block data: a tile-record load, or even
+    // a selection on one, per block costs the producer more than the MMA's time for the block. A
+    // run is looked up when the loop leaves the last one, in the tile records read 32 at a time,
+    // one per lane. In the plan's order the whole set is one run at offset 0.
     const int set_tiles = (count + kTileRows - 1) / kTileRows;
     int rec_chunk = -1, rec_cls = kGathered;  // the class of the set's tile 32 * rec_chunk + lane
     int run_lo = 0, run_hi = kblocks, run_off = 0;  // blocks [run_lo, run_hi) and their offset
