@@ -48,7 +48,7 @@ def norm_bytes(t: int, h: int) -> int:
 
 # DRAM traffic of one QKV kernel launch from an ncu capture of this workload, keyed by the
 # hash of the kernel source it was taken on (null once the kernel has changed).
-NCU_TRAFFIC = {"c684d9c7f878127e": 127496448}
+NCU_TRAFFIC = {"9ab96611dfcd50e6": 127521792}
 
 
 def src_hash(name: str) -> str:
