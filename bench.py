@@ -608,7 +608,8 @@ def run_backward(dev, flush) -> dict:
     """Backward of the bench layer's projection step (T = 4096, hidden 3584, QKV out 4608): the
     QKV GEMM's input gradient through both weight sets, add-RMSNorm backward (dx, rstd and the
     per-row weight partials), the norm-weight fold, and the gen set's weight gradient (1024 rows)
-    from token-order dqkv and y."""
+    from token-order dqkv and y; and the same chain in phase A (the gen set trained: the norm's
+    weight partials and fold of the gen rows only)."""
     import torch
 
     import mixture_transformers_token_gb300 as mot
@@ -636,14 +637,30 @@ def run_backward(dev, flush) -> dict:
         ("qkv_dw_gen", lambda: mot.mot_routed_gemm_dw(dqkv, y, ws, expert=1, out=dw_gen)),
     ]
     r = time_stages(stages, 50, 5, flush, stream)
+    # phase A of the BAGEL training rules trains the gen set only: the norm backward writes the
+    # gen rows' weight partials alone (every row's dx still) and the fold runs over the gen set
+    stages_a = [
+        stages[0],
+        ("add_rmsnorm_dx", lambda: mot.mot_add_rmsnorm_backward(dy, s_res, d["w_norm"], shape.eps, ws,
+                                                                d_res_out=dres, dx=dxn, rstd=rstd,
+                                                                dw_partials=part, partial_sets=mot.SET_GEN)),
+        ("rmsnorm_dweight", lambda: mot.mot_rmsnorm_dweight(part, ws, dw=dwn, sets=mot.SET_GEN)),
+        stages[3],
+    ]
+    ra = time_stages(stages_a, 50, 5, flush, stream)
 
     def whole():
         for _, fn in stages:
             fn()
 
-    # the same chain with events only around it: every kernel after the first is a programmatic
+    def whole_a():
+        for _, fn in stages_a:
+            fn()
+
+    # the same chains with events only around them: every kernel after the first is a programmatic
     # dependent of the one before, which the events between stages above rule out
     rw = time_stages([("step", whole)], 50, 5, flush, stream)
+    rwa = time_stages([("step", whole_a)], 50, 5, flush, stream)
     if mot.mot_device_status(ws) != 0:
         raise RuntimeError("device error flags set in the backward workload")
     pk = peaks()
@@ -651,6 +668,8 @@ def run_backward(dev, flush) -> dict:
     f_dx, f_dw = 2 * T * N_QKV * H, 2 * n_gen * N_QKV * H
     b_dx = 12 * T * H + 8 * T + 4 * H         # dy, s, d_res_out read; dx, fp32 partials, rstd written; plan; w
     b_dw = 4 * T * H + 8 * H                  # fp32 partials read; dw written
+    b_dx_a = 8 * T * H + 4 * n_gen * H + 8 * T + 4 * H   # phase A: the gen rows' partials only
+    b_dw_a = 4 * n_gen * H + 4 * H
 
     def gbs(b, name):
         return round(b / r[name] / 1e9, 1)
@@ -669,6 +688,15 @@ def run_backward(dev, flush) -> dict:
         "qkv_dw_gen_frac": round(f_dw / r["qkv_dw_gen"] / 1e12 / pk["bf16_tflops"], 4),
         "gen_rows": n_gen, "step_us": round(rw["step"] * 1e6, 2),
         "step_us_with_stage_events": round(r["step"] * 1e6, 2),
+        "phase_a": {
+            "what": "the gen set trained: norm-weight partials and fold of the gen rows only (dX, dx of every row)",
+            "add_rmsnorm_dx_us": round(ra["add_rmsnorm_dx"] * 1e6, 2),
+            "add_rmsnorm_dx_frac_hbm": round(b_dx_a / ra["add_rmsnorm_dx"] / 1e9 / pk["hbm_gbs"], 4),
+            "rmsnorm_dweight_us": round(ra["rmsnorm_dweight"] * 1e6, 2),
+            "rmsnorm_dweight_frac_hbm": round(b_dw_a / ra["rmsnorm_dweight"] / 1e9 / pk["hbm_gbs"], 4),
+            "step_us": round(rwa["step"] * 1e6, 2),
+            "step_us_with_stage_events": round(ra["step"] * 1e6, 2),
+        },
     }
 
 

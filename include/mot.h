@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define MOT_ABI_VERSION 3
+#define MOT_ABI_VERSION 4
 
 /* host-detected status codes (return values) */
 #define MOT_OK            0
@@ -74,6 +74,11 @@ extern "C" {
  * values. */
 #define MOT_A_PLAN_ORDER   0x100  /* row i of `a` is the plan's i-th row */
 #define MOT_OUT_PLAN_ORDER 0x200  /* row i of `out` is the plan's i-th row */
+
+/* weight-set masks of the norm backward's partials and fold */
+#define MOT_SET_UND  1
+#define MOT_SET_GEN  2
+#define MOT_SET_BOTH 3
 
 /* largest packed batch the library accepts */
 #define MOT_MAX_TOKENS (1 << 24)
@@ -352,6 +357,10 @@ int mot_routed_gemm_dw(const mot_bf16* dout, const mot_bf16* a, int64_t T, int N
  *             p[r][j] = dy[r][j] * (s[r][j] * rstd[r]) in blocks of 64 columns, rows in the
  *             plan's order: element (j / 64, i, j % 64) belongs to row perm[i] -- so each weight
  *             set's rows are one contiguous run in ascending order. mot_rmsnorm_dweight folds them.
+ *   partial_sets  MOT_SET_UND, MOT_SET_GEN or MOT_SET_BOTH (ignored without dw_partials): the
+ *             weight sets whose rows' partials are written; the other rows' entries are left as
+ *             they are. Phase A of [RFC-435] §3 trains the gen set only: MOT_SET_GEN writes a
+ *             quarter of the bytes on a layer of 3/4 und rows, and every row's dx is still formed.
  * Per row, every operation rounded on its own in fp32: rstd on the forward's fixed tree;
  * xh = s * rstd; g = dy * w[e]; dot = sum of g * xh on the same tree; c = dot / H;
  * dx = bf16(rstd * (g - xh * c) (+ d_res_out)). Geometry as mot_fused_add_rmsnorm; all
@@ -360,19 +369,23 @@ int mot_routed_gemm_dw(const mot_bf16* dout, const mot_bf16* a, int64_t T, int N
  */
 int mot_add_rmsnorm_backward(const mot_bf16* dy, const mot_bf16* d_res_out, const mot_bf16* s,
                              const mot_bf16* w, int64_t T, int H, float eps, void* ws, size_t ws_bytes,
-                             mot_bf16* dx, float* rstd, float* dw_partials, void* stream);
+                             mot_bf16* dx, float* rstd, float* dw_partials, int partial_sets, void* stream);
 
 /*
- * mot_rmsnorm_dweight -- gradient of both norm weight sets ([PR-503] gated-norm commit:
+ * mot_rmsnorm_dweight -- gradient of the norm weight sets ([PR-503] gated-norm commit:
  * per-row fp32 partials, then the ascending-row fp32 left fold).
- *   dw_partials  [H/64][T][64] fp32  mot_add_rmsnorm_backward's partials (plan order).
+ *   dw_partials  [H/64][T][64] fp32  mot_add_rmsnorm_backward's partials (plan order), written
+ *             for at least the sets folded here.
+ *   sets      MOT_SET_UND, MOT_SET_GEN or MOT_SET_BOTH: the weight sets folded; any other value
+ *             is MOT_ERR_ARG.
  *   ws        the same routing plan.
  *   dw        [2][H] fp32      out: dw[e][j] = ((p_r0 + p_r1) + p_r2) + ... over the rows
- *             r0 < r1 < ... of set e; +0 for a set without rows.
+ *             r0 < r1 < ... of each folded set e; +0 for a set without rows; the rows of the
+ *             sets not folded are left as they are.
  * Geometry: 256 <= H <= 8192, H a multiple of 256. Errors as mot_add_rmsnorm_backward.
  */
-int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, void* ws, size_t ws_bytes, float* dw,
-                        void* stream);
+int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, int sets, void* ws, size_t ws_bytes,
+                        float* dw, void* stream);
 
 /*
  * mot_flow_schedule_host -- the sampler's n step times from 1 down to 0 ([RFC-435] §3

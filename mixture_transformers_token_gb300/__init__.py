@@ -26,16 +26,18 @@ __all__ = [
     "mot_swiglu_interleave", "mot_rope_table_fill_host", "mot_device_status", "mot_routed_gemm_noalloc",
     "mot_routed_qkv_norm_rope_fp32", "mot_rope_table_fill_host_fp32", "mot_add_rmsnorm_backward",
     "mot_rmsnorm_dweight", "mot_routed_gemm_dx", "mot_routed_gemm_dw", "mot_joint_attention", "DEV_BAD_SEQUENCE",
-    "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "mot_gather_rows", "mot_selftest_wait_timeout",
+    "NOALLOC_MAX_TOKENS", "A_PLAN_ORDER", "OUT_PLAN_ORDER", "SET_UND", "SET_GEN", "SET_BOTH", "mot_gather_rows",
+    "mot_selftest_wait_timeout",
     "DEV_BAD_TIME", "mot_flow_workspace_bytes", "mot_flow_schedule_host", "mot_cfg_combine_renorm",
     "mot_flow_sde_step", "mot_flow_cfg_sde_step", "mot_flow_noise",
 ]
 
-ABI_VERSION = 3
+ABI_VERSION = 4
 EPI_CAST = 0
 EPI_SWIGLU = 1
 A_PLAN_ORDER = 0x100
 OUT_PLAN_ORDER = 0x200
+SET_UND, SET_GEN, SET_BOTH = 1, 2, 3  # weight-set masks of the norm backward's partials and fold
 DEV_BAD_MODALITY = 0x1
 DEV_TIMEOUT = 0x2
 DEV_PLAN_MISMATCH = 0x4
@@ -71,8 +73,8 @@ _SIGNATURES = {
     "mot_rope_table_fill_host": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
     "mot_rope_table_fill_host_fp32": (_c_i, [ctypes.c_double, _c_i, _c_i, _c_p]),
     "mot_add_rmsnorm_backward": (_c_i, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p, _c_p,
-                                        _c_p]),
-    "mot_rmsnorm_dweight": (_c_i, [_c_p, _c_i64, _c_i, _c_p, _c_sz, _c_p, _c_p]),
+                                        _c_i, _c_p]),
+    "mot_rmsnorm_dweight": (_c_i, [_c_p, _c_i64, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_dx": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_routed_gemm_dw": (_c_i, [_c_p, _c_p, _c_i64, _c_i, _c_i, _c_i, _c_i, _c_p, _c_sz, _c_p, _c_p]),
     "mot_joint_attention": (_c_i, [_c_p, _c_i64, _c_i, _c_i, _c_i, _c_p, _c_i, _c_f, _c_p, _c_sz, _c_p, _c_p]),
@@ -381,11 +383,11 @@ def mot_joint_attention(qkv, seqs, Hq: int, Hkv: int, D: int, ws, scale: float |
 
 
 def mot_add_rmsnorm_backward(dy, s, w, eps: float, ws, d_res_out=None, dx=None, rstd=None, dw_partials=None,
-                             stream=None):
+                             partial_sets: int = SET_BOTH, stream=None):
     """Input gradient of the fused add-RMSNorm: returns (dx [T][H] bf16, rstd [T] fp32).
     `s` is the forward's res_out and `ws` holds the routing plan of the forward's mod. If
-    `dw_partials` (fp32 [H/64][T][64]) is given, the per-row weight-gradient partials are
-    written there in the plan's row order."""
+    `dw_partials` (fp32 [H/64][T][64]) is given, the per-row weight-gradient partials of the
+    rows of the weight sets in `partial_sets` are written there in the plan's row order."""
     T, H = dy.shape
     _dev(dy, "dy", torch.bfloat16, 2)
     _dev(s, "s", torch.bfloat16, 2)
@@ -413,13 +415,14 @@ def mot_add_rmsnorm_backward(dy, s, w, eps: float, ws, d_res_out=None, dx=None, 
     _dev(rstd, "rstd", torch.float32, 1)
     _check("mot_add_rmsnorm_backward", _lib().mot_add_rmsnorm_backward(
         dy.data_ptr(), rp, s.data_ptr(), w.data_ptr(), T, H, eps, ws.data_ptr(), ws.numel(), dx.data_ptr(),
-        rstd.data_ptr(), pp, _stream(dy, stream)))
+        rstd.data_ptr(), pp, partial_sets, _stream(dy, stream)))
     return dx, rstd
 
 
-def mot_rmsnorm_dweight(dw_partials, ws, dw=None, stream=None):
-    """Gradient of both norm weight sets, [2][H] fp32: the ascending-row fp32 left fold of the
-    partials of mot_add_rmsnorm_backward over each set's rows."""
+def mot_rmsnorm_dweight(dw_partials, ws, dw=None, sets: int = SET_BOTH, stream=None):
+    """Gradient of the norm weight sets in `sets`, rows of dw [2][H] fp32: the ascending-row fp32
+    left fold of the partials of mot_add_rmsnorm_backward over each set's rows (the other set's
+    row of dw is left as it is)."""
     nb, T, c64 = dw_partials.shape
     _dev(dw_partials, "dw_partials", torch.float32, 3)
     _dev(ws, "ws", torch.uint8, 1)
@@ -430,7 +433,7 @@ def mot_rmsnorm_dweight(dw_partials, ws, dw=None, stream=None):
         dw = torch.empty((2, H), dtype=torch.float32, device=dw_partials.device)
     _dev(dw, "dw", torch.float32, 2)
     _check("mot_rmsnorm_dweight", _lib().mot_rmsnorm_dweight(
-        dw_partials.data_ptr(), T, H, ws.data_ptr(), ws.numel(), dw.data_ptr(), _stream(dw_partials, stream)))
+        dw_partials.data_ptr(), T, H, sets, ws.data_ptr(), ws.numel(), dw.data_ptr(), _stream(dw_partials, stream)))
     return dw
 
 

@@ -20,10 +20,12 @@
 //                          shared-memory slots; one consumer warp per slot runs the three passes
 //                          (sum of s^2, dot, output) with lane l on columns 256 j + 8 l + t (the
 //                          forward's tree layout), writes dx, the row's rstd and its partials.
-// rmsnorm_dw_fold_kernel   one CTA per (weight set, 64-column block): the set's partials, left
-//                          by the backward kernel as one contiguous run per column block,
+// rmsnorm_dw_fold_kernel   one CTA per (folded weight set, 64-column block): the set's partials,
+//                          left by the backward kernel as one contiguous run per column block,
 //                          stream in by TMA tiles; two warps fold one column per thread over
-//                          the set's rows in ascending order.
+//                          the set's rows in ascending order. Phase A of the BAGEL training
+//                          rules trains the gen set only: the backward kernel then writes the
+//                          gen rows' partials alone and the fold runs over the gen set alone.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -45,6 +47,7 @@ struct NormBwdArgs {
   uint4* dx;
   float* rstd;
   float* part;          // [H/64][T][64] per-row dweight partials by plan position, or null
+  int psets;            // bit e: write the partials of the rows of weight set e
   const uint8_t* ws;    // the routing plan: rows are visited in its order
   uint32_t* err;
   int consumers;        // consumer warps = row slots
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(32 * (1 + kBwdMaxConsumers), 1) add_rmsnorm_bw
     if (pos >= a.T) break;
     const int64_t row = perm[pos];
     const int e = pos < count0 ? 0 : 1;
+    const bool wpart = a.part != nullptr && ((a.psets >> e) & 1) != 0;  // this row's partials are wanted
     const uint32_t round = uint32_t(k / C);
     if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[c]), round & 1u, abort_flag, a.err))) break;
     {
@@ -253,7 +257,7 @@ __global__ void __launch_bounds__(32 * (1 + kBwdMaxConsumers), 1) add_rmsnorm_bw
           ow[t] = pack_bf2(ds0, ds1);
           pp[t] = f2_mul(dd, xh);
         }
-        if (a.part) {
+        if (wpart) {
           // columns 256 j + 8 lane + t: block 4 j + lane / 8, offset 8 (lane % 8) + t
           float4* pd = reinterpret_cast<float4*>(a.part + ((int64_t(4 * j + (lane >> 3)) * a.T + pos) << 6) +
                                                  8 * (lane & 7));
@@ -283,6 +287,7 @@ constexpr size_t kFoldSmem = 128 + kFoldStages * size_t(kFoldPartBytes) + 2 * kF
 struct FoldArgs {
   const uint8_t* ws;
   int T, H;
+  int set_lo;  // the first weight set folded; the grid covers it and the sets after it
   float* dw;
   uint32_t* err;
 };
@@ -305,7 +310,7 @@ __global__ void __launch_bounds__(kFoldThreads) rmsnorm_dw_fold_kernel(const __g
   pdl_trigger();  // a programmatic dependent: nothing is read before the preceding grid completes
   pdl_wait();
   const int ncb = a.H / kFoldCols;
-  const int e = int(blockIdx.x) / ncb, cb = int(blockIdx.x) % ncb;
+  const int e = a.set_lo + int(blockIdx.x) / ncb, cb = int(blockIdx.x) % ncb;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(a.ws);
   if (hdr->magic != kPlanMagic || hdr->T != a.T) {
@@ -382,10 +387,12 @@ using namespace mot;
 
 extern "C" int mot_add_rmsnorm_backward(const mot_bf16* dy, const mot_bf16* d_res_out, const mot_bf16* s,
                                         const mot_bf16* w, int64_t T, int H, float eps, void* ws, size_t ws_bytes,
-                                        mot_bf16* dx, float* rstd, float* dw_partials, void* stream) {
+                                        mot_bf16* dx, float* rstd, float* dw_partials, int partial_sets,
+                                        void* stream) {
   if (!dy || !s || !w || !ws || !dx || !rstd) return MOT_ERR_NULL;
   if (T < 1 || T > MOT_MAX_TOKENS || H < 256 || H > 8192 || H % 256 != 0) return MOT_ERR_GEOMETRY;
   if (!(eps > 0.0f) || !(eps < 3.0e38f)) return MOT_ERR_ARG;
+  if (dw_partials && (partial_sets < MOT_SET_UND || partial_sets > MOT_SET_BOTH)) return MOT_ERR_ARG;
   if (!aligned16(dy) || (d_res_out && !aligned16(d_res_out)) || !aligned16(s) || !aligned16(w) || !aligned16(ws) ||
       !aligned16(dx) || !aligned16(rstd) || (dw_partials && !aligned16(dw_partials)))
     return MOT_ERR_ALIGN;
@@ -407,6 +414,7 @@ extern "C" int mot_add_rmsnorm_backward(const mot_bf16* dy, const mot_bf16* d_re
   a.dx = reinterpret_cast<uint4*>(dx);
   a.rstd = rstd;
   a.part = dw_partials;
+  a.psets = partial_sets;
   a.ws = static_cast<const uint8_t*>(ws);
   a.err = &static_cast<PlanHeader*>(ws)->error;
   const size_t row_bytes = size_t(H) * 2;
@@ -431,10 +439,11 @@ extern "C" int mot_add_rmsnorm_backward(const mot_bf16* dy, const mot_bf16* d_re
   return e == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }
 
-extern "C" int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, void* ws, size_t ws_bytes, float* dw,
-                                   void* stream) {
+extern "C" int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, int sets, void* ws, size_t ws_bytes,
+                                   float* dw, void* stream) {
   if (!dw_partials || !ws || !dw) return MOT_ERR_NULL;
   if (T < 1 || T > MOT_MAX_TOKENS || H < 256 || H > 8192 || H % 256 != 0) return MOT_ERR_GEOMETRY;
+  if (sets < MOT_SET_UND || sets > MOT_SET_BOTH) return MOT_ERR_ARG;
   if (!aligned16(dw_partials) || !aligned16(ws) || !aligned16(dw)) return MOT_ERR_ALIGN;
   if (ws_bytes < size_t(plan_bytes(T))) return MOT_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -464,7 +473,9 @@ extern "C" int mot_rmsnorm_dweight(const float* dw_partials, int64_t T, int H, v
   a.H = H;
   a.dw = dw;
   a.err = &static_cast<PlanHeader*>(ws)->error;
-  const cudaError_t e = launch_dependent(bwd::rmsnorm_dw_fold_kernel, dim3(2 * (H / bwd::kFoldCols)),
+  a.set_lo = sets == MOT_SET_GEN ? 1 : 0;
+  const int nsets = sets == MOT_SET_BOTH ? 2 : 1;
+  const cudaError_t e = launch_dependent(bwd::rmsnorm_dw_fold_kernel, dim3(nsets * (H / bwd::kFoldCols)),
                                          dim3(bwd::kFoldThreads), bwd::kFoldSmem, st, tm_part, a);
   return e == cudaSuccess ? MOT_OK : MOT_ERR_CUDA;
 }

@@ -145,22 +145,28 @@ def test_qkv_fp32_profile_rejects(lib):
 
 def test_norm_backward_rejects(lib):
     f = lib.mot_add_rmsnorm_backward
-    assert f(None, None, A, A, 8, 256, 1e-6, B, 1 << 20, C, C, None, None) == MOT_ERR_NULL
-    assert f(A, None, A, A, 8, 256, 1e-6, None, 1 << 20, C, C, None, None) == MOT_ERR_NULL
-    assert f(A, None, A, A, 8, 256, 1e-6, B, 1 << 20, C, None, None, None) == MOT_ERR_NULL
-    assert f(A, None, A, A, 8, 200, 1e-6, B, 1 << 20, C, C, None, None) == MOT_ERR_GEOMETRY
-    assert f(A, None, A, A, 8, 8448, 1e-6, B, 1 << 20, C, C, None, None) == MOT_ERR_GEOMETRY
-    assert f(A, None, A, A, 0, 256, 1e-6, B, 1 << 20, C, C, None, None) == MOT_ERR_GEOMETRY
-    assert f(A, None, A, A, 8, 256, 0.0, B, 1 << 20, C, C, None, None) == MOT_ERR_ARG
-    assert f(A, MIS, A, A, 8, 256, 1e-6, B, 1 << 20, C, C, None, None) == MOT_ERR_ALIGN
-    assert f(A, None, A, A, 8, 256, 1e-6, B, 1 << 20, C, MIS, None, None) == MOT_ERR_ALIGN
-    assert f(A, None, A, A, 8, 256, 1e-6, B, 1 << 20, C, C, MIS, None) == MOT_ERR_ALIGN
-    assert f(A, None, A, A, 1000, 256, 1e-6, B, 100, C, C, None, None) == MOT_ERR_WORKSPACE
+    assert f(None, None, A, A, 8, 256, 1e-6, B, 1 << 20, C, C, None, 3, None) == MOT_ERR_NULL
+    assert f(A, None, A, A, 8, 256, 1e-6, None, 1 << 20, C, C, None, 3, None) == MOT_ERR_NULL
+    assert f(A, None, A, A, 8, 256, 1e-6, B, 1 << 20, C, None, None, 3, None) == MOT_ERR_NULL
+    assert f(A, None, A, A, 8, 200, 1e-6, B, 1 << 20, C, C, None, 3, None) == MOT_ERR_GEOMETRY
+    assert f(A, None, A, A, 8, 8448, 1e-6, B, 1 << 20, C, C, None, 3, None) == MOT_ERR_GEOMETRY
+    assert f(A, None, A, A, 0, 256, 1e-6, B, 1 << 20, C, C, None, 3, None) == MOT_ERR_GEOMETRY
+    assert f(A, None, A, A, 8, 256, 0.0, B, 1 << 20, C, C, None, 3, None) == MOT_ERR_ARG
+    assert f(A, MIS, A, A, 8, 256, 1e-6, B, 1 << 20, C, C, None, 3, None) == MOT_ERR_ALIGN
+    assert f(A, None, A, A, 8, 256, 1e-6, B, 1 << 20, C, MIS, None, 3, None) == MOT_ERR_ALIGN
+    assert f(A, None, A, A, 8, 256, 1e-6, B, 1 << 20, C, C, MIS, 3, None) == MOT_ERR_ALIGN
+    assert f(A, None, A, A, 1000, 256, 1e-6, B, 100, C, C, None, 3, None) == MOT_ERR_WORKSPACE
+    # the partials' weight-set mask: MOT_SET_UND, MOT_SET_GEN or MOT_SET_BOTH; ignored without partials
+    for bad in (0, 4, -1):
+        assert f(A, None, A, A, 8, 256, 1e-6, B, 1 << 20, C, C, C, bad, None) == MOT_ERR_ARG
+    assert f(A, None, A, A, 1000, 256, 1e-6, B, 100, C, C, None, 0, None) == MOT_ERR_WORKSPACE
     g = lib.mot_rmsnorm_dweight
-    assert g(None, 8, 256, B, 1 << 20, C, None) == MOT_ERR_NULL
-    assert g(A, 8, 255, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
-    assert g(A, 8, 256, MIS, 1 << 20, C, None) == MOT_ERR_ALIGN
-    assert g(A, 1000, 256, B, 100, C, None) == MOT_ERR_WORKSPACE
+    assert g(None, 8, 256, 3, B, 1 << 20, C, None) == MOT_ERR_NULL
+    assert g(A, 8, 255, 3, B, 1 << 20, C, None) == MOT_ERR_GEOMETRY
+    assert g(A, 8, 256, 3, MIS, 1 << 20, C, None) == MOT_ERR_ALIGN
+    assert g(A, 1000, 256, 3, B, 100, C, None) == MOT_ERR_WORKSPACE
+    for bad in (0, 4, -1):
+        assert g(A, 8, 256, bad, B, 1 << 20, C, None) == MOT_ERR_ARG
 
 
 def test_gemm_backward_rejects(lib):

@@ -49,6 +49,39 @@ def _run_norm_bwd(inp, eps=1e-6):
     return dx, rstd, dw
 
 
+
+@pytest.mark.parametrize("T,H,sets", [(333, 768, mot.SET_GEN), (333, 768, mot.SET_UND), (4096, 3584, mot.SET_GEN),
+                                      (64, 256, mot.SET_GEN)])
+def test_norm_backward_and_fold_of_one_weight_set(T, H, sets):
+    # Phase A of the BAGEL training rules trains the gen set only: the partials of the other
+    # set's rows and its row of dw stay as they were; dx, rstd, the selected partials and the
+    # selected dw row equal the both-sets call bit for bit. (T = 64 at H = 256: Bernoulli rows
+    # of both sets; T = 4096: the bench layer, 3072 und rows then 1024 gen rows.)
+    mod = W.modality_blocks([(0, 3 * T // 4), (1, T - 3 * T // 4)]) if T == 4096 else None
+    inp = _norm_bwd_inputs(T, H, 11, mod=mod)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    ws = mot.mot_route_plan(d["mod"])
+    part_all = torch.empty((H // 64, T, 64), dtype=torch.float32, device="cuda")
+    dx_a, rstd_a = mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], 1e-6, ws, d_res_out=d["dro"],
+                                                dw_partials=part_all)
+    dw_all = mot.mot_rmsnorm_dweight(part_all, ws)
+    part = torch.full((H // 64, T, 64), 7.0, dtype=torch.float32, device="cuda")
+    dx, rstd = mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], 1e-6, ws, d_res_out=d["dro"], dw_partials=part,
+                                            partial_sets=sets)
+    dw = torch.full((2, H), 5.0, dtype=torch.float32, device="cuda")
+    mot.mot_rmsnorm_dweight(part, ws, dw=dw, sets=sets)
+    assert mot.mot_device_status(ws) == 0
+    assert torch.equal(dx.view(torch.int16), dx_a.view(torch.int16)) and torch.equal(rstd, rstd_a)
+    count0 = int((inp["mod"] == 0).sum())
+    sel = slice(0, count0) if sets == mot.SET_UND else slice(count0, T)
+    other = slice(count0, T) if sets == mot.SET_UND else slice(0, count0)
+    assert torch.equal(part[:, sel].view(torch.int32), part_all[:, sel].view(torch.int32))
+    assert bool((part[:, other] == 7.0).all())
+    e = 0 if sets == mot.SET_UND else 1
+    assert torch.equal(dw[e].view(torch.int32), dw_all[e].view(torch.int32))
+    assert bool((dw[1 - e] == 5.0).all())
+
+
 @pytest.mark.parametrize("T,H,seed,with_dres", [(64, 256, 1, True), (1, 256, 2, True), (333, 3584, 3, True),
                                                 (1000, 768, 4, False), (300, 5120, 5, True),
                                                 (4096, 3584, 6, True)])
