@@ -82,6 +82,32 @@ def test_norm_backward_and_fold_of_one_weight_set(T, H, sets):
     assert bool((dw[1 - e] == 5.0).all())
 
 
+
+@pytest.mark.parametrize("row_set", [0, 1])
+def test_one_set_masks_on_a_single_row(row_set):
+    # one row: the set without rows folds to +0, and the mask leaves the other entries alone
+    inp = _norm_bwd_inputs(1, 256, 12, mod=torch.tensor([row_set], dtype=torch.uint8))
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    ws = mot.mot_route_plan(d["mod"])
+    part = torch.full((4, 1, 64), 7.0, dtype=torch.float32, device="cuda")
+    other = mot.SET_UND if row_set == 1 else mot.SET_GEN
+    mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], 1e-6, ws, d_res_out=d["dro"], dw_partials=part,
+                                 partial_sets=other)
+    assert bool((part == 7.0).all())  # the row is not in the selected set
+    dw = torch.full((2, 256), 5.0, dtype=torch.float32, device="cuda")
+    mot.mot_rmsnorm_dweight(part, ws, dw=dw, sets=other)
+    e_other = 0 if other == mot.SET_UND else 1
+    assert torch.equal(dw[e_other].view(torch.int32), torch.zeros(256, dtype=torch.int32, device="cuda"))  # +0
+    assert bool((dw[row_set] == 5.0).all())
+    mine = mot.SET_GEN if row_set == 1 else mot.SET_UND
+    mot.mot_add_rmsnorm_backward(d["dy"], d["s"], d["w"], 1e-6, ws, d_res_out=d["dro"], dw_partials=part,
+                                 partial_sets=mine)
+    mot.mot_rmsnorm_dweight(part, ws, dw=dw, sets=mine)
+    assert mot.mot_device_status(ws) == 0
+    # a fold over one row is that row's partial
+    assert torch.equal(dw[row_set].view(torch.int32), part[:, 0, :].reshape(256).view(torch.int32))
+
+
 @pytest.mark.parametrize("T,H,seed,with_dres", [(64, 256, 1, True), (1, 256, 2, True), (333, 3584, 3, True),
                                                 (1000, 768, 4, False), (300, 5120, 5, True),
                                                 (4096, 3584, 6, True)])
